@@ -1,0 +1,481 @@
+/*
+ * dsa_oracle.c -- plain, slow, CPU oracle for the gated DSA attention step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or helper with
+ * the CUDA library; the two meet only in the seeded input buffers.
+ *
+ * Every function evaluates the plain definition in double precision from the
+ * same BF16 inputs the CUDA path reads (decoded exactly), one query row at a
+ * time, with no blocking, fusion or reordering beyond what the definition
+ * states.  Rows are spread over POSIX threads; each row is computed by one
+ * thread in a fixed order, so results do not depend on the thread count.
+ *
+ * Sources (page title, section):
+ *   [K31]  "Kimi-K3.1-Pro", NeMo AutoModel model coverage:
+ *          - Implementation Limits, bullet 1: a fused indexer produces top-k
+ *            coordinates; sparse MLA attends directly to the selected latent KV.
+ *          - Implementation Limits, bullet 2: BF16 indexer projections with FP32
+ *            score accumulation; the indexer scans all causal keys; sparse MLA
+ *            neither expands per-head K/V nor attends to unselected keys.
+ *          - Implementation Limits, bullet 4: a sequence of at most 2,048 valid
+ *            tokens keeps every causal key.
+ *          - Implementation Limits, closing paragraph: the output gate is kept.
+ *   [ARCH] "Kimi K3.1 Pro" (archdiff, attn-gate): summary line (24 gated DSA
+ *          layers, top-2,048, no positional encoding); blueprint list items
+ *          "LayerNorm on the indexer key", "Partial RoPE / NoPE", and
+ *          "Output gate + sink: sigma(x W_g) (.) o".
+ *   [CFG]  "nemo_automodel.components.models.kimi_k3" (v0.4 API),
+ *          KimiK3TextConfig: kv_lora_rank 512, qk_nope_head_dim 128,
+ *          qk_rope_head_dim 64, v_head_dim 128, num_attention_heads 96,
+ *          mla_use_nope True, mla_use_output_gate True.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   - indexer score I[t,s] = sum_j w[t,j] * max(0, q[t,j,:] . k[s,:]), one shared
+ *     key per token, no extra scale (the pages do not give the indexer's form);
+ *   - causal means s <= t, self included, and self is not forced into the set;
+ *   - ordering for top-k: larger score first, then smaller key index;
+ *   - value vector = the first 512 latent dims; the 64 k_pe dims only enter
+ *     the logits; no rotation anywhere (NoPE);
+ *   - the gate acts element-wise on the per-head value after W_UV, i.e. on the
+ *     H*dv = 96*128 wide attention output, with W_g shaped [H*dv, hid].
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define OR_OK 0
+#define OR_BAD_ARG 1
+#define OR_BAD_INDEX 2
+#define OR_NOMEM 3
+
+/* ------------------------------------------------------------------------- */
+/* BF16 decode (exact) and threading                                          */
+/* ------------------------------------------------------------------------- */
+
+static double bf(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+static int g_threads = 0;
+
+int oracle_set_threads(int n) {
+  g_threads = n;
+  return OR_OK;
+}
+
+int oracle_get_threads(void) {
+  if (g_threads > 0) return g_threads;
+  long n = sysconf(_SC_NPROCESSORS_ONLN);
+  return n > 0 ? (int)n : 1;
+}
+
+typedef void (*row_fn)(void* ctx, int64_t r);
+
+typedef struct {
+  row_fn fn;
+  void* ctx;
+  int64_t n;
+  int64_t next;
+  pthread_mutex_t mu;
+} pool_t;
+
+static void* pool_worker(void* arg) {
+  pool_t* p = (pool_t*)arg;
+  for (;;) {
+    pthread_mutex_lock(&p->mu);
+    int64_t r = p->next++;
+    pthread_mutex_unlock(&p->mu);
+    if (r >= p->n) break;
+    p->fn(p->ctx, r);
+  }
+  return NULL;
+}
+
+static void parallel_rows(int64_t n, row_fn fn, void* ctx) {
+  int nt = oracle_get_threads();
+  if (nt > n) nt = (int)(n > 0 ? n : 1);
+  pool_t p;
+  p.fn = fn;
+  p.ctx = ctx;
+  p.n = n;
+  p.next = 0;
+  pthread_mutex_init(&p.mu, NULL);
+  if (nt <= 1) {
+    pool_worker(&p);
+  } else {
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nt);
+    int started = 0;
+    for (int i = 0; i < nt; ++i)
+      if (pthread_create(&th[i], NULL, pool_worker, &p) == 0) ++started;
+    if (started == 0) pool_worker(&p);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    free(th);
+  }
+  pthread_mutex_destroy(&p.mu);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Indexer scores  [K31 Impl. Limits b2; ARCH summary; reading above]         */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+  const uint16_t *q, *w, *k;
+  const int32_t *q_start, *kv_len;
+  int Tq, S_max, H_I, D_I;
+  const int64_t* rows;
+  double* out;
+  int err;
+} idx_ctx;
+
+static void indexer_row(void* vctx, int64_t r) {
+  idx_ctx* c = (idx_ctx*)vctx;
+  int64_t flat = c->rows[r];
+  int b = (int)(flat / c->Tq), i = (int)(flat % c->Tq);
+  int64_t t = (int64_t)c->q_start[b] + i; /* absolute query position */
+  double* o = c->out + r * (int64_t)c->S_max;
+  for (int64_t s = 0; s < c->S_max; ++s) o[s] = NAN;
+  if (t >= c->kv_len[b] || t >= c->S_max) { c->err = OR_BAD_ARG; return; }
+  const uint16_t* q = c->q + flat * (int64_t)c->H_I * c->D_I;
+  const uint16_t* w = c->w + flat * (int64_t)c->H_I;
+  const uint16_t* kb = c->k + (int64_t)b * c->S_max * c->D_I;
+  /* every causal key s <= t is scored */
+  for (int64_t s = 0; s <= t; ++s) {
+    const uint16_t* k = kb + s * c->D_I;
+    double score = 0.0;
+    for (int j = 0; j < c->H_I; ++j) {
+      double dot = 0.0;
+      for (int d = 0; d < c->D_I; ++d) dot += bf(q[j * c->D_I + d]) * bf(k[d]);
+      double relu = dot > 0.0 ? dot : 0.0;
+      score += bf(w[j]) * relu;
+    }
+    o[s] = score;
+  }
+}
+
+/* q_idx [B,Tq,H_I,D_I], w [B,Tq,H_I], k_idx [B,S_max,D_I] (BF16 bits);
+ * out [n_rows, S_max]: score of key s for s <= t, NaN beyond. */
+int oracle_indexer_scores(const uint16_t* q_idx, const uint16_t* w, const uint16_t* k_idx,
+                          const int32_t* q_start, const int32_t* kv_len, int B, int Tq,
+                          int S_max, int H_I, int D_I, int64_t n_rows, const int64_t* rows,
+                          double* out) {
+  if (!q_idx || !w || !k_idx || !q_start || !kv_len || !rows || !out) return OR_BAD_ARG;
+  if (B <= 0 || Tq <= 0 || S_max <= 0 || H_I <= 0 || D_I <= 0 || n_rows < 0) return OR_BAD_ARG;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= (int64_t)B * Tq) return OR_BAD_ARG;
+  idx_ctx c = {q_idx, w, k_idx, q_start, kv_len, Tq, S_max, H_I, D_I, rows, out, OR_OK};
+  parallel_rows(n_rows, indexer_row, &c);
+  return c.err;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Top-k selection  [K31 Impl. Limits b1 (coordinates), b4 (<= k keeps all)]  */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+  double score;
+  int32_t s;
+} cand_t;
+
+static int cand_cmp(const void* a, const void* b) {
+  const cand_t* x = (const cand_t*)a;
+  const cand_t* y = (const cand_t*)b;
+  if (x->score > y->score) return -1; /* larger score first */
+  if (x->score < y->score) return 1;
+  return (x->s < y->s) ? -1 : (x->s > y->s); /* then smaller index */
+}
+
+typedef struct {
+  const double* scores;
+  const int32_t* n_valid;
+  int S_max, topk;
+  int32_t* out_idx;
+  double* kth;
+  int err;
+} topk_ctx;
+
+static void topk_row(void* vctx, int64_t r) {
+  topk_ctx* c = (topk_ctx*)vctx;
+  int n = c->n_valid[r];
+  int32_t* o = c->out_idx + r * (int64_t)c->topk;
+  for (int j = 0; j < c->topk; ++j) o[j] = -1;
+  if (n <= c->topk) {
+    /* a query with at most k causal keys keeps every one of them */
+    for (int s = 0; s < n; ++s) o[s] = s;
+    c->kth[r] = -INFINITY;
+    return;
+  }
+  cand_t* v = (cand_t*)malloc(sizeof(cand_t) * (size_t)n);
+  if (!v) { c->err = OR_NOMEM; return; }
+  const double* sc = c->scores + r * (int64_t)c->S_max;
+  for (int s = 0; s < n; ++s) { v[s].score = sc[s]; v[s].s = s; }
+  qsort(v, (size_t)n, sizeof(cand_t), cand_cmp);
+  for (int j = 0; j < c->topk; ++j) o[j] = v[j].s;
+  c->kth[r] = v[c->topk - 1].score;
+  free(v);
+}
+
+/* scores [n_rows, S_max] (first n_valid[r] entries used); out_idx [n_rows, topk]
+ * sorted by (score desc, index asc), -1 padded; kth[r] = k-th largest score, or
+ * -inf when every key is kept. */
+int oracle_topk(const double* scores, const int32_t* n_valid, int64_t n_rows, int S_max,
+                int topk, int32_t* out_idx, double* kth) {
+  if (!scores || !n_valid || !out_idx || !kth || topk <= 0 || S_max <= 0) return OR_BAD_ARG;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (n_valid[r] < 0 || n_valid[r] > S_max) return OR_BAD_ARG;
+  topk_ctx c = {scores, n_valid, S_max, topk, out_idx, kth, OR_OK};
+  parallel_rows(n_rows, topk_row, &c);
+  return c.err;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Sparse MLA in latent space  [K31 Impl. Limits b1-b2; ARCH NoPE; CFG dims]  */
+/* ------------------------------------------------------------------------- */
+
+#define RLAT 576
+#define VLAT 512
+
+typedef struct {
+  const uint16_t *q, *kv;
+  const int32_t *idx, *q_start, *kv_len;
+  int Tq, S_max, H, topk;
+  double scale;
+  const int64_t* rows;
+  double *o, *lse;
+  int dense;
+  int err;
+} mla_ctx;
+
+static void mla_row(void* vctx, int64_t r) {
+  mla_ctx* c = (mla_ctx*)vctx;
+  int64_t flat = c->rows[r];
+  int b = (int)(flat / c->Tq), i = (int)(flat % c->Tq);
+  int64_t t = (int64_t)c->q_start[b] + i;
+  const uint16_t* kvb = c->kv + (int64_t)b * c->S_max * RLAT;
+  double* o = c->o + r * (int64_t)c->H * VLAT;
+  double* lse = c->lse + r * (int64_t)c->H;
+  if (t >= c->kv_len[b] || t >= c->S_max) { c->err = OR_BAD_ARG; return; }
+
+  /* the set of attended keys: the given indices (skipping -1), or all s <= t */
+  int n = 0;
+  int32_t* sel;
+  if (c->dense) {
+    n = (int)(t + 1);
+    sel = (int32_t*)malloc(sizeof(int32_t) * (size_t)n);
+    if (!sel) { c->err = OR_NOMEM; return; }
+    for (int s = 0; s < n; ++s) sel[s] = s;
+  } else {
+    const int32_t* ix = c->idx + flat * (int64_t)c->topk;
+    sel = (int32_t*)malloc(sizeof(int32_t) * (size_t)c->topk);
+    if (!sel) { c->err = OR_NOMEM; return; }
+    for (int j = 0; j < c->topk; ++j) {
+      int32_t s = ix[j];
+      if (s < 0) continue;
+      if (s > t || s >= c->kv_len[b]) { c->err = OR_BAD_INDEX; continue; }
+      sel[n++] = s;
+    }
+  }
+  double* z = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  if (!z) { free(sel); c->err = OR_NOMEM; return; }
+  for (int h = 0; h < c->H; ++h) {
+    const uint16_t* q = c->q + (flat * c->H + h) * (int64_t)RLAT;
+    double* oh = o + (int64_t)h * VLAT;
+    for (int d = 0; d < VLAT; ++d) oh[d] = 0.0;
+    if (n == 0) { lse[h] = -INFINITY; continue; }
+    /* logits over the full 576-wide row: 512 c_kv dims + 64 unrotated k_pe dims */
+    double m = -INFINITY;
+    for (int j = 0; j < n; ++j) {
+      const uint16_t* row = kvb + (int64_t)sel[j] * RLAT;
+      double dot = 0.0;
+      for (int d = 0; d < RLAT; ++d) dot += bf(q[d]) * bf(row[d]);
+      z[j] = dot * c->scale;
+      if (z[j] > m) m = z[j];
+    }
+    double l = 0.0;
+    for (int j = 0; j < n; ++j) {
+      double p = exp(z[j] - m);
+      l += p;
+      const uint16_t* row = kvb + (int64_t)sel[j] * RLAT;
+      for (int d = 0; d < VLAT; ++d) oh[d] += p * bf(row[d]); /* value = first 512 dims */
+    }
+    for (int d = 0; d < VLAT; ++d) oh[d] /= l;
+    lse[h] = m + log(l);
+  }
+  free(z);
+  free(sel);
+}
+
+static int mla_common(const uint16_t* q_lat, const uint16_t* kv, const int32_t* idx,
+                      const int32_t* q_start, const int32_t* kv_len, int B, int Tq, int S_max,
+                      int H, int topk, double scale, int64_t n_rows, const int64_t* rows,
+                      double* o, double* lse, int dense) {
+  if (!q_lat || !kv || !q_start || !kv_len || !rows || !o || !lse) return OR_BAD_ARG;
+  if (!dense && (!idx || topk <= 0)) return OR_BAD_ARG;
+  if (B <= 0 || Tq <= 0 || S_max <= 0 || H <= 0 || n_rows < 0) return OR_BAD_ARG;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= (int64_t)B * Tq) return OR_BAD_ARG;
+  mla_ctx c = {q_lat, kv, idx, q_start, kv_len, Tq, S_max, H, topk, scale,
+               rows, o, lse, dense, OR_OK};
+  parallel_rows(n_rows, mla_row, &c);
+  return c.err;
+}
+
+/* q_lat [B,Tq,H,576], kv [B,S_max,576] (BF16 bits), idx [B,Tq,topk] (-1 = unused);
+ * o [n_rows,H,512], lse [n_rows,H] (natural log). */
+int oracle_sparse_mla(const uint16_t* q_lat, const uint16_t* kv, const int32_t* idx,
+                      const int32_t* q_start, const int32_t* kv_len, int B, int Tq, int S_max,
+                      int H, int topk, double scale, int64_t n_rows, const int64_t* rows,
+                      double* o, double* lse) {
+  return mla_common(q_lat, kv, idx, q_start, kv_len, B, Tq, S_max, H, topk, scale, n_rows,
+                    rows, o, lse, 0);
+}
+
+/* Dense causal MLA over every key s <= t: the dense-mask reference path. */
+int oracle_dense_mla(const uint16_t* q_lat, const uint16_t* kv, const int32_t* q_start,
+                     const int32_t* kv_len, int B, int Tq, int S_max, int H, double scale,
+                     int64_t n_rows, const int64_t* rows, double* o, double* lse) {
+  return mla_common(q_lat, kv, NULL, q_start, kv_len, B, Tq, S_max, H, 0, scale, n_rows, rows,
+                    o, lse, 1);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Explicit (non-absorbed) MLA: per-head K/V expanded through W_UK / W_UV      */
+/* [K31 Impl. Limits b2: sparse MLA avoids this expansion; CFG dims]          */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+  const double *q_nope, *q_pe, *W_UK, *W_UV, *c_kv, *k_pe;
+  const int32_t* sel;
+  int H, dn, dr, R, dv, K;
+  double scale;
+  double* out;
+} exp_ctx;
+
+static void explicit_row(void* vctx, int64_t r) {
+  exp_ctx* c = (exp_ctx*)vctx;
+  const int32_t* sel = c->sel + r * (int64_t)c->K;
+  int n = 0;
+  for (int j = 0; j < c->K; ++j)
+    if (sel[j] >= 0) ++n;
+  double* z = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  double* kh = (double*)malloc(sizeof(double) * (size_t)c->dn);
+  double* vh = (double*)malloc(sizeof(double) * (size_t)c->dv);
+  for (int h = 0; h < c->H; ++h) {
+    const double* qn = c->q_nope + (r * c->H + h) * (int64_t)c->dn;
+    const double* qp = c->q_pe + (r * c->H + h) * (int64_t)c->dr;
+    const double* Wk = c->W_UK + (int64_t)h * c->dn * c->R; /* [dn, R] */
+    const double* Wv = c->W_UV + (int64_t)h * c->dv * c->R; /* [dv, R] */
+    double* oh = c->out + (r * c->H + h) * (int64_t)c->dv;
+    for (int e = 0; e < c->dv; ++e) oh[e] = 0.0;
+    if (n == 0) continue;
+    double m = -INFINITY;
+    int jj = 0;
+    for (int j = 0; j < c->K; ++j) {
+      int s = sel[j];
+      if (s < 0) continue;
+      const double* ck = c->c_kv + (int64_t)s * c->R;
+      /* k_nope_h[s] = W_UK_h c_kv[s] */
+      for (int a = 0; a < c->dn; ++a) {
+        double acc = 0.0;
+        for (int d = 0; d < c->R; ++d) acc += Wk[(int64_t)a * c->R + d] * ck[d];
+        kh[a] = acc;
+      }
+      double dot = 0.0;
+      for (int a = 0; a < c->dn; ++a) dot += qn[a] * kh[a];
+      const double* kp = c->k_pe + (int64_t)s * c->dr;
+      for (int a = 0; a < c->dr; ++a) dot += qp[a] * kp[a];
+      z[jj] = dot * c->scale;
+      if (z[jj] > m) m = z[jj];
+      ++jj;
+    }
+    double l = 0.0;
+    jj = 0;
+    for (int j = 0; j < c->K; ++j) {
+      int s = sel[j];
+      if (s < 0) continue;
+      double p = exp(z[jj++] - m);
+      l += p;
+      const double* ck = c->c_kv + (int64_t)s * c->R;
+      /* v_h[s] = W_UV_h c_kv[s] */
+      for (int e = 0; e < c->dv; ++e) {
+        double acc = 0.0;
+        for (int d = 0; d < c->R; ++d) acc += Wv[(int64_t)e * c->R + d] * ck[d];
+        vh[e] = acc;
+      }
+      for (int e = 0; e < c->dv; ++e) oh[e] += p * vh[e];
+    }
+    for (int e = 0; e < c->dv; ++e) oh[e] /= l;
+  }
+  free(z);
+  free(kh);
+  free(vh);
+}
+
+/* q_nope [n,H,dn], q_pe [n,H,dr], W_UK [H,dn,R], W_UV [H,dv,R], c_kv [S,R],
+ * k_pe [S,dr], sel [n,K] (-1 = unused) -> out [n,H,dv]; all double. */
+int oracle_explicit_mla(const double* q_nope, const double* q_pe, const double* W_UK,
+                        const double* W_UV, const double* c_kv, const double* k_pe,
+                        const int32_t* sel, int64_t n, int H, int dn, int dr, int R, int dv,
+                        int K, double scale, double* out) {
+  if (!q_nope || !q_pe || !W_UK || !W_UV || !c_kv || !k_pe || !sel || !out) return OR_BAD_ARG;
+  if (n < 0 || H <= 0 || dn <= 0 || dr < 0 || R <= 0 || dv <= 0 || K <= 0) return OR_BAD_ARG;
+  exp_ctx c = {q_nope, q_pe, W_UK, W_UV, c_kv, k_pe, sel, H, dn, dr, R, dv, K, scale, out};
+  parallel_rows(n, explicit_row, &c);
+  return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Output gate  [ARCH "Output gate + sink"; K31 Impl. Limits closing para;    */
+/*               CFG mla_use_output_gate, v_head_dim]                        */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+  const uint16_t *x, *W_g, *W_uv;
+  const double* o_lat;
+  int hid, H, dv, R;
+  const int64_t* rows;
+  double* out;
+} gate_ctx;
+
+static void gate_row(void* vctx, int64_t r) {
+  gate_ctx* c = (gate_ctx*)vctx;
+  int64_t t = c->rows[r];
+  const uint16_t* x = c->x + t * (int64_t)c->hid;
+  double* o = c->out + r * (int64_t)c->H * c->dv;
+  for (int h = 0; h < c->H; ++h) {
+    const double* ol = c->o_lat + (t * c->H + h) * (int64_t)c->R;
+    for (int e = 0; e < c->dv; ++e) {
+      int64_t col = (int64_t)h * c->dv + e;
+      /* g = x . W_g[col, :] */
+      const uint16_t* wg = c->W_g + col * c->hid;
+      double g = 0.0;
+      for (int d = 0; d < c->hid; ++d) g += bf(x[d]) * bf(wg[d]);
+      /* per-head value after the up-projection: u = W_UV_h[e, :] . o_lat_h */
+      const uint16_t* wu = c->W_uv + ((int64_t)h * c->dv + e) * c->R;
+      double u = 0.0;
+      for (int d = 0; d < c->R; ++d) u += bf(wu[d]) * ol[d];
+      o[col] = u / (1.0 + exp(-g)); /* sigma(g) * u */
+    }
+  }
+}
+
+/* x [N,hid], W_g [H*dv,hid], W_uv [H,dv,R] (BF16 bits); o_lat [N,H,R] double;
+ * out [n_rows, H*dv]. */
+int oracle_gate(const uint16_t* x, const uint16_t* W_g, const double* o_lat, const uint16_t* W_uv,
+                int64_t N, int hid, int H, int dv, int R, int64_t n_rows, const int64_t* rows,
+                double* out) {
+  if (!x || !W_g || !o_lat || !W_uv || !rows || !out) return OR_BAD_ARG;
+  if (N <= 0 || hid <= 0 || H <= 0 || dv <= 0 || R <= 0 || n_rows < 0) return OR_BAD_ARG;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= N) return OR_BAD_ARG;
+  gate_ctx c = {x, W_g, W_uv, o_lat, hid, H, dv, R, rows, out};
+  parallel_rows(n_rows, gate_row, &c);
+  return OR_OK;
+}

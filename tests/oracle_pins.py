@@ -1,0 +1,404 @@
+"""Pins that tie the CPU oracle to facts fixed outside itself.
+
+Each ``pin_*`` function takes a loaded oracle library and raises
+AssertionError when the oracle disagrees with a hand-worked example, a closed
+form, an invariant, a library routine or a brute force on tiny inputs.  The
+same functions run against the real oracle (test_oracle_pins.py) and against
+copies with a planted mistake (test_oracle_mutants.py), which must each fail at
+least one pin.
+"""
+
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+import oracle
+from workloads import bf16_round, bf16_to_f32, normal_bf16
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+SCALE = 1.0 / math.sqrt(192.0)
+
+
+def _bf(a):
+    a = np.asarray(a, np.float32)
+    h = bf16_round(a)
+    assert np.array_equal(bf16_to_f32(h), a), "fixture value not exact in BF16"
+    return h
+
+
+# ----------------------------------------------------------------------------
+# indexer
+# ----------------------------------------------------------------------------
+
+def pin_indexer_worked_example(lib):
+    """Hand-worked example in tests/golden/indexer_worked.json."""
+    g = json.load(open(os.path.join(GOLDEN, "indexer_worked.json")))
+    q = np.array(g["q"], np.float32)              # [H_I, D_I]
+    T = len(g["k"])
+    q_idx = _bf(np.broadcast_to(q, (1, T) + q.shape).copy())
+    w = _bf(np.broadcast_to(np.array(g["w"], np.float32), (1, T, q.shape[0])).copy())
+    k = _bf(np.array(g["k"], np.float32)[None])
+    qs, kl = np.zeros(1, np.int32), np.full(1, T, np.int32)
+    sc = oracle.indexer_scores(q_idx, w, k, qs, kl, lib=lib)
+    for t in range(T):
+        for s in range(T):
+            e = g["scores"][t][s]
+            if e is None:
+                assert math.isnan(sc[t, s]), (t, s, sc[t, s])
+            else:
+                assert sc[t, s] == e, (t, s, sc[t, s], e)
+    idx, kth = oracle.topk(sc, np.arange(1, T + 1, dtype=np.int32), g["topk"], lib=lib)
+    for t in range(T):
+        got = [int(v) for v in idx[t] if v >= 0]
+        assert sorted(got) == sorted(g["selected"][t]), (t, got)
+        if g["kth"][t] is None:
+            assert kth[t] == -math.inf
+        else:
+            assert kth[t] == g["kth"][t]
+
+
+def pin_indexer_single_head_is_relu_dot(lib):
+    """H_I = 1, w = 1 reduces to ReLU(q.k): compare with a numpy matmul."""
+    rng = np.random.default_rng(7)
+    T, D = 40, 64
+    q = bf16_round(rng.standard_normal((1, T, 1, D), dtype=np.float32))
+    k = bf16_round(rng.standard_normal((1, T, D), dtype=np.float32))
+    w = bf16_round(np.ones((1, T, 1), np.float32))
+    sc = oracle.indexer_scores(q, w, k, np.zeros(1, np.int32), np.full(1, T, np.int32), lib=lib)
+    ref = np.maximum(bf16_to_f32(q[0, :, 0]).astype(np.float64)
+                     @ bf16_to_f32(k[0]).astype(np.float64).T, 0.0)
+    for t in range(T):
+        np.testing.assert_allclose(sc[t, :t + 1], ref[t, :t + 1], rtol=1e-12, atol=1e-12)
+        assert np.all(np.isnan(sc[t, t + 1:]))
+
+
+def pin_indexer_invariances(lib):
+    """Permuting heads (q and w together) leaves scores unchanged; doubling w doubles
+    them exactly; a head whose weight is negative lowers the score."""
+    cfg_T, H, D = 24, 4, 64
+    q = normal_bf16(3, "q_idx", (1, cfg_T, H, D))
+    w = normal_bf16(3, "w", (1, cfg_T, H))
+    k = normal_bf16(3, "k_idx", (1, cfg_T, D))
+    qs, kl = np.zeros(1, np.int32), np.full(1, cfg_T, np.int32)
+    base = oracle.indexer_scores(q, w, k, qs, kl, lib=lib)
+    perm = np.array([2, 0, 3, 1])
+    sc_p = oracle.indexer_scores(q[:, :, perm], w[:, :, perm], k, qs, kl, lib=lib)
+    np.testing.assert_allclose(sc_p, base, rtol=1e-12, atol=1e-12, equal_nan=True)
+    w2 = bf16_round(bf16_to_f32(w) * 2.0)
+    sc2 = oracle.indexer_scores(q, w2, k, qs, kl, lib=lib)
+    np.testing.assert_array_equal(sc2, 2.0 * base)
+    # all weights negative and all dots positive -> strictly negative scores
+    qpos = bf16_round(np.abs(bf16_to_f32(q)) + 0.5)
+    kpos = bf16_round(np.abs(bf16_to_f32(k)) + 0.5)
+    wneg = bf16_round(-np.abs(bf16_to_f32(w)) - 0.25)
+    scn = oracle.indexer_scores(qpos, wneg, kpos, qs, kl, lib=lib)
+    for t in range(cfg_T):
+        assert np.all(scn[t, :t + 1] < 0)
+
+
+def pin_indexer_relu_clips(lib):
+    """When every q.k is negative the ReLU zeroes every head: scores are exactly 0,
+    whatever the (possibly negative) head weights."""
+    T, H, D = 16, 4, 64
+    q = bf16_round(np.full((1, T, H, D), 0.5, np.float32))
+    k = bf16_round(-np.abs(bf16_to_f32(normal_bf16(5, "k_idx", (1, T, D)))) - 0.125)
+    w = normal_bf16(5, "w", (1, T, H))
+    sc = oracle.indexer_scores(q, w, k, np.zeros(1, np.int32), np.full(1, T, np.int32), lib=lib)
+    for t in range(T):
+        assert np.all(sc[t, :t + 1] == 0.0)
+
+
+def pin_indexer_causal_window(lib):
+    """Query i of a chunk sits at q_start+i and scores keys 0..q_start+i (self included)."""
+    T, H, D = 32, 2, 64
+    q_start = 20
+    q = normal_bf16(9, "q_idx", (1, 4, H, D))
+    w = normal_bf16(9, "w", (1, 4, H))
+    k = normal_bf16(9, "k_idx", (1, T, D))
+    sc = oracle.indexer_scores(q, w, k, np.array([q_start], np.int32),
+                               np.array([q_start + 4], np.int32), lib=lib)
+    for i in range(4):
+        t = q_start + i
+        assert not np.isnan(sc[i, t]), "the query's own key must be scored"
+        assert np.all(~np.isnan(sc[i, :t + 1]))
+        assert np.all(np.isnan(sc[i, t + 1:]))
+        # brute force for key s = t
+        qq = bf16_to_f32(q[0, i]).astype(np.float64)
+        kk = bf16_to_f32(k[0, t]).astype(np.float64)
+        ww = bf16_to_f32(w[0, i]).astype(np.float64)
+        e = sum(ww[j] * max(0.0, float(qq[j] @ kk)) for j in range(H))
+        assert abs(sc[i, t] - e) <= 1e-12 * max(1.0, abs(e))
+
+
+# ----------------------------------------------------------------------------
+# top-k
+# ----------------------------------------------------------------------------
+
+def pin_topk_planted_permutation(lib):
+    """H_I = 1, w = 1, q = e_0 and k[s,0] = a seeded permutation of 1..n: the score of
+    key s is its planted value, so the top-k set is known by construction."""
+    n, D, k = 200, 64, 50
+    vals = np.random.default_rng(11).permutation(n).astype(np.float32) + 1.0  # exact in BF16
+    kk = np.zeros((1, n, D), np.float32)
+    kk[0, :, 0] = vals
+    q = np.zeros((1, n, 1, D), np.float32)
+    q[..., 0] = 1.0
+    w = np.ones((1, n, 1), np.float32)
+    idx, kth, sc, nv = oracle.indexer_topk(_bf(q), _bf(w), _bf(kk), np.zeros(1, np.int32),
+                                           np.full(1, n, np.int32), k, lib=lib)
+    for t in range(n):
+        if t + 1 <= k:
+            expect = set(range(t + 1))
+        else:
+            order = np.argsort(-vals[:t + 1], kind="stable")
+            expect = set(order[:k].tolist())
+            assert kth[t] == np.sort(vals[:t + 1])[::-1][k - 1]
+        got = set(int(v) for v in idx[t] if v >= 0)
+        assert got == expect, t
+        assert len([v for v in idx[t] if v >= 0]) == min(t + 1, k)
+
+
+def pin_topk_brute_force_rank(lib):
+    """Brute force on tiny rows with many exact ties: key s is selected iff fewer than
+    k keys beat it, where s' beats s when its score is larger, or equal with s' < s."""
+    rng = np.random.default_rng(13)
+    n_rows, S, k = 60, 30, 7
+    scores = rng.integers(-3, 4, size=(n_rows, S)).astype(np.float64)
+    n_valid = rng.integers(1, S + 1, size=n_rows).astype(np.int32)
+    idx, kth = oracle.topk(scores, n_valid, k, lib=lib)
+    for r in range(n_rows):
+        n = int(n_valid[r])
+        expect = set()
+        for s in range(n):
+            beats = sum(1 for s2 in range(n)
+                        if scores[r, s2] > scores[r, s] or (scores[r, s2] == scores[r, s] and s2 < s))
+            if beats < k:
+                expect.add(s)
+        got = [int(v) for v in idx[r] if v >= 0]
+        assert len(got) == len(set(got)) == min(n, k)
+        assert set(got) == expect, r
+        assert np.all(idx[r, len(got):] == -1)
+        if n > k:
+            assert kth[r] == sorted(scores[r, :n], reverse=True)[k - 1]
+
+
+def pin_topk_all_equal_takes_lowest(lib):
+    """All scores equal: the tie rule keeps the k smallest key indices."""
+    S, k = 64, 10
+    scores = np.full((1, S), 1.5)
+    idx, kth = oracle.topk(scores, np.array([S], np.int32), k, lib=lib)
+    assert sorted(int(v) for v in idx[0]) == list(range(k))
+    assert kth[0] == 1.5
+
+
+# ----------------------------------------------------------------------------
+# sparse / dense latent attention
+# ----------------------------------------------------------------------------
+
+def _mla_inputs(seed, T, H):
+    q = normal_bf16(seed, "q_lat", (1, T, H, 576))
+    kv = normal_bf16(seed, "kv", (1, T, 576))
+    return q, kv, np.zeros(1, np.int32), np.full(1, T, np.int32)
+
+
+def pin_mla_single_key(lib):
+    """One selected key: the output is that key's 512 value dims exactly, lse = its logit."""
+    T, H = 12, 3
+    q, kv, qs, kl = _mla_inputs(21, T, H)
+    idx = np.full((1, T, 4), -1, np.int32)
+    sel = [min(t, (5 * t) % (t + 1)) for t in range(T)]
+    idx[0, :, 2] = sel
+    o, lse = oracle.sparse_mla(q, kv, idx, qs, kl, SCALE, lib=lib)
+    kvf = bf16_to_f32(kv[0]).astype(np.float64)
+    for t in range(T):
+        s = sel[t]
+        for h in range(H):
+            np.testing.assert_array_equal(o[t, h], kvf[s, :512])
+            z = float(bf16_to_f32(q[0, t, h]).astype(np.float64) @ kvf[s]) * SCALE
+            assert abs(lse[t, h] - z) <= 1e-12 * max(1.0, abs(z))
+
+
+def pin_mla_uniform_logits(lib):
+    """q = 0 makes every logit 0: output = mean of the selected values, lse = ln(n)."""
+    T, H = 10, 2
+    _, kv, qs, kl = _mla_inputs(22, T, H)
+    q = np.zeros((1, T, H, 576), np.uint16)
+    o, lse = oracle.dense_mla(q, kv, qs, kl, SCALE, lib=lib)
+    kvf = bf16_to_f32(kv[0]).astype(np.float64)
+    for t in range(T):
+        np.testing.assert_allclose(o[t, 0], kvf[:t + 1, :512].mean(0), rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(lse[t], math.log(t + 1), rtol=0, atol=1e-14)
+
+
+def pin_mla_two_keys_closed_form(lib):
+    """Two keys whose logits differ by a known amount: p0 = 1 / (1 + exp(z1 - z0)).
+    Key 0 has 1 in a rope dim and key 1 has 0 there, so the rope dims must enter the
+    logits, and the 1/sqrt(192) scale is checked exactly."""
+    H = 1
+    q = np.zeros((1, 2, H, 576), np.float32)
+    q[0, 1, 0, 540] = 16.0            # a rope dim (>= 512)
+    kv = np.zeros((1, 2, 576), np.float32)
+    kv[0, 0, 540] = 1.0
+    kv[0, 0, :512] = np.linspace(-1, 1, 512, dtype=np.float32)
+    kv[0, 1, :512] = 0.5
+    qh, kvh = _bf(q), bf16_round(kv)
+    o, lse = oracle.dense_mla(qh, kvh, np.zeros(1, np.int32), np.full(1, 2, np.int32), SCALE,
+                              lib=lib)
+    z0 = 16.0 / math.sqrt(192.0)
+    p0 = 1.0 / (1.0 + math.exp(-z0))
+    v = bf16_to_f32(kvh[0]).astype(np.float64)
+    np.testing.assert_allclose(o[1, 0], p0 * v[0, :512] + (1 - p0) * v[1, :512], rtol=1e-13,
+                               atol=1e-15)
+    assert abs(lse[1, 0] - (z0 + math.log1p(math.exp(-z0)))) < 1e-13
+
+
+def pin_mla_dense_matches_library_sdpa(lib):
+    """Dense causal MLA against torch's scaled_dot_product_attention in float64 (CPU),
+    with the latent rows as a single shared key/value head (value = first 512 dims)."""
+    import torch
+    T, H = 20, 4
+    q, kv, qs, kl = _mla_inputs(23, T, H)
+    o, lse = oracle.dense_mla(q, kv, qs, kl, SCALE, lib=lib)
+    qf = torch.from_numpy(bf16_to_f32(q[0]).astype(np.float64))        # [T,H,576]
+    kf = torch.from_numpy(bf16_to_f32(kv[0]).astype(np.float64))       # [T,576]
+    Q = qf.permute(1, 0, 2)[None]                                       # [1,H,T,576]
+    K = kf[None, None].expand(1, H, T, 576)
+    V = kf[None, None, :, :512].expand(1, H, T, 512)
+    ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, is_causal=True, scale=SCALE)
+    np.testing.assert_allclose(o, ref[0].permute(1, 0, 2).numpy(), rtol=1e-10, atol=1e-12)
+    logits = (Q @ K.transpose(-1, -2)) * SCALE
+    mask = torch.ones(T, T, dtype=torch.bool).tril()
+    ref_lse = torch.logsumexp(logits.masked_fill(~mask, -math.inf), dim=-1)[0].T
+    np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def pin_mla_sparse_full_set_equals_dense(lib):
+    """T <= k: every causal key is selected, so sparse MLA equals dense causal MLA
+    ("Kimi-K3.1-Pro", Implementation Limits, bullet 4).  The index order and -1
+    padding must not matter."""
+    T, H, k = 24, 3, 32
+    q, kv, qs, kl = _mla_inputs(24, T, H)
+    rng = np.random.default_rng(5)
+    idx = np.full((1, T, k), -1, np.int32)
+    for t in range(T):
+        pos = rng.permutation(k)[:t + 1]
+        idx[0, t, pos] = rng.permutation(t + 1)
+    o_s, l_s = oracle.sparse_mla(q, kv, idx, qs, kl, SCALE, lib=lib)
+    o_d, l_d = oracle.dense_mla(q, kv, qs, kl, SCALE, lib=lib)
+    np.testing.assert_allclose(o_s, o_d, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l_s, l_d, rtol=1e-13, atol=1e-13)
+
+
+def pin_mla_subset_brute_force(lib):
+    """A strict subset of keys: brute-force softmax over exactly that subset."""
+    T, H = 16, 2
+    q, kv, qs, kl = _mla_inputs(25, T, H)
+    sel = {t: sorted({0, t, t // 2, (3 * t) // 4}) for t in range(T)}
+    idx = np.full((1, T, 4), -1, np.int32)
+    for t in range(T):
+        idx[0, t, :len(sel[t])] = sel[t]
+    o, lse = oracle.sparse_mla(q, kv, idx, qs, kl, SCALE, lib=lib)
+    kvf = bf16_to_f32(kv[0]).astype(np.float64)
+    for t in (3, 9, 15):
+        for h in range(H):
+            qv = bf16_to_f32(q[0, t, h]).astype(np.float64)
+            z = np.array([qv @ kvf[s] for s in sel[t]]) * SCALE
+            e = np.exp(z - z.max())
+            ref = (e[:, None] * kvf[sel[t], :512]).sum(0) / e.sum()
+            np.testing.assert_allclose(o[t, h], ref, rtol=1e-12, atol=1e-13)
+            assert abs(lse[t, h] - (z.max() + math.log(e.sum()))) < 1e-12
+
+
+def pin_mla_rejects_noncausal_index(lib):
+    """An index beyond the query's position is not a causal key: the oracle refuses."""
+    T, H = 8, 1
+    q, kv, qs, kl = _mla_inputs(26, T, H)
+    idx = np.full((1, T, 2), -1, np.int32)
+    idx[0, 3, 0] = 5
+    try:
+        oracle.sparse_mla(q, kv, idx, qs, kl, SCALE, lib=lib)
+    except oracle.OracleError:
+        return
+    raise AssertionError("non-causal index accepted")
+
+
+def pin_absorbed_equals_explicit(lib):
+    """The absorbed latent form (q_lat = [W_UK^T q_nope | q_pe], values = c_kv, then
+    W_UV) equals explicit per-head expansion of K and V ("Kimi-K3.1-Pro",
+    Implementation Limits, bullet 2).  Inputs are chosen so q_lat is exact in BF16."""
+    rng = np.random.default_rng(31)
+    H, dn, dr, R, dv, S, n = 2, 128, 64, 512, 128, 9, 5
+    W_UK = rng.integers(-1, 2, size=(H, dn, R)).astype(np.float64) * (rng.random((H, dn, R)) < 0.05)
+    q_nope = rng.integers(-2, 3, size=(n, H, dn)).astype(np.float64) * 0.125
+    q_pe = bf16_to_f32(bf16_round(rng.standard_normal((n, H, dr), dtype=np.float32))).astype(np.float64)
+    c_kv = bf16_to_f32(bf16_round(rng.standard_normal((S, R), dtype=np.float32))).astype(np.float64)
+    k_pe = bf16_to_f32(bf16_round(rng.standard_normal((S, dr), dtype=np.float32))).astype(np.float64)
+    W_UV = rng.standard_normal((H, dv, R)) * 0.02
+    q_abs = np.einsum("nha,har->nhr", q_nope, W_UK)
+    q_lat = np.concatenate([q_abs, q_pe], axis=-1)                     # [n,H,576]
+    q_lat_bf = bf16_round(q_lat.astype(np.float32))
+    assert np.array_equal(bf16_to_f32(q_lat_bf).astype(np.float64), q_lat)
+    kv = np.concatenate([c_kv, k_pe], axis=-1)
+    kv_bf = bf16_round(kv.astype(np.float32))
+    sel = np.full((n, 6), -1, np.int32)
+    for i in range(n):  # query i sits at position S-n+i
+        sel[i, :4] = np.sort(rng.choice(S - n + i + 1, 4, replace=False))
+    o_lat, _ = oracle.sparse_mla(q_lat_bf[None], kv_bf[None], sel[None],
+                                 np.array([S - n], np.int32), np.array([S], np.int32),
+                                 SCALE, lib=lib)
+    absorbed = np.einsum("her,nhr->nhe", W_UV, o_lat)
+    explicit = oracle.explicit_mla(q_nope, q_pe, W_UK, W_UV, c_kv, k_pe, sel, SCALE, lib=lib)
+    np.testing.assert_allclose(absorbed, explicit, rtol=1e-10, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------
+# gate
+# ----------------------------------------------------------------------------
+
+def _gate_inputs(seed, N, hid, H, dv):
+    x = normal_bf16(seed, "x", (N, hid))
+    W_g = normal_bf16(seed, "W_g", (H * dv, hid), std=0.02)
+    W_uv = normal_bf16(seed, "W_uv", (H, dv, 512), std=0.02)
+    o_lat = np.random.default_rng(seed).standard_normal((N, H, 512)) * 0.1
+    return x, W_g, W_uv, o_lat
+
+
+def pin_gate_zero_weight_is_half(lib):
+    """W_g = 0 gives sigma(0) = 1/2: out = 0.5 * (W_uv_h . o_lat_h)."""
+    N, hid, H, dv = 6, 64, 3, 16
+    x, _, W_uv, o_lat = _gate_inputs(41, N, hid, H, dv)
+    W_g = np.zeros((H * dv, hid), np.uint16)
+    out = oracle.gate(x, W_g, o_lat, W_uv, lib=lib)
+    u = np.einsum("her,nhr->nhe", bf16_to_f32(W_uv).astype(np.float64), o_lat).reshape(N, H * dv)
+    np.testing.assert_allclose(out, 0.5 * u, rtol=1e-13, atol=1e-15)
+
+
+def pin_gate_matches_library(lib):
+    """Against torch.sigmoid / torch matmul in float64 on the CPU."""
+    import torch
+    N, hid, H, dv = 7, 96, 2, 32
+    x, W_g, W_uv, o_lat = _gate_inputs(42, N, hid, H, dv)
+    out = oracle.gate(x, W_g, o_lat, W_uv, lib=lib)
+    X = torch.from_numpy(bf16_to_f32(x).astype(np.float64))
+    G = torch.from_numpy(bf16_to_f32(W_g).astype(np.float64))
+    U = torch.from_numpy(bf16_to_f32(W_uv).astype(np.float64))
+    O = torch.from_numpy(o_lat)
+    ref = torch.sigmoid(X @ G.T) * torch.einsum("her,nhr->nhe", U, O).reshape(N, H * dv)
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12, atol=1e-14)
+
+
+def pin_gate_row_subset(lib):
+    """Evaluating a subset of rows gives the same values as the full evaluation."""
+    N, hid, H, dv = 9, 32, 2, 8
+    x, W_g, W_uv, o_lat = _gate_inputs(43, N, hid, H, dv)
+    full = oracle.gate(x, W_g, o_lat, W_uv, lib=lib)
+    rows = np.array([8, 0, 4])
+    part = oracle.gate(x, W_g, o_lat, W_uv, rows=rows, lib=lib)
+    np.testing.assert_array_equal(part, full[rows])
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,50 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins catch
+each one.  The real oracle source is never modified: every mutant is a textual
+edit of a temporary copy, compiled into a temporary directory.  CPU only."""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "dsa_oracle.c")
+
+MUTANTS = {
+    "relu_dropped": ("double relu = dot > 0.0 ? dot : 0.0;", "double relu = dot;"),
+    "head_weight_dropped": ("score += bf(w[j]) * relu;", "score += relu;"),
+    "causal_excludes_self": ("for (int64_t s = 0; s <= t; ++s) {", "for (int64_t s = 0; s < t; ++s) {"),
+    "tie_break_reversed": ("return (x->s < y->s) ? -1 : (x->s > y->s);",
+                           "return (x->s > y->s) ? -1 : (x->s < y->s);"),
+    "short_rows_sorted_not_all": ("if (n <= c->topk) {", "if (n < 0) {"),
+    "rope_dims_dropped": ("for (int d = 0; d < RLAT; ++d) dot += bf(q[d]) * bf(row[d]);",
+                          "for (int d = 0; d < VLAT; ++d) dot += bf(q[d]) * bf(row[d]);"),
+    "scale_dropped": ("z[j] = dot * c->scale;", "z[j] = dot;"),
+    "value_shifted_into_rope": ("oh[d] += p * bf(row[d]); /* value",
+                                "oh[d] += p * bf(row[d + 64]); /* value"),
+    "lse_without_max": ("lse[h] = m + log(l);", "lse[h] = log(l);"),
+    "softmax_not_normalised": ("for (int d = 0; d < VLAT; ++d) oh[d] /= l;", ""),
+    "gate_without_sigmoid": ("o[col] = u / (1.0 + exp(-g));", "o[col] = u * g;"),
+    "gate_sign_flipped": ("o[col] = u / (1.0 + exp(-g));", "o[col] = u / (1.0 + exp(g));"),
+    "explicit_value_uses_key_weight": ("acc += Wv[(int64_t)e * c->R + d] * ck[d];",
+                                       "acc += Wk[(int64_t)e * c->R + d] * ck[d];"),
+    "sparse_ignores_minus_one_wrongly": ("if (s < 0) continue;\n      if (s > t",
+                                         "if (s < 0) s = 0;\n      if (s > t"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique/absent"
+    mpath = tmp_path / "mutant.c"
+    mpath.write_text(src.replace(old, new))
+    lib = oracle.load(oracle.build(force=True, src=str(mpath), out=str(tmp_path / "libm.so")))
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, oracle.OracleError) as e:  # the pin noticed
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches mutant {name}"
