@@ -1,0 +1,183 @@
+/*
+ * dsa.h -- C ABI of libdsa.so: the gated DSA attention step on one GB300 (sm_103a).
+ *
+ * The step, per query token t of a sequence:
+ *   1. lightning indexer: score every causal key s <= t,
+ *        I[t,s] = sum_j w[t,j] * max(0, q_I[t,j,:] . k_I[s,:])
+ *      (BF16 inputs, FP32 accumulation) and keep the top-k keys;
+ *   2. sparse MLA in latent space over the kept rows only:
+ *        z_s = scale * q_lat[t,h,:] . KV[s,:]   (576 = 512 c_kv + 64 unrotated k_pe)
+ *        o_lat[t,h,:] = softmax_s(z) . KV[s, 0:512],  lse[t,h] = log sum_s exp(z_s);
+ *   3. output gate: out[t, h*dv+e] = sigmoid(x[t] . W_g[h*dv+e]) * (W_uv[h,e,:] . o_lat[t,h,:]).
+ *
+ * Sources (page title, section):
+ *   "Kimi-K3.1-Pro" (NeMo AutoModel model coverage), Implementation Limits:
+ *     bullet 1 (a fused indexer yields top-k coordinates; sparse MLA attends
+ *     directly to the selected latent KV), bullet 2 (BF16 indexer projections,
+ *     FP32 score accumulation, all causal keys scanned, no per-head K/V
+ *     expansion), bullet 4 (<= 2,048 valid tokens keep every causal key),
+ *     closing paragraph (the output gate is kept; packed documents must be
+ *     contiguous).
+ *   "Kimi K3.1 Pro" (archdiff, attn-gate): summary (top-2,048 DSA indexer in
+ *     the gated MLA layers, no positional encoding); blueprint entries
+ *     "LayerNorm on the indexer key" and the output gate sigma(x W_g) (.) o.
+ *   "nemo_automodel.components.models.kimi_k3" (v0.4 API), KimiK3TextConfig:
+ *     num_attention_heads 96, kv_lora_rank 512, qk_nope_head_dim 128,
+ *     qk_rope_head_dim 64 (softmax scale 1/sqrt(192)), v_head_dim 128,
+ *     hidden_size 7168, mla_use_nope, mla_use_output_gate.
+ *   The indexer's head count, head dim and head-weighted ReLU form are not on
+ *   the pages; this library adopts the form above (64 heads x 128, or 4 x 64).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; BF16 values
+ *     are passed as uint16_t bit patterns.  Arrays are dense row-major in the
+ *     shapes given.  The library allocates, frees and synchronises nothing
+ *     (except dsa_read_device_status, which synchronises `stream`), keeps no
+ *     global state and launches only on `stream` (NULL = legacy default stream).
+ *   - Causality: query i of sequence b sits at absolute position
+ *     q_start[b] + i and sees keys 0 .. q_start[b] + i.  q_start and kv_len are
+ *     device int32 arrays of length B with kv_len[b] >= q_start[b] + Tq and
+ *     kv_len[b] <= max_kv_len.  Single prefill: q_start = 0, kv_len = T.
+ *     Chunk c of a chunked prefill: q_start = c*C, kv_len = (c+1)*C.
+ *     Decode: Tq = 1, q_start = L-1, kv_len = L (the new token's rows are
+ *     already in the cache).  One contiguous document per sequence.
+ *   - Workspace: caller-owned device memory of at least dsa_workspace_bytes()
+ *     bytes, 256-byte aligned, prepared once by dsa_workspace_init().  Its
+ *     first 256 bytes hold a sticky device status word.  One workspace must
+ *     not be used by two calls that may run concurrently.
+ *   - Errors: arguments are checked on the host before any launch and a
+ *     failing check returns DSA_ERR_INVALID_ARGUMENT / DSA_ERR_UNSUPPORTED /
+ *     DSA_ERR_WORKSPACE_TOO_SMALL with nothing launched.  A failed launch
+ *     returns DSA_ERR_CUDA.  Conditions only the device can see (an index out
+ *     of range or not causal, a page id outside the pool, inconsistent
+ *     q_start/kv_len, a wait that ran out of time) are recorded in the status
+ *     word and read back with dsa_read_device_status(); the affected rows are
+ *     skipped, never dereferenced.  Kernels never trap.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* dsa_stream_t;
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARGUMENT = 1,  /* null pointer, bad size, misaligned buffer */
+  DSA_ERR_UNSUPPORTED = 2,       /* dims or page size this build does not compile */
+  DSA_ERR_CUDA = 3,              /* a CUDA runtime call or launch failed */
+  DSA_ERR_DEVICE_TIMEOUT = 4,    /* device: a bounded wait ran out */
+  DSA_ERR_BAD_INDEX = 5,         /* device: index / page id / length out of range */
+  DSA_ERR_WORKSPACE_TOO_SMALL = 6
+} dsa_status_t;
+
+/*
+ * A store of per-token rows (indexer keys: width D_I; latent KV: width 576),
+ * BF16, either contiguous or paged.
+ *   contiguous (block_table == NULL): base = [B, seq_stride, width]; row s of
+ *     sequence b is base + (b*seq_stride + s)*width.  seq_stride >= max_kv_len.
+ *   paged: base = pool [num_pages, page_size, width]; row s of sequence b is
+ *     pool[block_table[b*max_pages + s/page_size]][s % page_size].
+ *     block_table is a device int32 array [B, max_pages]; page_size must be 64;
+ *     entries used by a call must lie in [0, num_pages) (checked on device).
+ * base must be 16-byte aligned.
+ */
+typedef struct {
+  const void* base;
+  int64_t seq_stride;
+  const int32_t* block_table;
+  int32_t max_pages;
+  int32_t page_size;
+  int32_t num_pages;
+} dsa_rows_t;
+
+typedef enum {
+  DSA_OP_INDEXER_TOPK = 0,
+  DSA_OP_SPARSE_MLA = 1,
+  DSA_OP_GATE = 2
+} dsa_op_t;
+
+/* Bytes of workspace an op needs for the given sizes (heads = H_I for the
+ * indexer, H for sparse MLA, ignored for the gate).  Always >= 256. */
+size_t dsa_workspace_bytes(dsa_op_t op, int B, int Tq, int max_kv_len, int heads, int topk);
+
+/* Zero the status header of a workspace (asynchronous on `stream`). */
+dsa_status_t dsa_workspace_init(void* workspace, size_t ws_bytes, dsa_stream_t stream);
+
+/*
+ * Lightning indexer + top-k ("Kimi-K3.1-Pro", Implementation Limits, bullets
+ * 1, 2 and 4; "Kimi K3.1 Pro" archdiff summary: top-2,048).
+ *   q_idx  [B, Tq, H_I, D_I] BF16   indexer queries
+ *   w      [B, Tq, H_I]      BF16   per-head weights (any sign)
+ *   k_idx  rows of width D_I BF16   LayerNorm'd indexer keys
+ *   out_idx[B, Tq, topk]     int32  written: for a query at position t, exactly
+ *          min(t+1, topk) distinct key positions in [0, t], in unspecified
+ *          order, followed by -1 padding.  Among keys with equal scores at the
+ *          cut, which ones are kept is unspecified.
+ * Supported: (H_I, D_I) in {(64,128), (4,64)}; 1 <= topk <= 2048, topk a
+ * multiple of 4; Tq >= 1.  Tq == 1 selects the decode kernels (key ranges
+ * split across the GPU, a linear score vector per request in the workspace,
+ * then a radix select); Tq > 1 the fused prefill kernel, which keeps every
+ * score on chip.
+ */
+dsa_status_t dsa_indexer_topk(const uint16_t* q_idx, const uint16_t* w, const dsa_rows_t* k_idx,
+                              const int32_t* q_start, const int32_t* kv_len, int B, int Tq,
+                              int H_I, int D_I, int max_kv_len, int topk, int32_t* out_idx,
+                              void* workspace, size_t ws_bytes, dsa_stream_t stream);
+
+/*
+ * Sparse MLA forward in latent space ("Kimi-K3.1-Pro", Implementation Limits,
+ * bullets 1-2; KimiK3TextConfig dims; no rotation of the 64 k_pe dims).
+ *   q_lat [B, Tq, H, 576] BF16   absorbed queries ([W_UK^T q_nope | q_pe])
+ *   kv    rows of width 576 BF16 latent cache ([c_kv(512) | k_pe(64)])
+ *   idx   [B, Tq, topk] int32    key positions; -1 entries are skipped; any
+ *         other entry must satisfy 0 <= s <= t (else BAD_INDEX, entry skipped)
+ *   scale                        softmax scale (1/sqrt(192) for this model)
+ *   o_lat [B, Tq, H, 512] BF16   softmax-weighted sum of KV[s, 0:512]
+ *   lse   [B, Tq, H] float or NULL   natural-log log-sum-exp of the logits
+ * A query with no valid index gets o_lat = 0 and lse = -inf.
+ * Supported: H in {8, 96}; 1 <= topk <= 2048.
+ */
+dsa_status_t sparse_mla_fwd(const uint16_t* q_lat, const dsa_rows_t* kv, const int32_t* idx,
+                            const int32_t* q_start, const int32_t* kv_len, int B, int Tq, int H,
+                            int topk, int max_kv_len, float scale, uint16_t* o_lat, float* lse,
+                            void* workspace, size_t ws_bytes, dsa_stream_t stream);
+
+/*
+ * Output gate ("Kimi K3.1 Pro" archdiff blueprint: sigma(x W_g) (.) o;
+ * "Kimi-K3.1-Pro", Implementation Limits, closing paragraph: the gate is kept;
+ * KimiK3TextConfig mla_use_output_gate, v_head_dim 128).
+ *   x     [N, hid] BF16          layer input
+ *   W_g   [H*dv, hid] BF16       gate weight, one row per output feature
+ *   o_lat [N, H, 512] BF16       sparse MLA output
+ *   W_uv  [H, dv, 512] BF16      per-head value up-projection
+ *   out   [N, H*dv] BF16         sigmoid(x . W_g[c]) * (W_uv[h,e] . o_lat[n,h]), c = h*dv+e
+ * Supported: dv == 128, hid % 64 == 0, H >= 1; N >= 1.
+ */
+dsa_status_t mla_gate_apply(const uint16_t* x, const uint16_t* W_g, const uint16_t* o_lat,
+                            const uint16_t* W_uv, int N, int hid, int H, int dv, uint16_t* out,
+                            void* workspace, size_t ws_bytes, dsa_stream_t stream);
+
+/* Synchronise `stream`, return the first device-side error recorded in the
+ * workspace (DSA_OK if none) and clear it.  `where` / `detail` (nullable)
+ * receive the site tag and detail value. */
+dsa_status_t dsa_read_device_status(void* workspace, dsa_stream_t stream, uint32_t* where,
+                                    uint32_t* detail);
+
+/* Static string for a status code. */
+const char* dsa_status_string(dsa_status_t status);
+
+/* Library ABI version (incremented on incompatible changes). */
+int dsa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

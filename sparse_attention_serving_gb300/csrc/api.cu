@@ -1,0 +1,252 @@
+// api.cu -- the C ABI of libdsa.so (declared in include/dsa.h): host-side
+// argument checks, workspace layout, tensor-map encoding and dispatch.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "dsa_status.cuh"
+#include "internal.h"
+
+namespace dsa {
+
+// ---------------------------------------------------------------------------
+// tensor maps (driver entry point fetched through the runtime: no link-time
+// dependency on libcuda, so the library loads on machines without a driver)
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+bool encode_tmap_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows,
+                    bool swizzle128) {
+  auto enc = encoder();
+  if (enc == nullptr || rows == 0 || cols == 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r =
+      enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE,
+          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+int indexer_prefill_max_topk(int H_I, int D_I);
+dsa_status_t indexer_prefill_launch(const IndexerArgs& a, cudaStream_t stream);
+
+size_t indexer_scratch_bytes(int B, int Tq, int max_kv_len, int H_I, int topk) {
+  (void)B; (void)Tq; (void)max_kv_len; (void)H_I; (void)topk;
+  return 0;
+}
+
+dsa_status_t indexer_launch(const IndexerArgs& a, cudaStream_t stream) {
+  return indexer_prefill_launch(a, stream);
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Resolve and check a row store.  width = row width in elements.
+dsa_status_t resolve_rows(const dsa_rows_t* r, int B, int max_kv_len, int width, RowStore* out) {
+  if (r == nullptr || r->base == nullptr || !aligned(r->base, 16)) return DSA_ERR_INVALID_ARGUMENT;
+  RowStore s{};
+  s.base = static_cast<const uint16_t*>(r->base);
+  if (r->block_table == nullptr) {
+    if (r->seq_stride < max_kv_len) return DSA_ERR_INVALID_ARGUMENT;
+    s.seq_stride = r->seq_stride;
+    s.total_rows = static_cast<int64_t>(B) * r->seq_stride;
+  } else {
+    if (r->page_size != kPage) return DSA_ERR_UNSUPPORTED;
+    if (r->num_pages <= 0 || r->max_pages <= 0) return DSA_ERR_INVALID_ARGUMENT;
+    if (static_cast<int64_t>(r->max_pages) * kPage < max_kv_len) return DSA_ERR_INVALID_ARGUMENT;
+    if (!aligned(r->block_table, 4)) return DSA_ERR_INVALID_ARGUMENT;
+    s.block_table = r->block_table;
+    s.max_pages = r->max_pages;
+    s.num_pages = r->num_pages;
+    s.total_rows = static_cast<int64_t>(r->num_pages) * kPage;
+  }
+  if (s.total_rows >= (int64_t(1) << 31)) return DSA_ERR_UNSUPPORTED;  // TMA row coordinates are int32
+  (void)width;
+  *out = s;
+  return DSA_OK;
+}
+
+dsa_status_t check_ws(void* ws, size_t bytes, size_t need) {
+  if (ws == nullptr || !aligned(ws, 256)) return DSA_ERR_INVALID_ARGUMENT;
+  if (bytes < need) return DSA_ERR_WORKSPACE_TOO_SMALL;
+  return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dsa_abi_version(void) { return 1; }
+
+const char* dsa_status_string(dsa_status_t s) {
+  switch (s) {
+    case DSA_OK: return "ok";
+    case DSA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case DSA_ERR_UNSUPPORTED: return "unsupported size or configuration";
+    case DSA_ERR_CUDA: return "CUDA error";
+    case DSA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case DSA_ERR_BAD_INDEX: return "index, page id or length out of range";
+    case DSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+size_t dsa_workspace_bytes(dsa_op_t op, int B, int Tq, int max_kv_len, int heads, int topk) {
+  size_t extra = 0;
+  if (B > 0 && Tq > 0) {
+    if (op == DSA_OP_INDEXER_TOPK) extra = indexer_scratch_bytes(B, Tq, max_kv_len, heads, topk);
+    if (op == DSA_OP_SPARSE_MLA) extra = sparse_mla_scratch_bytes(B, Tq, heads, topk);
+  }
+  return kWorkspaceHeader + ((extra + 255) / 256) * 256;
+}
+
+dsa_status_t dsa_workspace_init(void* workspace, size_t ws_bytes, dsa_stream_t stream) {
+  if (workspace == nullptr || ws_bytes < kWorkspaceHeader || !aligned(workspace, 256))
+    return DSA_ERR_INVALID_ARGUMENT;
+  return cudaMemsetAsync(workspace, 0, kWorkspaceHeader, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? DSA_OK
+             : DSA_ERR_CUDA;
+}
+
+dsa_status_t dsa_read_device_status(void* workspace, dsa_stream_t stream, uint32_t* where,
+                                    uint32_t* detail) {
+  if (workspace == nullptr || !aligned(workspace, 256)) return DSA_ERR_INVALID_ARGUMENT;
+  uint32_t h[3] = {0, 0, 0};
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(h, workspace, sizeof h, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof h, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  if (where) *where = h[1];
+  if (detail) *detail = h[2];
+  return static_cast<dsa_status_t>(h[0]);
+}
+
+dsa_status_t dsa_indexer_topk(const uint16_t* q_idx, const uint16_t* w, const dsa_rows_t* k_idx,
+                              const int32_t* q_start, const int32_t* kv_len, int B, int Tq,
+                              int H_I, int D_I, int max_kv_len, int topk, int32_t* out_idx,
+                              void* workspace, size_t ws_bytes, dsa_stream_t stream) {
+  if (!q_idx || !w || !q_start || !kv_len || !out_idx) return DSA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q_idx, 16) || !aligned(w, 2) || !aligned(out_idx, 4) || !aligned(q_start, 4) ||
+      !aligned(kv_len, 4))
+    return DSA_ERR_INVALID_ARGUMENT;
+  if (B <= 0 || Tq <= 0 || max_kv_len <= 0 || topk <= 0) return DSA_ERR_INVALID_ARGUMENT;
+  if (!((H_I == 64 && D_I == 128) || (H_I == 4 && D_I == 64))) return DSA_ERR_UNSUPPORTED;
+  if (topk > 2048 || topk % 4 != 0 || topk > indexer_prefill_max_topk(H_I, D_I))
+    return DSA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * Tq * H_I >= (int64_t(1) << 31)) return DSA_ERR_UNSUPPORTED;
+  IndexerArgs a{};
+  dsa_status_t st = resolve_rows(k_idx, B, max_kv_len, D_I, &a.k);
+  if (st != DSA_OK) return st;
+  st = check_ws(workspace, ws_bytes,
+                dsa_workspace_bytes(DSA_OP_INDEXER_TOPK, B, Tq, max_kv_len, H_I, topk));
+  if (st != DSA_OK) return st;
+  a.q_idx = q_idx;
+  a.w = w;
+  a.q_start = q_start;
+  a.kv_len = kv_len;
+  a.B = B;
+  a.Tq = Tq;
+  a.H_I = H_I;
+  a.D_I = D_I;
+  a.max_kv_len = max_kv_len;
+  a.topk = topk;
+  a.out_idx = out_idx;
+  a.status = static_cast<uint32_t*>(workspace);
+  a.scratch = static_cast<uint8_t*>(workspace) + kWorkspaceHeader;
+  a.scratch_bytes = ws_bytes - kWorkspaceHeader;
+  return indexer_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t sparse_mla_fwd(const uint16_t* q_lat, const dsa_rows_t* kv, const int32_t* idx,
+                            const int32_t* q_start, const int32_t* kv_len, int B, int Tq, int H,
+                            int topk, int max_kv_len, float scale, uint16_t* o_lat, float* lse,
+                            void* workspace, size_t ws_bytes, dsa_stream_t stream) {
+  if (!q_lat || !idx || !q_start || !kv_len || !o_lat) return DSA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q_lat, 16) || !aligned(idx, 4) || !aligned(o_lat, 16) ||
+      (lse != nullptr && !aligned(lse, 4)) || !aligned(q_start, 4) || !aligned(kv_len, 4))
+    return DSA_ERR_INVALID_ARGUMENT;
+  if (B <= 0 || Tq <= 0 || max_kv_len <= 0 || topk <= 0) return DSA_ERR_INVALID_ARGUMENT;
+  if (!(scale > 0.f) || scale != scale) return DSA_ERR_INVALID_ARGUMENT;
+  if (H != 96 && H != 8) return DSA_ERR_UNSUPPORTED;
+  if (topk > 2048) return DSA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * Tq * H >= (int64_t(1) << 31) ||
+      static_cast<int64_t>(B) * Tq >= (int64_t(1) << 31) / 8)
+    return DSA_ERR_UNSUPPORTED;
+  SparseMlaArgs a{};
+  dsa_status_t st = resolve_rows(kv, B, max_kv_len, kRlat, &a.kv);
+  if (st != DSA_OK) return st;
+  st = check_ws(workspace, ws_bytes, dsa_workspace_bytes(DSA_OP_SPARSE_MLA, B, Tq, max_kv_len, H, topk));
+  if (st != DSA_OK) return st;
+  a.q_lat = q_lat;
+  a.idx = idx;
+  a.q_start = q_start;
+  a.kv_len = kv_len;
+  a.B = B;
+  a.Tq = Tq;
+  a.H = H;
+  a.topk = topk;
+  a.max_kv_len = max_kv_len;
+  a.scale = scale;
+  a.o_lat = o_lat;
+  a.lse = lse;
+  a.status = static_cast<uint32_t*>(workspace);
+  a.scratch = static_cast<uint8_t*>(workspace) + kWorkspaceHeader;
+  a.scratch_bytes = ws_bytes - kWorkspaceHeader;
+  return sparse_mla_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t mla_gate_apply(const uint16_t* x, const uint16_t* W_g, const uint16_t* o_lat,
+                            const uint16_t* W_uv, int N, int hid, int H, int dv, uint16_t* out,
+                            void* workspace, size_t ws_bytes, dsa_stream_t stream) {
+  if (!x || !W_g || !o_lat || !W_uv || !out) return DSA_ERR_INVALID_ARGUMENT;
+  if (!aligned(x, 16) || !aligned(W_g, 16) || !aligned(o_lat, 16) || !aligned(W_uv, 16) ||
+      !aligned(out, 16))
+    return DSA_ERR_INVALID_ARGUMENT;
+  if (N <= 0 || hid <= 0 || H <= 0 || dv <= 0) return DSA_ERR_INVALID_ARGUMENT;
+  if (dv != 128 || hid % 64 != 0 || H % 2 != 0) return DSA_ERR_UNSUPPORTED;
+  dsa_status_t st = check_ws(workspace, ws_bytes, dsa_workspace_bytes(DSA_OP_GATE, N, 1, 0, H, 0));
+  if (st != DSA_OK) return st;
+  GateArgs a{x, W_g, o_lat, W_uv, N, hid, H, dv, out, static_cast<uint32_t*>(workspace)};
+  return gate_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,448 @@
+// indexer.cu -- lightning indexer + top-k on sm_103a.
+//
+// Score of key s for query t (the head-weighted ReLU form adopted for the
+// indexer; BF16 inputs with FP32 accumulation and every causal key scanned,
+// "Kimi-K3.1-Pro", NeMo AutoModel, Implementation Limits, bullet 2):
+//   I[t,s] = sum_j w[t,j] * max(0, q[t,j,:] . k[s,:]),   s <= t
+// The top-k keys per query are kept ("Kimi K3.1 Pro" archdiff summary: top-2,048;
+// a query with at most k causal keys keeps all of them, Implementation Limits,
+// bullet 4).
+//
+// Prefill (Tq > 1): one fused kernel, no score buffer in global memory.
+//   A CTA owns QT consecutive queries of one sequence (QT * H_I = 256 or 64
+//   accumulator columns) and streams every causal key tile of 128 keys:
+//     D^T[128 keys x QT*H_I] = K_tile[128 x D_I] . Q^T[D_I x QT*H_I]   (tcgen05, M=128)
+//   with TMEM double-buffered, so the head reduction of one tile overlaps the
+//   MMA of the next.  Each epilogue thread owns one key (a TMEM lane) and
+//   reduces over heads without any cross-lane traffic; scores above the
+//   query's running threshold are appended to a per-query candidate buffer in
+//   shared memory.  When a buffer nears capacity a radix select (4 x 8-bit
+//   digits over order-preserving keys) keeps the top k and raises the
+//   threshold to the k-th score.  The final select writes the indices.
+#include <cmath>
+
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "sm103.cuh"
+
+namespace dsa {
+namespace idx {
+
+constexpr int BKEY = 128;  // keys per tile (MMA M)
+constexpr int NST = 2;     // key-tile stages
+constexpr int NEPI = 8;    // epilogue warps
+constexpr int NTHREADS = 64 + NEPI * 32;
+
+enum : uint32_t {
+  SITE_QPOS = 0x200, SITE_PAGE = 0x201, SITE_W_Q = 0x210, SITE_W_KE = 0x211, SITE_W_KF = 0x212,
+  SITE_W_DE = 0x213, SITE_W_DF = 0x214, SITE_W_DRAIN = 0x215
+};
+
+template <int H_I, int D_I>
+struct Cfg {
+  static constexpr int QT = (H_I >= 64) ? 256 / H_I : 16;  // queries per CTA
+  static constexpr int N = QT * H_I;                          // MMA N
+  static constexpr int NCH = D_I / 64;                        // 64-dim chunks
+  static constexpr int Q_BYTES = NCH * N * 128;
+  static constexpr int K_STAGE = NCH * BKEY * 128;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_W = OFF_K + NST * K_STAGE;
+  static constexpr int OFF_MISC = OFF_W + QT * H_I * 4;
+  static constexpr int MISC_BYTES = 4096;
+  static constexpr int OFF_CAND = OFF_MISC + MISC_BYTES;
+  static constexpr int AVAIL = 232448 - 1024 - OFF_CAND;
+  static constexpr int CAP = (AVAIL / (QT * 8)) / 32 * 32;  // candidates per query
+  static constexpr int SMEM_BYTES = OFF_CAND + QT * CAP * 8 + 1024;
+  static constexpr int EPT = (CAP + NEPI * 32 - 1) / (NEPI * 32);  // candidates per thread in a select
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(N % 16 == 0 && N <= 256, "MMA N");
+};
+
+struct Params {
+  const uint16_t* w;
+  const int32_t* q_start;
+  const int32_t* kv_len;
+  const int32_t* block_table;
+  int64_t seq_stride;
+  int32_t max_pages, num_pages;
+  int paged;
+  int Tq, topk, max_kv_len, ntq;  // ntq = query tiles per sequence
+  int32_t* out_idx;
+  uint32_t* status;
+};
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+__device__ __forceinline__ bool vflag(const volatile int* p) { return *p != 0; }
+
+// Keep exactly `k` of the `n` candidates of one query (the k largest scores;
+// ties at the cut are broken arbitrarily) and return the k-th score.  Called
+// by all epilogue threads together; `gtid` in [0, NEPI*32).
+template <int EPT>
+__device__ float select_topk(float* cs, int32_t* ci, int n, int k, int gtid, int* hist,
+                             int* sel, int* ctr) {
+  uint32_t key[EPT];
+  int32_t id[EPT];
+  constexpr int G = NEPI * 32;
+#pragma unroll
+  for (int u = 0; u < EPT; ++u) {
+    const int e = gtid + u * G;
+    key[u] = e < n ? order_key(cs[e]) : 0u;
+    id[u] = e < n ? ci[e] : -1;
+  }
+  uint32_t prefix = 0, mask = 0;
+  int need = k;
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    if (gtid < 256) hist[gtid] = 0;
+    named_bar_sync(1, G);
+#pragma unroll
+    for (int u = 0; u < EPT; ++u)
+      if (id[u] >= 0 && (key[u] & mask) == prefix) atomicAdd(&hist[(key[u] >> shift) & 255], 1);
+    named_bar_sync(1, G);
+    if (gtid < 32) {
+      // lane l covers digits 255-8l .. 248-8l (descending)
+      int c[8], tot = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) { c[e] = hist[255 - 8 * gtid - e]; tot += c[e]; }
+      int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (gtid >= o) incl += v;
+      }
+      const int excl = incl - tot;
+      if (excl < need && need <= incl) {
+        int run = excl;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (run < need && need <= run + c[e]) {
+            sel[0] = 255 - 8 * gtid - e;
+            sel[1] = need - run;
+          }
+          run += c[e];
+        }
+      }
+    }
+    named_bar_sync(1, G);
+    prefix |= static_cast<uint32_t>(sel[0]) << shift;
+    mask |= 255u << shift;
+    need = sel[1];
+  }
+  // keep every key > prefix and the first `need` keys == prefix
+  if (gtid == 0) { ctr[0] = 0; ctr[1] = 0; }
+  named_bar_sync(1, G);
+#pragma unroll
+  for (int u = 0; u < EPT; ++u) {
+    if (id[u] < 0) continue;
+    bool keep = key[u] > prefix;
+    if (!keep && key[u] == prefix) keep = atomicAdd(&ctr[1], 1) < need;
+    if (keep) {
+      const int pos = atomicAdd(&ctr[0], 1);
+      cs[pos] = key_to_float(key[u]);
+      ci[pos] = id[u];
+    }
+  }
+  named_bar_sync(1, G);
+  return key_to_float(prefix);
+}
+
+template <int H_I, int D_I>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    indexer_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_k, const Params p) {
+  using C = Cfg<H_I, D_I>;
+  constexpr int QT = C::QT, N = C::N, NCH = C::NCH, CAP = C::CAP;
+  constexpr uint32_t IDESC = idesc_bf16(128, N, false, false);
+  constexpr int G = NEPI * 32;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  float* w_s = reinterpret_cast<float*>(sm + C::OFF_W);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_MISC);  // 16 barriers
+  // B_Q 0, K full 1..2, K empty 3..4, D full 5..6, D empty 7..8, drain 9
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
+  volatile int* g_abort = s_abort + 1;   // [4]
+  int* cnt = const_cast<int*>(s_abort) + 8;  // [QT] candidates per query
+  float* thr = reinterpret_cast<float*>(cnt + 64);  // [QT]
+  int* hist = reinterpret_cast<int*>(thr + 64);     // [256]
+  int* sel = hist + 256;                            // [2]
+  int* ctr = sel + 2;                               // [2]
+  float* cand_s = reinterpret_cast<float*>(sm + C::OFF_CAND);
+  int32_t* cand_i = reinterpret_cast<int32_t*>(cand_s + QT * CAP);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // heavier (later) query tiles first
+  const int b = blockIdx.x / p.ntq;
+  const int qt = p.ntq - 1 - (blockIdx.x % p.ntq);
+  const int qi0 = qt * QT;
+  const int nq = min(QT, p.Tq - qi0);
+  const int q_start = __ldg(p.q_start + b);
+  const int L = __ldg(p.kv_len + b);
+  const int t0 = q_start + qi0;
+  const int t_last = t0 + nq - 1;
+  const bool ok_pos = q_start >= 0 && t_last < L && L <= p.max_kv_len;
+  int32_t* out = p.out_idx + (static_cast<int64_t>(b) * p.Tq + qi0) * p.topk;
+
+  if (!ok_pos) {
+    if (tid == 0) status_raise(p.status, DSA_ERR_BAD_INDEX, SITE_QPOS, (uint32_t)t_last);
+    for (int e = tid; e < nq * p.topk; e += NTHREADS) out[e] = -1;
+    return;
+  }
+  if (t_last + 1 <= p.topk) {
+    // every query of the tile keeps all of its causal keys
+    for (int e = tid; e < nq * p.topk; e += NTHREADS) {
+      const int q = e / p.topk, j = e % p.topk;
+      out[e] = j <= t0 + q ? j : -1;
+    }
+    return;
+  }
+
+  const int ntiles = (t_last + BKEY) / BKEY;
+  if (tid == 0) {
+    for (int k = 0; k < 10; ++k) mbar_init(&bars[k], (k == 7 || k == 8) ? G : 1);
+    s_abort[0] = 0;
+    for (int k = 0; k < 4; ++k) g_abort[k] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  for (int e = tid; e < QT * H_I; e += NTHREADS) {
+    const int q = e / H_I;
+    w_s[e] = q < nq ? __bfloat162float(__ushort_as_bfloat16(
+                          p.w[(static_cast<int64_t>(b) * p.Tq + qi0) * H_I + e]))
+                    : 0.f;
+  }
+  for (int q = tid; q < QT; q += NTHREADS) {
+    cnt[q] = 0;
+    thr[q] = -INFINITY;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (warp == 0) {
+    // ============================ producer ===================================
+    int last_use[NST] = {-1, -1};
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      mbar_expect_tx(&bars[0], C::Q_BYTES);
+      const int qrow = (b * p.Tq + qi0) * H_I;
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) tma_load_2d(sm + C::OFF_Q + c * N * 128, &tm_q, &bars[0], 64 * c, qrow);
+      for (int kt = 0; kt < ntiles; ++kt) {
+        const int st = kt % NST, use = kt / NST;
+        if (use > 0 && !mbar_wait(&bars[3 + st], (use - 1) & 1, p.status, kWaitLimitNs, SITE_W_KE)) {
+          s_abort[0] = 1;
+          break;
+        }
+        if (vflag(s_abort)) break;
+        mbar_expect_tx(&bars[1 + st], C::K_STAGE);
+        last_use[st] = use;
+        uint8_t* dst = sm + C::OFF_K + st * C::K_STAGE;
+        if (!p.paged) {
+          const int row = static_cast<int>(static_cast<int64_t>(b) * p.seq_stride + kt * BKEY);
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) tma_load_2d(dst + c * BKEY * 128, &tm_k, &bars[1 + st], 64 * c, row);
+        } else {
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int pg = kt * 2 + hf;
+            int pid = 0;
+            if (pg * kPage < L) {
+              pid = pg < p.max_pages ? __ldg(p.block_table + static_cast<int64_t>(b) * p.max_pages + pg) : -1;
+              if (pid < 0 || pid >= p.num_pages) {
+                status_raise(p.status, DSA_ERR_BAD_INDEX, SITE_PAGE, (uint32_t)pid);
+                pid = 0;  // read a valid page; its keys are never selected (flagged above)
+              }
+            }
+#pragma unroll
+            for (int c = 0; c < NCH; ++c)
+              tma_load_2d(dst + c * BKEY * 128 + hf * 64 * 128, &tm_k, &bars[1 + st], 64 * c, pid * kPage);
+          }
+        }
+      }
+      for (int st = 0; st < NST; ++st)
+        if (last_use[st] >= 0) mbar_wait(&bars[1 + st], last_use[st] & 1, p.status, kWaitLimitNs, SITE_W_KF);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ============================ MMA issuer ==================================
+    if (lane == 0) {
+      bool ok = mbar_wait(&bars[0], 0, p.status, kWaitLimitNs, SITE_W_Q);
+      const uint32_t qb = smem_u32(sm + C::OFF_Q);
+      for (int kt = 0; kt < ntiles && ok; ++kt) {
+        if (vflag(s_abort)) { ok = false; break; }
+        const int st = kt % NST, buf = kt & 1;
+        if (kt >= 2 && !mbar_wait(&bars[7 + buf], ((kt >> 1) - 1) & 1, p.status, kWaitLimitNs, SITE_W_DE)) { ok = false; break; }
+        if (!mbar_wait(&bars[1 + st], (kt / NST) & 1, p.status, kWaitLimitNs, SITE_W_KF)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kb = smem_u32(sm + C::OFF_K + st * C::K_STAGE);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + buf * 256, smem_desc(kb + c * BKEY * 128 + kk * 32, 16, 1024),
+                      smem_desc(qb + c * N * 128 + kk * 32, 16, 1024), IDESC, (c | kk) ? 1u : 0u);
+        umma_commit(&bars[3 + st]);
+        umma_commit(&bars[5 + buf]);
+      }
+      if (!ok) s_abort[0] = 1;
+      umma_commit(&bars[9]);
+      mbar_wait(&bars[9], 0, p.status, kWaitLimitNs, SITE_W_DRAIN);
+    }
+    __syncwarp();
+  } else {
+    // ========================== epilogue (8 warps) ============================
+    const int gtid = tid - 64;
+    const int sub = warp & 3;
+    const int half = (warp - 2) >> 2;
+    constexpr int QH = QT / 2;  // queries per epilogue half
+    const uint32_t lane_base = static_cast<uint32_t>(sub * 32) << 16;
+    const int key_lane = sub * 32 + lane;
+    for (int kt = 0; kt < ntiles; ++kt) {
+      const int buf = kt & 1;
+      const bool w_ok = mbar_wait(&bars[5 + buf], (kt >> 1) & 1, p.status, kWaitLimitNs, SITE_W_DF);
+      if (!w_ok || vflag(s_abort)) g_abort[(kt & 1) * 2] = 1;
+      named_bar_sync(1, G);
+      if (vflag(&g_abort[(kt & 1) * 2])) break;
+      tc_fence_after();
+      float acc[QH];
+#pragma unroll
+      for (int q = 0; q < QH; ++q) acc[q] = 0.f;
+      constexpr int COLS = QH * H_I;  // this half's accumulator columns
+      const uint32_t col0 = buf * 256 + half * COLS;
+#pragma unroll
+      for (int u = 0; u < COLS / 32; ++u) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_base + col0 + u * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int col = u * 32 + e;
+          const int q = col / H_I;
+          const float v = fmaxf(__uint_as_float(r[e]), 0.f);
+          acc[q] = fmaf(w_s[(half * QH + q) * H_I + (col % H_I)], v, acc[q]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars[7 + buf]);
+      // append candidates above each query's threshold
+      const int s = kt * BKEY + key_lane;
+#pragma unroll
+      for (int q = 0; q < QH; ++q) {
+        const int qq = half * QH + q;
+        const bool take = qq < nq && s <= t0 + qq && acc[q] > thr[qq];
+        const uint32_t bal = __ballot_sync(0xffffffffu, take);
+        if (bal) {
+          int base = 0;
+          if (lane == 0) base = atomicAdd(&cnt[qq], __popc(bal));
+          base = __shfl_sync(0xffffffffu, base, 0);
+          if (take) {
+            const int pos = base + __popc(bal & ((1u << lane) - 1u));
+            cand_s[qq * CAP + pos] = acc[q];
+            cand_i[qq * CAP + pos] = s;
+          }
+        }
+      }
+      named_bar_sync(1, G);
+      // shrink any buffer that could overflow on the next tile
+      for (int qq = 0; qq < nq; ++qq) {
+        if (cnt[qq] > CAP - BKEY) {
+          const float kth = select_topk<C::EPT>(cand_s + qq * CAP, cand_i + qq * CAP, cnt[qq], p.topk,
+                                                gtid, hist, sel, ctr);
+          if (gtid == 0) {
+            cnt[qq] = p.topk;
+            thr[qq] = kth;
+          }
+          named_bar_sync(1, G);
+        }
+      }
+    }
+    // final selection and output (the abort decision is made uniform by one
+    // writer before a group barrier)
+    if (gtid == 0) g_abort[1] = vflag(s_abort) ? 1 : 0;
+    named_bar_sync(1, G);
+    const bool aborted = vflag(&g_abort[1]);
+    for (int qq = 0; qq < nq; ++qq) {
+      if (!aborted && cnt[qq] > p.topk) {
+        select_topk<C::EPT>(cand_s + qq * CAP, cand_i + qq * CAP, cnt[qq], p.topk, gtid, hist, sel,
+                            ctr);
+        if (gtid == 0) cnt[qq] = p.topk;
+        named_bar_sync(1, G);
+      }
+      const int n = aborted ? 0 : cnt[qq];
+      int32_t* o = out + static_cast<int64_t>(qq) * p.topk;
+      for (int e = gtid; e < p.topk; e += G) o[e] = e < n ? cand_i[qq * CAP + e] : -1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace idx
+
+template <int H_I, int D_I>
+static dsa_status_t prefill_launch(const IndexerArgs& a, cudaStream_t stream) {
+  using C = idx::Cfg<H_I, D_I>;
+  if (a.topk > C::CAP - idx::BKEY) return DSA_ERR_UNSUPPORTED;
+  CUtensorMap tq, tk;
+  const uint64_t qrows = static_cast<uint64_t>(a.B) * a.Tq * H_I;
+  if (!encode_tmap_2d(&tq, a.q_idx, qrows, D_I, D_I * 2, 64, C::N, true)) return DSA_ERR_CUDA;
+  const bool paged = a.k.block_table != nullptr;
+  if (!encode_tmap_2d(&tk, a.k.base, a.k.total_rows, D_I, D_I * 2, 64, paged ? 64 : 128, true))
+    return DSA_ERR_CUDA;
+  idx::Params p{};
+  p.w = a.w;
+  p.q_start = a.q_start;
+  p.kv_len = a.kv_len;
+  p.block_table = a.k.block_table;
+  p.seq_stride = a.k.seq_stride;
+  p.max_pages = a.k.max_pages;
+  p.num_pages = a.k.num_pages;
+  p.paged = paged;
+  p.Tq = a.Tq;
+  p.topk = a.topk;
+  p.max_kv_len = a.max_kv_len;
+  p.ntq = (a.Tq + C::QT - 1) / C::QT;
+  p.out_idx = a.out_idx;
+  p.status = a.status;
+  auto kern = idx::indexer_prefill_kernel<H_I, D_I>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+      cudaSuccess)
+    return DSA_ERR_CUDA;
+  kern<<<static_cast<unsigned>(a.B * p.ntq), idx::NTHREADS, C::SMEM_BYTES, stream>>>(tq, tk, p);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+int indexer_prefill_max_topk(int H_I, int D_I) {
+  if (H_I == 64 && D_I == 128) return idx::Cfg<64, 128>::CAP - idx::BKEY;
+  if (H_I == 4 && D_I == 64) return idx::Cfg<4, 64>::CAP - idx::BKEY;
+  return 0;
+}
+
+dsa_status_t indexer_prefill_launch(const IndexerArgs& a, cudaStream_t stream) {
+  if (a.H_I == 64 && a.D_I == 128) return prefill_launch<64, 128>(a, stream);
+  if (a.H_I == 4 && a.D_I == 64) return prefill_launch<4, 64>(a, stream);
+  return DSA_ERR_UNSUPPORTED;
+}
+
+}  // namespace dsa

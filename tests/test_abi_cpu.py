@@ -1,0 +1,114 @@
+"""The C ABI library loads, exports every entry point include/dsa.h declares,
+and rejects bad arguments on the host before any launch.  CPU only: no call
+here reaches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    from sparse_attention_serving_gb300 import build
+    build.build()
+    import sparse_attention_serving_gb300 as m
+    return m
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s+(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_three_entry_points():
+    names = declared_functions()
+    for n in ("dsa_indexer_topk", "sparse_mla_fwd", "mla_gate_apply"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(dsa):
+    lib = ctypes.CDLL(dsa.LIB_PATH)
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in dsa.h but not exported"
+    for n in dsa.EXPORTS:
+        assert n in names
+
+
+def test_status_strings(dsa):
+    assert dsa.lib.dsa_abi_version() == 1
+    for code in range(7):
+        assert dsa.status_string(code) and dsa.status_string(code) != "unknown status"
+    assert dsa.status_string(99) == "unknown status"
+
+
+def test_workspace_bytes_has_header(dsa):
+    for op in (dsa.OP_INDEXER_TOPK, dsa.OP_SPARSE_MLA, dsa.OP_GATE):
+        n = dsa.workspace_bytes(op, 2, 8192, 8192, 96, 2048)
+        assert n >= 256 and n % 256 == 0
+
+
+def _rows(base=0, bt=0, stride=0, maxp=0, page=0, npages=0):
+    from sparse_attention_serving_gb300 import _Rows
+    return _Rows(base, stride, bt, maxp, page, npages)
+
+
+def test_host_argument_checks(dsa):
+    lib = dsa.lib
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # aligned, never dereferenced: every call below fails its host checks
+    ws = P(1 << 24)
+    r = _rows(base=1 << 20, stride=128)
+    # null pointers
+    assert lib.dsa_indexer_topk(None, fake, ctypes.byref(r), fake, fake, 1, 128, 64, 128, 128, 64,
+                                fake, ws, 1 << 20, None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    # unsupported indexer dims
+    assert lib.dsa_indexer_topk(fake, fake, ctypes.byref(r), fake, fake, 1, 128, 32, 128, 128, 64,
+                                fake, ws, 1 << 20, None) == dsa.DSA_ERR_UNSUPPORTED
+    # top-k not a multiple of 4 / above 2048
+    assert lib.dsa_indexer_topk(fake, fake, ctypes.byref(r), fake, fake, 1, 128, 64, 128, 128, 62,
+                                fake, ws, 1 << 20, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert lib.dsa_indexer_topk(fake, fake, ctypes.byref(r), fake, fake, 1, 128, 64, 128, 128, 4096,
+                                fake, ws, 1 << 20, None) == dsa.DSA_ERR_UNSUPPORTED
+    # contiguous stride shorter than max_kv_len
+    assert lib.dsa_indexer_topk(fake, fake, ctypes.byref(_rows(base=1 << 20, stride=64)), fake,
+                                fake, 1, 128, 64, 128, 128, 64, fake, ws, 1 << 20,
+                                None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    # paged store with a page size other than 64
+    assert lib.dsa_indexer_topk(fake, fake,
+                                ctypes.byref(_rows(base=1 << 20, bt=1 << 20, maxp=4, page=32,
+                                                   npages=8)),
+                                fake, fake, 1, 128, 64, 128, 128, 64, fake, ws, 1 << 20,
+                                None) == dsa.DSA_ERR_UNSUPPORTED
+    # workspace too small / misaligned
+    assert lib.dsa_indexer_topk(fake, fake, ctypes.byref(r), fake, fake, 1, 128, 64, 128, 128, 64,
+                                fake, ws, 16, None) == dsa.DSA_ERR_WORKSPACE_TOO_SMALL
+    assert lib.dsa_indexer_topk(fake, fake, ctypes.byref(r), fake, fake, 1, 128, 64, 128, 128, 64,
+                                fake, P((1 << 24) + 8), 1 << 20, None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    # sparse MLA: unsupported heads, bad scale, misaligned q
+    kvr = _rows(base=1 << 20, stride=128)
+    assert lib.sparse_mla_fwd(fake, ctypes.byref(kvr), fake, fake, fake, 1, 128, 64, 128, 128,
+                              ctypes.c_float(0.07), fake, None, ws, 1 << 20,
+                              None) == dsa.DSA_ERR_UNSUPPORTED
+    assert lib.sparse_mla_fwd(fake, ctypes.byref(kvr), fake, fake, fake, 1, 128, 96, 128, 128,
+                              ctypes.c_float(-1.0), fake, None, ws, 1 << 20,
+                              None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert lib.sparse_mla_fwd(P((1 << 20) + 2), ctypes.byref(kvr), fake, fake, fake, 1, 128, 96,
+                              128, 128, ctypes.c_float(0.07), fake, None, ws, 1 << 20,
+                              None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    # gate: dv other than 128, odd head count, hid not a multiple of 64
+    assert lib.mla_gate_apply(fake, fake, fake, fake, 16, 1024, 8, 64, fake, ws, 1 << 20,
+                              None) == dsa.DSA_ERR_UNSUPPORTED
+    assert lib.mla_gate_apply(fake, fake, fake, fake, 16, 1024, 7, 128, fake, ws, 1 << 20,
+                              None) == dsa.DSA_ERR_UNSUPPORTED
+    assert lib.mla_gate_apply(fake, fake, fake, fake, 16, 1000, 8, 128, fake, ws, 1 << 20,
+                              None) == dsa.DSA_ERR_UNSUPPORTED
+    assert lib.mla_gate_apply(fake, fake, None, fake, 16, 1024, 8, 128, fake, ws, 1 << 20,
+                              None) == dsa.DSA_ERR_INVALID_ARGUMENT
