@@ -58,13 +58,19 @@ int num_sms() {
 
 int indexer_prefill_max_topk(int H_I, int D_I);
 dsa_status_t indexer_prefill_launch(const IndexerArgs& a, cudaStream_t stream);
+dsa_status_t indexer_decode_launch(const IndexerArgs& a, cudaStream_t stream);
+size_t indexer_decode_scratch_bytes(int B, int max_kv_len);
 
+// Tq == 1 (one new token per request) takes the split decode path, which keeps
+// a linear FP32 score vector per request in the workspace; Tq > 1 takes the
+// fused prefill kernel, which keeps every score on chip.
 size_t indexer_scratch_bytes(int B, int Tq, int max_kv_len, int H_I, int topk) {
-  (void)B; (void)Tq; (void)max_kv_len; (void)H_I; (void)topk;
-  return 0;
+  (void)H_I; (void)topk;
+  return Tq == 1 ? indexer_decode_scratch_bytes(B, max_kv_len) : 0;
 }
 
 dsa_status_t indexer_launch(const IndexerArgs& a, cudaStream_t stream) {
+  if (a.Tq == 1) return indexer_decode_launch(a, stream);
   return indexer_prefill_launch(a, stream);
 }
 

@@ -1,0 +1,440 @@
+// indexer_decode.cu -- lightning indexer + top-k for decode (one new query per
+// request, Tq == 1) on sm_103a.
+//
+// Same score as the prefill kernel, I[s] = sum_j w[j] * max(0, q[j,:] . k[s,:])
+// over every key s < L of the request ("Kimi-K3.1-Pro", NeMo AutoModel,
+// Implementation Limits, bullet 2), then the top-k keys ("Kimi K3.1 Pro"
+// archdiff summary: top-2,048).  Decode reads every cached indexer key once
+// and does little arithmetic per byte, so it is bound by HBM bandwidth:
+//
+//   decode_scores  persistent CTAs walk (request, 2,048-key chunk) work items;
+//                  a 5-deep TMA ring streams the paged keys (two 64-token pages
+//                  per 128-key tile), one tcgen05 MMA per tile computes
+//                  D^T[128 keys x H_I] = K_tile . q^T, and the epilogue reduces
+//                  over heads and writes one FP32 score per key: a linear
+//                  score vector per request in the workspace (4 bytes per key
+//                  against 256 bytes of key read).
+//   decode_select  one CTA per request: radix select (11 + 11 + 10 bits over
+//                  order-preserving keys) of the k largest scores, then writes
+//                  their positions.
+#include <cmath>
+
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "sm103.cuh"
+
+namespace dsa {
+namespace idxd {
+
+constexpr int BKEY = 128;
+constexpr int CH_TILES = 16;  // tiles per work item (2,048 keys)
+constexpr int NST = 5;
+constexpr int NTHREADS = 192;  // producer, MMA, 4 epilogue warps
+constexpr int MAXB = 1024;     // requests per call handled by the work decomposition
+
+enum : uint32_t {
+  SITE_LEN = 0x400, SITE_PAGE = 0x401, SITE_W_QE = 0x410, SITE_W_QF = 0x411, SITE_W_KE = 0x412,
+  SITE_W_KF = 0x413, SITE_W_DE = 0x414, SITE_W_DF = 0x415, SITE_W_DRAIN = 0x416
+};
+
+template <int H_I, int D_I>
+struct Cfg {
+  static constexpr int NCH = D_I / 64;
+  static constexpr int Q_BYTES = NCH * H_I * 128 < 1024 ? 1024 : NCH * H_I * 128;
+  static constexpr int K_STAGE = NCH * BKEY * 128;
+  static constexpr int N = H_I < 16 ? 16 : H_I;  // MMA N (rows of q beyond H_I are ignored)
+  static constexpr int OFF_Q = 0;                    // two q slots
+  static constexpr int OFF_K = 2 * (Q_BYTES > N * 128 * NCH ? Q_BYTES : N * 128 * NCH);
+  static constexpr int OFF_MISC = OFF_K + NST * K_STAGE;
+  static constexpr int MISC_BYTES = 8192 + 1024;     // barriers + work prefix sums
+  static constexpr int SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+struct Params {
+  const uint16_t* w;
+  const int32_t* kv_len;
+  const int32_t* block_table;
+  int64_t seq_stride;
+  int32_t max_pages, num_pages;
+  int paged;
+  int B, max_kv_len;
+  float* scores;  // [B, max_kv_len]
+  uint32_t* status;
+};
+
+__device__ __forceinline__ bool vflag(const volatile int* p) { return *p != 0; }
+
+// Map work item `it` to (request, first tile) through the chunk prefix sums.
+__device__ __forceinline__ void item_of(const int* pre, int B, int it, int& b, int& c) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= it) lo = mid; else hi = mid - 1;
+  }
+  b = lo;
+  c = it - pre[lo];
+}
+
+template <int H_I, int D_I>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    decode_scores_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k, const Params p) {
+  using C = Cfg<H_I, D_I>;
+  constexpr int NCH = C::NCH, N = C::N;
+  constexpr int QSLOT = C::OFF_K / 2;
+  constexpr uint32_t IDESC = idesc_bf16(128, N, false, false);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_MISC);
+  // q full [2] 0..1, q empty [2] 2..3, k full [NST] 4.., k empty [NST], d full [4], d empty [4], drain
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = bars + 2;
+  uint64_t* k_full = bars + 4;
+  uint64_t* k_empty = k_full + NST;
+  uint64_t* d_full = k_empty + NST;
+  uint64_t* d_empty = d_full + 4;
+  uint64_t* drain = d_empty + 4;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 32);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
+  int* pre = const_cast<int*>(s_abort) + 4;  // [MAXB + 1] chunk prefix sums
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int k = 0; k < 2; ++k) { mbar_init(&q_full[k], 1); mbar_init(&q_empty[k], 1); }
+    for (int k = 0; k < NST; ++k) { mbar_init(&k_full[k], 1); mbar_init(&k_empty[k], 1); }
+    for (int k = 0; k < 4; ++k) { mbar_init(&d_full[k], 1); mbar_init(&d_empty[k], 128); }
+    mbar_init(drain, 1);
+    s_abort[0] = 0;
+    fence_mbar_init();
+    // per-request chunk counts -> prefix sums
+    int acc = 0;
+    for (int b = 0; b < p.B; ++b) {
+      pre[b] = acc;
+      int L = __ldg(p.kv_len + b);
+      if (L < 0 || L > p.max_kv_len) {
+        status_raise(p.status, DSA_ERR_BAD_INDEX, SITE_LEN, (uint32_t)L);
+        L = 0;
+      }
+      acc += (L + CH_TILES * BKEY - 1) / (CH_TILES * BKEY);
+    }
+    pre[p.B] = acc;
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const int total = pre[p.B];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      int kcount = 0, n_items = 0;
+      int last_k[NST];
+      for (int k = 0; k < NST; ++k) last_k[k] = -1;
+      int last_q[2] = {-1, -1};
+      for (int it = blockIdx.x; it < total && !vflag(s_abort); it += gridDim.x, ++n_items) {
+        int b, c;
+        item_of(pre, p.B, it, b, c);
+        const int L = __ldg(p.kv_len + b);
+        const int qs = n_items & 1, quse = n_items >> 1;
+        if (quse > 0 && !mbar_wait(&q_empty[qs], (quse - 1) & 1, p.status, kWaitLimitNs, SITE_W_QE)) {
+          s_abort[0] = 1;
+          break;
+        }
+        mbar_expect_tx(&q_full[qs], NCH * N * 128);
+        last_q[qs] = quse;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch)
+          tma_load_2d(sm + C::OFF_Q + qs * QSLOT + ch * N * 128, &tm_q, &q_full[qs], 64 * ch, b * H_I);
+        const int t0 = c * CH_TILES;
+        const int t1 = min(t0 + CH_TILES, (L + BKEY - 1) / BKEY);
+        for (int kt = t0; kt < t1; ++kt, ++kcount) {
+          const int st = kcount % NST, use = kcount / NST;
+          if (use > 0 && !mbar_wait(&k_empty[st], (use - 1) & 1, p.status, kWaitLimitNs, SITE_W_KE)) {
+            s_abort[0] = 1;
+            break;
+          }
+          mbar_expect_tx(&k_full[st], C::K_STAGE);
+          last_k[st] = use;
+          uint8_t* dst = sm + C::OFF_K + st * C::K_STAGE;
+          if (!p.paged) {
+            const int row = static_cast<int>(static_cast<int64_t>(b) * p.seq_stride + kt * BKEY);
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch)
+              tma_load_2d(dst + ch * BKEY * 128, &tm_k, &k_full[st], 64 * ch, row);
+          } else {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int pg = kt * 2 + hf;
+              int pid = 0;
+              if (pg * kPage < L) {
+                pid = pg < p.max_pages ? __ldg(p.block_table + static_cast<int64_t>(b) * p.max_pages + pg) : -1;
+                if (pid < 0 || pid >= p.num_pages) {
+                  status_raise(p.status, DSA_ERR_BAD_INDEX, SITE_PAGE, (uint32_t)pid);
+                  pid = 0;
+                }
+              }
+#pragma unroll
+              for (int ch = 0; ch < NCH; ++ch)
+                tma_load_2d(dst + ch * BKEY * 128 + hf * 64 * 128, &tm_k, &k_full[st], 64 * ch, pid * kPage);
+            }
+          }
+        }
+      }
+      for (int k = 0; k < NST; ++k)
+        if (last_k[k] >= 0) mbar_wait(&k_full[k], last_k[k] & 1, p.status, kWaitLimitNs, SITE_W_KF);
+      for (int k = 0; k < 2; ++k)
+        if (last_q[k] >= 0) mbar_wait(&q_full[k], last_q[k] & 1, p.status, kWaitLimitNs, SITE_W_QF);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int kcount = 0, dcount = 0, n_items = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < total && ok; it += gridDim.x, ++n_items) {
+        int b, c;
+        item_of(pre, p.B, it, b, c);
+        const int L = __ldg(p.kv_len + b);
+        const int qs = n_items & 1;
+        if (!mbar_wait(&q_full[qs], (n_items >> 1) & 1, p.status, kWaitLimitNs, SITE_W_QF)) { ok = false; break; }
+        const uint32_t qb = smem_u32(sm + C::OFF_Q + qs * QSLOT);
+        const int t0 = c * CH_TILES;
+        const int t1 = min(t0 + CH_TILES, (L + BKEY - 1) / BKEY);
+        for (int kt = t0; kt < t1; ++kt, ++kcount, ++dcount) {
+          if (vflag(s_abort)) { ok = false; break; }
+          const int st = kcount % NST, buf = dcount & 3;
+          if (dcount >= 4 && !mbar_wait(&d_empty[buf], ((dcount >> 2) - 1) & 1, p.status, kWaitLimitNs, SITE_W_DE)) { ok = false; break; }
+          if (!mbar_wait(&k_full[st], (kcount / NST) & 1, p.status, kWaitLimitNs, SITE_W_KF)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kb = smem_u32(sm + C::OFF_K + st * C::K_STAGE);
+#pragma unroll
+          for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(tmem + buf * 64, smem_desc(kb + ch * BKEY * 128 + kk * 32, 16, 1024),
+                        smem_desc(qb + ch * N * 128 + kk * 32, 16, 1024), IDESC, (ch | kk) ? 1u : 0u);
+          umma_commit(&k_empty[st]);
+          umma_commit(&d_full[buf]);
+        }
+        if (ok) umma_commit(&q_empty[qs]);
+      }
+      if (!ok) s_abort[0] = 1;
+      umma_commit(drain);
+      mbar_wait(drain, 0, p.status, kWaitLimitNs, SITE_W_DRAIN);
+    }
+    __syncwarp();
+  } else {
+    // epilogue: thread = key lane of the tile; no group barrier is needed
+    const int sub = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(sub * 32) << 16;
+    int dcount = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+      int b, c;
+      item_of(pre, p.B, it, b, c);
+      const int L = __ldg(p.kv_len + b);
+      float wv[H_I];
+#pragma unroll
+      for (int j = 0; j < H_I; ++j)
+        wv[j] = __bfloat162float(__ushort_as_bfloat16(__ldg(p.w + static_cast<int64_t>(b) * H_I + j)));
+      const int t0 = c * CH_TILES;
+      const int t1 = min(t0 + CH_TILES, (L + BKEY - 1) / BKEY);
+      float* out = p.scores + static_cast<int64_t>(b) * p.max_kv_len;
+      for (int kt = t0; kt < t1; ++kt, ++dcount) {
+        const int buf = dcount & 3;
+        if (!mbar_wait(&d_full[buf], (dcount >> 2) & 1, p.status, kWaitLimitNs, SITE_W_DF) || vflag(s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float acc = 0.f;
+#pragma unroll
+        for (int j0 = 0; j0 < H_I; j0 += (H_I < 32 ? H_I : 32)) {
+          uint32_t r[32];
+          if constexpr (H_I >= 32) {
+            tmem_ld32(tmem + lane_base + buf * 64 + j0, r);
+          } else {
+            uint32_t(&r16)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[0]);
+            tmem_ld16(tmem + lane_base + buf * 64 + j0, r16);
+          }
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < (H_I < 32 ? H_I : 32); ++e)
+            acc = fmaf(wv[j0 + e], fmaxf(__uint_as_float(r[e]), 0.f), acc);
+        }
+        tc_fence_before();
+        mbar_arrive(&d_empty[buf]);
+        const int s = kt * BKEY + sub * 32 + lane;
+        if (s < L) out[s] = acc;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Block-wide: find, over `nb` bins counted from the top digit down, the bin in
+// which the `need`-th largest element falls; returns (bin, remaining need).
+template <int NB>
+__device__ void find_bin(const int* hist, int need, int* out2, int* wsum) {
+  constexpr int PER = NB / 1024;  // bins per thread
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int c[PER], tot = 0;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) { c[e] = hist[NB - 1 - (tid * PER + e)]; tot += c[e]; }
+  int incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = wsum[lane];
+    int iv = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, iv, o);
+      if (lane >= o) iv += u;
+    }
+    wsum[32 + lane] = iv - v;  // exclusive prefix over warps
+  }
+  __syncthreads();
+  const int excl = wsum[32 + warp] + incl - tot;
+  if (excl < need && need <= excl + tot) {
+    int run = excl;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      if (run < need && need <= run + c[e]) {
+        out2[0] = NB - 1 - (tid * PER + e);
+        out2[1] = need - run;
+      }
+      run += c[e];
+    }
+  }
+  __syncthreads();
+}
+
+// One CTA (1024 threads) per request: the k largest of scores[0..L).
+__global__ void __launch_bounds__(1024) decode_select_kernel(const float* __restrict__ scores,
+                                                             const int32_t* __restrict__ kv_len,
+                                                             int max_kv_len, int topk,
+                                                             int32_t* __restrict__ out_idx) {
+  __shared__ int hist[2048];
+  __shared__ int wsum[64];
+  __shared__ int sel[2];
+  __shared__ int ctr[2];
+  const int b = blockIdx.x, tid = threadIdx.x;
+  int L = __ldg(kv_len + b);
+  if (L < 0 || L > max_kv_len) L = 0;  // flagged by the score kernel
+  int32_t* out = out_idx + static_cast<int64_t>(b) * topk;
+  if (L <= topk) {
+    for (int e = tid; e < topk; e += 1024) out[e] = e < L ? e : -1;
+    return;
+  }
+  const float* sc = scores + static_cast<int64_t>(b) * max_kv_len;
+  uint32_t prefix = 0, mask = 0;
+  int need = topk;
+  // digits: bits 31..21 (11), 20..10 (11), 9..0 (10)
+  const int shifts[3] = {21, 10, 0};
+  const int widths[3] = {11, 11, 10};
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int sh = shifts[pass];
+    const uint32_t dm = (1u << widths[pass]) - 1u;
+    for (int e = tid; e < 2048; e += 1024) hist[e] = 0;
+    __syncthreads();
+    for (int e = tid; e < L; e += 1024) {
+      const uint32_t k = order_key(sc[e]);
+      if ((k & mask) == prefix) atomicAdd(&hist[(k >> sh) & dm], 1);
+    }
+    __syncthreads();
+    if (widths[pass] == 11)
+      find_bin<2048>(hist, need, sel, wsum);
+    else
+      find_bin<1024>(hist, need, sel, wsum);
+    prefix |= static_cast<uint32_t>(sel[0]) << sh;
+    mask |= dm << sh;
+    need = sel[1];
+    __syncthreads();
+  }
+  if (tid == 0) { ctr[0] = 0; ctr[1] = 0; }
+  __syncthreads();
+  for (int e = tid; e < L; e += 1024) {
+    const uint32_t k = order_key(sc[e]);
+    bool keep = k > prefix;
+    if (!keep && k == prefix) keep = atomicAdd(&ctr[1], 1) < need;
+    if (keep) out[atomicAdd(&ctr[0], 1)] = e;
+  }
+}
+
+}  // namespace idxd
+
+size_t indexer_decode_scratch_bytes(int B, int max_kv_len) {
+  return static_cast<size_t>(B) * max_kv_len * sizeof(float) + 256;
+}
+
+template <int H_I, int D_I>
+static dsa_status_t decode_launch(const IndexerArgs& a, cudaStream_t stream) {
+  using C = idxd::Cfg<H_I, D_I>;
+  if (a.B > idxd::MAXB) return DSA_ERR_UNSUPPORTED;
+  if (a.scratch == nullptr || a.scratch_bytes < indexer_decode_scratch_bytes(a.B, a.max_kv_len))
+    return DSA_ERR_WORKSPACE_TOO_SMALL;
+  CUtensorMap tq, tk;
+  // q rows: one request = H_I rows of D_I; the box reads N rows (extra rows are ignored)
+  if (!encode_tmap_2d(&tq, a.q_idx, static_cast<uint64_t>(a.B) * H_I, D_I, D_I * 2, 64, C::N, true))
+    return DSA_ERR_CUDA;
+  const bool paged = a.k.block_table != nullptr;
+  if (!encode_tmap_2d(&tk, a.k.base, a.k.total_rows, D_I, D_I * 2, 64, paged ? 64 : 128, true))
+    return DSA_ERR_CUDA;
+  idxd::Params p{};
+  p.w = a.w;
+  p.kv_len = a.kv_len;
+  p.block_table = a.k.block_table;
+  p.seq_stride = a.k.seq_stride;
+  p.max_pages = a.k.max_pages;
+  p.num_pages = a.k.num_pages;
+  p.paged = paged;
+  p.B = a.B;
+  p.max_kv_len = a.max_kv_len;
+  p.scores = static_cast<float*>(a.scratch);
+  p.status = a.status;
+  auto kern = idxd::decode_scores_kernel<H_I, D_I>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+      cudaSuccess)
+    return DSA_ERR_CUDA;
+  const int max_items = a.B * ((a.max_kv_len + idxd::CH_TILES * idxd::BKEY - 1) /
+                               (idxd::CH_TILES * idxd::BKEY));
+  const int grid = max_items < num_sms() ? max_items : num_sms();
+  kern<<<grid, idxd::NTHREADS, C::SMEM_BYTES, stream>>>(tq, tk, p);
+  if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+  idxd::decode_select_kernel<<<a.B, 1024, 0, stream>>>(p.scores, a.kv_len, a.max_kv_len, a.topk,
+                                                        a.out_idx);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+dsa_status_t indexer_decode_launch(const IndexerArgs& a, cudaStream_t stream) {
+  if (a.H_I == 64 && a.D_I == 128) return decode_launch<64, 128>(a, stream);
+  if (a.H_I == 4 && a.D_I == 64) return decode_launch<4, 64>(a, stream);
+  return DSA_ERR_UNSUPPORTED;
+}
+
+}  // namespace dsa

@@ -363,7 +363,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int sub = warp & 3;             // TMEM lane quarter this warp may access
     const int h = sub * 32 + lane;        // head owned in the softmax
     const uint32_t lane_base = static_cast<uint32_t>(sub * 32) << 16;
-    float m_ref = -INFINITY, l_sum = 0.f;
+    // l_sum: sum of the BF16-rounded P fed to the PV product (normalises O);
+    // l_exact: the unrounded sum (log-sum-exp)
+    float m_ref = -INFINITY, l_sum = 0.f, l_exact = 0.f;
     bool ok = true;
     uint8_t* prow = sm + OFF_P;
     for (int jj = 0; jj < nb; ++jj) {
@@ -398,16 +400,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (mb > m_ref + 64.f) m_new = mb;
       const float alpha = (m_new == m_ref) ? 1.f : exp2f(m_ref - m_new);
       l_sum *= alpha;
+      l_exact *= alpha;
       uint32_t pk[32];
-      float lsum_blk = 0.f;
+      float lsum_blk = 0.f, lex_blk = 0.f;
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
         const float p0 = exp2f(z[c] - m_new), p1 = exp2f(z[c + 1] - m_new);
         const uint32_t v = pack_bf16x2(p0, p1);
         pk[c >> 1] = v;
         lsum_blk += __uint_as_float(v << 16) + __uint_as_float(v & 0xffff0000u);
+        lex_blk += p0 + p1;
       }
       l_sum += lsum_blk;
+      l_exact += lex_blk;
       m_ref = m_new;
       // P^T buffer and O^T are free once the previous block's PV product is done
       if (jj >= 1) {
@@ -458,7 +463,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     // ------------------------------ epilogue ---------------------------------
     if (h < H) s_invl[h] = l_sum > 0.f ? 1.f / l_sum : 0.f;
-    float lse2 = (l_sum > 0.f) ? m_ref + log2f(l_sum) : -INFINITY;
+    float lse2 = (l_exact > 0.f) ? m_ref + log2f(l_exact) : -INFINITY;
     bool have_o = ok && nb > 0;
     if (have_o) {
       const bool w_ok = mbar_wait(&bars[B_O], (nb - 1) & 1, p.status, kWaitLimitNs, SITE_W_O);

@@ -13,8 +13,8 @@ HEADER = os.path.join(ROOT, "include", "dsa.h")
 
 @pytest.fixture(scope="module")
 def dsa():
-    from sparse_attention_serving_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import sparse_attention_serving_gb300 as m
     return m
 

@@ -15,7 +15,7 @@ Workload shapes follow the pages' workloads:
   ``num_attention_heads 96``, ``kv_lora_rank 512``, ``qk_rope_head_dim 64``,
   ``v_head_dim 128``, ``hidden_size 7168``.
 
-Every array has its own counter-free stream ``default_rng([seed, stream_id])``
+Every array has its own streams ``default_rng([seed, stream_id, sub, slab])``
 (PCG64), so any array, or any chunk of the queries, can be drawn without
 drawing the others first.  Activations are N(0, 1), weights N(0, 0.02), all
 rounded to BF16 by round-to-nearest-even and stored as ``uint16``.
@@ -111,18 +111,34 @@ def _rng(seed: int, name: str, sub: int = 0) -> np.random.Generator:
 
 
 def normal_bf16(seed: int, name: str, shape, std: float = 1.0, sub: int = 0) -> np.ndarray:
-    """Seeded N(0, std^2) draw rounded to BF16, generated in slabs to bound memory."""
+    """Seeded N(0, std^2) draw rounded to BF16.
+
+    The array is drawn in slabs of 2^22 values; slab i comes from its own stream
+    default_rng([seed, stream_id, sub, i]), so slabs are drawn in parallel and
+    the result does not depend on the thread count.
+    """
     shape = tuple(int(s) for s in shape)
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.uint16)
-    rng = _rng(seed, name, sub)
-    slab = 1 << 24
-    for o in range(0, n, slab):
+    slab = 1 << 22
+    nslab = (n + slab - 1) // slab
+
+    def one(i):
+        o = i * slab
         m = min(slab, n - o)
-        v = rng.standard_normal(m, dtype=np.float32)
+        v = np.random.default_rng([seed, _STREAM[name], sub, i]).standard_normal(m, dtype=np.float32)
         if std != 1.0:
             v *= np.float32(std)
         out[o:o + m] = bf16_round(v)
+
+    if nslab <= 1:
+        for i in range(nslab):
+            one(i)
+    else:
+        import concurrent.futures as cf
+        import os
+        with cf.ThreadPoolExecutor(max_workers=min(nslab, os.cpu_count() or 1, 32)) as ex:
+            list(ex.map(one, range(nslab)))
     return out.reshape(shape)
 
 
@@ -143,16 +159,23 @@ def prefill_queries(cfg: Config, q0: int = 0, nq: int | None = None) -> dict:
     w = np.empty((B, nq, cfg.H_I), np.uint16)
     q_lat = np.empty((B, nq, cfg.H, R_LAT), np.uint16)
     blk = 256  # query rows per draw block (sub-stream = block number)
-    for b in range(B):
-        for t0 in range((q0 // blk) * blk, q0 + nq, blk):
-            sub = b * (1 << 20) + t0 // blk
-            a = normal_bf16(cfg.seed, "q_idx", (blk, cfg.H_I, cfg.D_I), sub=sub)
-            c = normal_bf16(cfg.seed, "w", (blk, cfg.H_I), sub=sub)
-            d = normal_bf16(cfg.seed, "q_lat", (blk, cfg.H, R_LAT), sub=sub)
-            lo, hi = max(t0, q0), min(t0 + blk, q0 + nq)
-            q_idx[b, lo - q0:hi - q0] = a[lo - t0:hi - t0]
-            w[b, lo - q0:hi - q0] = c[lo - t0:hi - t0]
-            q_lat[b, lo - q0:hi - q0] = d[lo - t0:hi - t0]
+    jobs = [(b, t0) for b in range(B) for t0 in range((q0 // blk) * blk, q0 + nq, blk)]
+
+    def one(job):
+        b, t0 = job
+        sub = b * (1 << 20) + t0 // blk
+        a = normal_bf16(cfg.seed, "q_idx", (blk, cfg.H_I, cfg.D_I), sub=sub)
+        c = normal_bf16(cfg.seed, "w", (blk, cfg.H_I), sub=sub)
+        d = normal_bf16(cfg.seed, "q_lat", (blk, cfg.H, R_LAT), sub=sub)
+        lo, hi = max(t0, q0), min(t0 + blk, q0 + nq)
+        q_idx[b, lo - q0:hi - q0] = a[lo - t0:hi - t0]
+        w[b, lo - q0:hi - q0] = c[lo - t0:hi - t0]
+        q_lat[b, lo - q0:hi - q0] = d[lo - t0:hi - t0]
+
+    import concurrent.futures as cf
+    import os
+    with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 1, 16)) as ex:
+        list(ex.map(one, jobs))
     return {"q_idx": q_idx, "w": w, "q_lat": q_lat}
 
 
