@@ -164,6 +164,40 @@ dsa_status_t mla_gate_apply(const uint16_t* x, const uint16_t* W_g, const uint16
                             const uint16_t* W_uv, int N, int hid, int H, int dv, uint16_t* out,
                             void* workspace, size_t ws_bytes, dsa_stream_t stream);
 
+/*
+ * sparse_mla_fwd_noalloc -- sparse_mla_fwd for callers that cannot allocate
+ * device memory.  The pages have no counterpart to this entry point; it exists
+ * for deployment only.
+ *
+ * Who needs it: code that runs inside a host framework which owns all device
+ * memory (an inference server that hands its memory to a fixed pool at
+ * start-up, a plugin interface that passes tensors in and out but offers no
+ * scratch), where this call may not reach cudaMalloc.  It takes the same
+ * arguments and gives the same results as sparse_mla_fwd, with no workspace:
+ *   - Scratch (the split-K partial results used when B*Tq is below the SM
+ *     count) lives in one fixed 32 MiB array of device memory inside this
+ *     library, held by every GPU that loads the library until the process
+ *     exits.  Sizes whose partials do not fit (B*Tq*splits*H*513*4 bytes above
+ *     32 MiB minus 256) are rejected with DSA_ERR_WORKSPACE_TOO_SMALL before
+ *     anything is launched.  The call allocates and frees nothing.
+ *   - The first call on a device looks up that array's device address (with
+ *     the caller's current device); make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the array and it keeps the last call's
+ *     contents: two calls whose kernels may overlap on the GPU (different
+ *     streams without ordering) race on it.  Serialise them.
+ *   - device_status: NULL, or a caller-owned device array of 3 uint32 that
+ *     starts at zero; device-side errors (bad index, bad page id, a wait that
+ *     ran out) are recorded there as in the workspace status word.  With NULL
+ *     they are recorded in the array's own header, which each call clears, and
+ *     cannot be read back.
+ */
+dsa_status_t sparse_mla_fwd_noalloc(const uint16_t* q_lat, const dsa_rows_t* kv,
+                                    const int32_t* idx, const int32_t* q_start,
+                                    const int32_t* kv_len, int B, int Tq, int H, int topk,
+                                    int max_kv_len, float scale, uint16_t* o_lat, float* lse,
+                                    uint32_t* device_status, dsa_stream_t stream);
+
 /* Synchronise `stream`, return the first device-side error recorded in the
  * workspace (DSA_OK if none) and clear it.  `where` / `detail` (nullable)
  * receive the site tag and detail value. */
