@@ -7,15 +7,16 @@
 //   o    = sum_s softmax(z)_s * KV[s, 0:512],       lse = log sum_s exp(z_s)
 //
 // One CTA per query (or per query x key-split for small batches):
-//   warp 0      producer: TMA load of the query's 96x576 q_lat block; TMA
-//               gather4 of the selected rows, 64 keys per block, into a ring of
-//               16 KB "pair" slots (two 64-dim chunks, dims 0..511) and 8 KB
-//               "rope" slots (dims 512..575), 128-byte swizzled.
-//   warp 1      tcgen05 issuer (one lane):
+//   warps 0-3   producer: TMA load of the query's 96x576 q_lat block; 16-byte
+//               cp.async gather of the selected rows, 64 keys per block, into a
+//               ring of 16 KB "pair" slots (two 64-dim chunks, dims 0..511) and
+//               8 KB "rope" slots (dims 512..575), 128-byte swizzled.  (TMA
+//               tile::gather4 moves these 1,152-byte rows about 4x slower.)
+//   warp 4      tcgen05 issuer (one lane):
 //                 S  [128 x 64]  = Q [128(96 heads) x 576] . KV_blk^T   (M=128, N=64)
 //                 O^T[512 x 96] += V_blk^T [512 x 64] . P^T [64 x 96]   (4 x M=128, N=96)
 //               S double-buffered in TMEM columns 384..511, O^T in 0..383.
-//   warps 2-5   softmax (one lane per head; the row max and sum stay in the
+//   warps 5-8   softmax (one lane per head; the row max and sum stay in the
 //               thread), write P^T as BF16 into shared memory, then the
 //               epilogue (O^T / l -> BF16 o_lat, lse).
 // Q rows 96..127 of the M=128 operand alias the next 64-dim chunk of Q (or the
@@ -49,7 +50,9 @@ constexpr int MISC_BYTES = 2048;
 constexpr int SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-constexpr int NTHREADS = 192;
+constexpr int NPROD = 128;                 // producer threads (warps 0-3)
+constexpr int MMA_WARP = NPROD / 32;       // warp 4
+constexpr int NTHREADS = NPROD + 32 + 128; // + MMA warp + 4 softmax warps
 constexpr uint32_t S_COL = 384;
 
 // barrier indices
@@ -76,6 +79,7 @@ enum : uint32_t {
 };
 
 struct Params {
+  const uint16_t* kv;  // row store base (contiguous or page pool)
   const int32_t* idx;
   const int32_t* q_start;
   const int32_t* kv_len;
@@ -97,7 +101,7 @@ __device__ __forceinline__ bool vload(const volatile int* p) { return *p != 0; }
 template <int H>
 __global__ void __launch_bounds__(NTHREADS, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q,
-                      const __grid_constant__ CUtensorMap tm_kv, const Params p) {
+                      const Params p) {
   constexpr int HN = (H + 15) / 16 * 16;  // N of the PV product
   constexpr int QRS = H * 128;            // bytes of one 64-dim chunk of Q
   constexpr uint32_t IDESC_S = idesc_bf16(128, BK, false, false);
@@ -113,8 +117,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   volatile int* g_abort = s_abort + 1;      // [4] softmax-group abort, by iteration parity x checkpoint
   volatile int* s_resc = s_abort + 5;       // [2] any head needs O^T rescale, by parity
   int* s_nvalid = const_cast<int*>(s_abort + 7);
-  int* s_wsum = s_nvalid + 1;               // [8]
-  float* s_alpha = reinterpret_cast<float*>(s_wsum + 8);  // [128]
+  int* s_wsum = s_nvalid + 1;               // [16]
+  float* s_alpha = reinterpret_cast<float*>(s_wsum + 16);  // [128]
   float* s_invl = s_alpha + 128;                          // [128]
   int32_t* rows = reinterpret_cast<int32_t*>(sm + OFF_ROWS);
 
@@ -126,6 +130,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int k = 0; k < NBAR; ++k) {
       uint32_t cnt = 1;
       if (k == B_SE || k == B_SE + 1 || k == B_P) cnt = 128;
+      if ((k >= B_PF && k < B_PF + NPAIR) || (k >= B_RF && k < B_RF + NROPE)) cnt = NPROD;
       mbar_init(&bars[k], cnt);
     }
     s_abort[0] = 0;
@@ -133,7 +138,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     s_resc[0] = 0; s_resc[1] = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == MMA_WARP) {
     tmem_alloc(tslot, 512);
     tmem_relinquish();
   }
@@ -201,83 +206,70 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   const uint32_t tmem = *tslot;
 
-  if (warp == 0) {
-    // =========================== producer ===================================
-    uint32_t last_pair_use[NPAIR], last_rope_use[NROPE];
-#pragma unroll
-    for (int k = 0; k < NPAIR; ++k) last_pair_use[k] = 0xffffffffu;
-#pragma unroll
-    for (int k = 0; k < NROPE; ++k) last_rope_use[k] = 0xffffffffu;
+  if (warp < NPROD / 32) {
+    // ====================== producer (4 warps, cp.async) ======================
+    // Each 16-byte unit of a selected row is copied by one thread straight into
+    // its 128-byte-swizzled place; a warp covers 4 keys x 8 units of one 64-dim
+    // chunk (4 x 128 contiguous bytes of global memory).
+    const int ptid = tid;  // 0..127
     if (nb > 0) {
-      if (lane == 0) {
+      if (ptid == 0) {
         tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_kv);
         mbar_expect_tx(&bars[B_Q], 9u * H * 128u);
+#pragma unroll 1
+        for (int c = 0; c < 9; ++c)
+          tma_load_2d(sm + OFF_Q + c * QRS, &tm_q, &bars[B_Q], 64 * c, qflat * H);
       }
-      __syncwarp();
-      if (lane < 9)
-        tma_load_2d(sm + OFF_Q + lane * QRS, &tm_q, &bars[B_Q], 64 * lane, qflat * H);
       bool ok = true;
       for (int jj = 0; jj < nb && ok; ++jj) {
         const int kb = (blk0 + jj) * BK;  // first list entry of the block
         // parts in the order the MMA consumes them: pair 0, rope, pair 1..3
-        for (int part = 0; part < 5 && ok; ++part) {
+        for (int part = 0; part < 5; ++part) {
           const bool rope = part == 1;
           const int pr = part == 0 ? 0 : part - 1;  // pair index 0..3
-          int slot;
-          uint32_t use;
           uint64_t *full, *empty;
+          uint32_t use;
           uint8_t* dst;
           if (rope) {
-            slot = jj % NROPE;
+            const int slot = jj % NROPE;
             use = jj / NROPE;
             full = &bars[B_RF + slot];
             empty = &bars[B_RE + slot];
             dst = sm + OFF_ROPE + slot * CHUNK;
           } else {
             const uint32_t g = 4u * jj + pr;
-            slot = g % NPAIR;
+            const int slot = g % NPAIR;
             use = g / NPAIR;
             full = &bars[B_PF + slot];
             empty = &bars[B_PE + slot];
             dst = sm + OFF_PAIR + slot * PAIR;
           }
-          if (lane == 0) {
-            if (use > 0 && !mbar_wait(empty, (use - 1) & 1, p.status, kWaitLimitNs,
-                                      rope ? SITE_W_RE : SITE_W_PE)) {
-              s_abort[0] = 1;
-            }
-            if (!vload(s_abort)) mbar_expect_tx(full, rope ? CHUNK : PAIR);
-          }
-          __syncwarp();
+          if (use > 0 && !mbar_wait(empty, (use - 1) & 1, p.status, kWaitLimitNs,
+                                    rope ? SITE_W_RE : SITE_W_PE))
+            s_abort[0] = 1;
           if (vload(s_abort)) { ok = false; break; }
-          if (rope) {
-            last_rope_use[slot] = use;
-            if (lane < 16) {
-              const int* r = rows + kb + 4 * lane;
-              tma_gather4(dst + lane * 512, &tm_kv, full, 512, r[0], r[1], r[2], r[3]);
+          const uint32_t dbase = smem_u32(dst);
+          const int nunits = rope ? 4 : 8;  // per thread
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (i < nunits) {
+              const int u = ptid + NPROD * i;
+              const int ln = u & 31, grp = u >> 5;
+              const int h2 = grp >> 4, kg = grp & 15;
+              const int key = kg * 4 + (ln >> 3), unit = ln & 7;
+              const int c = rope ? 8 : 2 * pr + h2;
+              const uint16_t* src =
+                  p.kv + static_cast<int64_t>(rows[kb + key]) * kRlat + c * 64 + unit * 8;
+              cp_async_16(dbase + h2 * CHUNK + sw128_unit(key, unit), src);
             }
-          } else {
-            last_pair_use[slot] = use;
-            const int c = 2 * pr + (lane >> 4);
-            const int g4 = lane & 15;
-            const int* r = rows + kb + 4 * g4;
-            tma_gather4(dst + (lane >> 4) * CHUNK + g4 * 512, &tm_kv, full, 64 * c, r[0], r[1],
-                        r[2], r[3]);
           }
+          cp_async_arrive(full);
         }
       }
-      // drain: every fill this warp issued has landed before the CTA may exit
-      if (lane == 0) {
-        for (int k = 0; k < NPAIR; ++k)
-          if (last_pair_use[k] != 0xffffffffu)
-            mbar_wait(&bars[B_PF + k], last_pair_use[k] & 1, p.status, kWaitLimitNs, SITE_W_PF);
-        for (int k = 0; k < NROPE; ++k)
-          if (last_rope_use[k] != 0xffffffffu)
-            mbar_wait(&bars[B_RF + k], last_rope_use[k] & 1, p.status, kWaitLimitNs, SITE_W_RF);
-      }
+      // every copy this thread issued has landed before the CTA may exit
+      asm volatile("cp.async.wait_all;" ::: "memory");
     }
-  } else if (warp == 1) {
+  } else if (warp == MMA_WARP) {
     // ============================ MMA issuer =================================
     if (nb > 0 && lane == 0) {
       const uint32_t q_base = smem_u32(sm + OFF_Q);
@@ -290,6 +282,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int slot = g % NPAIR;
         if (!mbar_wait(&bars[B_PF + slot], (g / NPAIR) & 1, p.status, kWaitLimitNs, SITE_W_PF))
           return false;
+        fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tensor core reads
         tc_fence_after();
         const uint32_t sb = smem_u32(sm + OFF_PAIR + slot * PAIR);
 #pragma unroll
@@ -336,6 +329,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int rs = jj % NROPE;
           if (!mbar_wait(&bars[B_RF + rs], (jj / NROPE) & 1, p.status, kWaitLimitNs,
                          SITE_W_RF)) { ok = false; break; }
+          fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t rb = smem_u32(sm + OFF_ROPE + rs * CHUNK);
 #pragma unroll
@@ -359,7 +353,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     __syncwarp();
   } else {
-    // ====================== softmax + epilogue (warps 2..5) ====================
+    // ====================== softmax + epilogue (warps 5..8) ====================
     const int sub = warp & 3;             // TMEM lane quarter this warp may access
     const int h = sub * 32 + lane;        // head owned in the softmax
     const uint32_t lane_base = static_cast<uint32_t>(sub * 32) << 16;
@@ -458,7 +452,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       named_bar_sync(1, 128);
-      if (tid == 64) s_resc[jj & 1] = 0;  // reused two blocks later, after two barriers
+      if (warp == MMA_WARP + 1 && lane == 0) s_resc[jj & 1] = 0;  // reused two blocks later, after two barriers
       mbar_arrive(&bars[B_P]);
     }
     // ------------------------------ epilogue ---------------------------------
@@ -522,7 +516,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -586,14 +580,13 @@ size_t sparse_mla_scratch_bytes(int B, int Tq, int H, int topk) {
 template <int H>
 static dsa_status_t launch_h(const SparseMlaArgs& a, cudaStream_t stream) {
   using namespace mla;
-  CUtensorMap tq, tkv;
+  CUtensorMap tq;
   const uint64_t qrows = static_cast<uint64_t>(a.B) * a.Tq * H;
   if (!encode_tmap_2d(&tq, a.q_lat, qrows, kRlat, kRlat * 2, 64, H, true))
     return DSA_ERR_CUDA;
-  if (!encode_tmap_2d(&tkv, a.kv.base, a.kv.total_rows, kRlat, kRlat * 2, 64, 1, true))
-    return DSA_ERR_CUDA;
   const int ns = mla_nsplit(a.B, a.Tq);
   Params p{};
+  p.kv = a.kv.base;
   p.idx = a.idx;
   p.q_start = a.q_start;
   p.kv_len = a.kv_len;
@@ -622,7 +615,7 @@ static dsa_status_t launch_h(const SparseMlaArgs& a, cudaStream_t stream) {
       cudaSuccess)
     return DSA_ERR_CUDA;
   const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(a.B) * a.Tq * ns);
-  kern<<<grid, NTHREADS, SMEM_BYTES, stream>>>(tq, tkv, p);
+  kern<<<grid, NTHREADS, SMEM_BYTES, stream>>>(tq, p);
   if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
   if (ns > 1) {
     const int64_t nq = static_cast<int64_t>(a.B) * a.Tq;
