@@ -47,9 +47,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Rasterise in groups of GT token tiles: a group's x tiles stay in L2 while
+  // the CTAs sweep every head pair, so W_g (176 MB at 96 heads x hidden 7168,
+  // larger than L2) is streamed from DRAM once per group instead of once per
+  // token tile.
+  constexpr int GT = 16;
   const int npair = p.H / 2;
-  const int hp = blockIdx.x % npair;       // head pair
-  const int n0 = (blockIdx.x / npair) * 128;
+  const int ntt = (p.N + 127) / 128;
+  const int grp = blockIdx.x / (GT * npair);
+  const int rem = blockIdx.x - grp * GT * npair;
+  const int gt = min(GT, ntt - grp * GT);
+  const int hp = rem / gt;                 // head pair
+  const int n0 = (grp * GT + rem % gt) * 128;
   const int kg = p.hid / 64;               // G stages
   const int nstage = kg + 16;              // + 8 U stages per head
 

@@ -30,7 +30,6 @@ namespace dsa {
 namespace idx {
 
 constexpr int BKEY = 128;  // keys per tile (MMA M)
-constexpr int NST = 2;     // key-tile stages
 constexpr int NEPI = 8;    // epilogue warps
 constexpr int NTHREADS = 64 + NEPI * 32;
 
@@ -41,9 +40,13 @@ enum : uint32_t {
 
 template <int H_I, int D_I>
 struct Cfg {
-  static constexpr int QT = (H_I >= 64) ? 256 / H_I : 16;  // queries per CTA
+  // Two queries per CTA at 64 heads (N = 128): fewer queries share the
+  // candidate space, so each buffer holds ~6K candidates and a query needs
+  // about two radix selections instead of five.
+  static constexpr int QT = (H_I >= 64) ? 128 / H_I : 16;  // queries per CTA
   static constexpr int N = QT * H_I;                          // MMA N
   static constexpr int NCH = D_I / 64;                        // 64-dim chunks
+  static constexpr int NST = 3;                               // key-tile stages
   static constexpr int Q_BYTES = NCH * N * 128;
   static constexpr int K_STAGE = NCH * BKEY * 128;
   static constexpr int OFF_Q = 0;
@@ -53,7 +56,8 @@ struct Cfg {
   static constexpr int MISC_BYTES = 4096;
   static constexpr int OFF_CAND = OFF_MISC + MISC_BYTES;
   static constexpr int AVAIL = 232448 - 1024 - OFF_CAND;
-  static constexpr int CAP = (AVAIL / (QT * 8)) / 32 * 32;  // candidates per query
+  static constexpr int CAP_RAW = (AVAIL / (QT * 8)) / 32 * 32;
+  static constexpr int CAP = CAP_RAW > 6144 ? 6144 : CAP_RAW;  // candidates per query
   static constexpr int SMEM_BYTES = OFF_CAND + QT * CAP * 8 + 1024;
   static constexpr int EPT = (CAP + NEPI * 32 - 1) / (NEPI * 32);  // candidates per thread in a select
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -169,7 +173,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                            ~static_cast<uintptr_t>(1023));
   float* w_s = reinterpret_cast<float*>(sm + C::OFF_W);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_MISC);  // 16 barriers
-  // B_Q 0, K full 1..2, K empty 3..4, D full 5..6, D empty 7..8, drain 9
+  // B_Q 0, K full 1..3, K empty 4..6, D full 7..8, D empty 9..10, drain 11
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
   volatile int* g_abort = s_abort + 1;   // [4]
@@ -210,7 +214,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   const int ntiles = (t_last + BKEY) / BKEY;
   if (tid == 0) {
-    for (int k = 0; k < 10; ++k) mbar_init(&bars[k], (k == 7 || k == 8) ? G : 1);
+    for (int k = 0; k < 12; ++k) mbar_init(&bars[k], (k == 9 || k == 10) ? G : 1);
     s_abort[0] = 0;
     for (int k = 0; k < 4; ++k) g_abort[k] = 0;
     fence_mbar_init();
@@ -236,7 +240,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (warp == 0) {
     // ============================ producer ===================================
-    int last_use[NST] = {-1, -1};
+    int last_use[C::NST];
+    for (int k = 0; k < C::NST; ++k) last_use[k] = -1;
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -245,8 +250,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
       for (int c = 0; c < NCH; ++c) tma_load_2d(sm + C::OFF_Q + c * N * 128, &tm_q, &bars[0], 64 * c, qrow);
       for (int kt = 0; kt < ntiles; ++kt) {
-        const int st = kt % NST, use = kt / NST;
-        if (use > 0 && !mbar_wait(&bars[3 + st], (use - 1) & 1, p.status, kWaitLimitNs, SITE_W_KE)) {
+        const int st = kt % C::NST, use = kt / C::NST;
+        if (use > 0 && !mbar_wait(&bars[4 + st], (use - 1) & 1, p.status, kWaitLimitNs, SITE_W_KE)) {
           s_abort[0] = 1;
           break;
         }
@@ -276,7 +281,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
       }
-      for (int st = 0; st < NST; ++st)
+      for (int st = 0; st < C::NST; ++st)
         if (last_use[st] >= 0) mbar_wait(&bars[1 + st], last_use[st] & 1, p.status, kWaitLimitNs, SITE_W_KF);
     }
     __syncwarp();
@@ -287,9 +292,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint32_t qb = smem_u32(sm + C::OFF_Q);
       for (int kt = 0; kt < ntiles && ok; ++kt) {
         if (vflag(s_abort)) { ok = false; break; }
-        const int st = kt % NST, buf = kt & 1;
-        if (kt >= 2 && !mbar_wait(&bars[7 + buf], ((kt >> 1) - 1) & 1, p.status, kWaitLimitNs, SITE_W_DE)) { ok = false; break; }
-        if (!mbar_wait(&bars[1 + st], (kt / NST) & 1, p.status, kWaitLimitNs, SITE_W_KF)) { ok = false; break; }
+        const int st = kt % C::NST, buf = kt & 1;
+        if (kt >= 2 && !mbar_wait(&bars[9 + buf], ((kt >> 1) - 1) & 1, p.status, kWaitLimitNs, SITE_W_DE)) { ok = false; break; }
+        if (!mbar_wait(&bars[1 + st], (kt / C::NST) & 1, p.status, kWaitLimitNs, SITE_W_KF)) { ok = false; break; }
         tc_fence_after();
         const uint32_t kb = smem_u32(sm + C::OFF_K + st * C::K_STAGE);
 #pragma unroll
@@ -298,12 +303,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int kk = 0; kk < 4; ++kk)
             umma_bf16(tmem + buf * 256, smem_desc(kb + c * BKEY * 128 + kk * 32, 16, 1024),
                       smem_desc(qb + c * N * 128 + kk * 32, 16, 1024), IDESC, (c | kk) ? 1u : 0u);
-        umma_commit(&bars[3 + st]);
-        umma_commit(&bars[5 + buf]);
+        umma_commit(&bars[4 + st]);
+        umma_commit(&bars[7 + buf]);
       }
       if (!ok) s_abort[0] = 1;
-      umma_commit(&bars[9]);
-      mbar_wait(&bars[9], 0, p.status, kWaitLimitNs, SITE_W_DRAIN);
+      umma_commit(&bars[11]);
+      mbar_wait(&bars[11], 0, p.status, kWaitLimitNs, SITE_W_DRAIN);
     }
     __syncwarp();
   } else {
@@ -316,7 +321,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int key_lane = sub * 32 + lane;
     for (int kt = 0; kt < ntiles; ++kt) {
       const int buf = kt & 1;
-      const bool w_ok = mbar_wait(&bars[5 + buf], (kt >> 1) & 1, p.status, kWaitLimitNs, SITE_W_DF);
+      const bool w_ok = mbar_wait(&bars[7 + buf], (kt >> 1) & 1, p.status, kWaitLimitNs, SITE_W_DF);
       if (!w_ok || vflag(s_abort)) g_abort[(kt & 1) * 2] = 1;
       named_bar_sync(1, G);
       if (vflag(&g_abort[(kt & 1) * 2])) break;
@@ -340,7 +345,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&bars[7 + buf]);
+      mbar_arrive(&bars[9 + buf]);
       // append candidates above each query's threshold
       const int s = kt * BKEY + key_lane;
 #pragma unroll

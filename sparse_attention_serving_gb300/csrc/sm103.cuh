@@ -77,7 +77,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_test(bar, parity)) return true;
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_test(bar, parity)) return true;
     if (globaltimer_ns() - t0 > limit_ns) {
       status_raise(status, DSA_ERR_DEVICE_TIMEOUT, where);
       return false;

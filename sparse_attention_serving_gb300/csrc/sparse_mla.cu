@@ -6,22 +6,33 @@
 //   z_s  = scale * q_lat[t,h,:] . KV[s,:]          over the 576-wide rows s in idx[t]
 //   o    = sum_s softmax(z)_s * KV[s, 0:512],       lse = log sum_s exp(z_s)
 //
-// One CTA per query (or per query x key-split for small batches):
+// One CTA per query (or per query x key-split for small batches), blocks of 64
+// list entries:
 //   warps 0-3   producer: TMA load of the query's 96x576 q_lat block; 16-byte
-//               cp.async gather of the selected rows, 64 keys per block, into a
-//               ring of 16 KB "pair" slots (two 64-dim chunks, dims 0..511) and
-//               8 KB "rope" slots (dims 512..575), 128-byte swizzled.  (TMA
+//               cp.async gather of the selected rows into a ring of six 16 KB
+//               "pair" slots (two 64-dim chunks, dims 0..511) and one 8 KB
+//               "rope" slot (dims 512..575), 128-byte swizzled.  Each thread
+//               copies one 16-byte unit of four fixed keys, so its shared and
+//               global addresses are computed once per block.  (TMA
 //               tile::gather4 moves these 1,152-byte rows about 4x slower.)
 //   warp 4      tcgen05 issuer (one lane):
 //                 S  [128 x 64]  = Q [128(96 heads) x 576] . KV_blk^T   (M=128, N=64)
 //                 O^T[512 x 96] += V_blk^T [512 x 64] . P^T [64 x 96]   (4 x M=128, N=96)
 //               S double-buffered in TMEM columns 384..511, O^T in 0..383.
-//   warps 5-8   softmax (one lane per head; the row max and sum stay in the
-//               thread), write P^T as BF16 into shared memory, then the
-//               epilogue (O^T / l -> BF16 o_lat, lse).
+//               With six pair slots, the first two pairs and the rope chunk of
+//               block j+1 are multiplied while the softmax of block j runs.
+//   warps 5-8   softmax (one lane per head; row max and sum stay in the
+//               thread; one named barrier per block), P^T written as BF16,
+//               then the epilogue (O^T / l staged through shared memory into
+//               coalesced BF16 rows of o_lat, and lse).
 // Q rows 96..127 of the M=128 operand alias the next 64-dim chunk of Q (or the
 // P^T buffer after the last chunk): they only feed accumulator rows no thread
 // reads, so 96 heads cost 108 KB of shared memory instead of 144 KB.
+//
+// The index list is not compacted: a block covers 64 consecutive list entries
+// and entries that are -1 (or invalid, which is also flagged) are masked out
+// of the softmax.  Blocks run up to the last valid entry, so a list with its
+// valid entries first (as dsa_indexer_topk writes it) wastes no work.
 #include <cmath>
 
 #include <cuda_bf16.h>
@@ -32,11 +43,10 @@
 namespace dsa {
 namespace mla {
 
-constexpr int BK = 64;                    // keys per block
+constexpr int BK = 64;                    // list entries (keys) per block
 constexpr int CHUNK = BK * 128;           // 64 keys x 64 dims x 2 B
 constexpr int PAIR = 2 * CHUNK;
-constexpr int NPAIR = 5;                  // pair slots (a block uses 4)
-constexpr int NROPE = 2;                  // rope slots (a block uses 1)
+constexpr int NPAIR = 6;                  // pair slots (a block uses 4)
 constexpr int MAX_TOPK = 2048;
 constexpr int OFF_Q = 0;
 constexpr int Q_BYTES = 9 * 96 * 128;     // 110592
@@ -44,30 +54,30 @@ constexpr int OFF_P = OFF_Q + Q_BYTES;    // P^T, up to 96 rows x 128 B
 constexpr int P_BYTES = 96 * 128;
 constexpr int OFF_PAIR = OFF_P + P_BYTES;
 constexpr int OFF_ROPE = OFF_PAIR + NPAIR * PAIR;
-constexpr int OFF_ROWS = OFF_ROPE + NROPE * CHUNK;
-constexpr int OFF_MISC = OFF_ROWS + MAX_TOPK * 4;
+constexpr int OFF_MISC = OFF_ROPE + CHUNK;
 constexpr int MISC_BYTES = 2048;
 constexpr int SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-constexpr int NPROD = 128;                 // producer threads (warps 0-3)
-constexpr int MMA_WARP = NPROD / 32;       // warp 4
-constexpr int NTHREADS = NPROD + 32 + 128; // + MMA warp + 4 softmax warps
+constexpr int NPROD = 128;                  // producer threads (warps 0-3)
+constexpr int MMA_WARP = NPROD / 32;        // warp 4
+constexpr int SMX_WARP0 = MMA_WARP + 1;     // warps 5-8
+constexpr int NTHREADS = NPROD + 32 + 128;
 constexpr uint32_t S_COL = 384;
 
 // barrier indices
 enum {
   B_Q = 0,
-  B_PF = 1,   // pair full [5]
-  B_PE = 6,   // pair empty [5]
-  B_RF = 11,  // rope full [2]
-  B_RE = 13,  // rope empty [2]
-  B_SF = 15,  // S full [2]
-  B_SE = 17,  // S empty [2]
-  B_P = 19,   // P^T written (and O^T rescaled)
-  B_O = 20,   // O^T accumulated for a block
-  B_DRAIN = 21,
-  NBAR = 22
+  B_PF = 1,             // pair full [6]
+  B_PE = B_PF + NPAIR,  // pair empty [6]
+  B_RF = B_PE + NPAIR,  // rope full
+  B_RE = B_RF + 1,      // rope empty
+  B_SF = B_RE + 1,      // S full [2]
+  B_SE = B_SF + 2,      // S empty [2]
+  B_P = B_SE + 2,       // P^T written (and O^T rescaled)
+  B_O = B_P + 1,        // O^T accumulated for a block
+  B_DRAIN = B_O + 1,
+  NBAR = B_DRAIN + 1
 };
 
 // status site tags
@@ -98,10 +108,29 @@ struct Params {
 
 __device__ __forceinline__ bool vload(const volatile int* p) { return *p != 0; }
 
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Physical row of list entry s for the query at position t of sequence b, or
+// -1 when the entry is unused (-1) or invalid (not causal, page outside the pool).
+__device__ __forceinline__ int entry_row(const Params& p, int b, int t, int s) {
+  if (s < 0 || s > t) return -1;
+  if (p.paged) {
+    const int pg = s >> 6;
+    const int pid =
+        pg < p.max_pages ? __ldg(p.block_table + static_cast<int64_t>(b) * p.max_pages + pg) : -1;
+    if (pid < 0 || pid >= p.num_pages) return -1;
+    return pid * kPage + (s & (kPage - 1));
+  }
+  return static_cast<int>(static_cast<int64_t>(b) * p.seq_stride + s);
+}
+
 template <int H>
 __global__ void __launch_bounds__(NTHREADS, 1)
-    sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q,
-                      const Params p) {
+    sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const Params p) {
   constexpr int HN = (H + 15) / 16 * 16;  // N of the PV product
   constexpr int QRS = H * 128;            // bytes of one 64-dim chunk of Q
   constexpr uint32_t IDESC_S = idesc_bf16(128, BK, false, false);
@@ -111,16 +140,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_MISC);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 24);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
-  volatile int* g_abort = s_abort + 1;      // [4] softmax-group abort, by iteration parity x checkpoint
-  volatile int* s_resc = s_abort + 5;       // [2] any head needs O^T rescale, by parity
-  int* s_nvalid = const_cast<int*>(s_abort + 7);
-  int* s_wsum = s_nvalid + 1;               // [16]
-  float* s_alpha = reinterpret_cast<float*>(s_wsum + 16);  // [128]
-  float* s_invl = s_alpha + 128;                          // [128]
-  int32_t* rows = reinterpret_cast<int32_t*>(sm + OFF_ROWS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_MISC);           // NBAR (< 32)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_MISC + 256);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + OFF_MISC + 260);
+  volatile int* g_abort = s_abort + 1;  // [3] softmax-group abort, by iteration mod 3
+  volatile int* s_resc = s_abort + 4;   // [3] some head needs an O^T rescale, by iteration mod 3
+  int* s_red = reinterpret_cast<int*>(sm + OFF_MISC + 320);               // [16]
+  float* s_alpha = reinterpret_cast<float*>(sm + OFF_MISC + 384);         // [2][128]
+  float* s_invl = reinterpret_cast<float*>(sm + OFF_MISC + 384 + 1024);   // [128]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qflat = blockIdx.x / p.nsplit, sp = blockIdx.x % p.nsplit;
@@ -130,12 +157,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int k = 0; k < NBAR; ++k) {
       uint32_t cnt = 1;
       if (k == B_SE || k == B_SE + 1 || k == B_P) cnt = 128;
-      if ((k >= B_PF && k < B_PF + NPAIR) || (k >= B_RF && k < B_RF + NROPE)) cnt = NPROD;
+      if ((k >= B_PF && k < B_PF + NPAIR) || k == B_RF) cnt = NPROD;
       mbar_init(&bars[k], cnt);
     }
     s_abort[0] = 0;
-    for (int k = 0; k < 4; ++k) g_abort[k] = 0;
-    s_resc[0] = 0; s_resc[1] = 0;
+    for (int k = 0; k < 3; ++k) { g_abort[k] = 0; s_resc[k] = 0; }
     fence_mbar_init();
   }
   if (warp == MMA_WARP) {
@@ -143,125 +169,112 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tmem_relinquish();
   }
 
-  // ---- validate and compact the query's index list (stable order) ----------
+  // ---- validate the index list; find the last valid entry ------------------
   const int t = __ldg(p.q_start + b) + qi;
   const int L = __ldg(p.kv_len + b);
   const bool q_ok = t >= 0 && t < L && L <= p.max_kv_len;
   if (!q_ok && tid == 0) status_raise(p.status, DSA_ERR_BAD_INDEX, SITE_QPOS, (uint32_t)t);
-  constexpr int MAXPER = (MAX_TOPK + NTHREADS - 1) / NTHREADS;
-  const int per = (p.topk + NTHREADS - 1) / NTHREADS;
   const int32_t* ix = p.idx + static_cast<int64_t>(qflat) * p.topk;
-  int loc[MAXPER];
-  int cnt = 0;
-#pragma unroll
-  for (int u = 0; u < MAXPER; ++u) {
-    loc[u] = -1;
-    const int e = tid * per + u;
-    if (u < per && e < p.topk && q_ok) {
+  int last = -1;
+  if (q_ok) {
+    for (int e = tid; e < p.topk; e += NTHREADS) {
       const int s = __ldg(ix + e);
-      if (s >= 0) {
-        if (s > t) {
-          status_raise(p.status, DSA_ERR_BAD_INDEX, SITE_IDX, (uint32_t)s);
-        } else if (p.paged) {
-          const int pg = s >> 6;
-          const int pid = pg < p.max_pages
-                              ? __ldg(p.block_table + static_cast<int64_t>(b) * p.max_pages + pg)
-                              : -1;
-          if (pid < 0 || pid >= p.num_pages)
-            status_raise(p.status, DSA_ERR_BAD_INDEX, SITE_PAGE, (uint32_t)pid);
-          else
-            loc[u] = pid * kPage + (s & (kPage - 1));
-        } else {
-          loc[u] = static_cast<int>(static_cast<int64_t>(b) * p.seq_stride + s);
-        }
+      if (s < 0) continue;
+      if (entry_row(p, b, t, s) >= 0) {
+        last = e;
+      } else if (sp == 0) {
+        status_raise(p.status, DSA_ERR_BAD_INDEX, s > t ? SITE_IDX : SITE_PAGE, (uint32_t)s);
       }
     }
-    cnt += loc[u] >= 0 ? 1 : 0;
   }
-  int incl = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) s_wsum[warp] = incl;
+  last = __reduce_max_sync(0xffffffffu, last);
+  if (lane == 0) s_red[warp] = last;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  int off = incl - cnt;
-  int n_valid = 0;
-  for (int w = 0; w < NTHREADS / 32; ++w) {
-    if (w < warp) off += s_wsum[w];
-    n_valid += s_wsum[w];
-  }
-#pragma unroll
-  for (int u = 0; u < MAXPER; ++u)
-    if (loc[u] >= 0) rows[off++] = loc[u];
-  __syncthreads();
-  const int nb_total = (n_valid + BK - 1) / BK;
-  for (int e = n_valid + tid; e < nb_total * BK; e += NTHREADS) rows[e] = rows[0];
+  int n_list = -1;
+  for (int w = 0; w < NTHREADS / 32; ++w) n_list = max(n_list, s_red[w]);
+  n_list += 1;  // entries [0, n_list) hold every valid key
+  const int nb_total = (n_list + BK - 1) / BK;
   const int bps = (nb_total + p.nsplit - 1) / p.nsplit;
   const int blk0 = min(sp * bps, nb_total);
   const int nb = min(nb_total, blk0 + bps) - blk0;
-  __syncthreads();
   const uint32_t tmem = *tslot;
+  // a valid physical row to read in place of unused entries (masked later)
+  const int dummy_row = p.paged ? 0 : static_cast<int>(static_cast<int64_t>(b) * p.seq_stride);
 
   if (warp < NPROD / 32) {
     // ====================== producer (4 warps, cp.async) ======================
-    // Each 16-byte unit of a selected row is copied by one thread straight into
-    // its 128-byte-swizzled place; a warp covers 4 keys x 8 units of one 64-dim
-    // chunk (4 x 128 contiguous bytes of global memory).
-    const int ptid = tid;  // 0..127
+    // thread: 16-byte unit u = lane & 7 of keys 4w + (lane >> 3) + 16i, i = 0..3
+    const int w = warp, unit = lane & 7;
+    int key[4];
+    uint32_t doff[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      key[i] = 4 * w + (lane >> 3) + 16 * i;
+      doff[i] = sw128_unit(key[i], unit);
+    }
     if (nb > 0) {
-      if (ptid == 0) {
+      if (tid == 0) {
         tma_prefetch_desc(&tm_q);
         mbar_expect_tx(&bars[B_Q], 9u * H * 128u);
 #pragma unroll 1
         for (int c = 0; c < 9; ++c)
           tma_load_2d(sm + OFF_Q + c * QRS, &tm_q, &bars[B_Q], 64 * c, qflat * H);
       }
+      // raw list entries of the next block, fetched one block ahead
+      int s_next[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e = blk0 * BK + key[i];
+        s_next[i] = e < n_list ? __ldg(ix + e) : -1;
+      }
       bool ok = true;
       for (int jj = 0; jj < nb && ok; ++jj) {
-        const int kb = (blk0 + jj) * BK;  // first list entry of the block
-        // parts in the order the MMA consumes them: pair 0, rope, pair 1..3
+        const uint16_t* src[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = entry_row(p, b, t, s_next[i]);
+          src[i] = p.kv + static_cast<int64_t>(r >= 0 ? r : dummy_row) * kRlat + unit * 8;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int e = (blk0 + jj + 1) * BK + key[i];
+          s_next[i] = (jj + 1 < nb && e < n_list) ? __ldg(ix + e) : -1;
+        }
+        // parts in the order the MMA consumes them: pair 0, pair 1, rope, pair 2, pair 3
         for (int part = 0; part < 5; ++part) {
-          const bool rope = part == 1;
-          const int pr = part == 0 ? 0 : part - 1;  // pair index 0..3
+          const bool rope = part == 2;
+          const int pr = part < 2 ? part : part - 1;  // pair index 0..3
           uint64_t *full, *empty;
           uint32_t use;
-          uint8_t* dst;
+          uint32_t dbase;
           if (rope) {
-            const int slot = jj % NROPE;
-            use = jj / NROPE;
-            full = &bars[B_RF + slot];
-            empty = &bars[B_RE + slot];
-            dst = sm + OFF_ROPE + slot * CHUNK;
+            use = jj;
+            full = &bars[B_RF];
+            empty = &bars[B_RE];
+            dbase = smem_u32(sm + OFF_ROPE);
           } else {
             const uint32_t g = 4u * jj + pr;
             const int slot = g % NPAIR;
             use = g / NPAIR;
             full = &bars[B_PF + slot];
             empty = &bars[B_PE + slot];
-            dst = sm + OFF_PAIR + slot * PAIR;
+            dbase = smem_u32(sm + OFF_PAIR + slot * PAIR);
           }
           if (use > 0 && !mbar_wait(empty, (use - 1) & 1, p.status, kWaitLimitNs,
                                     rope ? SITE_W_RE : SITE_W_PE))
             s_abort[0] = 1;
           if (vload(s_abort)) { ok = false; break; }
-          const uint32_t dbase = smem_u32(dst);
-          const int nunits = rope ? 4 : 8;  // per thread
+          if (rope) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (i < nunits) {
-              const int u = ptid + NPROD * i;
-              const int ln = u & 31, grp = u >> 5;
-              const int h2 = grp >> 4, kg = grp & 15;
-              const int key = kg * 4 + (ln >> 3), unit = ln & 7;
-              const int c = rope ? 8 : 2 * pr + h2;
-              const uint16_t* src =
-                  p.kv + static_cast<int64_t>(rows[kb + key]) * kRlat + c * 64 + unit * 8;
-              cp_async_16(dbase + h2 * CHUNK + sw128_unit(key, unit), src);
-            }
+            for (int i = 0; i < 4; ++i) cp_async_16(dbase + doff[i], src[i] + 8 * 64);
+          } else {
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                cp_async_16(dbase + h2 * CHUNK + doff[i], src[i] + (2 * pr + h2) * 64);
           }
           cp_async_arrive(full);
         }
@@ -324,25 +337,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                        SITE_W_SE)) { ok = false; break; }
         tc_fence_after();
         bool first = true;
-        if (!s_pair(jj, 0, d, first)) { ok = false; break; }
+        if (!s_pair(jj, 0, d, first) || !s_pair(jj, 1, d, first)) { ok = false; break; }
         {  // rope chunk
-          const int rs = jj % NROPE;
-          if (!mbar_wait(&bars[B_RF + rs], (jj / NROPE) & 1, p.status, kWaitLimitNs,
-                         SITE_W_RF)) { ok = false; break; }
+          if (!mbar_wait(&bars[B_RF], jj & 1, p.status, kWaitLimitNs, SITE_W_RF)) {
+            ok = false;
+            break;
+          }
           fence_proxy_async_smem();
           tc_fence_after();
-          const uint32_t rb = smem_u32(sm + OFF_ROPE + rs * CHUNK);
+          const uint32_t rb = smem_u32(sm + OFF_ROPE);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             umma_bf16(d, smem_desc(q_base + 8 * QRS + kk * 32, 16, 1024),
                       smem_desc(rb + kk * 32, 16, 1024), IDESC_S, 1u);
-          umma_commit(&bars[B_RE + rs]);
+          umma_commit(&bars[B_RE]);
         }
         if (jj >= 1 && !pv(jj - 1)) { ok = false; break; }
-        if (!s_pair(jj, 1, d, first) || !s_pair(jj, 2, d, first) || !s_pair(jj, 3, d, first)) {
-          ok = false;
-          break;
-        }
+        if (!s_pair(jj, 2, d, first) || !s_pair(jj, 3, d, first)) { ok = false; break; }
         umma_commit(&bars[B_SF + sbuf]);
       }
       if (ok && !vload(s_abort)) ok = pv(nb - 1);
@@ -356,69 +367,86 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ====================== softmax + epilogue (warps 5..8) ====================
     const int sub = warp & 3;             // TMEM lane quarter this warp may access
     const int h = sub * 32 + lane;        // head owned in the softmax
+    const int gt = tid - SMX_WARP0 * 32;  // 0..127 within the group
     const uint32_t lane_base = static_cast<uint32_t>(sub * 32) << 16;
     // l_sum: sum of the BF16-rounded P fed to the PV product (normalises O);
     // l_exact: the unrounded sum (log-sum-exp)
     float m_ref = -INFINITY, l_sum = 0.f, l_exact = 0.f;
     bool ok = true;
-    uint8_t* prow = sm + OFF_P;
+    uint8_t* prow = sm + OFF_P + (h >> 3) * 1024 + (h & 7) * 128;
+    // validity of list entries kb + lane and kb + 32 + lane, fetched one block ahead
+    int e_lo = -1, e_hi = -1;
+    if (nb > 0) {
+      const int kb = blk0 * BK;
+      e_lo = kb + lane < n_list ? __ldg(ix + kb + lane) : -1;
+      e_hi = kb + 32 + lane < n_list ? __ldg(ix + kb + 32 + lane) : -1;
+    }
     for (int jj = 0; jj < nb; ++jj) {
-      const int sbuf = jj & 1;
+      const int sbuf = jj & 1, k3 = jj % 3;
+      const uint32_t m_lo = __ballot_sync(0xffffffffu, entry_row(p, b, t, e_lo) >= 0);
+      const uint32_t m_hi = __ballot_sync(0xffffffffu, entry_row(p, b, t, e_hi) >= 0);
+      if (jj + 1 < nb) {
+        const int kb = (blk0 + jj + 1) * BK;
+        e_lo = kb + lane < n_list ? __ldg(ix + kb + lane) : -1;
+        e_hi = kb + 32 + lane < n_list ? __ldg(ix + kb + 32 + lane) : -1;
+      }
       bool w_ok = mbar_wait(&bars[B_SF + sbuf], (jj >> 1) & 1, p.status, kWaitLimitNs, SITE_W_SF);
-      if (!w_ok || vload(s_abort)) { g_abort[(jj & 1) * 2] = 1; }
-      named_bar_sync(1, 128);
-      if (vload(&g_abort[(jj & 1) * 2])) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[64];
-      {
+      if (w_ok) {
         uint32_t(&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
         uint32_t(&c)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
         tmem_ld32(tmem + lane_base + S_COL + BK * sbuf, a);
         tmem_ld32(tmem + lane_base + S_COL + BK * sbuf + 32, c);
+        tmem_ld_wait();
       }
-      tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&bars[B_SE + sbuf]);
-      const int kb = (blk0 + jj) * BK;
-      const int nvk = min(BK, n_valid - kb);
-      float z[64];
-      float mb = -INFINITY;
+      // block max over valid keys (raw logits; the scale is positive)
+      float mx[8];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) mx[g] = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        z[c] = c < nvk ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
-        mb = fmaxf(mb, z[c]);
+        const bool v = ((c < 32 ? m_lo >> c : m_hi >> (c - 32)) & 1u) != 0;
+        const float x = __uint_as_float(sr[c]);
+        mx[c & 7] = v ? fmaxf(mx[c & 7], x) : mx[c & 7];
       }
+      const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float mb2 = mb * p.scale_log2;
       // lazy reference max: keep the current one unless this block exceeds it by
       // more than 2^64; P = 2^(z - m_ref) then stays far inside the FP32/BF16 range
-      float m_new = m_ref;
-      if (mb > m_ref + 64.f) m_new = mb;
-      const float alpha = (m_new == m_ref) ? 1.f : exp2f(m_ref - m_new);
-      l_sum *= alpha;
-      l_exact *= alpha;
+      const float m_new = (mb2 > m_ref + 64.f) ? mb2 : m_ref;
+      const float alpha = (m_new == m_ref) ? 1.f : ex2(m_ref - m_new);
+      const float neg_m = -m_new;
       uint32_t pk[32];
-      float lsum_blk = 0.f, lex_blk = 0.f;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f}, le[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
-        const float p0 = exp2f(z[c] - m_new), p1 = exp2f(z[c + 1] - m_new);
-        const uint32_t v = pack_bf16x2(p0, p1);
-        pk[c >> 1] = v;
-        lsum_blk += __uint_as_float(v << 16) + __uint_as_float(v & 0xffff0000u);
-        lex_blk += p0 + p1;
+        const bool v0 = ((c < 32 ? m_lo >> c : m_hi >> (c - 32)) & 1u) != 0;
+        const bool v1 = ((c + 1 < 32 ? m_lo >> (c + 1) : m_hi >> (c - 31)) & 1u) != 0;
+        const float p0 = v0 ? ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, neg_m)) : 0.f;
+        const float p1 = v1 ? ex2(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, neg_m)) : 0.f;
+        const uint32_t pv2 = pack_bf16x2(p0, p1);
+        pk[c >> 1] = pv2;
+        ls[(c >> 1) & 3] += __uint_as_float(pv2 << 16) + __uint_as_float(pv2 & 0xffff0000u);
+        le[(c >> 1) & 3] += p0 + p1;
       }
-      l_sum += lsum_blk;
-      l_exact += lex_blk;
+      l_sum = l_sum * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+      l_exact = l_exact * alpha + ((le[0] + le[1]) + (le[2] + le[3]));
       m_ref = m_new;
       // P^T buffer and O^T are free once the previous block's PV product is done
-      if (jj >= 1) {
+      if (jj >= 1 && w_ok)
         w_ok = mbar_wait(&bars[B_O], (jj - 1) & 1, p.status, kWaitLimitNs, SITE_W_O);
-        if (!w_ok || vload(s_abort)) g_abort[(jj & 1) * 2 + 1] = 1;
-      }
-      s_alpha[h] = alpha;
-      if (jj >= 1 && h < H && alpha != 1.f) s_resc[jj & 1] = 1;
+      s_alpha[sbuf * 128 + h] = alpha;
+      if (jj >= 1 && h < H && alpha != 1.f) s_resc[k3] = 1;
+      if (!w_ok || vload(s_abort)) g_abort[k3] = 1;
       named_bar_sync(1, 128);
-      if (vload(&g_abort[(jj & 1) * 2 + 1])) { ok = false; break; }
+      if (vload(&g_abort[k3])) { ok = false; break; }
+      if (gt == 0) s_resc[(jj + 2) % 3] = 0;  // its readers (iteration jj-1) are all past this barrier
       tc_fence_after();
-      if (vload(&s_resc[jj & 1])) {
+      if (vload(&s_resc[k3])) {
         // rare: rescale every O^T column by its head's alpha
 #pragma unroll 1
         for (int i = 0; i < 4; ++i) {
@@ -430,15 +458,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              r[e] = __float_as_uint(__uint_as_float(r[e]) * s_alpha[c0 + e]);
+              r[e] = __float_as_uint(__uint_as_float(r[e]) * s_alpha[sbuf * 128 + c0 + e]);
             tmem_st16(ta, r);
           }
         }
         tmem_st_wait();
       }
-      // write this head's row of P^T (K-major: row = head, 64 keys = 128 B)
+      // this head's row of P^T (K-major: row = head, 64 keys = 128 B)
       if (h < HN) {
-        uint8_t* row = prow + (h >> 3) * 1024 + (h & 7) * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           uint4 v;
@@ -446,72 +473,76 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             v = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
           else
             v = make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(row + (((u ^ h) & 7) << 4)) = v;
+          *reinterpret_cast<uint4*>(prow + (((u ^ h) & 7) << 4)) = v;
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      named_bar_sync(1, 128);
-      if (warp == MMA_WARP + 1 && lane == 0) s_resc[jj & 1] = 0;  // reused two blocks later, after two barriers
       mbar_arrive(&bars[B_P]);
     }
     // ------------------------------ epilogue ---------------------------------
-    if (h < H) s_invl[h] = l_sum > 0.f ? 1.f / l_sum : 0.f;
-    float lse2 = (l_exact > 0.f) ? m_ref + log2f(l_exact) : -INFINITY;
+    if (h < 128) s_invl[h] = l_sum > 0.f ? 1.f / l_sum : 0.f;
+    const float lse2 = (l_exact > 0.f) ? m_ref + log2f(l_exact) : -INFINITY;
     bool have_o = ok && nb > 0;
-    if (have_o) {
-      const bool w_ok = mbar_wait(&bars[B_O], (nb - 1) & 1, p.status, kWaitLimitNs, SITE_W_O);
-      if (!w_ok) have_o = false;
-    }
+    if (have_o)
+      have_o = mbar_wait(&bars[B_O], (nb - 1) & 1, p.status, kWaitLimitNs, SITE_W_O);
+    if (!have_o) g_abort[0] = 1;  // sticky: every thread below writes zeros
     named_bar_sync(1, 128);
+    have_o = !vload(&g_abort[0]) && !vload(s_abort) && ok && nb > 0;
     tc_fence_after();
-    if (p.nsplit == 1) {
-      if (h < H && p.lse != nullptr)
-        p.lse[static_cast<int64_t>(qflat) * H + h] = have_o ? lse2 * 0.6931471805599453f : -INFINITY;
-      uint16_t* ob = p.o_lat + static_cast<int64_t>(qflat) * H * kVlat;
+    const int64_t pq = static_cast<int64_t>(qflat) * p.nsplit + sp;
+    if (h < H) {
+      if (p.nsplit == 1) {
+        if (p.lse != nullptr)
+          p.lse[static_cast<int64_t>(qflat) * H + h] = have_o ? lse2 * 0.6931471805599453f : -INFINITY;
+      } else {
+        p.part_lse[pq * H + h] = have_o ? lse2 : -INFINITY;
+      }
+    }
+    // O^T tile i (128 dims x H heads): each thread owns one dim, stages its
+    // H values into [head][128 dims] in the (now idle) pair slots, then the
+    // group writes whole 256-byte (BF16) or 512-byte (FP32) rows.
+    uint8_t* stage = sm + OFF_PAIR;
+    const int dloc = 32 * sub + lane;
 #pragma unroll 1
-      for (int i = 0; i < 4; ++i) {
-        const int dim = 128 * i + 32 * sub + lane;
+    for (int i = 0; i < 4; ++i) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < HN; c0 += 16) {
-          uint32_t r[16];
-          if (have_o) {
-            tmem_ld16(tmem + lane_base + i * HN + c0, r);
-            tmem_ld_wait();
-          }
+      for (int c0 = 0; c0 < HN; c0 += 16) {
+        uint32_t r[16];
+        if (have_o) {
+          tmem_ld16(tmem + lane_base + i * HN + c0, r);
+          tmem_ld_wait();
+        }
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int hh = c0 + e;
-            if (hh < H) {
-              const float v = have_o ? __uint_as_float(r[e]) * s_invl[hh] : 0.f;
-              ob[static_cast<int64_t>(hh) * kVlat + dim] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-            }
+        for (int e = 0; e < 16; ++e) {
+          const int hh = c0 + e;
+          if (hh < H) {
+            const float v = have_o ? __uint_as_float(r[e]) * s_invl[hh] : 0.f;
+            if (p.nsplit == 1)
+              reinterpret_cast<uint16_t*>(stage)[hh * 128 + dloc] =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(v));
+            else
+              reinterpret_cast<float*>(stage)[hh * 128 + dloc] = v;
           }
         }
       }
-    } else {
-      const int64_t pq = static_cast<int64_t>(qflat) * p.nsplit + sp;
-      if (h < H) p.part_lse[pq * H + h] = have_o ? lse2 : -INFINITY;
-      float* ob = p.part_o + pq * H * kVlat;
-#pragma unroll 1
-      for (int i = 0; i < 4; ++i) {
-        const int dim = 128 * i + 32 * sub + lane;
-#pragma unroll 1
-        for (int c0 = 0; c0 < HN; c0 += 16) {
-          uint32_t r[16];
-          if (have_o) {
-            tmem_ld16(tmem + lane_base + i * HN + c0, r);
-            tmem_ld_wait();
-          }
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int hh = c0 + e;
-            if (hh < H)
-              ob[static_cast<int64_t>(hh) * kVlat + dim] =
-                  have_o ? __uint_as_float(r[e]) * s_invl[hh] : 0.f;
-          }
+      named_bar_sync(1, 128);
+      if (p.nsplit == 1) {
+        uint16_t* ob = p.o_lat + static_cast<int64_t>(qflat) * H * kVlat + 128 * i;
+        for (int v = gt; v < H * 16; v += 128) {  // 16 x 16 B per head row
+          const int hh = v >> 4, q16 = v & 15;
+          *reinterpret_cast<uint4*>(ob + static_cast<int64_t>(hh) * kVlat + q16 * 8) =
+              reinterpret_cast<const uint4*>(stage)[hh * 16 + q16];
+        }
+      } else {
+        float* ob = p.part_o + pq * H * kVlat + 128 * i;
+        for (int v = gt; v < H * 32; v += 128) {  // 32 x 16 B per head row
+          const int hh = v >> 5, q16 = v & 31;
+          *reinterpret_cast<float4*>(ob + static_cast<int64_t>(hh) * kVlat + q16 * 4) =
+              reinterpret_cast<const float4*>(stage)[hh * 32 + q16];
         }
       }
+      named_bar_sync(1, 128);
     }
   }
   tc_fence_before();
