@@ -4,6 +4,8 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -54,6 +56,14 @@ int num_sms() {
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
     return 148;
   return n;
+}
+
+dsa_status_t launch_status(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) return DSA_OK;
+  if (std::getenv("DSA_VERBOSE") != nullptr)
+    std::fprintf(stderr, "libdsa: %s: %s\n", what, cudaGetErrorString(e));
+  return DSA_ERR_CUDA;
 }
 
 int indexer_prefill_max_topk(int H_I, int D_I);

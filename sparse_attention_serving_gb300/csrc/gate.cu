@@ -196,10 +196,10 @@ dsa_status_t gate_launch(const GateArgs& a, cudaStream_t stream) {
   Params p{a.N, a.hid, a.H, a.out, a.status};
   if (cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
       cudaSuccess)
-    return DSA_ERR_CUDA;
+    return launch_status("cudaFuncSetAttribute");
   const unsigned grid = static_cast<unsigned>(((a.N + 127) / 128) * (a.H / 2));
   gate_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(tx, twg, to, twu, p);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return launch_status("gate");
 }
 
 }  // namespace dsa

@@ -433,9 +433,9 @@ static dsa_status_t prefill_launch(const IndexerArgs& a, cudaStream_t stream) {
   auto kern = idx::indexer_prefill_kernel<H_I, D_I>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
       cudaSuccess)
-    return DSA_ERR_CUDA;
+    return launch_status("cudaFuncSetAttribute");
   kern<<<static_cast<unsigned>(a.B * p.ntq), idx::NTHREADS, C::SMEM_BYTES, stream>>>(tq, tk, p);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return launch_status("indexer_prefill");
 }
 
 int indexer_prefill_max_topk(int H_I, int D_I) {

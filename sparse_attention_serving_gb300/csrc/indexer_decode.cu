@@ -420,15 +420,15 @@ static dsa_status_t decode_launch(const IndexerArgs& a, cudaStream_t stream) {
   auto kern = idxd::decode_scores_kernel<H_I, D_I>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
       cudaSuccess)
-    return DSA_ERR_CUDA;
+    return launch_status("cudaFuncSetAttribute");
   const int max_items = a.B * ((a.max_kv_len + idxd::CH_TILES * idxd::BKEY - 1) /
                                (idxd::CH_TILES * idxd::BKEY));
   const int grid = max_items < num_sms() ? max_items : num_sms();
   kern<<<grid, idxd::NTHREADS, C::SMEM_BYTES, stream>>>(tq, tk, p);
-  if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+  if (launch_status("decode_scores_kernel") != DSA_OK) return DSA_ERR_CUDA;
   idxd::decode_select_kernel<<<a.B, 1024, 0, stream>>>(p.scores, a.kv_len, a.max_kv_len, a.topk,
                                                         a.out_idx);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return launch_status("indexer_decode");
 }
 
 dsa_status_t indexer_decode_launch(const IndexerArgs& a, cudaStream_t stream) {

@@ -79,4 +79,8 @@ dsa_status_t gate_launch(const GateArgs& a, cudaStream_t stream);
 
 int num_sms();
 
+// DSA_ERR_CUDA when the last launch failed (the CUDA error text goes to stderr
+// when the environment variable DSA_VERBOSE is set), else DSA_OK.
+dsa_status_t launch_status(const char* what);
+
 }  // namespace dsa

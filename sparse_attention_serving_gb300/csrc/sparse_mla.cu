@@ -21,8 +21,9 @@
 //               S double-buffered in TMEM columns 384..511, O^T in 0..383.
 //               With six pair slots, the first two pairs and the rope chunk of
 //               block j+1 are multiplied while the softmax of block j runs.
-//   warps 5-8   softmax (one lane per head; row max and sum stay in the
-//               thread; one named barrier per block), P^T written as BF16,
+//   warps 5-12  softmax (two warps per TMEM lane quarter: a thread owns one
+//               head and 32 of the block's 64 keys; row max and sums stay in
+//               the thread; one named barrier per block), P^T written as BF16,
 //               then the epilogue (O^T / l staged through shared memory into
 //               coalesced BF16 rows of o_lat, and lse).
 // Q rows 96..127 of the M=128 operand alias the next 64-dim chunk of Q (or the
@@ -61,8 +62,9 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 constexpr int NPROD = 128;                  // producer threads (warps 0-3)
 constexpr int MMA_WARP = NPROD / 32;        // warp 4
-constexpr int SMX_WARP0 = MMA_WARP + 1;     // warps 5-8
-constexpr int NTHREADS = NPROD + 32 + 128;
+constexpr int SMX_WARP0 = MMA_WARP + 1;     // warps 5-12
+constexpr int NSMX = 256;                   // softmax / epilogue threads
+constexpr int NTHREADS = NPROD + 32 + NSMX;
 constexpr uint32_t S_COL = 384;
 
 // barrier indices
@@ -147,7 +149,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   volatile int* s_resc = s_abort + 4;   // [3] some head needs an O^T rescale, by iteration mod 3
   int* s_red = reinterpret_cast<int*>(sm + OFF_MISC + 320);               // [16]
   float* s_alpha = reinterpret_cast<float*>(sm + OFF_MISC + 384);         // [2][128]
-  float* s_invl = reinterpret_cast<float*>(sm + OFF_MISC + 384 + 1024);   // [128]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qflat = blockIdx.x / p.nsplit, sp = blockIdx.x % p.nsplit;
@@ -156,13 +157,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (tid == 0) {
     for (int k = 0; k < NBAR; ++k) {
       uint32_t cnt = 1;
-      if (k == B_SE || k == B_SE + 1 || k == B_P) cnt = 128;
+      if (k == B_SE || k == B_SE + 1 || k == B_P) cnt = NSMX;
       if ((k >= B_PF && k < B_PF + NPAIR) || k == B_RF) cnt = NPROD;
       mbar_init(&bars[k], cnt);
     }
     s_abort[0] = 0;
     for (int k = 0; k < 3; ++k) { g_abort[k] = 0; s_resc[k] = 0; }
     fence_mbar_init();
+    // the query block does not depend on the index list: start it now
+    tma_prefetch_desc(&tm_q);
+    mbar_expect_tx(&bars[B_Q], 9u * H * 128u);
+#pragma unroll 1
+    for (int c = 0; c < 9; ++c)
+      tma_load_2d(sm + OFF_Q + c * QRS, &tm_q, &bars[B_Q], 64 * c, qflat * H);
   }
   if (warp == MMA_WARP) {
     tmem_alloc(tslot, 512);
@@ -214,14 +221,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       key[i] = 4 * w + (lane >> 3) + 16 * i;
       doff[i] = sw128_unit(key[i], unit);
     }
+    // the query block was requested at start-up; with no work it must still land
+    if (nb == 0 && tid == 0) mbar_wait(&bars[B_Q], 0, p.status, kWaitLimitNs, SITE_W_Q);
     if (nb > 0) {
-      if (tid == 0) {
-        tma_prefetch_desc(&tm_q);
-        mbar_expect_tx(&bars[B_Q], 9u * H * 128u);
-#pragma unroll 1
-        for (int c = 0; c < 9; ++c)
-          tma_load_2d(sm + OFF_Q + c * QRS, &tm_q, &bars[B_Q], 64 * c, qflat * H);
-      }
       // raw list entries of the next block, fetched one block ahead
       int s_next[4];
 #pragma unroll
@@ -364,17 +366,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     __syncwarp();
   } else {
-    // ====================== softmax + epilogue (warps 5..8) ====================
-    const int sub = warp & 3;             // TMEM lane quarter this warp may access
-    const int h = sub * 32 + lane;        // head owned in the softmax
-    const int gt = tid - SMX_WARP0 * 32;  // 0..127 within the group
+    // ================ softmax + epilogue (warps 5..12, 8 warps) ================
+    // Two warps per TMEM lane quarter: thread (half, h) owns head h and the
+    // keys 32*half .. 32*half+31 of each block.  Both halves take the block max
+    // over all 64 keys (cheap), so they agree on the reference without talking.
+    const int sub = warp & 3;                         // TMEM lane quarter
+    const int half = (warp - SMX_WARP0) >> 2;         // 0: keys 0-31, 1: keys 32-63
+    const int h = sub * 32 + lane;                    // head owned in the softmax
+    const int gt = tid - SMX_WARP0 * 32;              // 0..255 within the group
     const uint32_t lane_base = static_cast<uint32_t>(sub * 32) << 16;
     // l_sum: sum of the BF16-rounded P fed to the PV product (normalises O);
-    // l_exact: the unrounded sum (log-sum-exp)
+    // l_exact: the unrounded sum (log-sum-exp); both over this thread's keys
     float m_ref = -INFINITY, l_sum = 0.f, l_exact = 0.f;
     bool ok = true;
     uint8_t* prow = sm + OFF_P + (h >> 3) * 1024 + (h & 7) * 128;
-    // validity of list entries kb + lane and kb + 32 + lane, fetched one block ahead
+    // list entries kb + lane and kb + 32 + lane, fetched one block ahead
     int e_lo = -1, e_hi = -1;
     if (nb > 0) {
       const int kb = blk0 * BK;
@@ -392,25 +398,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       bool w_ok = mbar_wait(&bars[B_SF + sbuf], (jj >> 1) & 1, p.status, kWaitLimitNs, SITE_W_SF);
       tc_fence_after();
-      uint32_t sr[64];
+      // own 32 keys and the partner half's 32 (needed only for the block max)
+      uint32_t own[32], oth[32];
       if (w_ok) {
-        uint32_t(&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-        uint32_t(&c)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-        tmem_ld32(tmem + lane_base + S_COL + BK * sbuf, a);
-        tmem_ld32(tmem + lane_base + S_COL + BK * sbuf + 32, c);
+        tmem_ld32(tmem + lane_base + S_COL + BK * sbuf + 32 * half, own);
+        tmem_ld32(tmem + lane_base + S_COL + BK * sbuf + 32 * (1 - half), oth);
         tmem_ld_wait();
       }
       tc_fence_before();
       mbar_arrive(&bars[B_SE + sbuf]);
-      // block max over valid keys (raw logits; the scale is positive)
+      const uint32_t mine = half ? m_hi : m_lo;
+      const uint32_t other = half ? m_lo : m_hi;
+      // block max over all 64 valid keys (raw logits; the scale is positive)
       float mx[8];
 #pragma unroll
       for (int g = 0; g < 8; ++g) mx[g] = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const bool v = ((c < 32 ? m_lo >> c : m_hi >> (c - 32)) & 1u) != 0;
-        const float x = __uint_as_float(sr[c]);
-        mx[c & 7] = v ? fmaxf(mx[c & 7], x) : mx[c & 7];
+      for (int c = 0; c < 32; ++c) {
+        mx[c & 7] = ((mine >> c) & 1u) ? fmaxf(mx[c & 7], __uint_as_float(own[c])) : mx[c & 7];
+        mx[c & 7] = ((other >> c) & 1u) ? fmaxf(mx[c & 7], __uint_as_float(oth[c])) : mx[c & 7];
       }
       const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
@@ -420,14 +426,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const float m_new = (mb2 > m_ref + 64.f) ? mb2 : m_ref;
       const float alpha = (m_new == m_ref) ? 1.f : ex2(m_ref - m_new);
       const float neg_m = -m_new;
-      uint32_t pk[32];
+      uint32_t pk[16];
       float ls[4] = {0.f, 0.f, 0.f, 0.f}, le[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        const bool v0 = ((c < 32 ? m_lo >> c : m_hi >> (c - 32)) & 1u) != 0;
-        const bool v1 = ((c + 1 < 32 ? m_lo >> (c + 1) : m_hi >> (c - 31)) & 1u) != 0;
-        const float p0 = v0 ? ex2(fmaf(__uint_as_float(sr[c]), p.scale_log2, neg_m)) : 0.f;
-        const float p1 = v1 ? ex2(fmaf(__uint_as_float(sr[c + 1]), p.scale_log2, neg_m)) : 0.f;
+      for (int c = 0; c < 32; c += 2) {
+        const float p0 = ((mine >> c) & 1u) ? ex2(fmaf(__uint_as_float(own[c]), p.scale_log2, neg_m)) : 0.f;
+        const float p1 = ((mine >> (c + 1)) & 1u) ? ex2(fmaf(__uint_as_float(own[c + 1]), p.scale_log2, neg_m)) : 0.f;
         const uint32_t pv2 = pack_bf16x2(p0, p1);
         pk[c >> 1] = pv2;
         ls[(c >> 1) & 3] += __uint_as_float(pv2 << 16) + __uint_as_float(pv2 & 0xffff0000u);
@@ -439,17 +443,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // P^T buffer and O^T are free once the previous block's PV product is done
       if (jj >= 1 && w_ok)
         w_ok = mbar_wait(&bars[B_O], (jj - 1) & 1, p.status, kWaitLimitNs, SITE_W_O);
-      s_alpha[sbuf * 128 + h] = alpha;
+      s_alpha[sbuf * 128 + h] = alpha;  // both halves write the same value
       if (jj >= 1 && h < H && alpha != 1.f) s_resc[k3] = 1;
       if (!w_ok || vload(s_abort)) g_abort[k3] = 1;
-      named_bar_sync(1, 128);
+      named_bar_sync(1, NSMX);
       if (vload(&g_abort[k3])) { ok = false; break; }
       if (gt == 0) s_resc[(jj + 2) % 3] = 0;  // its readers (iteration jj-1) are all past this barrier
       tc_fence_after();
       if (vload(&s_resc[k3])) {
-        // rare: rescale every O^T column by its head's alpha
+        // rare: rescale every O^T column by its head's alpha (half 0: tiles 0-1, half 1: 2-3)
 #pragma unroll 1
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 2 * half; i < 2 * half + 2; ++i) {
 #pragma unroll 1
           for (int c0 = 0; c0 < HN; c0 += 16) {
             uint32_t r[16];
@@ -464,16 +468,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         tmem_st_wait();
       }
-      // this head's row of P^T (K-major: row = head, 64 keys = 128 B)
+      // this thread's half of its head's row of P^T (K-major: row = head, 64 keys = 128 B)
       if (h < HN) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 4; ++u) {
           uint4 v;
           if (h < H)
             v = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
           else
             v = make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(prow + (((u ^ h) & 7) << 4)) = v;
+          *reinterpret_cast<uint4*>(prow + ((((4 * half + u) ^ h) & 7) << 4)) = v;
         }
       }
       fence_proxy_async_smem();
@@ -481,68 +485,80 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_arrive(&bars[B_P]);
     }
     // ------------------------------ epilogue ---------------------------------
-    if (h < 128) s_invl[h] = l_sum > 0.f ? 1.f / l_sum : 0.f;
-    const float lse2 = (l_exact > 0.f) ? m_ref + log2f(l_exact) : -INFINITY;
     bool have_o = ok && nb > 0;
     if (have_o)
       have_o = mbar_wait(&bars[B_O], (nb - 1) & 1, p.status, kWaitLimitNs, SITE_W_O);
     if (!have_o) g_abort[0] = 1;  // sticky: every thread below writes zeros
-    named_bar_sync(1, 128);
+    // combine the two halves' sums through the (now idle) rope slot
+    float* s_l = reinterpret_cast<float*>(sm + OFF_ROPE);  // [2 halves][2 sums][128]
+    s_l[(half * 2 + 0) * 128 + h] = l_sum;
+    s_l[(half * 2 + 1) * 128 + h] = l_exact;
+    named_bar_sync(1, NSMX);
     have_o = !vload(&g_abort[0]) && !vload(s_abort) && ok && nb > 0;
     tc_fence_after();
-    const int64_t pq = static_cast<int64_t>(qflat) * p.nsplit + sp;
-    if (h < H) {
-      if (p.nsplit == 1) {
-        if (p.lse != nullptr)
-          p.lse[static_cast<int64_t>(qflat) * H + h] = have_o ? lse2 * 0.6931471805599453f : -INFINITY;
-      } else {
-        p.part_lse[pq * H + h] = have_o ? lse2 : -INFINITY;
+    float* s_invl = s_l + 4 * 128;  // [128]
+    if (half == 0) {
+      const float lt = s_l[0 * 128 + h] + s_l[2 * 128 + h];
+      const float lx = s_l[1 * 128 + h] + s_l[3 * 128 + h];
+      s_invl[h] = lt > 0.f ? 1.f / lt : 0.f;
+      const float lse2 = (lx > 0.f) ? m_ref + log2f(lx) : -INFINITY;
+      const int64_t pq = static_cast<int64_t>(qflat) * p.nsplit + sp;
+      if (h < H) {
+        if (p.nsplit == 1) {
+          if (p.lse != nullptr)
+            p.lse[static_cast<int64_t>(qflat) * H + h] =
+                have_o ? lse2 * 0.6931471805599453f : -INFINITY;
+        } else {
+          p.part_lse[pq * H + h] = have_o ? lse2 : -INFINITY;
+        }
       }
     }
-    // O^T tile i (128 dims x H heads): each thread owns one dim, stages its
-    // H values into [head][128 dims] in the (now idle) pair slots, then the
-    // group writes whole 256-byte (BF16) or 512-byte (FP32) rows.
-    uint8_t* stage = sm + OFF_PAIR;
+    named_bar_sync(1, NSMX);
+    // O^T tile i (128 dims x H heads): each thread owns one dim of the tiles of
+    // its half (0: tiles 0-1, 1: tiles 2-3), stages its H values as [head][128
+    // dims] in the (now idle) pair slots, then its half writes whole 256-byte
+    // (BF16) or 512-byte (FP32) rows.
+    const int64_t pq = static_cast<int64_t>(qflat) * p.nsplit + sp;
+    uint8_t* stage = sm + OFF_PAIR + half * (p.nsplit == 1 ? H * 256 : H * 512);
     const int dloc = 32 * sub + lane;
+    const int ht = gt & 127;  // thread index within the half
 #pragma unroll 1
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll 1
-      for (int c0 = 0; c0 < HN; c0 += 16) {
-        uint32_t r[16];
-        if (have_o) {
-          tmem_ld16(tmem + lane_base + i * HN + c0, r);
-          tmem_ld_wait();
-        }
+    for (int ti = 0; ti < 2; ++ti) {
+      const int i = 2 * half + ti;
+      uint32_t r[HN];
+      if (have_o) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int hh = c0 + e;
-          if (hh < H) {
-            const float v = have_o ? __uint_as_float(r[e]) * s_invl[hh] : 0.f;
-            if (p.nsplit == 1)
-              reinterpret_cast<uint16_t*>(stage)[hh * 128 + dloc] =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(v));
-            else
-              reinterpret_cast<float*>(stage)[hh * 128 + dloc] = v;
-          }
-        }
+        for (int c0 = 0; c0 < HN; c0 += 16)
+          tmem_ld16(tmem + lane_base + i * HN + c0,
+                    *reinterpret_cast<uint32_t(*)[16]>(&r[c0]));
+        tmem_ld_wait();
       }
-      named_bar_sync(1, 128);
+#pragma unroll
+      for (int hh = 0; hh < H; ++hh) {
+        const float v = have_o ? __uint_as_float(r[hh]) * s_invl[hh] : 0.f;
+        if (p.nsplit == 1)
+          reinterpret_cast<uint16_t*>(stage)[hh * 128 + dloc] =
+              __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        else
+          reinterpret_cast<float*>(stage)[hh * 128 + dloc] = v;
+      }
+      named_bar_sync(1, NSMX);
       if (p.nsplit == 1) {
         uint16_t* ob = p.o_lat + static_cast<int64_t>(qflat) * H * kVlat + 128 * i;
-        for (int v = gt; v < H * 16; v += 128) {  // 16 x 16 B per head row
+        for (int v = ht; v < H * 16; v += 128) {  // 16 x 16 B per head row
           const int hh = v >> 4, q16 = v & 15;
           *reinterpret_cast<uint4*>(ob + static_cast<int64_t>(hh) * kVlat + q16 * 8) =
               reinterpret_cast<const uint4*>(stage)[hh * 16 + q16];
         }
       } else {
         float* ob = p.part_o + pq * H * kVlat + 128 * i;
-        for (int v = gt; v < H * 32; v += 128) {  // 32 x 16 B per head row
+        for (int v = ht; v < H * 32; v += 128) {  // 32 x 16 B per head row
           const int hh = v >> 5, q16 = v & 31;
           *reinterpret_cast<float4*>(ob + static_cast<int64_t>(hh) * kVlat + q16 * 4) =
               reinterpret_cast<const float4*>(stage)[hh * 32 + q16];
         }
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, NSMX);
     }
   }
   tc_fence_before();
@@ -644,16 +660,16 @@ static dsa_status_t launch_h(const SparseMlaArgs& a, cudaStream_t stream) {
   auto kern = sparse_mla_kernel<H>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
       cudaSuccess)
-    return DSA_ERR_CUDA;
+    return launch_status("cudaFuncSetAttribute");
   const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(a.B) * a.Tq * ns);
   kern<<<grid, NTHREADS, SMEM_BYTES, stream>>>(tq, p);
-  if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+  if (launch_status("sparse_mla_kernel") != DSA_OK) return DSA_ERR_CUDA;
   if (ns > 1) {
     const int64_t nq = static_cast<int64_t>(a.B) * a.Tq;
     const int64_t threads = nq * H * (kVlat / 4);
     combine_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
         p.part_o, p.part_lse, static_cast<int>(nq), H, ns, a.o_lat, a.lse);
-    if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+    if (launch_status("combine_kernel") != DSA_OK) return DSA_ERR_CUDA;
   }
   return DSA_OK;
 }
