@@ -204,6 +204,16 @@ dsa_status_t sparse_mla_fwd_noalloc(const uint16_t* q_lat, const dsa_rows_t* kv,
 dsa_status_t dsa_read_device_status(void* workspace, dsa_stream_t stream, uint32_t* where,
                                     uint32_t* detail);
 
+/*
+ * Failure-path self-test (no counterpart on the pages): launch one CTA whose
+ * bounded mbarrier wait is never satisfied, so it gives up after limit_ns
+ * (at most 200 ms), records DSA_ERR_DEVICE_TIMEOUT in the workspace status
+ * word and returns.  Read the result with dsa_read_device_status().  This is
+ * the same bounded wait every kernel uses; no kernel traps or spins forever.
+ */
+dsa_status_t dsa_selftest_wait_timeout(void* workspace, size_t ws_bytes, uint64_t limit_ns,
+                                       dsa_stream_t stream);
+
 /* Static string for a status code. */
 const char* dsa_status_string(dsa_status_t status);
 

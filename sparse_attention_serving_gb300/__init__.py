@@ -49,12 +49,13 @@ class _Rows(ctypes.Structure):
 
 
 EXPORTS = ("dsa_abi_version", "dsa_status_string", "dsa_workspace_bytes", "dsa_workspace_init",
-           "dsa_read_device_status", "dsa_indexer_topk", "sparse_mla_fwd", "mla_gate_apply")
+           "dsa_read_device_status", "dsa_indexer_topk", "sparse_mla_fwd", "mla_gate_apply",
+           "dsa_selftest_wait_timeout")
 
 
 def _load(path: str = LIB_PATH):
     if not os.path.exists(path):
-        raise ImportError(f"{path} is missing: build it with `python -m sparse_attention_serving_gb300.build`"
+        raise ImportError(f"{path} is missing: build it with `python sparse_attention_serving_gb300/build.py`"
                           " (there is no fallback path)")
     lib = ctypes.CDLL(path)
     P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -69,8 +70,9 @@ def _load(path: str = LIB_PATH):
     lib.sparse_mla_fwd.argtypes = [P, ctypes.POINTER(_Rows), P, P, P, I, I, I, I, I,
                                    ctypes.c_float, P, P, P, Z, P]
     lib.mla_gate_apply.argtypes = [P, P, P, P, I, I, I, I, P, P, Z, P]
+    lib.dsa_selftest_wait_timeout.argtypes = [P, Z, ctypes.c_uint64, P]
     for f in ("dsa_workspace_init", "dsa_read_device_status", "dsa_indexer_topk",
-              "sparse_mla_fwd", "mla_gate_apply"):
+              "sparse_mla_fwd", "mla_gate_apply", "dsa_selftest_wait_timeout"):
         getattr(lib, f).restype = I
     return lib
 
@@ -156,6 +158,13 @@ def read_device_status(workspace: torch.Tensor, stream=None):
     code = lib.dsa_read_device_status(_ptr(workspace), _stream(stream), ctypes.byref(where),
                                       ctypes.byref(detail))
     return int(code), int(where.value), int(detail.value)
+
+
+def selftest_wait_timeout(workspace: torch.Tensor, limit_ns: int = 20_000_000, stream=None):
+    """Run the device failure-path self-test; returns (code, where, detail) read back."""
+    _check(lib.dsa_selftest_wait_timeout(_ptr(workspace), workspace.numel(), int(limit_ns),
+                                         _stream(stream)), "dsa_selftest_wait_timeout")
+    return read_device_status(workspace, stream)
 
 
 def _ws(workspace, op, B, Tq, max_kv_len, heads, topk, device, stream):

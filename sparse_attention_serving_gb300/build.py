@@ -1,6 +1,6 @@
 """Build libdsa.so in-tree with nvcc for sm_103a (one -gencode, parallel TUs).
 
-    python -m sparse_attention_serving_gb300.build [--force] [--verbose]
+    python sparse_attention_serving_gb300/build.py [--force] [--verbose]
 
 Each ``csrc/*.cu`` file becomes an object compiled in parallel; the objects are
 linked with the static CUDA runtime into ``libdsa.so`` next to this file.  The

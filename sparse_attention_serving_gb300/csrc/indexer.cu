@@ -319,6 +319,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     constexpr int QH = QT / 2;  // queries per epilogue half
     const uint32_t lane_base = static_cast<uint32_t>(sub * 32) << 16;
     const int key_lane = sub * 32 + lane;
+    // this thread's head weights (its half's queries), kept in registers
+    float wreg[QH * H_I];
+#pragma unroll
+    for (int c = 0; c < QH * H_I; ++c) wreg[c] = w_s[half * QH * H_I + c];
     for (int kt = 0; kt < ntiles; ++kt) {
       const int buf = kt & 1;
       const bool w_ok = mbar_wait(&bars[7 + buf], (kt >> 1) & 1, p.status, kWaitLimitNs, SITE_W_DF);
@@ -326,10 +330,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       named_bar_sync(1, G);
       if (vflag(&g_abort[(kt & 1) * 2])) break;
       tc_fence_after();
-      float acc[QH];
-#pragma unroll
-      for (int q = 0; q < QH; ++q) acc[q] = 0.f;
+      // head reduction: 4 independent FMA chains per query (the MMA's FP32
+      // accumulators are summed in a fixed order: chain c takes heads c, c+4, ...)
       constexpr int COLS = QH * H_I;  // this half's accumulator columns
+      constexpr int NCHAIN = 4;
+      float acc[QH][NCHAIN];
+#pragma unroll
+      for (int q = 0; q < QH; ++q)
+#pragma unroll
+        for (int c = 0; c < NCHAIN; ++c) acc[q][c] = 0.f;
       const uint32_t col0 = buf * 256 + half * COLS;
 #pragma unroll
       for (int u = 0; u < COLS / 32; ++u) {
@@ -341,9 +350,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int col = u * 32 + e;
           const int q = col / H_I;
           const float v = fmaxf(__uint_as_float(r[e]), 0.f);
-          acc[q] = fmaf(w_s[(half * QH + q) * H_I + (col % H_I)], v, acc[q]);
+          acc[q][e % NCHAIN] = fmaf(wreg[col], v, acc[q][e % NCHAIN]);
         }
       }
+      float score[QH];
+#pragma unroll
+      for (int q = 0; q < QH; ++q) score[q] = (acc[q][0] + acc[q][1]) + (acc[q][2] + acc[q][3]);
       tc_fence_before();
       mbar_arrive(&bars[9 + buf]);
       // append candidates above each query's threshold
@@ -351,7 +363,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
       for (int q = 0; q < QH; ++q) {
         const int qq = half * QH + q;
-        const bool take = qq < nq && s <= t0 + qq && acc[q] > thr[qq];
+        const bool take = qq < nq && s <= t0 + qq && score[q] > thr[qq];
         const uint32_t bal = __ballot_sync(0xffffffffu, take);
         if (bal) {
           int base = 0;
@@ -359,7 +371,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           base = __shfl_sync(0xffffffffu, base, 0);
           if (take) {
             const int pos = base + __popc(bal & ((1u << lane) - 1u));
-            cand_s[qq * CAP + pos] = acc[q];
+            cand_s[qq * CAP + pos] = score[q];
             cand_i[qq * CAP + pos] = s;
           }
         }
