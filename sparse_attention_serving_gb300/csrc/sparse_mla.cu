@@ -22,8 +22,10 @@
 //               With six pair slots, the first two pairs and the rope chunk of
 //               block j+1 are multiplied while the softmax of block j runs.
 //   warps 5-12  softmax (two warps per TMEM lane quarter: a thread owns one
-//               head and 32 of the block's 64 keys; row max and sums stay in
-//               the thread; one named barrier per block), P^T written as BF16,
+//               head and 32 of the block's 64 keys; P = 2^(z - m_ref) against
+//               a lazy reference max, which only moves -- through a rarer,
+//               synchronised path that rescales O^T -- when an exponent would
+//               exceed 64; one named barrier per block), P^T written as BF16,
 //               then the epilogue (O^T / l staged through shared memory into
 //               coalesced BF16 rows of o_lat, and lse).
 // Q rows 96..127 of the M=128 operand alias the next 64-dim chunk of Q (or the
@@ -147,8 +149,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + OFF_MISC + 260);
   volatile int* g_abort = s_abort + 1;  // [3] softmax-group abort, by iteration mod 3
   volatile int* s_resc = s_abort + 4;   // [3] some head needs an O^T rescale, by iteration mod 3
-  int* s_red = reinterpret_cast<int*>(sm + OFF_MISC + 320);               // [16]
-  float* s_alpha = reinterpret_cast<float*>(sm + OFF_MISC + 384);         // [2][128]
+  float* s_cmax = reinterpret_cast<float*>(sm + OFF_MISC + 256 + 64);   // [2][128] rare path
+  int* s_red = reinterpret_cast<int*>(s_cmax);                           // [16] prologue only
+  float* s_alpha = s_cmax + 256;                                         // [128] rare path
+  volatile uint8_t* s_hover = reinterpret_cast<volatile uint8_t*>(s_alpha + 128);  // [128]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qflat = blockIdx.x / p.nsplit, sp = blockIdx.x % p.nsplit;
@@ -163,6 +167,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     s_abort[0] = 0;
     for (int k = 0; k < 3; ++k) { g_abort[k] = 0; s_resc[k] = 0; }
+    for (int k = 0; k < 128; ++k) s_hover[k] = 0;
     fence_mbar_init();
     // the query block does not depend on the index list: start it now
     tma_prefetch_desc(&tm_q);
@@ -368,18 +373,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else {
     // ================ softmax + epilogue (warps 5..12, 8 warps) ================
     // Two warps per TMEM lane quarter: thread (half, h) owns head h and the
-    // keys 32*half .. 32*half+31 of each block.  Both halves take the block max
-    // over all 64 keys (cheap), so they agree on the reference without talking.
+    // keys 32*half .. 32*half+31 of each block.  Both halves of a head move the
+    // reference max together (through s_cmax, on the rare path only).
     const int sub = warp & 3;                         // TMEM lane quarter
     const int half = (warp - SMX_WARP0) >> 2;         // 0: keys 0-31, 1: keys 32-63
     const int h = sub * 32 + lane;                    // head owned in the softmax
     const int gt = tid - SMX_WARP0 * 32;              // 0..255 within the group
     const uint32_t lane_base = static_cast<uint32_t>(sub * 32) << 16;
-    // l_sum: sum of the BF16-rounded P fed to the PV product (normalises O);
-    // l_exact: the unrounded sum (log-sum-exp); both over this thread's keys
-    float m_ref = -INFINITY, l_sum = 0.f, l_exact = 0.f;
+    // l_sum: this thread's share (its 32 keys) of sum_s 2^(z_s - m_ref)
+    float m_ref = -INFINITY, l_sum = 0.f;
     bool ok = true;
     uint8_t* prow = sm + OFF_P + (h >> 3) * 1024 + (h & 7) * 128;
+    const float c2 = p.scale_log2;
     // list entries kb + lane and kb + 32 + lane, fetched one block ahead
     int e_lo = -1, e_hi = -1;
     if (nb > 0) {
@@ -391,6 +396,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int sbuf = jj & 1, k3 = jj % 3;
       const uint32_t m_lo = __ballot_sync(0xffffffffu, entry_row(p, b, t, e_lo) >= 0);
       const uint32_t m_hi = __ballot_sync(0xffffffffu, entry_row(p, b, t, e_hi) >= 0);
+      const uint32_t mine = half ? m_hi : m_lo;
       if (jj + 1 < nb) {
         const int kb = (blk0 + jj + 1) * BK;
         e_lo = kb + lane < n_list ? __ldg(ix + kb + lane) : -1;
@@ -398,76 +404,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       bool w_ok = mbar_wait(&bars[B_SF + sbuf], (jj >> 1) & 1, p.status, kWaitLimitNs, SITE_W_SF);
       tc_fence_after();
-      // own 32 keys and the partner half's 32 (needed only for the block max)
-      uint32_t own[32], oth[32];
+      uint32_t own[32];
       if (w_ok) {
         tmem_ld32(tmem + lane_base + S_COL + BK * sbuf + 32 * half, own);
-        tmem_ld32(tmem + lane_base + S_COL + BK * sbuf + 32 * (1 - half), oth);
         tmem_ld_wait();
       }
       tc_fence_before();
       mbar_arrive(&bars[B_SE + sbuf]);
-      const uint32_t mine = half ? m_hi : m_lo;
-      const uint32_t other = half ? m_lo : m_hi;
-      // block max over all 64 valid keys (raw logits; the scale is positive)
-      float mx[8];
-#pragma unroll
-      for (int g = 0; g < 8; ++g) mx[g] = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        mx[c & 7] = ((mine >> c) & 1u) ? fmaxf(mx[c & 7], __uint_as_float(own[c])) : mx[c & 7];
-        mx[c & 7] = ((other >> c) & 1u) ? fmaxf(mx[c & 7], __uint_as_float(oth[c])) : mx[c & 7];
-      }
-      const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float mb2 = mb * p.scale_log2;
-      // lazy reference max: keep the current one unless this block exceeds it by
-      // more than 2^64; P = 2^(z - m_ref) then stays far inside the FP32/BF16 range
-      const float m_new = (mb2 > m_ref + 64.f) ? mb2 : m_ref;
-      const float alpha = (m_new == m_ref) ? 1.f : ex2(m_ref - m_new);
-      const float neg_m = -m_new;
+      // Common path: P = 2^(z - m_ref) against the running reference max.  Any
+      // exponent above 64 (or no reference yet) sends the whole group through
+      // the rare path below, which moves the reference and rescales O^T.
+      const float neg_m = -m_ref;
+      bool over = (m_ref == -INFINITY);
       uint32_t pk[16];
-      float ls[4] = {0.f, 0.f, 0.f, 0.f}, le[4] = {0.f, 0.f, 0.f, 0.f};
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      if (mine == 0xffffffffu) {
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        const float p0 = ((mine >> c) & 1u) ? ex2(fmaf(__uint_as_float(own[c]), p.scale_log2, neg_m)) : 0.f;
-        const float p1 = ((mine >> (c + 1)) & 1u) ? ex2(fmaf(__uint_as_float(own[c + 1]), p.scale_log2, neg_m)) : 0.f;
-        const uint32_t pv2 = pack_bf16x2(p0, p1);
-        pk[c >> 1] = pv2;
-        ls[(c >> 1) & 3] += __uint_as_float(pv2 << 16) + __uint_as_float(pv2 & 0xffff0000u);
-        le[(c >> 1) & 3] += p0 + p1;
+        for (int c = 0; c < 32; c += 2) {
+          const float a0 = fmaf(__uint_as_float(own[c]), c2, neg_m);
+          const float a1 = fmaf(__uint_as_float(own[c + 1]), c2, neg_m);
+          over |= fmaxf(a0, a1) > 64.f;
+          const float p0 = ex2(a0), p1 = ex2(a1);
+          pk[c >> 1] = pack_bf16x2(p0, p1);
+          ls[(c >> 1) & 3] += p0 + p1;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const bool v0 = ((mine >> c) & 1u) != 0, v1 = ((mine >> (c + 1)) & 1u) != 0;
+          const float a0 = v0 ? fmaf(__uint_as_float(own[c]), c2, neg_m) : -INFINITY;
+          const float a1 = v1 ? fmaf(__uint_as_float(own[c + 1]), c2, neg_m) : -INFINITY;
+          over |= fmaxf(a0, a1) > 64.f;
+          const float p0 = ex2(a0), p1 = ex2(a1);
+          pk[c >> 1] = pack_bf16x2(p0, p1);
+          ls[(c >> 1) & 3] += p0 + p1;
+        }
       }
-      l_sum = l_sum * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-      l_exact = l_exact * alpha + ((le[0] + le[1]) + (le[2] + le[3]));
-      m_ref = m_new;
+      float blk_sum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
       // P^T buffer and O^T are free once the previous block's PV product is done
       if (jj >= 1 && w_ok)
         w_ok = mbar_wait(&bars[B_O], (jj - 1) & 1, p.status, kWaitLimitNs, SITE_W_O);
-      s_alpha[sbuf * 128 + h] = alpha;  // both halves write the same value
-      if (jj >= 1 && h < H && alpha != 1.f) s_resc[k3] = 1;
-      if (!w_ok || vload(s_abort)) g_abort[k3] = 1;
-      named_bar_sync(1, NSMX);
-      if (vload(&g_abort[k3])) { ok = false; break; }
-      if (gt == 0) s_resc[(jj + 2) % 3] = 0;  // its readers (iteration jj-1) are all past this barrier
-      tc_fence_after();
-      if (vload(&s_resc[k3])) {
-        // rare: rescale every O^T column by its head's alpha (half 0: tiles 0-1, half 1: 2-3)
-#pragma unroll 1
-        for (int i = 2 * half; i < 2 * half + 2; ++i) {
-#pragma unroll 1
-          for (int c0 = 0; c0 < HN; c0 += 16) {
-            uint32_t r[16];
-            const uint32_t ta = tmem + lane_base + i * HN + c0;
-            tmem_ld16(ta, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              r[e] = __float_as_uint(__uint_as_float(r[e]) * s_alpha[sbuf * 128 + c0 + e]);
-            tmem_st16(ta, r);
-          }
-        }
-        tmem_st_wait();
-      }
       // this thread's half of its head's row of P^T (K-major: row = head, 64 keys = 128 B)
       if (h < HN) {
 #pragma unroll
@@ -481,6 +457,80 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       fence_proxy_async_smem();
+      if (over && h < H) {
+        s_hover[h] = 1;
+        s_resc[k3] = 1;
+      }
+      if (!w_ok || vload(s_abort)) g_abort[k3] = 1;
+      named_bar_sync(1, NSMX);
+      if (vload(&g_abort[k3])) { ok = false; break; }
+      if (gt == 0) s_resc[(jj + 2) % 3] = 0;  // its readers (iteration jj-1) are all past this barrier
+      if (!vload(&s_resc[k3])) {
+        l_sum += blk_sum;
+      } else {
+        // ---- rare path (first block, or an exponent above 64): uniform ----
+        float cm = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if ((mine >> c) & 1u) cm = fmaxf(cm, __uint_as_float(own[c]));
+        s_cmax[half * 128 + h] = cm;
+        named_bar_sync(1, NSMX);
+        const bool hov = h < H && s_hover[h] != 0;
+        float alpha = 1.f;
+        if (hov) {
+          const float mb2 = fmaxf(s_cmax[h], s_cmax[128 + h]) * c2;
+          if (mb2 != -INFINITY) {
+            alpha = (m_ref == -INFINITY) ? 0.f : ex2(m_ref - mb2);
+            m_ref = mb2;
+            const float nm = -mb2;
+            float rs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const bool v0 = ((mine >> c) & 1u) != 0, v1 = ((mine >> (c + 1)) & 1u) != 0;
+              const float p0 = v0 ? ex2(fmaf(__uint_as_float(own[c]), c2, nm)) : 0.f;
+              const float p1 = v1 ? ex2(fmaf(__uint_as_float(own[c + 1]), c2, nm)) : 0.f;
+              pk[c >> 1] = pack_bf16x2(p0, p1);
+              rs[(c >> 1) & 3] += p0 + p1;
+            }
+            blk_sum = (rs[0] + rs[1]) + (rs[2] + rs[3]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(prow + ((((4 * half + u) ^ h) & 7) << 4)) =
+                  make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          } else {
+            // no valid key seen yet for this head: nothing to weigh
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(prow + ((((4 * half + u) ^ h) & 7) << 4)) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            blk_sum = 0.f;
+          }
+        }
+        l_sum = l_sum * alpha + blk_sum;
+        if (half == 0) s_alpha[h] = alpha;
+        fence_proxy_async_smem();
+        named_bar_sync(1, NSMX);
+        if (half == 0) s_hover[h] = 0;  // read by both halves before the barrier above
+        tc_fence_after();
+        if (jj >= 1) {
+          // rescale every O^T column by its head's alpha (half 0: tiles 0-1, half 1: 2-3)
+#pragma unroll 1
+          for (int i = 2 * half; i < 2 * half + 2; ++i) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < HN; c0 += 16) {
+              uint32_t r[16];
+              const uint32_t ta = tmem + lane_base + i * HN + c0;
+              tmem_ld16(ta, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                r[e] = __float_as_uint(__uint_as_float(r[e]) * s_alpha[c0 + e]);
+              tmem_st16(ta, r);
+            }
+          }
+          tmem_st_wait();
+        }
+      }
       tc_fence_before();
       mbar_arrive(&bars[B_P]);
     }
@@ -490,17 +540,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       have_o = mbar_wait(&bars[B_O], (nb - 1) & 1, p.status, kWaitLimitNs, SITE_W_O);
     if (!have_o) g_abort[0] = 1;  // sticky: every thread below writes zeros
     // combine the two halves' sums through the (now idle) rope slot
-    float* s_l = reinterpret_cast<float*>(sm + OFF_ROPE);  // [2 halves][2 sums][128]
-    s_l[(half * 2 + 0) * 128 + h] = l_sum;
-    s_l[(half * 2 + 1) * 128 + h] = l_exact;
+    float* s_l = reinterpret_cast<float*>(sm + OFF_ROPE);  // [2 halves][128]
+    s_l[half * 128 + h] = l_sum;
     named_bar_sync(1, NSMX);
     have_o = !vload(&g_abort[0]) && !vload(s_abort) && ok && nb > 0;
     tc_fence_after();
-    float* s_invl = s_l + 4 * 128;  // [128]
+    float* s_invl = s_l + 2 * 128;  // [128]
     if (half == 0) {
-      const float lt = s_l[0 * 128 + h] + s_l[2 * 128 + h];
-      const float lx = s_l[1 * 128 + h] + s_l[3 * 128 + h];
-      s_invl[h] = lt > 0.f ? 1.f / lt : 0.f;
+      const float lx = s_l[h] + s_l[128 + h];
+      s_invl[h] = lx > 0.f ? 1.f / lx : 0.f;
       const float lse2 = (lx > 0.f) ? m_ref + log2f(lx) : -INFINITY;
       const int64_t pq = static_cast<int64_t>(qflat) * p.nsplit + sp;
       if (h < H) {
