@@ -89,74 +89,120 @@ __device__ __forceinline__ bool vflag(const volatile int* p) { return *p != 0; }
 // Keep exactly `k` of the `n` candidates of one query (the k largest scores;
 // ties at the cut are broken arbitrarily) and return the k-th score.  Called
 // by all epilogue threads together; `gtid` in [0, NEPI*32).
+//
+// Radix select over order-preserving 32-bit keys.  The candidates of a query
+// share their top bits (sign, most of the exponent), so the digits start at the
+// highest bit where the smallest and largest key differ (so the first digit
+// already spreads them over the bins), and the search stops as soon as the bin
+// holding the k-th key is kept whole.
 template <int EPT>
 __device__ float select_topk(float* cs, int32_t* ci, int n, int k, int gtid, int* hist,
                              int* sel, int* ctr) {
   uint32_t key[EPT];
   int32_t id[EPT];
   constexpr int G = NEPI * 32;
+  const int lane = gtid & 31;
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
 #pragma unroll
   for (int u = 0; u < EPT; ++u) {
     const int e = gtid + u * G;
     key[u] = e < n ? order_key(cs[e]) : 0u;
     id[u] = e < n ? ci[e] : -1;
+    if (id[u] >= 0) {
+      kmin = min(kmin, key[u]);
+      kmax = max(kmax, key[u]);
+    }
   }
-  uint32_t prefix = 0, mask = 0;
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (gtid == 0) {
+    ctr[2] = static_cast<int>(0xffffffffu);
+    ctr[3] = 0;
+  }
+  named_bar_sync(1, G);
+  if (lane == 0) {
+    atomicMin(reinterpret_cast<unsigned*>(&ctr[2]), kmin);
+    atomicMax(reinterpret_cast<unsigned*>(&ctr[3]), kmax);
+  }
+  named_bar_sync(1, G);
+  const uint32_t lo = static_cast<uint32_t>(ctr[2]), hi = static_cast<uint32_t>(ctr[3]);
+  const uint32_t diff = lo ^ hi;
+  uint32_t prefix, mask;
   int need = k;
+  if (diff == 0u) {
+    prefix = hi;
+    mask = 0xffffffffu;
+  } else {
+    const int top = 31 - __clz(diff);  // highest differing bit
+    mask = top >= 31 ? 0u : ~((2u << top) - 1u);
+    prefix = hi & mask;
+    int shift = top - 7;
 #pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    if (gtid < 256) hist[gtid] = 0;
-    named_bar_sync(1, G);
+    while (true) {
+      const int width = shift >= 0 ? 8 : 8 + shift;
+      if (shift < 0) shift = 0;
+      const uint32_t dm = (1u << width) - 1u;
+      if (gtid < 256) hist[gtid] = 0;
+      named_bar_sync(1, G);
 #pragma unroll
-    for (int u = 0; u < EPT; ++u)
-      if (id[u] >= 0 && (key[u] & mask) == prefix) atomicAdd(&hist[(key[u] >> shift) & 255], 1);
-    named_bar_sync(1, G);
-    if (gtid < 32) {
-      // lane l covers digits 255-8l .. 248-8l (descending)
-      int c[8], tot = 0;
+      for (int u = 0; u < EPT; ++u)
+        if (id[u] >= 0 && (key[u] & mask) == prefix) atomicAdd(&hist[(key[u] >> shift) & dm], 1);
+      named_bar_sync(1, G);
+      if (gtid < 32) {
+        // lane l covers digits 255-8l .. 248-8l (descending)
+        int c[8], tot = 0;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) { c[e] = hist[255 - 8 * gtid - e]; tot += c[e]; }
-      int incl = tot;
+        for (int e = 0; e < 8; ++e) { c[e] = hist[255 - 8 * gtid - e]; tot += c[e]; }
+        int incl = tot;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (gtid >= o) incl += v;
-      }
-      const int excl = incl - tot;
-      if (excl < need && need <= incl) {
-        int run = excl;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (gtid >= o) incl += v;
+        }
+        const int excl = incl - tot;
+        if (excl < need && need <= incl) {
+          int run = excl;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (run < need && need <= run + c[e]) {
-            sel[0] = 255 - 8 * gtid - e;
-            sel[1] = need - run;
+          for (int e = 0; e < 8; ++e) {
+            if (run < need && need <= run + c[e]) {
+              sel[0] = 255 - 8 * gtid - e;
+              sel[1] = need - run;
+              sel[2] = c[e];
+            }
+            run += c[e];
           }
-          run += c[e];
         }
       }
+      named_bar_sync(1, G);
+      prefix |= static_cast<uint32_t>(sel[0]) << shift;
+      mask |= dm << shift;
+      need = sel[1];
+      if (sel[2] == need || shift == 0) break;  // bin kept whole, or every bit fixed
+      shift -= 8;
     }
-    named_bar_sync(1, G);
-    prefix |= static_cast<uint32_t>(sel[0]) << shift;
-    mask |= 255u << shift;
-    need = sel[1];
   }
-  // keep every key > prefix and the first `need` keys == prefix
-  if (gtid == 0) { ctr[0] = 0; ctr[1] = 0; }
+  // keep every key whose masked value is above the prefix, and `need` of those
+  // equal to it; the k-th score is the smallest key kept
+  if (gtid == 0) { ctr[0] = 0; ctr[1] = 0; ctr[2] = static_cast<int>(0xffffffffu); }
   named_bar_sync(1, G);
+  uint32_t kept_min = 0xffffffffu;
 #pragma unroll
   for (int u = 0; u < EPT; ++u) {
     if (id[u] < 0) continue;
-    bool keep = key[u] > prefix;
-    if (!keep && key[u] == prefix) keep = atomicAdd(&ctr[1], 1) < need;
+    const uint32_t m = key[u] & mask;
+    bool keep = m > prefix;
+    if (!keep && m == prefix) keep = atomicAdd(&ctr[1], 1) < need;
     if (keep) {
       const int pos = atomicAdd(&ctr[0], 1);
       cs[pos] = key_to_float(key[u]);
       ci[pos] = id[u];
+      kept_min = min(kept_min, key[u]);
     }
   }
+  kept_min = __reduce_min_sync(0xffffffffu, kept_min);
+  if (lane == 0) atomicMin(reinterpret_cast<unsigned*>(&ctr[2]), kept_min);
   named_bar_sync(1, G);
-  return key_to_float(prefix);
+  return key_to_float(static_cast<uint32_t>(ctr[2]));
 }
 
 template <int H_I, int D_I>
@@ -180,8 +226,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   int* cnt = const_cast<int*>(s_abort) + 8;  // [QT] candidates per query
   float* thr = reinterpret_cast<float*>(cnt + 64);  // [QT]
   int* hist = reinterpret_cast<int*>(thr + 64);     // [256]
-  int* sel = hist + 256;                            // [2]
-  int* ctr = sel + 2;                               // [2]
+  int* sel = hist + 256;                            // [4]
+  int* ctr = sel + 4;                               // [4]
   float* cand_s = reinterpret_cast<float*>(sm + C::OFF_CAND);
   int32_t* cand_i = reinterpret_cast<int32_t*>(cand_s + QT * CAP);
 

@@ -14,9 +14,9 @@
 //                  over heads and writes one FP32 score per key: a linear
 //                  score vector per request in the workspace (4 bytes per key
 //                  against 256 bytes of key read).
-//   decode_select  one CTA per request: radix select (11 + 11 + 10 bits over
-//                  order-preserving keys) of the k largest scores, then writes
-//                  their positions.
+//   decode_select  one CTA per request: radix select (8-bit digits from the
+//                  highest bit where the scores differ) of the k largest
+//                  scores, then writes their positions.
 #include <cmath>
 
 #include <cuda_bf16.h>
@@ -290,59 +290,53 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Block-wide: find, over `nb` bins counted from the top digit down, the bin in
-// which the `need`-th largest element falls; returns (bin, remaining need).
-template <int NB>
-__device__ void find_bin(const int* hist, int need, int* out2, int* wsum) {
-  constexpr int PER = NB / 1024;  // bins per thread
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int c[PER], tot = 0;
+// Block-wide (1024 threads): find the bin of the 256 (counted from the top
+// digit down) in which the `need`-th largest element falls; writes
+// (digit, remaining need, bin count) to out3.
+__device__ void find_bin256(const int* hist, int need, int* out3) {
+  if (threadIdx.x < 32) {
+    const int l = threadIdx.x;
+    int c[8], tot = 0;
 #pragma unroll
-  for (int e = 0; e < PER; ++e) { c[e] = hist[NB - 1 - (tid * PER + e)]; tot += c[e]; }
-  int incl = tot;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) wsum[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int v = wsum[lane];
-    int iv = v;
+    for (int e = 0; e < 8; ++e) { c[e] = hist[255 - 8 * l - e]; tot += c[e]; }
+    int incl = tot;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, iv, o);
-      if (lane >= o) iv += u;
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (l >= o) incl += v;
     }
-    wsum[32 + lane] = iv - v;  // exclusive prefix over warps
-  }
-  __syncthreads();
-  const int excl = wsum[32 + warp] + incl - tot;
-  if (excl < need && need <= excl + tot) {
-    int run = excl;
+    const int excl = incl - tot;
+    if (excl < need && need <= incl) {
+      int run = excl;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) {
-      if (run < need && need <= run + c[e]) {
-        out2[0] = NB - 1 - (tid * PER + e);
-        out2[1] = need - run;
+      for (int e = 0; e < 8; ++e) {
+        if (run < need && need <= run + c[e]) {
+          out3[0] = 255 - 8 * l - e;
+          out3[1] = need - run;
+          out3[2] = c[e];
+        }
+        run += c[e];
       }
-      run += c[e];
     }
   }
   __syncthreads();
 }
 
-// One CTA (1024 threads) per request: the k largest of scores[0..L).
+// One CTA (1024 threads) per request: the k largest of scores[0..L).  Radix
+// select over order-preserving keys: digits start at the highest bit where the
+// smallest and largest score differ (scores share sign and most exponent
+// bits), each warp counts into its own histogram, and the passes stop as soon
+// as the bin holding the k-th key is kept whole.
 __global__ void __launch_bounds__(1024) decode_select_kernel(const float* __restrict__ scores,
                                                              const int32_t* __restrict__ kv_len,
                                                              int max_kv_len, int topk,
                                                              int32_t* __restrict__ out_idx) {
-  __shared__ int hist[2048];
-  __shared__ int wsum[64];
-  __shared__ int sel[2];
+  __shared__ int hist[256];
+  __shared__ int whist[32 * 256];
+  __shared__ int sel[4];
+  __shared__ unsigned red[4];
   __shared__ int ctr[2];
-  const int b = blockIdx.x, tid = threadIdx.x;
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   int L = __ldg(kv_len + b);
   if (L < 0 || L > max_kv_len) L = 0;  // flagged by the score kernel
   int32_t* out = out_idx + static_cast<int64_t>(b) * topk;
@@ -351,37 +345,66 @@ __global__ void __launch_bounds__(1024) decode_select_kernel(const float* __rest
     return;
   }
   const float* sc = scores + static_cast<int64_t>(b) * max_kv_len;
-  uint32_t prefix = 0, mask = 0;
+  if (tid == 0) { red[0] = 0xffffffffu; red[1] = 0u; }
+  __syncthreads();
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  for (int e = tid; e < L; e += 1024) {
+    const uint32_t k = order_key(sc[e]);
+    kmin = min(kmin, k);
+    kmax = max(kmax, k);
+  }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) { atomicMin(&red[0], kmin); atomicMax(&red[1], kmax); }
+  __syncthreads();
+  const uint32_t diff = red[0] ^ red[1];
+  uint32_t prefix, mask;
   int need = topk;
-  // digits: bits 31..21 (11), 20..10 (11), 9..0 (10)
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
+  if (diff == 0u) {
+    prefix = red[1];
+    mask = 0xffffffffu;
+  } else {
+    const int top = 31 - __clz(diff);
+    mask = top >= 31 ? 0u : ~((2u << top) - 1u);
+    prefix = red[1] & mask;
+    int shift = top - 7;
 #pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
-    const int sh = shifts[pass];
-    const uint32_t dm = (1u << widths[pass]) - 1u;
-    for (int e = tid; e < 2048; e += 1024) hist[e] = 0;
-    __syncthreads();
-    for (int e = tid; e < L; e += 1024) {
-      const uint32_t k = order_key(sc[e]);
-      if ((k & mask) == prefix) atomicAdd(&hist[(k >> sh) & dm], 1);
+    while (true) {
+      const int width = shift >= 0 ? 8 : 8 + shift;
+      if (shift < 0) shift = 0;
+      const uint32_t dm = (1u << width) - 1u;
+      // one private 256-bin histogram per warp, summed afterwards
+      for (int e = tid; e < 32 * 256; e += 1024) whist[e] = 0;
+      __syncthreads();
+      int* mine = whist + (tid >> 5) * 256;
+      for (int e = tid; e < L; e += 1024) {
+        const uint32_t k = order_key(sc[e]);
+        if ((k & mask) == prefix) atomicAdd(&mine[(k >> shift) & dm], 1);
+      }
+      __syncthreads();
+      if (tid < 256) {
+        int acc = 0;
+#pragma unroll 8
+        for (int w = 0; w < 32; ++w) acc += whist[w * 256 + tid];
+        hist[tid] = acc;
+      }
+      __syncthreads();
+      find_bin256(hist, need, sel);
+      prefix |= static_cast<uint32_t>(sel[0]) << shift;
+      mask |= dm << shift;
+      need = sel[1];
+      const bool done = sel[2] == need || shift == 0;
+      __syncthreads();
+      if (done) break;
+      shift -= 8;
     }
-    __syncthreads();
-    if (widths[pass] == 11)
-      find_bin<2048>(hist, need, sel, wsum);
-    else
-      find_bin<1024>(hist, need, sel, wsum);
-    prefix |= static_cast<uint32_t>(sel[0]) << sh;
-    mask |= dm << sh;
-    need = sel[1];
-    __syncthreads();
   }
   if (tid == 0) { ctr[0] = 0; ctr[1] = 0; }
   __syncthreads();
   for (int e = tid; e < L; e += 1024) {
-    const uint32_t k = order_key(sc[e]);
-    bool keep = k > prefix;
-    if (!keep && k == prefix) keep = atomicAdd(&ctr[1], 1) < need;
+    const uint32_t m = order_key(sc[e]) & mask;
+    bool keep = m > prefix;
+    if (!keep && m == prefix) keep = atomicAdd(&ctr[1], 1) < need;
     if (keep) out[atomicAdd(&ctr[0], 1)] = e;
   }
 }
