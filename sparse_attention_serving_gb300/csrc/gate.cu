@@ -115,19 +115,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int st = s % NST;
         if (!mbar_wait(&bars[st], (s / NST) & 1, p.status, kWaitLimitNs, SITE_W_F)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t a = smem_u32(sm + st * STAGE);
-        const uint32_t bb = a + 16 * 1024;
+        const uint64_t ad = smem_desc(smem_u32(sm + st * STAGE), 16, 1024);
+        const uint64_t bd = desc_add(ad, 16 * 1024);
         if (s < kg) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem, smem_desc(a + kk * 32, 16, 1024), smem_desc(bb + kk * 32, 16, 1024),
-                      IDESC_G, (s | kk) ? 1u : 0u);
+            umma_bf16(tmem, desc_add(ad, kk * 32), desc_add(bd, kk * 32), IDESC_G,
+                      (s | kk) ? 1u : 0u);
         } else {
           const int u = s - kg, hh = u >> 3, kc = u & 7;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + 256 + hh * 128, smem_desc(a + kk * 32, 16, 1024),
-                      smem_desc(bb + kk * 32, 16, 1024), IDESC_U, (kc | kk) ? 1u : 0u);
+            umma_bf16(tmem + 256 + hh * 128, desc_add(ad, kk * 32), desc_add(bd, kk * 32),
+                      IDESC_U, (kc | kk) ? 1u : 0u);
         }
         umma_commit(&bars[NST + st]);
       }

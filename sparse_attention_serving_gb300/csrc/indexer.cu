@@ -335,20 +335,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ============================ MMA issuer ==================================
     if (lane == 0) {
       bool ok = mbar_wait(&bars[0], 0, p.status, kWaitLimitNs, SITE_W_Q);
-      const uint32_t qb = smem_u32(sm + C::OFF_Q);
+      const uint64_t qd0 = smem_desc(smem_u32(sm + C::OFF_Q), 16, 1024);
       for (int kt = 0; kt < ntiles && ok; ++kt) {
         if (vflag(s_abort)) { ok = false; break; }
         const int st = kt % C::NST, buf = kt & 1;
         if (kt >= 2 && !mbar_wait(&bars[9 + buf], ((kt >> 1) - 1) & 1, p.status, kWaitLimitNs, SITE_W_DE)) { ok = false; break; }
         if (!mbar_wait(&bars[1 + st], (kt / C::NST) & 1, p.status, kWaitLimitNs, SITE_W_KF)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t kb = smem_u32(sm + C::OFF_K + st * C::K_STAGE);
+        const uint64_t kd = smem_desc(smem_u32(sm + C::OFF_K + st * C::K_STAGE), 16, 1024);
 #pragma unroll
         for (int c = 0; c < NCH; ++c)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + buf * 256, smem_desc(kb + c * BKEY * 128 + kk * 32, 16, 1024),
-                      smem_desc(qb + c * N * 128 + kk * 32, 16, 1024), IDESC, (c | kk) ? 1u : 0u);
+            umma_bf16(tmem + buf * 256, desc_add(kd, c * BKEY * 128 + kk * 32),
+                      desc_add(qd0, c * N * 128 + kk * 32), IDESC, (c | kk) ? 1u : 0u);
         umma_commit(&bars[4 + st]);
         umma_commit(&bars[7 + buf]);
       }

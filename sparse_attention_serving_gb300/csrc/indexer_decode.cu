@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int L = __ldg(p.kv_len + b);
         const int qs = n_items & 1;
         if (!mbar_wait(&q_full[qs], (n_items >> 1) & 1, p.status, kWaitLimitNs, SITE_W_QF)) { ok = false; break; }
-        const uint32_t qb = smem_u32(sm + C::OFF_Q + qs * QSLOT);
+        const uint64_t qd = smem_desc(smem_u32(sm + C::OFF_Q + qs * QSLOT), 16, 1024);
         const int t0 = c * CH_TILES;
         const int t1 = min(t0 + CH_TILES, (L + BKEY - 1) / BKEY);
         for (int kt = t0; kt < t1; ++kt, ++kcount, ++dcount) {
@@ -214,13 +214,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (dcount >= 4 && !mbar_wait(&d_empty[buf], ((dcount >> 2) - 1) & 1, p.status, kWaitLimitNs, SITE_W_DE)) { ok = false; break; }
           if (!mbar_wait(&k_full[st], (kcount / NST) & 1, p.status, kWaitLimitNs, SITE_W_KF)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t kb = smem_u32(sm + C::OFF_K + st * C::K_STAGE);
+          const uint64_t kd = smem_desc(smem_u32(sm + C::OFF_K + st * C::K_STAGE), 16, 1024);
 #pragma unroll
           for (int ch = 0; ch < NCH; ++ch)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(tmem + buf * 64, smem_desc(kb + ch * BKEY * 128 + kk * 32, 16, 1024),
-                        smem_desc(qb + ch * N * 128 + kk * 32, 16, 1024), IDESC, (ch | kk) ? 1u : 0u);
+              umma_bf16(tmem + buf * 64, desc_add(kd, ch * BKEY * 128 + kk * 32),
+                        desc_add(qd, ch * N * 128 + kk * 32), IDESC, (ch | kk) ? 1u : 0u);
           umma_commit(&k_empty[st]);
           umma_commit(&d_full[buf]);
         }

@@ -237,6 +237,16 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
          (static_cast<uint64_t>(layout & 7u) << 61);
 }
 
+// A descriptor whose start address moves by `byte_off` (a multiple of 16).
+// The start address lives in the low 14 bits (address >> 4); shared-memory
+// addresses stay below 2^18 bytes, so the addition never carries out of it.
+// Precomputing a base descriptor and adding constant offsets keeps the single
+// MMA-issuing thread from spending tens of cycles per instruction on
+// descriptor arithmetic.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_off) {
+  return desc + static_cast<uint64_t>(byte_off >> 4);
+}
+
 // Instruction descriptor for kind::f16 with BF16 A/B and FP32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
                                                   bool b_mn_major) {

@@ -292,8 +292,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == MMA_WARP) {
     // ============================ MMA issuer =================================
     if (nb > 0 && lane == 0) {
-      const uint32_t q_base = smem_u32(sm + OFF_Q);
-      const uint32_t p_base = smem_u32(sm + OFF_P);
+      const uint64_t qd0 = smem_desc(smem_u32(sm + OFF_Q), 16, 1024);
+      const uint64_t pd0 = smem_desc(smem_u32(sm + OFF_P), 16, 1024);
+      const uint64_t rd0 = smem_desc(smem_u32(sm + OFF_ROPE), 16, 1024);
       bool ok = mbar_wait(&bars[B_Q], 0, p.status, kWaitLimitNs, SITE_W_Q);
       if (!ok) s_abort[0] = 1;
       tc_fence_after();
@@ -304,14 +305,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           return false;
         fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tensor core reads
         tc_fence_after();
-        const uint32_t sb = smem_u32(sm + OFF_PAIR + slot * PAIR);
+        const uint64_t sd = smem_desc(smem_u32(sm + OFF_PAIR + slot * PAIR), 16, 1024);
+        const uint64_t qd = desc_add(qd0, 2 * pr * QRS);
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
-          const int c = 2 * pr + h2;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            umma_bf16(d, smem_desc(q_base + c * QRS + kk * 32, 16, 1024),
-                      smem_desc(sb + h2 * CHUNK + kk * 32, 16, 1024), IDESC_S, first ? 0u : 1u);
+            umma_bf16(d, desc_add(qd, h2 * QRS + kk * 32), desc_add(sd, h2 * CHUNK + kk * 32),
+                      IDESC_S, first ? 0u : 1u);
             first = false;
           }
         }
@@ -324,11 +325,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int i = 0; i < 4; ++i) {
           const uint32_t g = 4u * jj + i;
           const int slot = g % NPAIR;
-          const uint32_t vb = smem_u32(sm + OFF_PAIR + slot * PAIR);
+          const uint64_t vd = smem_desc(smem_u32(sm + OFF_PAIR + slot * PAIR), CHUNK, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + i * HN, smem_desc(vb + kk * 2048, CHUNK, 1024),
-                      smem_desc(p_base + kk * 32, 16, 1024), IDESC_O,
+            umma_bf16(tmem + i * HN, desc_add(vd, kk * 2048), desc_add(pd0, kk * 32), IDESC_O,
                       (jj > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&bars[B_PE + slot]);
         }
@@ -352,11 +352,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           fence_proxy_async_smem();
           tc_fence_after();
-          const uint32_t rb = smem_u32(sm + OFF_ROPE);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d, smem_desc(q_base + 8 * QRS + kk * 32, 16, 1024),
-                      smem_desc(rb + kk * 32, 16, 1024), IDESC_S, 1u);
+            umma_bf16(d, desc_add(qd0, 8 * QRS + kk * 32), desc_add(rd0, kk * 32), IDESC_S, 1u);
           umma_commit(&bars[B_RE]);
         }
         if (jj >= 1 && !pv(jj - 1)) { ok = false; break; }
