@@ -15,19 +15,27 @@
 //               copies one 16-byte unit of four fixed keys, so its shared and
 //               global addresses are computed once per block.  (TMA
 //               tile::gather4 moves these 1,152-byte rows about 4x slower.)
-//   warp 4      tcgen05 issuer (one lane):
-//                 S  [128 x 64]  = Q [128(96 heads) x 576] . KV_blk^T   (M=128, N=64)
-//                 O^T[512 x 96] += V_blk^T [512 x 64] . P^T [64 x 96]   (4 x M=128, N=96)
-//               S double-buffered in TMEM columns 384..511, O^T in 0..383.
-//               With six pair slots, the first two pairs and the rope chunk of
-//               block j+1 are multiplied while the softmax of block j runs.
-//   warps 5-12  softmax (two warps per TMEM lane quarter: a thread owns one
+//   warps 4-11  softmax (two warps per TMEM lane quarter: a thread owns one
 //               head and 32 of the block's 64 keys; P = 2^(z - m_ref) against
 //               a lazy reference max, which only moves -- through a rarer,
 //               synchronised path that rescales O^T -- when an exponent would
-//               exceed 64; one named barrier per block), P^T written as BF16,
-//               then the epilogue (O^T / l staged through shared memory into
-//               coalesced BF16 rows of o_lat, and lse).
+//               exceed 64), P^T written as BF16, then the epilogue (O^T / l
+//               staged through shared memory into coalesced BF16 rows of
+//               o_lat, and lse).
+//   warp 12     tcgen05 issuer of the scores (one lane), TMEM owner:
+//                 S  [128 x 64]  = Q [128(96 heads) x 576] . KV_blk^T   (M=128, N=64)
+//   warp 13     tcgen05 issuer of the value product (one lane):
+//                 O^T[512 x 96] += V_blk^T [512 x 64] . P^T [64 x 96]   (4 x M=128, N=96)
+//               S double-buffered in TMEM columns 384..511, O^T in 0..383.
+//               With six pair slots, the first two pairs and the rope chunk of
+//               block j+1 are multiplied while the softmax of block j runs; two
+//               issuers let the value product of block j start the moment P^T
+//               is written, whatever loads the score issuer is waiting on, so
+//               the slots it frees reach the producer sooner.
+// Per 64-key block the tensor core reads about 328 KB of operands from shared
+// memory (Q alone is 144 KB of it) and the gather writes 72 KB, so the shared
+// memory port (128 B/clk) rather than the gather or the tensor pipe sets the
+// floor; more producer warps only contend for it.
 // Q rows 96..127 of the M=128 operand alias the next 64-dim chunk of Q (or the
 // P^T buffer after the last chunk): they only feed accumulator rows no thread
 // reads, so 96 heads cost 108 KB of shared memory instead of 144 KB.
@@ -62,11 +70,19 @@ constexpr int MISC_BYTES = 2048;
 constexpr int SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-constexpr int NPROD = 128;                  // producer threads (warps 0-3)
-constexpr int MMA_WARP = NPROD / 32;        // warp 4
-constexpr int SMX_WARP0 = MMA_WARP + 1;     // warps 5-12
-constexpr int NSMX = 256;                   // softmax / epilogue threads
-constexpr int NTHREADS = NPROD + 32 + NSMX;
+// Roles: warps 0-3 producer, 4-11 softmax, 12 score issuer, 13 value issuer.
+constexpr int NPROD = 128;                        // producer threads (warps 0-3)
+constexpr int NPW = NPROD / 32;
+constexpr int KPT = BK / (4 * NPW);               // keys per producer thread
+constexpr int SMX_WARP0 = NPW;                    // warps 4-11
+constexpr int NSMX = 256;                         // softmax / epilogue threads
+constexpr int MMA_WARP = SMX_WARP0 + NSMX / 32;   // warp 12: scores, TMEM owner
+constexpr int PV_WARP = MMA_WARP + 1;             // warp 13: value product
+constexpr int NTHREADS = NPROD + NSMX + 64;
+static_assert(KPT * 4 * NPW == BK, "producer key split");
+// 14 warps at 128 registers: the 4 warps that share an SM sub-partition
+// exactly fill its 16K-register file.
+static_assert(NTHREADS <= 448, "register budget of the 128-register build");
 constexpr uint32_t S_COL = 384;
 
 // barrier indices
@@ -78,8 +94,9 @@ enum {
   B_RE = B_RF + 1,      // rope empty
   B_SF = B_RE + 1,      // S full [2]
   B_SE = B_SF + 2,      // S empty [2]
-  B_P = B_SE + 2,       // P^T written (and O^T rescaled)
-  B_O = B_P + 1,        // O^T accumulated for a block
+  B_P = B_SE + 2,       // P^T written (common path)
+  B_RARE = B_P + 1,     // rare path done: P^T rewritten, O^T rescaled
+  B_O = B_RARE + 1,     // O^T accumulated for a block
   B_DRAIN = B_O + 1,
   NBAR = B_DRAIN + 1
 };
@@ -111,6 +128,24 @@ struct Params {
 };
 
 __device__ __forceinline__ bool vload(const volatile int* p) { return *p != 0; }
+
+// mbar_wait that gives up quietly (no status) once another role has aborted.
+__device__ __forceinline__ bool mbar_wait_unless(uint64_t* bar, uint32_t parity,
+                                                 const volatile int* abort_flag,
+                                                 uint32_t* status, uint32_t where) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_test(bar, parity)) return true;
+    if (vload(abort_flag)) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      status_raise(status, DSA_ERR_DEVICE_TIMEOUT, where);
+      return false;
+    }
+  }
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -150,7 +185,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   volatile int* g_abort = s_abort + 1;  // [3] softmax-group abort, by iteration mod 3
   volatile int* s_resc = s_abort + 4;   // [3] some head needs an O^T rescale, by iteration mod 3
   float* s_cmax = reinterpret_cast<float*>(sm + OFF_MISC + 256 + 64);   // [2][128] rare path
-  int* s_red = reinterpret_cast<int*>(s_cmax);                           // [16] prologue only
+  int* s_red = reinterpret_cast<int*>(s_cmax);                           // [14] prologue only
   float* s_alpha = s_cmax + 256;                                         // [128] rare path
   volatile uint8_t* s_hover = reinterpret_cast<volatile uint8_t*>(s_alpha + 128);  // [128]
 
@@ -161,7 +196,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (tid == 0) {
     for (int k = 0; k < NBAR; ++k) {
       uint32_t cnt = 1;
-      if (k == B_SE || k == B_SE + 1 || k == B_P) cnt = NSMX;
+      if (k == B_SE || k == B_SE + 1 || k == B_P || k == B_RARE) cnt = NSMX;
+      if (k == B_DRAIN) cnt = 2;  // both issuers
       if ((k >= B_PF && k < B_PF + NPAIR) || k == B_RF) cnt = NPROD;
       mbar_init(&bars[k], cnt);
     }
@@ -215,37 +251,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // a valid physical row to read in place of unused entries (masked later)
   const int dummy_row = p.paged ? 0 : static_cast<int>(static_cast<int64_t>(b) * p.seq_stride);
 
-  if (warp < NPROD / 32) {
+  if (warp < SMX_WARP0) {
     // ====================== producer (4 warps, cp.async) ======================
     // thread: 16-byte unit u = lane & 7 of keys 4w + (lane >> 3) + 16i, i = 0..3
     const int w = warp, unit = lane & 7;
-    int key[4];
-    uint32_t doff[4];
+    int key[KPT];
+    uint32_t doff[KPT];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      key[i] = 4 * w + (lane >> 3) + 16 * i;
+    for (int i = 0; i < KPT; ++i) {
+      key[i] = 4 * w + (lane >> 3) + 4 * NPW * i;
       doff[i] = sw128_unit(key[i], unit);
     }
     // the query block was requested at start-up; with no work it must still land
     if (nb == 0 && tid == 0) mbar_wait(&bars[B_Q], 0, p.status, kWaitLimitNs, SITE_W_Q);
     if (nb > 0) {
       // raw list entries of the next block, fetched one block ahead
-      int s_next[4];
+      int s_next[KPT];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < KPT; ++i) {
         const int e = blk0 * BK + key[i];
         s_next[i] = e < n_list ? __ldg(ix + e) : -1;
       }
       bool ok = true;
       for (int jj = 0; jj < nb && ok; ++jj) {
-        const uint16_t* src[4];
+        const uint16_t* src[KPT];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < KPT; ++i) {
           const int r = entry_row(p, b, t, s_next[i]);
           src[i] = p.kv + static_cast<int64_t>(r >= 0 ? r : dummy_row) * kRlat + unit * 8;
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < KPT; ++i) {
           const int e = (blk0 + jj + 1) * BK + key[i];
           s_next[i] = (jj + 1 < nb && e < n_list) ? __ldg(ix + e) : -1;
         }
@@ -275,12 +311,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (vload(s_abort)) { ok = false; break; }
           if (rope) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) cp_async_16(dbase + doff[i], src[i] + 8 * 64);
+            for (int i = 0; i < KPT; ++i) cp_async_16(dbase + doff[i], src[i] + 8 * 64);
           } else {
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
+              for (int i = 0; i < KPT; ++i)
                 cp_async_16(dbase + h2 * CHUNK + doff[i], src[i] + (2 * pr + h2) * 64);
           }
           cp_async_arrive(full);
@@ -289,87 +325,104 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // every copy this thread issued has landed before the CTA may exit
       asm volatile("cp.async.wait_all;" ::: "memory");
     }
-  } else if (warp == MMA_WARP) {
-    // ============================ MMA issuer =================================
-    if (nb > 0 && lane == 0) {
-      const uint64_t qd0 = smem_desc(smem_u32(sm + OFF_Q), 16, 1024);
-      const uint64_t pd0 = smem_desc(smem_u32(sm + OFF_P), 16, 1024);
-      const uint64_t rd0 = smem_desc(smem_u32(sm + OFF_ROPE), 16, 1024);
-      bool ok = mbar_wait(&bars[B_Q], 0, p.status, kWaitLimitNs, SITE_W_Q);
-      if (!ok) s_abort[0] = 1;
-      tc_fence_after();
-      auto s_pair = [&](int jj, int pr, uint32_t d, bool& first) -> bool {
-        const uint32_t g = 4u * jj + pr;
-        const int slot = g % NPAIR;
-        if (!mbar_wait(&bars[B_PF + slot], (g / NPAIR) & 1, p.status, kWaitLimitNs, SITE_W_PF))
-          return false;
-        fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tensor core reads
+  } else if (warp >= MMA_WARP) {
+    if (warp == MMA_WARP) {
+      // ============================ MMA issuer =================================
+      if (nb > 0 && lane == 0) {
+        const uint64_t qd0 = smem_desc(smem_u32(sm + OFF_Q), 16, 1024);
+        const uint64_t rd0 = smem_desc(smem_u32(sm + OFF_ROPE), 16, 1024);
+        bool ok = mbar_wait(&bars[B_Q], 0, p.status, kWaitLimitNs, SITE_W_Q);
+        if (!ok) s_abort[0] = 1;
         tc_fence_after();
-        const uint64_t sd = smem_desc(smem_u32(sm + OFF_PAIR + slot * PAIR), 16, 1024);
-        const uint64_t qd = desc_add(qd0, 2 * pr * QRS);
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            umma_bf16(d, desc_add(qd, h2 * QRS + kk * 32), desc_add(sd, h2 * CHUNK + kk * 32),
-                      IDESC_S, first ? 0u : 1u);
-            first = false;
-          }
-        }
-        return true;
-      };
-      auto pv = [&](int jj) -> bool {
-        if (!mbar_wait(&bars[B_P], jj & 1, p.status, kWaitLimitNs, SITE_W_P)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t g = 4u * jj + i;
+        auto s_pair = [&](int jj, int pr, uint32_t d, bool& first) -> bool {
+          const uint32_t g = 4u * jj + pr;
           const int slot = g % NPAIR;
-          const uint64_t vd = smem_desc(smem_u32(sm + OFF_PAIR + slot * PAIR), CHUNK, 1024);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + i * HN, desc_add(vd, kk * 2048), desc_add(pd0, kk * 32), IDESC_O,
-                      (jj > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&bars[B_PE + slot]);
+          if (!mbar_wait(&bars[B_PF + slot], (g / NPAIR) & 1, p.status, kWaitLimitNs, SITE_W_PF))
+            return false;
+          fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tensor core reads
+          tc_fence_after();
+          const uint64_t sd = smem_desc(smem_u32(sm + OFF_PAIR + slot * PAIR), 16, 1024);
+          const uint64_t qd = desc_add(qd0, 2 * pr * QRS);
+  #pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+  #pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              umma_bf16(d, desc_add(qd, h2 * QRS + kk * 32), desc_add(sd, h2 * CHUNK + kk * 32),
+                        IDESC_S, first ? 0u : 1u);
+              first = false;
+            }
+          }
+          return true;
+        };
+        for (int jj = 0; jj < nb && ok; ++jj) {
+          if (vload(s_abort)) { ok = false; break; }
+          const int sbuf = jj & 1;
+          const uint32_t d = tmem + S_COL + BK * sbuf;
+          if (jj >= 2 &&
+              !mbar_wait(&bars[B_SE + sbuf], ((jj >> 1) - 1) & 1, p.status, kWaitLimitNs,
+                         SITE_W_SE)) { ok = false; break; }
+          tc_fence_after();
+          bool first = true;
+          if (!s_pair(jj, 0, d, first) || !s_pair(jj, 1, d, first)) { ok = false; break; }
+          {  // rope chunk
+            if (!mbar_wait(&bars[B_RF], jj & 1, p.status, kWaitLimitNs, SITE_W_RF)) {
+              ok = false;
+              break;
+            }
+            fence_proxy_async_smem();
+            tc_fence_after();
+  #pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(d, desc_add(qd0, 8 * QRS + kk * 32), desc_add(rd0, kk * 32), IDESC_S, 1u);
+            umma_commit(&bars[B_RE]);
+          }
+          if (!s_pair(jj, 2, d, first) || !s_pair(jj, 3, d, first)) { ok = false; break; }
+          umma_commit(&bars[B_SF + sbuf]);
         }
-        umma_commit(&bars[B_O]);
-        return true;
-      };
-      for (int jj = 0; jj < nb && ok; ++jj) {
-        if (vload(s_abort)) { ok = false; break; }
-        const int sbuf = jj & 1;
-        const uint32_t d = tmem + S_COL + BK * sbuf;
-        if (jj >= 2 &&
-            !mbar_wait(&bars[B_SE + sbuf], ((jj >> 1) - 1) & 1, p.status, kWaitLimitNs,
-                       SITE_W_SE)) { ok = false; break; }
-        tc_fence_after();
-        bool first = true;
-        if (!s_pair(jj, 0, d, first) || !s_pair(jj, 1, d, first)) { ok = false; break; }
-        {  // rope chunk
-          if (!mbar_wait(&bars[B_RF], jj & 1, p.status, kWaitLimitNs, SITE_W_RF)) {
-            ok = false;
-            break;
+        if (!ok) s_abort[0] = 1;
+        // drain: all issued MMAs complete before TMEM is released
+        umma_commit(&bars[B_DRAIN]);
+        mbar_wait(&bars[B_DRAIN], 0, p.status, kWaitLimitNs, SITE_W_DRAIN);
+      }
+      __syncwarp();
+    } else if (warp == PV_WARP) {
+      // ======================= value-product issuer ============================
+      if (nb > 0 && lane == 0) {
+        const uint64_t pd0 = smem_desc(smem_u32(sm + OFF_P), 16, 1024);
+        bool ok = true;
+        uint32_t nrare = 0;
+        auto pv = [&](int jj) -> bool {
+          if (!mbar_wait_unless(&bars[B_P], jj & 1, s_abort, p.status, SITE_W_P)) return false;
+          if (vload(&s_resc[jj % 3])) {
+            if (!mbar_wait_unless(&bars[B_RARE], nrare & 1, s_abort, p.status, SITE_W_P))
+              return false;
+            ++nrare;
           }
           fence_proxy_async_smem();
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d, desc_add(qd0, 8 * QRS + kk * 32), desc_add(rd0, kk * 32), IDESC_S, 1u);
-          umma_commit(&bars[B_RE]);
-        }
-        if (jj >= 1 && !pv(jj - 1)) { ok = false; break; }
-        if (!s_pair(jj, 2, d, first) || !s_pair(jj, 3, d, first)) { ok = false; break; }
-        umma_commit(&bars[B_SF + sbuf]);
+  #pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t g = 4u * jj + i;
+            const int slot = g % NPAIR;
+            const uint64_t vd = smem_desc(smem_u32(sm + OFF_PAIR + slot * PAIR), CHUNK, 1024);
+  #pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(tmem + i * HN, desc_add(vd, kk * 2048), desc_add(pd0, kk * 32), IDESC_O,
+                        (jj > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(&bars[B_PE + slot]);
+          }
+          umma_commit(&bars[B_O]);
+          return true;
+        };
+        for (int jj = 0; jj < nb && ok; ++jj) ok = pv(jj);
+        if (!ok) s_abort[0] = 1;
+        umma_commit(&bars[B_DRAIN]);
+        mbar_wait(&bars[B_DRAIN], 0, p.status, kWaitLimitNs, SITE_W_DRAIN);
       }
-      if (ok && !vload(s_abort)) ok = pv(nb - 1);
-      if (!ok) s_abort[0] = 1;
-      // drain: all issued MMAs complete before TMEM is released
-      umma_commit(&bars[B_DRAIN]);
-      mbar_wait(&bars[B_DRAIN], 0, p.status, kWaitLimitNs, SITE_W_DRAIN);
+      __syncwarp();
     }
-    __syncwarp();
   } else {
-    // ================ softmax + epilogue (warps 5..12, 8 warps) ================
+    // ================ softmax + epilogue (warps 4..11, 8 warps) ================
     // Two warps per TMEM lane quarter: thread (half, h) owns head h and the
     // keys 32*half .. 32*half+31 of each block.  Both halves of a head move the
     // reference max together (through s_cmax, on the rare path only).
@@ -460,9 +513,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         s_resc[k3] = 1;
       }
       if (!w_ok || vload(s_abort)) g_abort[k3] = 1;
+      // P^T is complete for the common path: the value product may start now;
+      // a block that takes the rare path holds it back (s_resc, B_RARE)
+      mbar_arrive(&bars[B_P]);
       named_bar_sync(1, NSMX);
-      if (vload(&g_abort[k3])) { ok = false; break; }
-      if (gt == 0) s_resc[(jj + 2) % 3] = 0;  // its readers (iteration jj-1) are all past this barrier
+      if (vload(&g_abort[k3])) {
+        s_abort[0] = 1;
+        ok = false;
+        break;
+      }
+      // slot (jj-1) mod 3 is free again: the softmax threads read it before this
+      // barrier and the value-product issuer before it committed B_O(jj-1)
+      if (gt == 0) s_resc[(jj + 2) % 3] = 0;
       if (!vload(&s_resc[k3])) {
         l_sum += blk_sum;
       } else {
@@ -528,9 +590,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           tmem_st_wait();
         }
+        tc_fence_before();
+        mbar_arrive(&bars[B_RARE]);
       }
-      tc_fence_before();
-      mbar_arrive(&bars[B_P]);
     }
     // ------------------------------ epilogue ---------------------------------
     bool have_o = ok && nb > 0;
