@@ -223,16 +223,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const bool q_ok = t >= 0 && t < L && L <= p.max_kv_len;
   if (!q_ok && tid == 0) status_raise(p.status, DSA_ERR_BAD_INDEX, SITE_QPOS, (uint32_t)t);
   const int32_t* ix = p.idx + static_cast<int64_t>(qflat) * p.topk;
+  // every load of the scan is issued before any is used: one memory round
+  // trip instead of one per entry (topk <= MAX_TOPK is checked on the host)
+  constexpr int SCAN = (MAX_TOPK + NTHREADS - 1) / NTHREADS;
+  int sv[SCAN];
+#pragma unroll
+  for (int i = 0; i < SCAN; ++i) {
+    const int e = tid + i * NTHREADS;
+    sv[i] = (q_ok && e < p.topk) ? __ldg(ix + e) : -1;
+  }
   int last = -1;
-  if (q_ok) {
-    for (int e = tid; e < p.topk; e += NTHREADS) {
-      const int s = __ldg(ix + e);
-      if (s < 0) continue;
-      if (entry_row(p, b, t, s) >= 0) {
-        last = e;
-      } else if (sp == 0) {
-        status_raise(p.status, DSA_ERR_BAD_INDEX, s > t ? SITE_IDX : SITE_PAGE, (uint32_t)s);
-      }
+#pragma unroll
+  for (int i = 0; i < SCAN; ++i) {
+    const int s = sv[i];
+    if (s < 0) continue;
+    if (entry_row(p, b, t, s) >= 0) {
+      last = tid + i * NTHREADS;
+    } else if (sp == 0) {
+      status_raise(p.status, DSA_ERR_BAD_INDEX, s > t ? SITE_IDX : SITE_PAGE, (uint32_t)s);
     }
   }
   last = __reduce_max_sync(0xffffffffu, last);
@@ -641,14 +649,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     *reinterpret_cast<uint32_t(*)[16]>(&r[c0]));
         tmem_ld_wait();
       }
+      // 1/l in groups of four heads (one 16-byte broadcast load each), so the
+      // loads do not serialise the conversion and staging stores
 #pragma unroll
-      for (int hh = 0; hh < H; ++hh) {
-        const float v = have_o ? __uint_as_float(r[hh]) * s_invl[hh] : 0.f;
-        if (p.nsplit == 1)
-          reinterpret_cast<uint16_t*>(stage)[hh * 128 + dloc] =
-              __bfloat16_as_ushort(__float2bfloat16_rn(v));
-        else
-          reinterpret_cast<float*>(stage)[hh * 128 + dloc] = v;
+      for (int h4 = 0; h4 < HN; h4 += 4) {
+        const float4 inv = *reinterpret_cast<const float4*>(s_invl + h4);
+        const float iv[4] = {inv.x, inv.y, inv.z, inv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int hh = h4 + e;
+          if (hh < H) {
+            const float v = have_o ? __uint_as_float(r[hh]) * iv[e] : 0.f;
+            if (p.nsplit == 1)
+              reinterpret_cast<uint16_t*>(stage)[hh * 128 + dloc] =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(v));
+            else
+              reinterpret_cast<float*>(stage)[hh * 128 + dloc] = v;
+          }
+        }
       }
       named_bar_sync(1, NSMX);
       if (p.nsplit == 1) {
