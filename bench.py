@@ -36,6 +36,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "DSA indexer+sparse-MLA tokens/s at T=8192,k=2048; % of TC / HBM roofline"
+# DRAM bytes (read + write) of one sparse_mla_kernel launch per query, from the
+# ncu capture summarised in profiles/sparse_mla_val4096.md (855 MB for 4,096
+# queries).  The traffic is q_lat + idx in and o_lat out, so it scales with the
+# number of queries; reset to None whenever the kernel changes.
+MLA_DRAM_BYTES_PER_QUERY = (491.704320e6 + 363.267584e6) / 4096
 
 
 def parse():
@@ -336,7 +341,10 @@ def run_ours(args, rank, world, local):
                      "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
                      "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a step)",
                      "peak_burst": pk_burst, "frac_of_burst": ach / pk_burst if pk_burst else None,
-                     "traffic": None,
+                     "traffic": (MLA_DRAM_BYTES_PER_QUERY * N
+                                 if MLA_DRAM_BYTES_PER_QUERY is not None else None),
+                     "traffic_unit": "bytes per launch (ncu dram read+write on val4096, "
+                                     "scaled by queries)",
                      "algorithmic": f"{pairs} (query, selected key) pairs x 2*H*(576+512) FLOP"},
         "gpu_launches": K * launches_per_step(dsa, B, T, cfg),
         "clocks": clk,
