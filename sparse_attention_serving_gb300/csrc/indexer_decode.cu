@@ -14,9 +14,13 @@
 //                  over heads and writes one FP32 score per key: a linear
 //                  score vector per request in the workspace (4 bytes per key
 //                  against 256 bytes of key read).
-//   decode_select  one CTA per request: radix select (8-bit digits from the
-//                  highest bit where the scores differ) of the k largest
-//                  scores, then writes their positions.
+//                  Each work item also records the smallest and largest score
+//                  of its request (one atomic per warp).
+//   decode_select  one CTA per request: a value histogram between those
+//                  extremes finds the bin of the k-th largest score, a second
+//                  pass writes the keys above it and keeps that bin's keys in
+//                  shared memory, and an exact radix select over them picks
+//                  the rest.
 #include <cmath>
 
 #include <cuda_bf16.h>
@@ -60,9 +64,18 @@ struct Params {
   int32_t max_pages, num_pages;
   int paged;
   int B, max_kv_len;
-  float* scores;  // [B, max_kv_len]
+  float* scores;     // [B, max_kv_len]
+  uint32_t* minmax;  // [B, 2]: min order key, min of the complemented order key
   uint32_t* status;
 };
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
 
 __device__ __forceinline__ bool vflag(const volatile int* p) { return *p != 0; }
 
@@ -248,9 +261,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int t0 = c * CH_TILES;
       const int t1 = min(t0 + CH_TILES, (L + BKEY - 1) / BKEY);
       float* out = p.scores + static_cast<int64_t>(b) * p.max_kv_len;
+      // running extremes of this item's scores as order keys (the select
+      // kernel bins by value between them)
+      uint32_t kmin = 0xffffffffu, kinv = 0xffffffffu;
       for (int kt = t0; kt < t1; ++kt, ++dcount) {
         const int buf = dcount & 3;
-        if (!mbar_wait(&d_full[buf], (dcount >> 2) & 1, p.status, kWaitLimitNs, SITE_W_DF) || vflag(s_abort)) {
+        // warp-uniform exit, so the warp reductions below stay convergent
+        const bool good =
+            mbar_wait(&d_full[buf], (dcount >> 2) & 1, p.status, kWaitLimitNs, SITE_W_DF) &&
+            !vflag(s_abort);
+        if (!__all_sync(0xffffffffu, good)) {
           ok = false;
           break;
         }
@@ -273,7 +293,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_before();
         mbar_arrive(&d_empty[buf]);
         const int s = kt * BKEY + sub * 32 + lane;
-        if (s < L) out[s] = acc;
+        if (s < L) {
+          out[s] = acc;
+          const uint32_t ok_ = order_key(acc);
+          kmin = min(kmin, ok_);
+          kinv = min(kinv, ~ok_);
+        }
+      }
+      kmin = __reduce_min_sync(0xffffffffu, kmin);
+      kinv = __reduce_min_sync(0xffffffffu, kinv);
+      if (lane == 0 && ok && kmin != 0xffffffffu) {
+        atomicMin(p.minmax + 2 * b, kmin);
+        atomicMin(p.minmax + 2 * b + 1, kinv);
       }
     }
   }
@@ -283,11 +314,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 256);
   }
-}
-
-__device__ __forceinline__ uint32_t order_key(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 // Block-wide (1024 threads): find the bin of the 256 (counted from the top
@@ -322,21 +348,107 @@ __device__ void find_bin256(const int* hist, int need, int* out3) {
   __syncthreads();
 }
 
-// One CTA (1024 threads) per request: the k largest of scores[0..L).  Radix
-// select over order-preserving keys: digits start at the highest bit where the
-// smallest and largest score differ (scores share sign and most exponent
-// bits), each warp counts into its own histogram, and the passes stop as soon
-// as the bin holding the k-th key is kept whole.
+// Block-wide (1024 threads): the bin of a 4096-bin histogram, counted from the
+// top bin down, in which the `need`-th largest element falls; writes (bin,
+// remaining need, bin count) to out3.  Thread t owns bins 4095-4t .. 4092-4t.
+__device__ void find_bin4096(const int* hist, int need, int* wsum, int* out3) {
+  const int t = threadIdx.x, l = t & 31, w = t >> 5;
+  int c[4], tot = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) { c[e] = hist[4095 - 4 * t - e]; tot += c[e]; }
+  int incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (l >= o) incl += v;
+  }
+  if (l == 31) wsum[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int x = wsum[l], y = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, y, o);
+      if (l >= o) y += v;
+    }
+    wsum[32 + l] = y - x;  // exclusive prefix of the warp totals
+  }
+  __syncthreads();
+  incl += wsum[32 + w];
+  const int excl = incl - tot;
+  if (excl < need && need <= incl) {
+    int run = excl;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (run < need && need <= run + c[e]) {
+        out3[0] = 4095 - 4 * t - e;
+        out3[1] = need - run;
+        out3[2] = c[e];
+      }
+      run += c[e];
+    }
+  }
+  __syncthreads();
+}
+
+constexpr int SEL_NBIN = 4096;
+constexpr int SEL_CAP = 8192;  // boundary-bin candidates kept in shared memory
+constexpr int SEL_SMEM = SEL_NBIN * 4 + SEL_CAP * 8;
+
+// Visit scores[0..L) of one row: aligned float4 loads, four in flight per
+// thread, with scalar head and tail.  f(e, x) is called once per element.
+template <class F>
+__device__ __forceinline__ void for_each_score(const float* sc, int L, F f) {
+  const int tid = threadIdx.x;
+  const int head = min(L, static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(sc) >> 2) & 3u)) & 3u));
+  if (tid < head) f(tid, sc[tid]);
+  const float4* v4 = reinterpret_cast<const float4*>(sc + head);
+  const int n4 = (L - head) >> 2;
+  for (int i0 = tid; i0 < n4; i0 += 4 * 1024) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i0 + u * 1024 < n4) v[u] = __ldg(v4 + i0 + u * 1024);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * 1024;
+      if (i < n4) {
+        const int e = head + 4 * i;
+        f(e, v[u].x); f(e + 1, v[u].y); f(e + 2, v[u].z); f(e + 3, v[u].w);
+      }
+    }
+  }
+  const int t0 = head + 4 * n4;
+  if (t0 + tid < L) f(t0 + tid, sc[t0 + tid]);
+}
+
+// One CTA (1024 threads) per request: the k largest of scores[0..L).
+//   1. The score kernel left the smallest and largest score of the request.
+//      One pass bins every score linearly between them into 4096 bins (a
+//      monotone map, so a higher bin holds only larger scores) and finds the
+//      bin holding the k-th largest.
+//   2. A second pass writes every key of a higher bin and copies the keys of
+//      that boundary bin (a handful for spread-out scores) to shared memory.
+//   3. A radix select over the candidates' order-preserving keys (8-bit
+//      digits, stopping once the bin of the k-th key is kept whole) picks the
+//      rest exactly.
+// A boundary bin too large for shared memory (scores piled on few values)
+// takes the slower path: radix passes over the whole row, with digits from the
+// highest bit where the smallest and largest score differ.
 __global__ void __launch_bounds__(1024) decode_select_kernel(const float* __restrict__ scores,
+                                                             const uint32_t* __restrict__ minmax,
                                                              const int32_t* __restrict__ kv_len,
                                                              int max_kv_len, int topk,
                                                              int32_t* __restrict__ out_idx) {
-  __shared__ int hist[256];
-  __shared__ int whist[32 * 256];
+  extern __shared__ __align__(16) uint8_t dsm[];
+  int* hist = reinterpret_cast<int*>(dsm);                   // [SEL_NBIN]
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(hist + SEL_NBIN);  // [SEL_CAP]
+  int* cidx = reinterpret_cast<int*>(ckey + SEL_CAP);        // [SEL_CAP]
+  __shared__ int h256[256];
+  __shared__ int wsum[64];
   __shared__ int sel[4];
-  __shared__ unsigned red[4];
-  __shared__ int ctr[2];
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  __shared__ int ctr[3];
+  const int b = blockIdx.x, tid = threadIdx.x;
   int L = __ldg(kv_len + b);
   if (L < 0 || L > max_kv_len) L = 0;  // flagged by the score kernel
   int32_t* out = out_idx + static_cast<int64_t>(b) * topk;
@@ -345,74 +457,114 @@ __global__ void __launch_bounds__(1024) decode_select_kernel(const float* __rest
     return;
   }
   const float* sc = scores + static_cast<int64_t>(b) * max_kv_len;
-  if (tid == 0) { red[0] = 0xffffffffu; red[1] = 0u; }
-  __syncthreads();
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
-  for (int e = tid; e < L; e += 1024) {
-    const uint32_t k = order_key(sc[e]);
-    kmin = min(kmin, k);
-    kmax = max(kmax, k);
+  const uint32_t kmin = __ldg(minmax + 2 * b), kmax = ~__ldg(minmax + 2 * b + 1);
+  if (kmin >= kmax) {
+    // every score equal (or no extremes recorded): any k positions are the top k
+    for (int e = tid; e < topk; e += 1024) out[e] = e;
+    return;
   }
-  kmin = __reduce_min_sync(0xffffffffu, kmin);
-  kmax = __reduce_max_sync(0xffffffffu, kmax);
-  if (lane == 0) { atomicMin(&red[0], kmin); atomicMax(&red[1], kmax); }
+  const float lo = key_float(kmin), hi = key_float(kmax);
+  const float scale = static_cast<float>(SEL_NBIN) / (hi - lo);
+  auto bin_of = [&](float x) -> int {
+    const float f = (x - lo) * scale;  // monotone in x
+    return f >= static_cast<float>(SEL_NBIN - 1) ? SEL_NBIN - 1 : (f > 0.f ? static_cast<int>(f) : 0);
+  };
+  for (int e = tid; e < SEL_NBIN; e += 1024) hist[e] = 0;
+  if (tid == 0) { ctr[0] = 0; ctr[1] = 0; ctr[2] = 0; }
   __syncthreads();
-  const uint32_t diff = red[0] ^ red[1];
-  uint32_t prefix, mask;
-  int need = topk;
-  if (diff == 0u) {
-    prefix = red[1];
-    mask = 0xffffffffu;
-  } else {
-    const int top = 31 - __clz(diff);
-    mask = top >= 31 ? 0u : ~((2u << top) - 1u);
-    prefix = red[1] & mask;
-    int shift = top - 7;
+  const bool binnable = scale > 0.f && scale < 3.0e38f;
+  if (binnable) for_each_score(sc, L, [&](int, float x) { atomicAdd(&hist[bin_of(x)], 1); });
+  __syncthreads();
+  int need = topk, bstar = -1;
+  if (binnable) {
+    find_bin4096(hist, need, wsum, sel);
+    bstar = sel[0];
+    need = sel[1];
+  }
+  if (binnable && sel[2] <= SEL_CAP) {
+    for_each_score(sc, L, [&](int e, float x) {
+      const int bn = bin_of(x);
+      if (bn > bstar) {
+        out[atomicAdd(&ctr[0], 1)] = e;
+      } else if (bn == bstar) {
+        const int c = atomicAdd(&ctr[1], 1);
+        ckey[c] = order_key(x);
+        cidx[c] = e;
+      }
+    });
+    __syncthreads();
+    const int nc = ctr[1];
+    uint32_t prefix = 0u, mask = 0u;
 #pragma unroll 1
-    while (true) {
-      const int width = shift >= 0 ? 8 : 8 + shift;
-      if (shift < 0) shift = 0;
-      const uint32_t dm = (1u << width) - 1u;
-      // one private 256-bin histogram per warp, summed afterwards
-      for (int e = tid; e < 32 * 256; e += 1024) whist[e] = 0;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      if (tid < 256) h256[tid] = 0;
       __syncthreads();
-      int* mine = whist + (tid >> 5) * 256;
-      for (int e = tid; e < L; e += 1024) {
-        const uint32_t k = order_key(sc[e]);
-        if ((k & mask) == prefix) atomicAdd(&mine[(k >> shift) & dm], 1);
+      for (int i = tid; i < nc; i += 1024) {
+        const uint32_t k = ckey[i];
+        if ((k & mask) == prefix) atomicAdd(&h256[(k >> shift) & 255u], 1);
       }
       __syncthreads();
-      if (tid < 256) {
-        int acc = 0;
-#pragma unroll 8
-        for (int w = 0; w < 32; ++w) acc += whist[w * 256 + tid];
-        hist[tid] = acc;
-      }
-      __syncthreads();
-      find_bin256(hist, need, sel);
+      find_bin256(h256, need, sel);
       prefix |= static_cast<uint32_t>(sel[0]) << shift;
-      mask |= dm << shift;
+      mask |= 255u << shift;
       need = sel[1];
-      const bool done = sel[2] == need || shift == 0;
+      const bool done = sel[2] == need;
       __syncthreads();
       if (done) break;
-      shift -= 8;
     }
+    for (int i = tid; i < nc; i += 1024) {
+      const uint32_t m = ckey[i] & mask;
+      bool keep = m > prefix;
+      if (!keep && m == prefix) keep = atomicAdd(&ctr[2], 1) < need;
+      if (keep) out[atomicAdd(&ctr[0], 1)] = cidx[i];
+    }
+    return;
   }
-  if (tid == 0) { ctr[0] = 0; ctr[1] = 0; }
-  __syncthreads();
-  for (int e = tid; e < L; e += 1024) {
-    const uint32_t m = order_key(sc[e]) & mask;
+  // ---- slow path: radix passes over the whole row ----
+  need = topk;
+  const uint32_t diff = kmin ^ kmax;
+  const int top = 31 - __clz(diff);
+  uint32_t mask = top >= 31 ? 0u : ~((2u << top) - 1u);
+  uint32_t prefix = kmax & mask;
+  int shift = top - 7;
+#pragma unroll 1
+  while (true) {
+    const int width = shift >= 0 ? 8 : 8 + shift;
+    if (shift < 0) shift = 0;
+    const uint32_t dm = (1u << width) - 1u;
+    if (tid < 256) h256[tid] = 0;
+    __syncthreads();
+    for_each_score(sc, L, [&](int, float x) {
+      const uint32_t k = order_key(x);
+      if ((k & mask) == prefix) atomicAdd(&h256[(k >> shift) & dm], 1);
+    });
+    __syncthreads();
+    find_bin256(h256, need, sel);
+    prefix |= static_cast<uint32_t>(sel[0]) << shift;
+    mask |= dm << shift;
+    need = sel[1];
+    const bool done = sel[2] == need || shift == 0;
+    __syncthreads();
+    if (done) break;
+    shift -= 8;
+  }
+  for_each_score(sc, L, [&](int e, float x) {
+    const uint32_t m = order_key(x) & mask;
     bool keep = m > prefix;
-    if (!keep && m == prefix) keep = atomicAdd(&ctr[1], 1) < need;
+    if (!keep && m == prefix) keep = atomicAdd(&ctr[2], 1) < need;
     if (keep) out[atomicAdd(&ctr[0], 1)] = e;
-  }
+  });
 }
 
 }  // namespace idxd
 
+// Scratch: the score rows [B, max_kv_len] FP32, then the per-request score
+// extremes [B, 2] (256-byte aligned).
+static size_t minmax_offset(int B, int max_kv_len) {
+  return (static_cast<size_t>(B) * max_kv_len * sizeof(float) + 255) / 256 * 256;
+}
 size_t indexer_decode_scratch_bytes(int B, int max_kv_len) {
-  return static_cast<size_t>(B) * max_kv_len * sizeof(float) + 256;
+  return minmax_offset(B, max_kv_len) + static_cast<size_t>(B) * 2 * sizeof(uint32_t) + 256;
 }
 
 template <int H_I, int D_I>
@@ -439,7 +591,13 @@ static dsa_status_t decode_launch(const IndexerArgs& a, cudaStream_t stream) {
   p.B = a.B;
   p.max_kv_len = a.max_kv_len;
   p.scores = static_cast<float*>(a.scratch);
+  p.minmax = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.scratch) +
+                                         minmax_offset(a.B, a.max_kv_len));
   p.status = a.status;
+  // extremes start at "none seen" (all ones for both minima)
+  if (cudaMemsetAsync(p.minmax, 0xff, static_cast<size_t>(a.B) * 2 * sizeof(uint32_t), stream) !=
+      cudaSuccess)
+    return launch_status("cudaMemsetAsync");
   auto kern = idxd::decode_scores_kernel<H_I, D_I>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
       cudaSuccess)
@@ -449,8 +607,11 @@ static dsa_status_t decode_launch(const IndexerArgs& a, cudaStream_t stream) {
   const int grid = max_items < num_sms() ? max_items : num_sms();
   kern<<<grid, idxd::NTHREADS, C::SMEM_BYTES, stream>>>(tq, tk, p);
   if (launch_status("decode_scores_kernel") != DSA_OK) return DSA_ERR_CUDA;
-  idxd::decode_select_kernel<<<a.B, 1024, 0, stream>>>(p.scores, a.kv_len, a.max_kv_len, a.topk,
-                                                        a.out_idx);
+  if (cudaFuncSetAttribute(idxd::decode_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           idxd::SEL_SMEM) != cudaSuccess)
+    return launch_status("cudaFuncSetAttribute");
+  idxd::decode_select_kernel<<<a.B, 1024, idxd::SEL_SMEM, stream>>>(
+      p.scores, p.minmax, a.kv_len, a.max_kv_len, a.topk, a.out_idx);
   return launch_status("indexer_decode");
 }
 

@@ -206,6 +206,30 @@ def test_decode_small_paged(dsa):
                    rows, "decode mla")
 
 
+def test_decode_select_ties_and_equal_scores(dsa):
+    """Decode top-k on score rows with heavy ties: request 0 draws its keys from
+    two distinct rows (about 10,000 keys share the k-th score, more than the
+    select kernel keeps in shared memory), request 1 has one key row repeated
+    (every score equal), request 2 is ordinary.  Any choice among tied keys is
+    valid; the near-tie rule checks the sets."""
+    cfg = Config("decode-ties", B=3, T=1, topk=2048, H_I=64, D_I=128, H=96, hid=1024, seed=23)
+    lens = np.array([20000, 20000, 5000], np.int32)
+    S = int(lens.max())
+    k_log = normal_bf16(cfg.seed, "k_idx", (cfg.B, S, cfg.D_I))
+    rng = np.random.default_rng([cfg.seed, 99])
+    pick = rng.integers(0, 2, size=S)
+    k_log[0] = k_log[0, pick]          # two distinct key rows
+    k_log[1] = k_log[1, :1]            # one key row everywhere
+    q = prefill_queries(Config(**{**cfg.__dict__, "T": 1}), 0, 1)
+    qs, kl = lens - 1, lens
+    idx = dsa.dsa_indexer_topk(bf(q["q_idx"]), bf(q["w"]), dsa.Rows(bf(k_log)), i32(qs), i32(kl),
+                               cfg.topk, S)
+    torch.cuda.synchronize()
+    gi = idx.cpu().numpy()
+    check_indexer_rows(gi, q["q_idx"], q["w"], k_log, qs, kl, cfg.topk, np.arange(cfg.B),
+                       "decode ties")
+
+
 def test_gate_zero_weight_gives_half(dsa):
     """W_g = 0: out = 0.5 * (W_uv_h . o_lat_h) exactly up to BF16 rounding."""
     cfg = CONFIGS["tiny"]
