@@ -488,6 +488,27 @@ def run_decode(args, rank, world, local, cfg):
     nbytes = decode_bytes(d["kv_len"], cfg.topk, cfg.H, cfg.H_I, cfg.D_I)
     ach = nbytes / t_step / 1e9
     idx_bytes = int(d["kv_len"].astype(np.int64).sum()) * cfg.D_I * 2
+    # the cache append that precedes a decode step (indexer-key LayerNorm + the
+    # two row writes), timed on its own after the steps so that the caches the
+    # steps read are not changed under them; not part of the step's number
+    from workloads import append_inputs
+    ap = append_inputs(cfg.seed, B, 1, cfg.D_I)
+    k_pre, kv_new = torch.from_numpy(ap["k_pre"]).to(dev), up(ap["kv_new"])
+    ws_app = dsa.new_workspace(dsa.workspace_bytes(dsa.OP_CACHE_APPEND, B, 1, 0, 0, 0), dev)
+    for _ in range(3):
+        dsa.dsa_cache_append(k_pre, kv_new, krows, kvrows, qs, workspace=ws_app)
+    torch.cuda.synchronize(dev)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(K):
+        dsa.dsa_cache_append(k_pre, kv_new, krows, kvrows, qs, workspace=ws_app)
+    a1.record(stream)
+    torch.cuda.synchronize(dev)
+    code, where, detail = dsa.read_device_status(ws_app)
+    if code != dsa.DSA_OK:
+        raise RuntimeError(f"append device status {code} at {where:#x} ({detail})")
+    t_app = a0.elapsed_time(a1) / K / 1e3
+    app_bytes = B * (cfg.D_I * 4 + 1152 + cfg.D_I * 2 + 1152)
     res = {
         "metric": METRIC, "value": B * world / t_step, "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": t_step * 1e3,
@@ -500,7 +521,10 @@ def run_decode(args, rank, world, local, cfg):
         "kernels": {"dsa_indexer_topk": {"ms": t_idx * 1e3,
                                          "gbs": idx_bytes / t_idx / 1e9,
                                          "frac": idx_bytes / t_idx / 1e9 / hbm},
-                    "sparse_mla_fwd": {"ms": t_mla * 1e3}},
+                    "sparse_mla_fwd": {"ms": t_mla * 1e3},
+                    "dsa_cache_append": {"us": t_app * 1e6, "gbs": app_bytes / t_app / 1e9,
+                                         "bytes": app_bytes,
+                                         "note": "timed separately, back to back; not in the step"}},
         "roofline": {"kernel": "decode step", "bound": "hbm", "achieved": ach, "peak": hbm,
                      "unit": "GB/s", "frac": ach / hbm, "traffic": None,
                      "algorithmic": f"{nbytes} compulsory bytes per step"},

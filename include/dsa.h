@@ -100,7 +100,8 @@ typedef struct {
 typedef enum {
   DSA_OP_INDEXER_TOPK = 0,
   DSA_OP_SPARSE_MLA = 1,
-  DSA_OP_GATE = 2
+  DSA_OP_GATE = 2,
+  DSA_OP_CACHE_APPEND = 3
 } dsa_op_t;
 
 /* Bytes of workspace an op needs for the given sizes (heads = H_I for the
@@ -163,6 +164,33 @@ dsa_status_t sparse_mla_fwd(const uint16_t* q_lat, const dsa_rows_t* kv, const i
 dsa_status_t mla_gate_apply(const uint16_t* x, const uint16_t* W_g, const uint16_t* o_lat,
                             const uint16_t* W_uv, int N, int hid, int H, int dv, uint16_t* out,
                             void* workspace, size_t ws_bytes, dsa_stream_t stream);
+
+/*
+ * The step just before the indexer: LayerNorm of the new tokens' indexer keys
+ * and their append, with the new latent rows, to the two caches ("Kimi K3.1
+ * Pro" archdiff blueprint: LayerNorm on the indexer key; eps is
+ * KimiK3TextConfig rms_norm_eps, 1e-5).  One call covers a decode step (Tq = 1)
+ * or a prefill chunk.
+ *   k_pre    [B, Tq, D_I] FP32   the new tokens' raw indexer keys
+ *   kv_new   [B, Tq, 576] BF16   their latent rows (c_kv then k_pe), copied as is
+ *   k_cache  rows of width D_I   row q_start[b]+i of sequence b is written with
+ *            BF16 (round to nearest even) of (x - mean(x)) / sqrt(var(x) + eps),
+ *            x = k_pre[b,i,:], var the population variance (unit gain, zero
+ *            bias), computed in FP32
+ *   kv_cache rows of width 576   row q_start[b]+i of sequence b := kv_new[b,i,:]
+ *   q_start  [B] int32 (device)  position of sequence b's first new token
+ * The caches' base pointers are written through: dsa_rows_t declares them const
+ * for the read-side calls that share it.  A row that does not exist -- a
+ * negative position, a page beyond max_pages, a block-table entry outside
+ * [0, num_pages), or past seq_stride when contiguous -- is not written and is
+ * recorded as DSA_ERR_BAD_INDEX in the workspace status word.
+ * Supported: D_I in {64, 128}; B, Tq >= 1; eps >= 0 and finite.  Workspace:
+ * dsa_workspace_bytes(DSA_OP_CACHE_APPEND, ...) = the 256-byte status header.
+ */
+dsa_status_t dsa_cache_append(const float* k_pre, const uint16_t* kv_new,
+                              const dsa_rows_t* k_cache, const dsa_rows_t* kv_cache,
+                              const int32_t* q_start, int B, int Tq, int D_I, float eps,
+                              void* workspace, size_t ws_bytes, dsa_stream_t stream);
 
 /*
  * sparse_mla_fwd_noalloc -- sparse_mla_fwd for callers that cannot allocate

@@ -55,6 +55,8 @@ def load(path: str | None = None):
         lib.oracle_explicit_mla.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i32, i32, i32,
                                             i32, f64, P]
         lib.oracle_gate.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, i64, P, P]
+        lib.oracle_layernorm.argtypes = [P, i64, i32, f64, P]
+        lib.oracle_bf16_rne.argtypes = [P, i64, P]
         lib.oracle_set_threads.argtypes = [i32]
         for f in ("oracle_indexer_scores", "oracle_topk", "oracle_sparse_mla", "oracle_dense_mla",
                   "oracle_explicit_mla", "oracle_gate", "oracle_set_threads",
@@ -221,3 +223,52 @@ def indexer_topk(q_idx, w, k_idx, q_start, kv_len, k, rows=None, lib=None):
     n_valid = (qs[rows // Tq] + rows % Tq + 1).astype(np.int32)
     idx, kth = topk(sc, n_valid, k, lib=lib)
     return idx, kth, sc, n_valid
+
+
+def layernorm(x, eps, lib=None) -> np.ndarray:
+    """x [..., D] float32 -> float64 LayerNorm over the last axis (unit gain, zero
+    bias, population variance) ("Kimi K3.1 Pro" archdiff blueprint: LayerNorm on
+    the indexer key)."""
+    lib = lib or load()
+    x = _c(x, np.float32)
+    D = x.shape[-1]
+    y = np.empty(x.shape, np.float64)
+    _check(lib.oracle_layernorm(_p(x), x.size // D, D, float(eps), _p(y)), "oracle_layernorm")
+    return y
+
+
+def bf16_rne(v, lib=None) -> np.ndarray:
+    """float64 -> BF16 bit patterns, round to nearest, ties to even."""
+    lib = lib or load()
+    v = _c(v, np.float64)
+    out = np.empty(v.shape, np.uint16)
+    _check(lib.oracle_bf16_rne(_p(v), v.size, _p(out)), "oracle_bf16_rne")
+    return out
+
+
+def cache_append(k_pre, kv_new, q_start, eps, k_cache, kv_cache, k_block_table=None,
+                 kv_block_table=None, page=64, lib=None):
+    """The cache append that precedes the indexer, on copies of the caches.
+
+    k_pre [B,Tq,D] float32, kv_new [B,Tq,576] BF16 bits, q_start [B]; caches are
+    contiguous [B,S,W] or page pools [P,page,W] with block tables [B,max_pages].
+    Row q_start[b]+i of sequence b receives BF16(LayerNorm(k_pre[b,i])) and
+    kv_new[b,i].  Returns (k_cache', kv_cache', (k_ln float64, positions))."""
+    lib = lib or load()
+    k_ln = layernorm(k_pre, eps, lib)
+    k_bits = bf16_rne(k_ln, lib)
+    kc, vc = np.array(k_cache, copy=True), np.array(kv_cache, copy=True)
+    B, Tq, _ = k_pre.shape
+
+    def place(cache, bt, b, pos, row):
+        if bt is None:
+            cache[b, pos] = row
+        else:
+            cache[bt[b, pos // page], pos % page] = row
+
+    for b in range(B):
+        for i in range(Tq):
+            pos = int(q_start[b]) + i
+            place(kc, k_block_table, b, pos, k_bits[b, i])
+            place(vc, kv_block_table, b, pos, kv_new[b, i])
+    return kc, vc, k_ln

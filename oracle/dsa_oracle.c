@@ -479,3 +479,55 @@ int oracle_gate(const uint16_t* x, const uint16_t* W_g, const double* o_lat, con
   parallel_rows(n_rows, gate_row, &c);
   return OR_OK;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Indexer-key LayerNorm  [ARCH "LayerNorm on the indexer key"; CFG          */
+/*                         rms_norm_eps for eps]                             */
+/* ------------------------------------------------------------------------- */
+
+/* x [n, D] float -> y [n, D] double:  y = (x - mean x) / sqrt(var x + eps),
+ * population variance over the row, unit gain and zero bias (the blueprint
+ * names the normalisation and nothing else).  Mean and variance are the plain
+ * sums of the definition in double, the variance over the centred values. */
+int oracle_layernorm(const float* x, int64_t n, int D, double eps, double* y) {
+  if (!x || !y || n < 0 || D <= 0 || !(eps >= 0.0)) return OR_BAD_ARG;
+  for (int64_t r = 0; r < n; ++r) {
+    const float* xr = x + r * (int64_t)D;
+    double* yr = y + r * (int64_t)D;
+    double mean = 0.0;
+    for (int d = 0; d < D; ++d) mean += (double)xr[d];
+    mean /= D;
+    double var = 0.0;
+    for (int d = 0; d < D; ++d) var += ((double)xr[d] - mean) * ((double)xr[d] - mean);
+    var /= D;
+    const double inv = 1.0 / sqrt(var + eps);
+    for (int d = 0; d < D; ++d) yr[d] = ((double)xr[d] - mean) * inv;
+  }
+  return OR_OK;
+}
+
+/* Round each double to the nearest BF16 value (8 significant bits, ties to
+ * even) and return the 16-bit patterns.  Written from the definition: the
+ * significand is scaled to [128, 256), rounded to an integer with the default
+ * round-half-even mode, and the result (exactly a float) gives the top half of
+ * its float bit pattern.  Finite values of normal float magnitude only. */
+int oracle_bf16_rne(const double* v, int64_t n, uint16_t* out) {
+  if (!v || !out || n < 0) return OR_BAD_ARG;
+  for (int64_t i = 0; i < n; ++i) {
+    const double a = v[i];
+    if (a == 0.0) {
+      out[i] = signbit(a) ? 0x8000u : 0x0000u;
+      continue;
+    }
+    if (!isfinite(a) || fabs(a) < 0x1p-126 || fabs(a) >= 0x1p127) return OR_BAD_ARG;
+    int e;
+    const double m = frexp(fabs(a), &e);   /* |a| = m * 2^e, m in [0.5, 1) */
+    double r = nearbyint(m * 256.0);       /* 8 significant bits */
+    if (r == 256.0) { r = 128.0; e += 1; }
+    const float f = (float)ldexp(a < 0 ? -r : r, e - 8);
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    out[i] = (uint16_t)(bits >> 16);
+  }
+  return OR_OK;
+}

@@ -10,6 +10,7 @@ Entry points (same names as the C ABI):
   dsa_indexer_topk  lightning indexer scores + top-k key positions
   sparse_mla_fwd    latent-space attention over the selected rows
   mla_gate_apply    sigmoid output gate applied after the per-head up-projection
+  dsa_cache_append  LayerNorm of new indexer keys + append of keys and latent rows
 """
 
 from __future__ import annotations
@@ -31,7 +32,8 @@ DSA_ERR_DEVICE_TIMEOUT = 4
 DSA_ERR_BAD_INDEX = 5
 DSA_ERR_WORKSPACE_TOO_SMALL = 6
 
-OP_INDEXER_TOPK, OP_SPARSE_MLA, OP_GATE = 0, 1, 2
+OP_INDEXER_TOPK, OP_SPARSE_MLA, OP_GATE, OP_CACHE_APPEND = 0, 1, 2, 3
+INDEXER_KEY_EPS = 1e-5   # KimiK3TextConfig rms_norm_eps
 RLAT, VLAT, PAGE = 576, 512, 64
 MLA_SCALE = 1.0 / math.sqrt(128 + 64)   # qk_nope_head_dim + qk_rope_head_dim
 
@@ -50,7 +52,7 @@ class _Rows(ctypes.Structure):
 
 EXPORTS = ("dsa_abi_version", "dsa_status_string", "dsa_workspace_bytes", "dsa_workspace_init",
            "dsa_read_device_status", "dsa_indexer_topk", "sparse_mla_fwd", "mla_gate_apply",
-           "dsa_selftest_wait_timeout")
+           "dsa_cache_append", "dsa_selftest_wait_timeout")
 
 
 def _load(path: str = LIB_PATH):
@@ -70,9 +72,11 @@ def _load(path: str = LIB_PATH):
     lib.sparse_mla_fwd.argtypes = [P, ctypes.POINTER(_Rows), P, P, P, I, I, I, I, I,
                                    ctypes.c_float, P, P, P, Z, P]
     lib.mla_gate_apply.argtypes = [P, P, P, P, I, I, I, I, P, P, Z, P]
+    lib.dsa_cache_append.argtypes = [P, P, ctypes.POINTER(_Rows), ctypes.POINTER(_Rows), P, I, I, I,
+                                     ctypes.c_float, P, Z, P]
     lib.dsa_selftest_wait_timeout.argtypes = [P, Z, ctypes.c_uint64, P]
     for f in ("dsa_workspace_init", "dsa_read_device_status", "dsa_indexer_topk",
-              "sparse_mla_fwd", "mla_gate_apply", "dsa_selftest_wait_timeout"):
+              "sparse_mla_fwd", "mla_gate_apply", "dsa_cache_append", "dsa_selftest_wait_timeout"):
         getattr(lib, f).restype = I
     return lib
 
@@ -237,3 +241,23 @@ def mla_gate_apply(x, W_g, o_lat, W_uv, out=None, workspace=None, stream=None):
                               _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
            "mla_gate_apply")
     return out
+
+
+def dsa_cache_append(k_pre, kv_new, k_cache: Rows, kv_cache: Rows, q_start,
+                     eps: float = INDEXER_KEY_EPS, workspace=None, stream=None):
+    """k_pre [B,Tq,D_I] float32, kv_new [B,Tq,576] bf16, caches as Rows (written in
+    place), q_start [B] int32: LayerNorm'd BF16 keys and the latent rows land at
+    positions q_start[b]+i.  Returns the workspace (its status word holds any
+    BAD_INDEX raised for rows the caches do not have)."""
+    _need(k_pre, torch.float32, "k_pre")
+    _need(kv_new, torch.bfloat16, "kv_new")
+    _need(q_start, torch.int32, "q_start")
+    B, Tq, D_I = k_pre.shape
+    if tuple(kv_new.shape) != (B, Tq, RLAT):
+        raise ValueError("kv_new must be [B, Tq, 576]")
+    ws = _ws(workspace, OP_CACHE_APPEND, B, Tq, 0, 0, 0, k_pre.device, stream)
+    kr, vr = k_cache.c(), kv_cache.c()
+    _check(lib.dsa_cache_append(_ptr(k_pre), _ptr(kv_new), ctypes.byref(kr), ctypes.byref(vr),
+                                _ptr(q_start), B, Tq, D_I, float(eps), _ptr(ws), ws.numel(),
+                                _stream(stream)), "dsa_cache_append")
+    return ws

@@ -265,4 +265,34 @@ dsa_status_t mla_gate_apply(const uint16_t* x, const uint16_t* W_g, const uint16
   return gate_launch(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+dsa_status_t dsa_cache_append(const float* k_pre, const uint16_t* kv_new,
+                              const dsa_rows_t* k_cache, const dsa_rows_t* kv_cache,
+                              const int32_t* q_start, int B, int Tq, int D_I, float eps,
+                              void* workspace, size_t ws_bytes, dsa_stream_t stream) {
+  if (!k_pre || !kv_new || !q_start) return DSA_ERR_INVALID_ARGUMENT;
+  if (!aligned(k_pre, 16) || !aligned(kv_new, 16) || !aligned(q_start, 4))
+    return DSA_ERR_INVALID_ARGUMENT;
+  if (B <= 0 || Tq <= 0 || !(eps >= 0.f) || !(eps < 3.0e38f)) return DSA_ERR_INVALID_ARGUMENT;
+  if (D_I != 64 && D_I != 128) return DSA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * Tq >= (int64_t(1) << 31)) return DSA_ERR_UNSUPPORTED;
+  AppendArgs a{};
+  // positions live on the device: only the structure is checked here, each
+  // row's existence on the device
+  dsa_status_t st = resolve_rows(k_cache, B, 0, D_I, &a.k_cache);
+  if (st != DSA_OK) return st;
+  st = resolve_rows(kv_cache, B, 0, kRlat, &a.kv_cache);
+  if (st != DSA_OK) return st;
+  st = check_ws(workspace, ws_bytes, dsa_workspace_bytes(DSA_OP_CACHE_APPEND, B, Tq, 0, 0, 0));
+  if (st != DSA_OK) return st;
+  a.k_pre = k_pre;
+  a.kv_new = kv_new;
+  a.q_start = q_start;
+  a.B = B;
+  a.Tq = Tq;
+  a.D_I = D_I;
+  a.eps = eps;
+  a.status = static_cast<uint32_t*>(workspace);
+  return cache_append_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

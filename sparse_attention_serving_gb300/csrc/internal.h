@@ -77,6 +77,19 @@ struct GateArgs {
 };
 dsa_status_t gate_launch(const GateArgs& a, cudaStream_t stream);
 
+// --- cache append (indexer-key LayerNorm + latent row copy) -----------------------
+struct AppendArgs {
+  const float* k_pre;
+  const uint16_t* kv_new;
+  RowStore k_cache;   // written through (base is cast to non-const)
+  RowStore kv_cache;
+  const int32_t* q_start;
+  int B, Tq, D_I;
+  float eps;
+  uint32_t* status;
+};
+dsa_status_t cache_append_launch(const AppendArgs& a, cudaStream_t stream);
+
 int num_sms();
 
 // DSA_ERR_CUDA when the last launch failed (the CUDA error text goes to stderr

@@ -401,4 +401,78 @@ def pin_gate_row_subset(lib):
     np.testing.assert_array_equal(part, full[rows])
 
 
+
+
+# ---------------------------------------------------------------------------
+# Indexer-key LayerNorm, BF16 rounding and the cache append
+# ("Kimi K3.1 Pro" archdiff blueprint: LayerNorm on the indexer key;
+#  KimiK3TextConfig rms_norm_eps)
+# ---------------------------------------------------------------------------
+
+def pin_layernorm_worked_example(lib):
+    g = json.load(open(os.path.join(GOLDEN, "layernorm_worked.json")))
+    y = oracle.layernorm(np.array([g["x"]], np.float32), g["eps"], lib)[0]
+    assert np.max(np.abs(y - np.array(g["y"]))) < g["y_tol"], y
+    bits = oracle.bf16_rne(y, lib)
+    assert [int(b, 16) for b in g["bf16"]] == bits.tolist(), [hex(b) for b in bits]
+
+
+def pin_layernorm_moments_closed_form(lib):
+    """mean(y) = 0 and mean(y^2) = var/(var + eps) for every row."""
+    rng = np.random.default_rng(31)
+    x = (rng.standard_normal((50, 128)) * rng.uniform(0.01, 5, (50, 1)) + rng.uniform(-3, 3, (50, 1)))
+    x = x.astype(np.float32)
+    eps = 1e-5
+    y = oracle.layernorm(x, eps, lib)
+    xd = x.astype(np.float64)
+    var = xd.var(axis=1)
+    assert np.max(np.abs(y.mean(axis=1))) < 1e-12
+    np.testing.assert_allclose((y * y).mean(axis=1), var / (var + eps), rtol=1e-12)
+
+
+def pin_layernorm_constant_row_is_zero(lib):
+    y = oracle.layernorm(np.full((3, 64), 2.75, np.float32), 1e-5, lib)
+    assert np.all(y == 0.0)
+
+
+def pin_layernorm_matches_library(lib):
+    import torch
+    rng = np.random.default_rng(32)
+    x = rng.standard_normal((20, 64)).astype(np.float32) * 3 + 1
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x.astype(np.float64)), (64,), eps=1e-5)
+    np.testing.assert_allclose(oracle.layernorm(x, 1e-5, lib), ref.numpy(), rtol=0, atol=1e-12)
+
+
+def pin_bf16_rounding_definition(lib):
+    """Ties to even at the two midpoints next to 1.0, and agreement with torch's
+    float32 -> bfloat16 conversion on values a float32 holds exactly."""
+    import torch
+    b = oracle.bf16_rne(np.array([1.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -1.5, 0.0, -0.0]), lib)
+    assert b.tolist() == [0x3F80, 0x3F80, 0x3F82, 0xBFC0, 0x0000, 0x8000], [hex(v) for v in b]
+    rng = np.random.default_rng(33)
+    v = (rng.standard_normal(4000) * np.exp(rng.uniform(-20, 20, 4000))).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(oracle.bf16_rne(v.astype(np.float64), lib), ref)
+
+
+def pin_cache_append_places_rows(lib):
+    """Rows land at q_start[b]+i through the block table; nothing else changes."""
+    rng = np.random.default_rng(34)
+    B, Tq, D, page = 2, 3, 64, 64
+    bt = np.array([[3, 0], [1, 2]], np.int32)
+    pool_k = rng.integers(0, 65535, (4, page, D), dtype=np.uint16)
+    pool_v = rng.integers(0, 65535, (4, page, 576), dtype=np.uint16)
+    k_pre = rng.standard_normal((B, Tq, D)).astype(np.float32)
+    kv_new = rng.integers(0, 65535, (B, Tq, 576), dtype=np.uint16)
+    q_start = np.array([62, 10], np.int32)
+    kc, vc, k_ln = oracle.cache_append(k_pre, kv_new, q_start, 1e-5, pool_k, pool_v, bt, bt, page, lib)
+    touched = {(3, 62), (3, 63), (0, 0), (1, 10), (1, 11), (1, 12)}
+    for p_ in range(4):
+        for s in range(page):
+            if (p_, s) not in touched:
+                assert np.array_equal(kc[p_, s], pool_k[p_, s]) and np.array_equal(vc[p_, s], pool_v[p_, s])
+    assert np.array_equal(vc[0, 0], kv_new[0, 2]) and np.array_equal(vc[1, 12], kv_new[1, 2])
+    assert np.array_equal(kc[3, 63], oracle.bf16_rne(k_ln[0, 1], lib))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -7,11 +7,15 @@
   qualify.
 * Floating-point outputs: max-abs <= 2e-2 and relative L2 <= 1e-2 against the
   float64 oracle; log-sum-exp within 1e-3 absolute.
+* BF16 results of an FP32 computation (the indexer-key LayerNorm): equal to the
+  oracle's rounding of its float64 value, except next to a rounding midpoint.
 """
 
 from __future__ import annotations
 
 import numpy as np
+
+from workloads import bf16_to_f32
 
 TIE_REL = 1e-3
 MAX_ABS = 2e-2
@@ -69,3 +73,35 @@ def check_lse(gpu: np.ndarray, ref: np.ndarray, what: str):
     m = float(d.max()) if d.size else 0.0
     assert m <= LSE_ABS, f"{what}: lse max-abs {m:.3g} > {LSE_ABS}"
     return m
+
+
+# BF16 results of an FP32 computation (the indexer-key LayerNorm) against the
+# float64 value v: the GPU's BF16 must lie between the round-to-nearest-even
+# BF16 values of v - delta and v + delta, where delta bounds the FP32
+# computation's own error.  For y = (x - mean) / sqrt(var + eps) computed in FP32
+# (a tree sum of at most 128 terms for the mean, one subtraction, a correctly
+# rounded square root, division and product) the error is below
+#   inv * (8 * 2^-24 * mean|x| + 2^-24 * |x - mean|) + 4 * 2^-24 * |y|,
+# inv = 1/sqrt(var + eps); the tests use 2^-20 in place of 8 * 2^-24 and
+# 2^-22 for the others, so near-zero outputs (x close to the mean, where the
+# subtraction cancels) get an absolute allowance and the rest a few 2^-24.
+def layernorm_delta(x: np.ndarray, v: np.ndarray, eps: float) -> np.ndarray:
+    x = np.asarray(x, np.float64)
+    mean = x.mean(axis=-1, keepdims=True)
+    inv = 1.0 / np.sqrt(((x - mean) ** 2).mean(axis=-1, keepdims=True) + eps)
+    mabs = np.abs(x).mean(axis=-1, keepdims=True)
+    return inv * (2.0 ** -20 * mabs + 2.0 ** -22 * np.abs(x - mean)) + 2.0 ** -22 * np.abs(v)
+
+
+def check_bf16_of(gpu_bits: np.ndarray, v: np.ndarray, delta: np.ndarray, what: str):
+    import oracle
+    gpu_bits = np.asarray(gpu_bits, np.uint16).ravel()
+    v = np.asarray(v, np.float64).ravel()
+    delta = np.asarray(delta, np.float64).ravel()
+    lo = bf16_to_f32(oracle.bf16_rne(v - delta)).astype(np.float64)
+    hi = bf16_to_f32(oracle.bf16_rne(v + delta)).astype(np.float64)
+    g = bf16_to_f32(gpu_bits).astype(np.float64)
+    ok = (g >= lo) & (g <= hi)
+    assert ok.all(), (f"{what}: {int((~ok).sum())} BF16 values outside rounding of the exact "
+                      f"value +- delta, e.g. gpu={g[~ok][:4]} exact={v[~ok][:4]} delta={delta[~ok][:4]}")
+    return int((gpu_bits != oracle.bf16_rne(v)).sum())

@@ -30,6 +30,10 @@ MUTANTS = {
                                        "acc += Wk[(int64_t)e * c->R + d] * ck[d];"),
     "sparse_ignores_minus_one_wrongly": ("if (s < 0) continue;\n      if (s > t",
                                          "if (s < 0) s = 0;\n      if (s > t"),
+    "layernorm_sample_variance": ("    var /= D;\n", "    var /= (D - 1);\n"),
+    "layernorm_eps_dropped": ("const double inv = 1.0 / sqrt(var + eps);",
+                              "const double inv = 1.0 / sqrt(var);"),
+    "bf16_ties_away_from_zero": ("double r = nearbyint(m * 256.0);", "double r = round(m * 256.0);"),
 }
 
 

@@ -37,7 +37,7 @@ PAGE = 64        # tokens per cache page
 # one stream id per array; never reuse an id for a different array
 _STREAM = {
     "x": 1, "W_g": 2, "W_uv": 3, "q_idx": 4, "w": 5, "k_idx": 6,
-    "q_lat": 7, "kv": 8, "pages": 9, "lens": 10,
+    "q_lat": 7, "kv": 8, "pages": 9, "lens": 10, "k_pre": 11, "kv_new": 12,
 }
 
 
@@ -286,3 +286,16 @@ def chunked(cfg: Config, c: int) -> dict:
     d["q_start"] = np.full(cfg.B, q0, np.int32)
     d["kv_len"] = np.full(cfg.B, q0 + cfg.chunk, np.int32)
     return d
+
+
+def append_inputs(seed: int, B: int, Tq: int, D_I: int) -> dict:
+    """New tokens for the cache append: raw indexer keys k_pre [B, Tq, D_I] FP32
+    (each row N(mu, sigma^2) with its own mu ~ U(-2, 2) and sigma ~ U(0.2, 4), so
+    that centring and scaling both matter) and latent rows kv_new [B, Tq, 576]
+    BF16 ~ N(0, 1)."""
+    r = _rng(seed, "k_pre")
+    mu = r.uniform(-2.0, 2.0, (B, Tq, 1))
+    sigma = r.uniform(0.2, 4.0, (B, Tq, 1))
+    k_pre = (r.standard_normal((B, Tq, D_I)) * sigma + mu).astype(np.float32)
+    kv_new = normal_bf16(seed, "kv_new", (B, Tq, R_LAT))
+    return {"k_pre": k_pre, "kv_new": kv_new}
