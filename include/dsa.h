@@ -151,6 +151,24 @@ dsa_status_t sparse_mla_fwd(const uint16_t* q_lat, const dsa_rows_t* kv, const i
                             void* workspace, size_t ws_bytes, dsa_stream_t stream);
 
 /*
+ * sparse_mla_fwd with a learnable attention sink ("Kimi K3.1 Pro" archdiff
+ * blueprint, "Output gate + sink"; whether K3.1 uses it is not settled by the
+ * pages, so it is a separate entry point).  Same arguments as sparse_mla_fwd
+ * plus
+ *   sink [H] FP32 (device)   per-head sink logit in natural-log units
+ * which joins each head's softmax denominator with no value row:
+ *   o = sum_s e^{z_s} v_s / (e^{sink} + sum_s e^{z_s}),
+ *   lse = log(e^{sink} + sum_s e^{z_s})
+ * A query with no valid entry gets o = 0 and lse = sink.  sink = -inf for a head
+ * gives sparse_mla_fwd's result for it.  sink must not be NULL.
+ */
+dsa_status_t sparse_mla_fwd_sink(const uint16_t* q_lat, const dsa_rows_t* kv, const int32_t* idx,
+                                 const int32_t* q_start, const int32_t* kv_len, int B, int Tq,
+                                 int H, int topk, int max_kv_len, float scale, const float* sink,
+                                 uint16_t* o_lat, float* lse, void* workspace, size_t ws_bytes,
+                                 dsa_stream_t stream);
+
+/*
  * Output gate ("Kimi K3.1 Pro" archdiff blueprint: sigma(x W_g) (.) o;
  * "Kimi-K3.1-Pro", Implementation Limits, closing paragraph: the gate is kept;
  * KimiK3TextConfig mla_use_output_gate, v_head_dim 128).

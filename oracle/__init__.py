@@ -55,6 +55,8 @@ def load(path: str | None = None):
         lib.oracle_explicit_mla.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i32, i32, i32,
                                             i32, f64, P]
         lib.oracle_gate.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, i64, P, P]
+        lib.oracle_sparse_mla_sink.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f64, P,
+                                               i64, P, P, P]
         lib.oracle_layernorm.argtypes = [P, i64, i32, f64, P]
         lib.oracle_bf16_rne.argtypes = [P, i64, P]
         lib.oracle_set_threads.argtypes = [i32]
@@ -136,12 +138,14 @@ def topk(scores, n_valid, k, lib=None):
     return idx, kth
 
 
-def sparse_mla(q_lat, kv, idx, q_start, kv_len, scale, rows=None, lib=None):
+def sparse_mla(q_lat, kv, idx, q_start, kv_len, scale, rows=None, lib=None, sink=None):
     """Latent-space attention over the selected rows only (value = first 512 dims).
 
     Follows "Kimi-K3.1-Pro" (NeMo AutoModel), Implementation Limits, bullets 1-2;
     dims from KimiK3TextConfig (v0.4 API); no rotation ("Kimi K3.1 Pro",
     archdiff summary: no positional encoding).  Returns (o [n,H,512], lse [n,H]).
+    sink: optional [H] learnable sink logits ("Kimi K3.1 Pro" archdiff blueprint,
+    "Output gate + sink"): one more term in the softmax denominator, no value.
     """
     lib = lib or load()
     B, Tq, H, R = q_lat.shape
@@ -153,8 +157,15 @@ def sparse_mla(q_lat, kv, idx, q_start, kv_len, scale, rows=None, lib=None):
     lse = np.empty((len(rows), H), np.float64)
     q, k, ix = _c(q_lat, np.uint16), _c(kv, np.uint16), _c(idx, np.int32)
     qs, kl = _c(q_start, np.int32), _c(kv_len, np.int32)
-    _check(lib.oracle_sparse_mla(_p(q), _p(k), _p(ix), _p(qs), _p(kl), B, Tq, S_max, H, topk_,
-                                 float(scale), len(rows), _p(rows), _p(o), _p(lse)), "sparse_mla")
+    if sink is None:
+        _check(lib.oracle_sparse_mla(_p(q), _p(k), _p(ix), _p(qs), _p(kl), B, Tq, S_max, H, topk_,
+                                     float(scale), len(rows), _p(rows), _p(o), _p(lse)), "sparse_mla")
+    else:
+        sk = _c(sink, np.float64)
+        assert sk.shape == (H,)
+        _check(lib.oracle_sparse_mla_sink(_p(q), _p(k), _p(ix), _p(qs), _p(kl), B, Tq, S_max, H,
+                                          topk_, float(scale), _p(sk), len(rows), _p(rows), _p(o),
+                                          _p(lse)), "sparse_mla_sink")
     return o, lse
 
 

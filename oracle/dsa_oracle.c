@@ -250,6 +250,7 @@ typedef struct {
   const int64_t* rows;
   double *o, *lse;
   int dense;
+  const double* sink; /* [H] learnable sink logits (natural log), or NULL */
   int err;
 } mla_ctx;
 
@@ -288,7 +289,8 @@ static void mla_row(void* vctx, int64_t r) {
     const uint16_t* q = c->q + (flat * c->H + h) * (int64_t)RLAT;
     double* oh = o + (int64_t)h * VLAT;
     for (int d = 0; d < VLAT; ++d) oh[d] = 0.0;
-    if (n == 0) { lse[h] = -INFINITY; continue; }
+    /* no attended key: all weight on the sink (if any), whose value is zero */
+    if (n == 0) { lse[h] = c->sink ? c->sink[h] : -INFINITY; continue; }
     /* logits over the full 576-wide row: 512 c_kv dims + 64 unrotated k_pe dims */
     double m = -INFINITY;
     for (int j = 0; j < n; ++j) {
@@ -298,6 +300,9 @@ static void mla_row(void* vctx, int64_t r) {
       z[j] = dot * c->scale;
       if (z[j] > m) m = z[j];
     }
+    /* learnable sink ([ARCH] "Output gate + sink"): one more logit in the
+     * denominator with no value row */
+    if (c->sink && c->sink[h] > m) m = c->sink[h];
     double l = 0.0;
     for (int j = 0; j < n; ++j) {
       double p = exp(z[j] - m);
@@ -305,6 +310,7 @@ static void mla_row(void* vctx, int64_t r) {
       const uint16_t* row = kvb + (int64_t)sel[j] * RLAT;
       for (int d = 0; d < VLAT; ++d) oh[d] += p * bf(row[d]); /* value = first 512 dims */
     }
+    if (c->sink) l += exp(c->sink[h] - m);
     for (int d = 0; d < VLAT; ++d) oh[d] /= l;
     lse[h] = m + log(l);
   }
@@ -315,14 +321,14 @@ static void mla_row(void* vctx, int64_t r) {
 static int mla_common(const uint16_t* q_lat, const uint16_t* kv, const int32_t* idx,
                       const int32_t* q_start, const int32_t* kv_len, int B, int Tq, int S_max,
                       int H, int topk, double scale, int64_t n_rows, const int64_t* rows,
-                      double* o, double* lse, int dense) {
+                      double* o, double* lse, int dense, const double* sink) {
   if (!q_lat || !kv || !q_start || !kv_len || !rows || !o || !lse) return OR_BAD_ARG;
   if (!dense && (!idx || topk <= 0)) return OR_BAD_ARG;
   if (B <= 0 || Tq <= 0 || S_max <= 0 || H <= 0 || n_rows < 0) return OR_BAD_ARG;
   for (int64_t r = 0; r < n_rows; ++r)
     if (rows[r] < 0 || rows[r] >= (int64_t)B * Tq) return OR_BAD_ARG;
   mla_ctx c = {q_lat, kv, idx, q_start, kv_len, Tq, S_max, H, topk, scale,
-               rows, o, lse, dense, OR_OK};
+               rows, o, lse, dense, sink, OR_OK};
   parallel_rows(n_rows, mla_row, &c);
   return c.err;
 }
@@ -334,7 +340,19 @@ int oracle_sparse_mla(const uint16_t* q_lat, const uint16_t* kv, const int32_t* 
                       int H, int topk, double scale, int64_t n_rows, const int64_t* rows,
                       double* o, double* lse) {
   return mla_common(q_lat, kv, idx, q_start, kv_len, B, Tq, S_max, H, topk, scale, n_rows,
-                    rows, o, lse, 0);
+                    rows, o, lse, 0, NULL);
+}
+
+/* The same with a learnable sink: sink [H] logits (natural log) that join the
+ * softmax denominator and carry no value: o = sum_s e^{z_s} v_s / (e^{sink} +
+ * sum_s e^{z_s}), lse = log(e^{sink} + sum_s e^{z_s}). */
+int oracle_sparse_mla_sink(const uint16_t* q_lat, const uint16_t* kv, const int32_t* idx,
+                           const int32_t* q_start, const int32_t* kv_len, int B, int Tq, int S_max,
+                           int H, int topk, double scale, const double* sink, int64_t n_rows,
+                           const int64_t* rows, double* o, double* lse) {
+  if (!sink) return OR_BAD_ARG;
+  return mla_common(q_lat, kv, idx, q_start, kv_len, B, Tq, S_max, H, topk, scale, n_rows,
+                    rows, o, lse, 0, sink);
 }
 
 /* Dense causal MLA over every key s <= t: the dense-mask reference path. */
@@ -342,7 +360,7 @@ int oracle_dense_mla(const uint16_t* q_lat, const uint16_t* kv, const int32_t* q
                      const int32_t* kv_len, int B, int Tq, int S_max, int H, double scale,
                      int64_t n_rows, const int64_t* rows, double* o, double* lse) {
   return mla_common(q_lat, kv, NULL, q_start, kv_len, B, Tq, S_max, H, 0, scale, n_rows, rows,
-                    o, lse, 1);
+                    o, lse, 1, NULL);
 }
 
 /* ------------------------------------------------------------------------- */

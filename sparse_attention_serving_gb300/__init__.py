@@ -52,7 +52,7 @@ class _Rows(ctypes.Structure):
 
 EXPORTS = ("dsa_abi_version", "dsa_status_string", "dsa_workspace_bytes", "dsa_workspace_init",
            "dsa_read_device_status", "dsa_indexer_topk", "sparse_mla_fwd", "mla_gate_apply",
-           "dsa_cache_append", "dsa_selftest_wait_timeout")
+           "dsa_cache_append", "sparse_mla_fwd_sink", "dsa_selftest_wait_timeout")
 
 
 def _load(path: str = LIB_PATH):
@@ -71,12 +71,15 @@ def _load(path: str = LIB_PATH):
     lib.dsa_indexer_topk.argtypes = [P, P, ctypes.POINTER(_Rows), P, P, I, I, I, I, I, I, P, P, Z, P]
     lib.sparse_mla_fwd.argtypes = [P, ctypes.POINTER(_Rows), P, P, P, I, I, I, I, I,
                                    ctypes.c_float, P, P, P, Z, P]
+    lib.sparse_mla_fwd_sink.argtypes = [P, ctypes.POINTER(_Rows), P, P, P, I, I, I, I, I,
+                                        ctypes.c_float, P, P, P, P, Z, P]
     lib.mla_gate_apply.argtypes = [P, P, P, P, I, I, I, I, P, P, Z, P]
     lib.dsa_cache_append.argtypes = [P, P, ctypes.POINTER(_Rows), ctypes.POINTER(_Rows), P, I, I, I,
                                      ctypes.c_float, P, Z, P]
     lib.dsa_selftest_wait_timeout.argtypes = [P, Z, ctypes.c_uint64, P]
     for f in ("dsa_workspace_init", "dsa_read_device_status", "dsa_indexer_topk",
-              "sparse_mla_fwd", "mla_gate_apply", "dsa_cache_append", "dsa_selftest_wait_timeout"):
+              "sparse_mla_fwd", "mla_gate_apply", "dsa_cache_append", "sparse_mla_fwd_sink",
+              "dsa_selftest_wait_timeout"):
         getattr(lib, f).restype = I
     return lib
 
@@ -201,9 +204,11 @@ def dsa_indexer_topk(q_idx, w, k_idx: Rows, q_start, kv_len, topk: int, max_kv_l
 
 
 def sparse_mla_fwd(q_lat, kv: Rows, idx, q_start, kv_len, max_kv_len: int, scale: float = MLA_SCALE,
-                   o_lat=None, lse=None, want_lse: bool = True, workspace=None, stream=None):
+                   o_lat=None, lse=None, want_lse: bool = True, workspace=None, stream=None,
+                   sink=None):
     """q_lat [B,Tq,H,576] bf16, kv Rows (width 576), idx [B,Tq,topk] int32 ->
-    (o_lat [B,Tq,H,512] bf16, lse [B,Tq,H] float32 or None)."""
+    (o_lat [B,Tq,H,512] bf16, lse [B,Tq,H] float32 or None).  sink: optional [H]
+    float32 learnable sink logits (calls sparse_mla_fwd_sink)."""
     _need(q_lat, torch.bfloat16, "q_lat")
     _need(idx, torch.int32, "idx")
     _need(q_start, torch.int32, "q_start")
@@ -219,10 +224,20 @@ def sparse_mla_fwd(q_lat, kv: Rows, idx, q_start, kv_len, max_kv_len: int, scale
         _need(lse, torch.float32, "lse")
     ws = _ws(workspace, OP_SPARSE_MLA, B, Tq, max_kv_len, H, topk, q_lat.device, stream)
     rows = kv.c()
-    _check(lib.sparse_mla_fwd(_ptr(q_lat), ctypes.byref(rows), _ptr(idx), _ptr(q_start),
-                              _ptr(kv_len), B, Tq, H, topk, int(max_kv_len), float(scale),
-                              _ptr(o_lat), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)),
-           "sparse_mla_fwd")
+    if sink is None:
+        _check(lib.sparse_mla_fwd(_ptr(q_lat), ctypes.byref(rows), _ptr(idx), _ptr(q_start),
+                                  _ptr(kv_len), B, Tq, H, topk, int(max_kv_len), float(scale),
+                                  _ptr(o_lat), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)),
+               "sparse_mla_fwd")
+    else:
+        _need(sink, torch.float32, "sink")
+        if tuple(sink.shape) != (H,):
+            raise ValueError("sink must be [H]")
+        _check(lib.sparse_mla_fwd_sink(_ptr(q_lat), ctypes.byref(rows), _ptr(idx), _ptr(q_start),
+                                       _ptr(kv_len), B, Tq, H, topk, int(max_kv_len),
+                                       float(scale), _ptr(sink), _ptr(o_lat), _ptr(lse),
+                                       _ptr(ws), ws.numel(), _stream(stream)),
+               "sparse_mla_fwd_sink")
     return o_lat, lse
 
 

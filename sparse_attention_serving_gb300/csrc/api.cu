@@ -212,11 +212,13 @@ dsa_status_t dsa_indexer_topk(const uint16_t* q_idx, const uint16_t* w, const ds
   return indexer_launch(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
-dsa_status_t sparse_mla_fwd(const uint16_t* q_lat, const dsa_rows_t* kv, const int32_t* idx,
+static dsa_status_t mla_fwd(const uint16_t* q_lat, const dsa_rows_t* kv, const int32_t* idx,
                             const int32_t* q_start, const int32_t* kv_len, int B, int Tq, int H,
-                            int topk, int max_kv_len, float scale, uint16_t* o_lat, float* lse,
-                            void* workspace, size_t ws_bytes, dsa_stream_t stream) {
+                            int topk, int max_kv_len, float scale, const float* sink,
+                            uint16_t* o_lat, float* lse, void* workspace, size_t ws_bytes,
+                            dsa_stream_t stream) {
   if (!q_lat || !idx || !q_start || !kv_len || !o_lat) return DSA_ERR_INVALID_ARGUMENT;
+  if (sink != nullptr && !aligned(sink, 4)) return DSA_ERR_INVALID_ARGUMENT;
   if (!aligned(q_lat, 16) || !aligned(idx, 4) || !aligned(o_lat, 16) ||
       (lse != nullptr && !aligned(lse, 4)) || !aligned(q_start, 4) || !aligned(kv_len, 4))
     return DSA_ERR_INVALID_ARGUMENT;
@@ -244,10 +246,29 @@ dsa_status_t sparse_mla_fwd(const uint16_t* q_lat, const dsa_rows_t* kv, const i
   a.scale = scale;
   a.o_lat = o_lat;
   a.lse = lse;
+  a.sink = sink;
   a.status = static_cast<uint32_t*>(workspace);
   a.scratch = static_cast<uint8_t*>(workspace) + kWorkspaceHeader;
   a.scratch_bytes = ws_bytes - kWorkspaceHeader;
   return sparse_mla_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t sparse_mla_fwd(const uint16_t* q_lat, const dsa_rows_t* kv, const int32_t* idx,
+                            const int32_t* q_start, const int32_t* kv_len, int B, int Tq, int H,
+                            int topk, int max_kv_len, float scale, uint16_t* o_lat, float* lse,
+                            void* workspace, size_t ws_bytes, dsa_stream_t stream) {
+  return mla_fwd(q_lat, kv, idx, q_start, kv_len, B, Tq, H, topk, max_kv_len, scale, nullptr,
+                 o_lat, lse, workspace, ws_bytes, stream);
+}
+
+dsa_status_t sparse_mla_fwd_sink(const uint16_t* q_lat, const dsa_rows_t* kv, const int32_t* idx,
+                                 const int32_t* q_start, const int32_t* kv_len, int B, int Tq,
+                                 int H, int topk, int max_kv_len, float scale, const float* sink,
+                                 uint16_t* o_lat, float* lse, void* workspace, size_t ws_bytes,
+                                 dsa_stream_t stream) {
+  if (sink == nullptr) return DSA_ERR_INVALID_ARGUMENT;
+  return mla_fwd(q_lat, kv, idx, q_start, kv_len, B, Tq, H, topk, max_kv_len, scale, sink, o_lat,
+                 lse, workspace, ws_bytes, stream);
 }
 
 dsa_status_t mla_gate_apply(const uint16_t* x, const uint16_t* W_g, const uint16_t* o_lat,

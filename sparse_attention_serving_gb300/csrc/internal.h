@@ -42,6 +42,7 @@ struct SparseMlaArgs {
   float scale;
   uint16_t* o_lat;
   float* lse;
+  const float* sink;   // [H] learnable sink logits (natural log), or null
   uint32_t* status;
   void* scratch;       // split partials (decode); may be null when nsplit == 1
   size_t scratch_bytes;

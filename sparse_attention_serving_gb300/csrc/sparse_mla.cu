@@ -122,6 +122,7 @@ struct Params {
   float scale_log2;  // scale * log2(e)
   uint16_t* o_lat;
   float* lse;
+  const float* sink;  // [H] learnable sink logits (natural log), or null
   float* part_o;     // [q, split, H, 512] normalised partial outputs (nsplit > 1)
   float* part_lse;   // [q, split, H] partial log2-sum-exp
   uint32_t* status;
@@ -612,18 +613,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     s_l[half * 128 + h] = l_sum;
     named_bar_sync(1, NSMX);
     have_o = !vload(&g_abort[0]) && !vload(s_abort) && ok && nb > 0;
+    // no valid entry and nothing failed: the output is zero, lse is the sink's
+    const bool empty_ok = nb == 0 && ok && !vload(s_abort);
     tc_fence_after();
     float* s_invl = s_l + 2 * 128;  // [128]
     if (half == 0) {
       const float lx = s_l[h] + s_l[128 + h];
-      s_invl[h] = lx > 0.f ? 1.f / lx : 0.f;
-      const float lse2 = (lx > 0.f) ? m_ref + log2f(lx) : -INFINITY;
+      float inv = lx > 0.f ? 1.f / lx : 0.f;
+      float lse2 = (lx > 0.f) ? m_ref + log2f(lx) : -INFINITY;
+      if (p.sink != nullptr && p.nsplit == 1 && (have_o || empty_ok)) {
+        // learnable sink: one more term 2^(s2 - M) in the denominator, no value;
+        // O^T was accumulated against m_ref, so it is rescaled by 2^(m_ref - M)
+        const float s2 = h < H ? __ldg(p.sink + h) * 1.4426950408889634f : -INFINITY;
+        const float mr = have_o ? m_ref : -INFINITY;
+        const float M = fmaxf(mr, s2);
+        if (M == -INFINITY) {
+          inv = 0.f;
+          lse2 = -INFINITY;
+        } else {
+          const float f = ex2(mr - M);
+          const float lt = (have_o ? lx : 0.f) * f + ex2(s2 - M);
+          inv = lt > 0.f ? f / lt : 0.f;
+          lse2 = M + log2f(lt);
+        }
+      }
+      s_invl[h] = inv;
       const int64_t pq = static_cast<int64_t>(qflat) * p.nsplit + sp;
       if (h < H) {
         if (p.nsplit == 1) {
           if (p.lse != nullptr)
             p.lse[static_cast<int64_t>(qflat) * H + h] =
-                have_o ? lse2 * 0.6931471805599453f : -INFINITY;
+                (have_o || (empty_ok && p.sink != nullptr)) ? lse2 * 0.6931471805599453f
+                                                            : -INFINITY;
         } else {
           p.part_lse[pq * H + h] = have_o ? lse2 : -INFINITY;
         }
@@ -695,11 +716,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
-// Merge the per-split partial results: lse = log2 sum_p 2^lse_p,
-// o = sum_p 2^(lse_p - lse) o_p.  One thread per (query, head, 4 dims).
+// Merge the per-split partial results: lse = log2 (sum_p 2^lse_p [+ 2^sink]),
+// o = sum_p 2^(lse_p - lse) o_p; a learnable sink (no value row) enters here
+// once, not in every split.  One thread per (query, head, 4 dims).
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_o,
                                                       const float* __restrict__ part_lse,
                                                       int nq, int H, int nsplit,
+                                                      const float* __restrict__ sink,
                                                       uint16_t* __restrict__ o_lat,
                                                       float* __restrict__ lse) {
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -708,7 +731,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   const int64_t qh = gid / per_qh;
   const int d4 = static_cast<int>(gid % per_qh) * 4;
   const int64_t q = qh / H, h = qh % H;
-  float mx = -INFINITY;
+  const float s2 = sink != nullptr ? __ldg(sink + h) * 1.4426950408889634f : -INFINITY;
+  float mx = s2;
   for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, part_lse[(q * nsplit + s) * H + h]);
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   float wsum = 0.f;
@@ -722,6 +746,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
           *reinterpret_cast<const float4*>(part_o + ((q * nsplit + s) * H + h) * kVlat + d4);
       acc[0] += wgt * v.x; acc[1] += wgt * v.y; acc[2] += wgt * v.z; acc[3] += wgt * v.w;
     }
+    if (s2 != -INFINITY) wsum += exp2f(s2 - mx);
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   uint16_t* o = o_lat + qh * kVlat + d4;
@@ -775,6 +800,7 @@ static dsa_status_t launch_h(const SparseMlaArgs& a, cudaStream_t stream) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.o_lat = a.o_lat;
   p.lse = a.lse;
+  p.sink = a.sink;
   p.status = a.status;
   if (ns > 1) {
     const size_t nq = static_cast<size_t>(a.B) * a.Tq;
@@ -794,7 +820,7 @@ static dsa_status_t launch_h(const SparseMlaArgs& a, cudaStream_t stream) {
     const int64_t nq = static_cast<int64_t>(a.B) * a.Tq;
     const int64_t threads = nq * H * (kVlat / 4);
     combine_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
-        p.part_o, p.part_lse, static_cast<int>(nq), H, ns, a.o_lat, a.lse);
+        p.part_o, p.part_lse, static_cast<int>(nq), H, ns, a.sink, a.o_lat, a.lse);
     if (launch_status("combine_kernel") != DSA_OK) return DSA_ERR_CUDA;
   }
   return DSA_OK;

@@ -39,9 +39,10 @@ def check_indexer_rows(gpu_idx: np.ndarray, q_idx, w, k_logical, q_start, kv_len
 
 
 def check_mla_rows(o_gpu: np.ndarray, lse_gpu: np.ndarray, q_lat, kv_logical, idx, q_start,
-                   kv_len, scale, rows, what=""):
+                   kv_len, scale, rows, what="", sink=None):
     B, Tq, H, _ = q_lat.shape
-    o_ref, lse_ref = oracle.sparse_mla(q_lat, kv_logical, idx, q_start, kv_len, scale, rows)
+    o_ref, lse_ref = oracle.sparse_mla(q_lat, kv_logical, idx, q_start, kv_len, scale, rows,
+                                       sink=sink)
     og = bf16_to_f32(o_gpu.reshape(B * Tq, H, 512)[rows])
     ma, rl = check_close(og, o_ref, f"{what} o_lat")
     if lse_gpu is not None:

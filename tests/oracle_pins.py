@@ -475,4 +475,68 @@ def pin_cache_append_places_rows(lib):
     assert np.array_equal(kc[3, 63], oracle.bf16_rne(k_ln[0, 1], lib))
 
 
+# ---------------------------------------------------------------------------
+# Learnable sink ("Kimi K3.1 Pro" archdiff blueprint, "Output gate + sink")
+# ---------------------------------------------------------------------------
+
+def pin_sink_minus_infinity_is_no_sink(lib):
+    T, H = 9, 3
+    q, kv, qs, kl = _mla_inputs(61, T, H)
+    idx = np.tile(np.arange(T, dtype=np.int32), (1, T, 1))
+    idx[0] = np.where(idx[0] <= np.arange(T)[:, None], idx[0], -1)
+    a = oracle.sparse_mla(q, kv, idx, qs, kl, SCALE, lib=lib)
+    b = oracle.sparse_mla(q, kv, idx, qs, kl, SCALE, lib=lib, sink=np.full(H, -np.inf))
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def pin_sink_single_key_closed_form(lib):
+    """One key with logit z and a sink s: o = v * sigma(z - s), lse = log(e^z + e^s)."""
+    T, H = 6, 2
+    q, kv, qs, kl = _mla_inputs(62, T, H)
+    idx = np.full((1, T, 4), -1, np.int32)
+    idx[0, :, 1] = np.arange(T) // 2
+    sink = np.array([0.7, -3.5])
+    o, lse = oracle.sparse_mla(q, kv, idx, qs, kl, SCALE, lib=lib, sink=sink)
+    kvf = bf16_to_f32(kv[0]).astype(np.float64)
+    for t in range(T):
+        s_ = t // 2
+        for h in range(H):
+            z = float(bf16_to_f32(q[0, t, h]).astype(np.float64) @ kvf[s_]) * SCALE
+            p = 1.0 / (1.0 + math.exp(sink[h] - z))
+            np.testing.assert_allclose(o[t, h], p * kvf[s_, :512], rtol=1e-12, atol=1e-15)
+            want = max(z, sink[h]) + math.log1p(math.exp(-abs(z - sink[h])))
+            assert abs(lse[t, h] - want) < 1e-12
+
+
+def pin_sink_uniform_logits(lib):
+    """q = 0: n keys of logit 0 and a sink s give o = mean(v) * n / (n + e^s) and
+    lse = log(n + e^s); with no attended key, o = 0 and lse = s."""
+    T, H = 7, 1
+    _, kv, qs, kl = _mla_inputs(63, T, H)
+    q = np.zeros((1, T, H, 576), np.uint16)
+    idx = np.full((1, T, T), -1, np.int32)
+    for t in range(1, T):
+        idx[0, t, :t] = np.arange(t)          # query t attends to keys 0..t-1; query 0 to none
+    sink = np.array([1.25])
+    o, lse = oracle.sparse_mla(q, kv, idx, qs, kl, SCALE, lib=lib, sink=sink)
+    kvf = bf16_to_f32(kv[0]).astype(np.float64)
+    assert np.all(o[0] == 0.0) and lse[0, 0] == 1.25
+    for t in range(1, T):
+        w = t / (t + math.exp(1.25))
+        np.testing.assert_allclose(o[t, 0], kvf[:t, :512].mean(0) * w, rtol=1e-12, atol=1e-15)
+        assert abs(lse[t, 0] - math.log(t + math.exp(1.25))) < 1e-12
+
+
+def pin_sink_dominant_limit(lib):
+    """A sink far above every logit takes all the weight: o = 0, lse = the sink
+    (finite: the sink must enter the running maximum, not overflow e^{s - m})."""
+    T, H = 4, 2
+    q, kv, qs, kl = _mla_inputs(64, T, H)
+    idx = np.zeros((1, T, 1), np.int32)
+    o, lse = oracle.sparse_mla(q, kv, idx, qs, kl, SCALE, lib=lib, sink=np.array([1000.0, 1000.0]))
+    assert np.all(o == 0.0)
+    np.testing.assert_array_equal(lse, np.full((T, H), 1000.0))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

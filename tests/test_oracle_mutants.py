@@ -34,6 +34,8 @@ MUTANTS = {
     "layernorm_eps_dropped": ("const double inv = 1.0 / sqrt(var + eps);",
                               "const double inv = 1.0 / sqrt(var);"),
     "bf16_ties_away_from_zero": ("double r = nearbyint(m * 256.0);", "double r = round(m * 256.0);"),
+    "sink_not_in_denominator": ("if (c->sink) l += exp(c->sink[h] - m);", ""),
+    "sink_does_not_move_max": ("if (c->sink && c->sink[h] > m) m = c->sink[h];", ""),
 }
 
 
