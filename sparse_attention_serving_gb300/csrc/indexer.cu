@@ -185,15 +185,53 @@ __device__ float select_topk(float* cs, int32_t* ci, int n, int k, int gtid, int
   // equal to it; the k-th score is the smallest key kept
   if (gtid == 0) { ctr[0] = 0; ctr[1] = 0; ctr[2] = static_cast<int>(0xffffffffu); }
   named_bar_sync(1, G);
+  // Positions come from one group-wide prefix sum, not from atomics: each
+  // thread counts its keys above the prefix (n_hi) and equal to it (n_eq),
+  // packed 16 + 16 bits (at most EPT each, at most CAP in total); keys above
+  // go to [0, total_hi) and the first `need` equal keys, in thread order,
+  // right after them.  (An atomic per key, or per warp and element slot, puts
+  // an atomic round trip on every iteration of the loop.)
+  int n_hi = 0, n_eq = 0;
+#pragma unroll
+  for (int u = 0; u < EPT; ++u) {
+    if (id[u] < 0) continue;
+    const uint32_t m = key[u] & mask;
+    n_hi += m > prefix;
+    n_eq += m == prefix;
+  }
+  const int packed = n_hi | (n_eq << 16);
+  int incl = packed;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int* wtot = hist;  // [8] warp totals (the histogram is no longer needed)
+  if (lane == 31) wtot[gtid >> 5] = incl;
+  named_bar_sync(1, G);
+  int before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < NEPI; ++w) {
+    const int t = wtot[w];
+    if (w < (gtid >> 5)) before += t;
+    total += t;
+  }
+  const int excl = before + incl - packed;
+  const int total_hi = total & 0xffff;
+  int pos_hi = excl & 0xffff, pos_eq = excl >> 16;
   uint32_t kept_min = 0xffffffffu;
 #pragma unroll
   for (int u = 0; u < EPT; ++u) {
     if (id[u] < 0) continue;
     const uint32_t m = key[u] & mask;
-    bool keep = m > prefix;
-    if (!keep && m == prefix) keep = atomicAdd(&ctr[1], 1) < need;
-    if (keep) {
-      const int pos = atomicAdd(&ctr[0], 1);
+    int pos = -1;
+    if (m > prefix) {
+      pos = pos_hi++;
+    } else if (m == prefix) {
+      if (pos_eq < need) pos = total_hi + pos_eq;
+      ++pos_eq;
+    }
+    if (pos >= 0) {
       cs[pos] = key_to_float(key[u]);
       ci[pos] = id[u];
       kept_min = min(kept_min, key[u]);
@@ -366,73 +404,91 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>(sub * 32) << 16;
     const int key_lane = sub * 32 + lane;
     // this thread's head weights (its half's queries), kept in registers
-    float wreg[QH * H_I];
+    int kt = 0;
+    bool stop = false;
+    while (kt < ntiles && !stop) {
+      // The head weights stay in registers through the tile loop only and are
+      // reloaded after a selection: with them dead during select_topk its
+      // candidate arrays fit in registers instead of spilling.
+      float wreg[QH * H_I];
 #pragma unroll
-    for (int c = 0; c < QH * H_I; ++c) wreg[c] = w_s[half * QH * H_I + c];
-    for (int kt = 0; kt < ntiles; ++kt) {
-      const int buf = kt & 1;
-      const bool w_ok = mbar_wait(&bars[7 + buf], (kt >> 1) & 1, p.status, kWaitLimitNs, SITE_W_DF);
-      if (!w_ok || vflag(s_abort)) g_abort[(kt & 1) * 2] = 1;
-      named_bar_sync(1, G);
-      if (vflag(&g_abort[(kt & 1) * 2])) break;
-      tc_fence_after();
-      // head reduction: 4 independent FMA chains per query (the MMA's FP32
-      // accumulators are summed in a fixed order: chain c takes heads c, c+4, ...)
-      constexpr int COLS = QH * H_I;  // this half's accumulator columns
-      constexpr int NCHAIN = 4;
-      float acc[QH][NCHAIN];
-#pragma unroll
-      for (int q = 0; q < QH; ++q)
-#pragma unroll
-        for (int c = 0; c < NCHAIN; ++c) acc[q][c] = 0.f;
-      const uint32_t col0 = buf * 256 + half * COLS;
-#pragma unroll
-      for (int u = 0; u < COLS / 32; ++u) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + col0 + u * 32, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int col = u * 32 + e;
-          const int q = col / H_I;
-          const float v = fmaxf(__uint_as_float(r[e]), 0.f);
-          acc[q][e % NCHAIN] = fmaf(wreg[col], v, acc[q][e % NCHAIN]);
+      for (int c = 0; c < QH * H_I; ++c) wreg[c] = w_s[half * QH * H_I + c];
+      bool want_sel = false;
+      for (; kt < ntiles; ++kt) {
+        const int buf = kt & 1;
+        const bool w_ok = mbar_wait(&bars[7 + buf], (kt >> 1) & 1, p.status, kWaitLimitNs, SITE_W_DF);
+        if (!w_ok || vflag(s_abort)) g_abort[(kt & 1) * 2] = 1;
+        named_bar_sync(1, G);
+        if (vflag(&g_abort[(kt & 1) * 2])) {
+          stop = true;
+          break;
         }
-      }
-      float score[QH];
+        tc_fence_after();
+        // head reduction: 4 independent FMA chains per query (the MMA's FP32
+        // accumulators are summed in a fixed order: chain c takes heads c, c+4, ...)
+        constexpr int COLS = QH * H_I;  // this half's accumulator columns
+        constexpr int NCHAIN = 4;
+        float acc[QH][NCHAIN];
 #pragma unroll
-      for (int q = 0; q < QH; ++q) score[q] = (acc[q][0] + acc[q][1]) + (acc[q][2] + acc[q][3]);
-      tc_fence_before();
-      mbar_arrive(&bars[9 + buf]);
-      // append candidates above each query's threshold
-      const int s = kt * BKEY + key_lane;
+        for (int q = 0; q < QH; ++q)
 #pragma unroll
-      for (int q = 0; q < QH; ++q) {
-        const int qq = half * QH + q;
-        const bool take = qq < nq && s <= t0 + qq && score[q] > thr[qq];
-        const uint32_t bal = __ballot_sync(0xffffffffu, take);
-        if (bal) {
-          int base = 0;
-          if (lane == 0) base = atomicAdd(&cnt[qq], __popc(bal));
-          base = __shfl_sync(0xffffffffu, base, 0);
-          if (take) {
-            const int pos = base + __popc(bal & ((1u << lane) - 1u));
-            cand_s[qq * CAP + pos] = score[q];
-            cand_i[qq * CAP + pos] = s;
+          for (int c = 0; c < NCHAIN; ++c) acc[q][c] = 0.f;
+        const uint32_t col0 = buf * 256 + half * COLS;
+#pragma unroll
+        for (int u = 0; u < COLS / 32; ++u) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + col0 + u * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int col = u * 32 + e;
+            const int q = col / H_I;
+            const float v = fmaxf(__uint_as_float(r[e]), 0.f);
+            acc[q][e % NCHAIN] = fmaf(wreg[col], v, acc[q][e % NCHAIN]);
           }
         }
-      }
-      named_bar_sync(1, G);
-      // shrink any buffer that could overflow on the next tile
-      for (int qq = 0; qq < nq; ++qq) {
-        if (cnt[qq] > CAP - BKEY) {
-          const float kth = select_topk<C::EPT>(cand_s + qq * CAP, cand_i + qq * CAP, cnt[qq], p.topk,
-                                                gtid, hist, sel, ctr);
-          if (gtid == 0) {
-            cnt[qq] = p.topk;
-            thr[qq] = kth;
+        float score[QH];
+#pragma unroll
+        for (int q = 0; q < QH; ++q) score[q] = (acc[q][0] + acc[q][1]) + (acc[q][2] + acc[q][3]);
+        tc_fence_before();
+        mbar_arrive(&bars[9 + buf]);
+        // append candidates above each query's threshold
+        const int s = kt * BKEY + key_lane;
+#pragma unroll
+        for (int q = 0; q < QH; ++q) {
+          const int qq = half * QH + q;
+          const bool take = qq < nq && s <= t0 + qq && score[q] > thr[qq];
+          const uint32_t bal = __ballot_sync(0xffffffffu, take);
+          if (bal) {
+            int base = 0;
+            if (lane == 0) base = atomicAdd(&cnt[qq], __popc(bal));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (take) {
+              const int pos = base + __popc(bal & ((1u << lane) - 1u));
+              cand_s[qq * CAP + pos] = score[q];
+              cand_i[qq * CAP + pos] = s;
+            }
           }
-          named_bar_sync(1, G);
+        }
+        named_bar_sync(1, G);
+        // a buffer that could overflow on the next tile is shrunk outside this loop
+        for (int qq = 0; qq < nq; ++qq) want_sel |= cnt[qq] > CAP - BKEY;
+        if (want_sel) {
+          ++kt;
+          break;
+        }
+      }
+      if (want_sel) {
+        for (int qq = 0; qq < nq; ++qq) {
+          if (cnt[qq] > CAP - BKEY) {
+            const float kth = select_topk<C::EPT>(cand_s + qq * CAP, cand_i + qq * CAP, cnt[qq],
+                                                  p.topk, gtid, hist, sel, ctr);
+            if (gtid == 0) {
+              cnt[qq] = p.topk;
+              thr[qq] = kth;
+            }
+            named_bar_sync(1, G);
+          }
         }
       }
     }

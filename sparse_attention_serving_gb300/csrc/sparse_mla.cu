@@ -352,9 +352,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tc_fence_after();
           const uint64_t sd = smem_desc(smem_u32(sm + OFF_PAIR + slot * PAIR), 16, 1024);
           const uint64_t qd = desc_add(qd0, 2 * pr * QRS);
-  #pragma unroll
+#pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
-  #pragma unroll
+#pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               umma_bf16(d, desc_add(qd, h2 * QRS + kk * 32), desc_add(sd, h2 * CHUNK + kk * 32),
                         IDESC_S, first ? 0u : 1u);
@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             fence_proxy_async_smem();
             tc_fence_after();
-  #pragma unroll
+#pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma_bf16(d, desc_add(qd0, 8 * QRS + kk * 32), desc_add(rd0, kk * 32), IDESC_S, 1u);
             umma_commit(&bars[B_RE]);
@@ -409,12 +409,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           fence_proxy_async_smem();
           tc_fence_after();
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < 4; ++i) {
             const uint32_t g = 4u * jj + i;
             const int slot = g % NPAIR;
             const uint64_t vd = smem_desc(smem_u32(sm + OFF_PAIR + slot * PAIR), CHUNK, 1024);
-  #pragma unroll
+#pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma_bf16(tmem + i * HN, desc_add(vd, kk * 2048), desc_add(pd0, kk * 32), IDESC_O,
                         (jj > 0 || kk > 0) ? 1u : 0u);
