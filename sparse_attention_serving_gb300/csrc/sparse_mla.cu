@@ -291,12 +291,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int e = tid + i * NPROD;
         sv[i] = (U.q_ok && e < p.topk) ? __ldg(U.ix + e) : -1;
       }
+      // paged: the block-table entries of all of them in a second batch (the
+      // same checks as entry_row, without one dependent load per entry)
+      int pid[SCAN];
+#pragma unroll
+      for (int i = 0; i < SCAN; ++i) {
+        const int s = sv[i], pg = s >> 6;
+        pid[i] = (p.paged && s >= 0 && s <= U.t && pg < p.max_pages)
+                     ? __ldg(p.block_table + static_cast<int64_t>(U.b) * p.max_pages + pg)
+                     : 0;
+      }
       int last = -1;
 #pragma unroll
       for (int i = 0; i < SCAN; ++i) {
         const int s = sv[i];
         if (s < 0) continue;
-        if (entry_row(p, U.b, U.t, s) >= 0) {
+        const bool valid = s <= U.t && (!p.paged || ((s >> 6) < p.max_pages && pid[i] >= 0 &&
+                                                     pid[i] < p.num_pages));
+        if (valid) {
           last = tid + i * NPROD;
         } else if (U.sp == 0) {
           status_raise(p.status, DSA_ERR_BAD_INDEX, s > U.t ? SITE_IDX : SITE_PAGE, (uint32_t)s);
