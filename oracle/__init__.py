@@ -59,6 +59,11 @@ def load(path: str | None = None):
                                                i64, P, P, P]
         lib.oracle_layernorm.argtypes = [P, i64, i32, f64, P]
         lib.oracle_bf16_rne.argtypes = [P, i64, P]
+        lib.oracle_e4m3_encode.argtypes = [P, i64, P]
+        lib.oracle_e4m3_decode.argtypes = [P, i64, P]
+        lib.oracle_quant_fp8.argtypes = [P, i64, i32, P, P]
+        lib.oracle_indexer_scores_fp8.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
+                                                  i64, P, P]
         lib.oracle_set_threads.argtypes = [i32]
         for f in ("oracle_indexer_scores", "oracle_topk", "oracle_sparse_mla", "oracle_dense_mla",
                   "oracle_explicit_mla", "oracle_gate", "oracle_set_threads",
@@ -283,3 +288,73 @@ def cache_append(k_pre, kv_new, q_start, eps, k_cache, kv_cache, k_block_table=N
             place(kc, k_block_table, b, pos, k_bits[b, i])
             place(vc, kv_block_table, b, pos, kv_new[b, i])
     return kc, vc, k_ln
+
+
+# ---------------------------------------------------------------------------
+# FP8 indexer variant ("Kimi-K3.1-Pro", NeMo AutoModel, Implementation Limits,
+# bullet 2: the FP8 indexer of some serving kernels, against the BF16 one).
+# Format and scaling are readings stated in dsa_oracle.c.
+# ---------------------------------------------------------------------------
+
+def e4m3_encode(x, lib=None) -> np.ndarray:
+    """float32 -> E4M3 codes (uint8), round to nearest even, saturating at +-448."""
+    lib = lib or load()
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, np.uint8)
+    _check(lib.oracle_e4m3_encode(_p(x), x.size, _p(out)), "oracle_e4m3_encode")
+    return out
+
+
+def e4m3_decode(c, lib=None) -> np.ndarray:
+    """E4M3 codes -> float64 values."""
+    lib = lib or load()
+    c = _c(c, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _check(lib.oracle_e4m3_decode(_p(c), c.size, _p(out)), "oracle_e4m3_decode")
+    return out
+
+
+def quant_fp8(x, lib=None):
+    """BF16 rows [..., D] -> (codes [..., D] uint8, scale [...] float32): one FP32
+    scale per row, scale = max(amax, 2^-100)/448, code = E4M3(x * (1/scale))."""
+    lib = lib or load()
+    x = _c(x, np.uint16)
+    D = x.shape[-1]
+    n = x.size // D
+    codes = np.empty(x.shape, np.uint8)
+    scale = np.empty(x.shape[:-1], np.float32)
+    _check(lib.oracle_quant_fp8(_p(x), n, D, _p(codes), _p(scale)), "oracle_quant_fp8")
+    return codes, scale
+
+
+def indexer_scores_fp8(q_codes, q_scale, w, k_codes, k_scale, q_start, kv_len, rows=None,
+                       lib=None):
+    """Indexer scores of the dequantised FP8 rows: I[t,s] = sum_j w[t,j] *
+    max(0, (q_scale[t,j] q[t,j]) . (k_scale[s] k[s])).  k_codes [B,S,D_I],
+    k_scale [B,S].  Returns [n_rows, S_max] float64, NaN beyond t."""
+    lib = lib or load()
+    B, Tq, H_I, D_I = q_codes.shape
+    S_max = k_codes.shape[1]
+    rows = _rows(rows, B, Tq)
+    out = np.empty((len(rows), S_max), np.float64)
+    q, qs = _c(q_codes, np.uint8), _c(q_scale, np.float32)
+    ww = _c(w, np.uint16)
+    k, ks = _c(k_codes, np.uint8), _c(k_scale, np.float32)
+    assert qs.shape == (B, Tq, H_I) and ks.shape == (B, S_max)
+    qst, kl = _c(q_start, np.int32), _c(kv_len, np.int32)
+    _check(lib.oracle_indexer_scores_fp8(_p(q), _p(qs), _p(ww), _p(k), _p(ks), _p(qst), _p(kl),
+                                         B, Tq, S_max, H_I, D_I, len(rows), _p(rows), _p(out)),
+           "indexer_scores_fp8")
+    return out
+
+
+def indexer_topk_fp8(q_codes, q_scale, w, k_codes, k_scale, q_start, kv_len, k, rows=None,
+                     lib=None):
+    """FP8 scores and top-k for the given rows; returns (idx, kth, scores, n_valid)."""
+    B, Tq = q_codes.shape[:2]
+    rows = _rows(rows, B, Tq)
+    sc = indexer_scores_fp8(q_codes, q_scale, w, k_codes, k_scale, q_start, kv_len, rows, lib=lib)
+    qs = np.asarray(q_start, np.int64)
+    n_valid = (qs[rows // Tq] + rows % Tq + 1).astype(np.int32)
+    idx, kth = topk(sc, n_valid, k, lib=lib)
+    return idx, kth, sc, n_valid

@@ -549,3 +549,159 @@ int oracle_bf16_rne(const double* v, int64_t n, uint16_t* out) {
   }
   return OR_OK;
 }
+
+/* ------------------------------------------------------------------------- */
+/* FP8 indexer variant  [K31 Impl. Limits b2: the FP8 indexer some serving    */
+/*                       kernels use, set against the BF16 one]              */
+/* ------------------------------------------------------------------------- */
+/* The pages name the FP8 indexer and nothing more.  Readings (also in the
+ * design notes):
+ *   - the 8-bit format is E4M3: sign, 4 exponent bits with bias 7, 3 mantissa
+ *     bits; exponent field 0 holds the subnormals m * 2^-9; the all-ones
+ *     pattern S.1111.111 is NaN, so the largest finite magnitude is
+ *     1.75 * 2^8 = 448; there is no infinity.  Encoding rounds to the nearest
+ *     representable value, ties to the even mantissa, and saturates to +-448;
+ *   - every row of D values (one indexer key, or one head of one query) has its
+ *     own FP32 scale: amax = max |x| over the BF16 row,
+ *     scale = max(amax, 2^-100) / 448, inv = 1 / scale, code = E4M3(x * inv),
+ *     each of the three a single IEEE float operation rounded to nearest;
+ *     the value a code stands for is scale * decode(code);
+ *   - scores are the BF16 indexer's formula on those values.
+ * The 2^-100 floor only keeps inv finite for an all-zero row (its codes are
+ * all zero, so its values are exactly zero). */
+
+#define E4M3_MAX 448.0
+
+/* Magnitude of an E4M3 code (sign ignored). */
+static double e4m3_mag(uint8_t c) {
+  const int ex = (c >> 3) & 15, m = c & 7;
+  if (ex == 0) return ldexp((double)m, -9);
+  return ldexp(8.0 + m, ex - 10); /* (1 + m/8) * 2^(ex-7) */
+}
+
+static uint8_t e4m3_encode1(float xf) {
+  const double x = (double)xf;
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  const double a = fabs(x);
+  if (!(a < E4M3_MAX)) return sign | 0x7E; /* saturate (also catches +-inf) */
+  /* quantum of the binade [2^e, 2^(e+1)) is 2^(e-3); the subnormal range
+   * [0, 2^-6) shares the quantum 2^-9 of the smallest normal binade */
+  int e2;
+  frexp(a, &e2);
+  int e = e2 - 1;
+  if (a == 0.0 || e < -6) e = -6;
+  const double q = ldexp(1.0, e - 3);
+  const double v = nearbyint(a / q) * q; /* a / q is exact; ties to even */
+  if (v >= E4M3_MAX) return sign | 0x7E;
+  /* find the code of v: exact search over the 127 finite magnitudes */
+  for (int c = 0; c <= 0x7E; ++c)
+    if (e4m3_mag((uint8_t)c) == v) return sign | (uint8_t)c;
+  return 0xFF; /* unreachable: v is on the E4M3 grid */
+}
+
+/* float -> E4M3 codes (round to nearest even, saturating). */
+int oracle_e4m3_encode(const float* x, int64_t n, uint8_t* out) {
+  if (!x || !out || n < 0) return OR_BAD_ARG;
+  for (int64_t i = 0; i < n; ++i) {
+    if (isnan(x[i])) return OR_BAD_ARG;
+    out[i] = e4m3_encode1(x[i]);
+  }
+  return OR_OK;
+}
+
+/* E4M3 codes -> values (NaN for the two NaN patterns). */
+int oracle_e4m3_decode(const uint8_t* c, int64_t n, double* out) {
+  if (!c || !out || n < 0) return OR_BAD_ARG;
+  for (int64_t i = 0; i < n; ++i) {
+    const uint8_t m = c[i] & 0x7F;
+    const double v = m == 0x7F ? NAN : e4m3_mag(m);
+    out[i] = (c[i] & 0x80) ? -v : v;
+  }
+  return OR_OK;
+}
+
+/* x [n, D] BF16 -> codes [n, D] E4M3 and scale [n] float, as stated above. */
+int oracle_quant_fp8(const uint16_t* x, int64_t n, int D, uint8_t* codes, float* scale) {
+  if (!x || !codes || !scale || n < 0 || D <= 0) return OR_BAD_ARG;
+  for (int64_t r = 0; r < n; ++r) {
+    const uint16_t* xr = x + r * (int64_t)D;
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+      const float a = (float)fabs(bf(xr[d]));
+      if (isnan(a) || isinf(a)) return OR_BAD_ARG;
+      if (a > amax) amax = a;
+    }
+    const float floor_ = 0x1p-100f;
+    const float s = (amax > floor_ ? amax : floor_) / 448.0f;
+    const float inv = 1.0f / s;
+    scale[r] = s;
+    for (int d = 0; d < D; ++d) {
+      const float t = (float)bf(xr[d]) * inv;
+      codes[r * (int64_t)D + d] = e4m3_encode1(t);
+    }
+  }
+  return OR_OK;
+}
+
+typedef struct {
+  const uint8_t *q, *k;
+  const float *qs, *ks;
+  const uint16_t* w;
+  const int32_t *q_start, *kv_len;
+  int Tq, S_max, H_I, D_I;
+  const int64_t* rows;
+  double* out;
+  int err;
+} idx8_ctx;
+
+static double dec8(uint8_t c) {
+  const double v = e4m3_mag(c & 0x7F);
+  return (c & 0x80) ? -v : v;
+}
+
+static void indexer_row_fp8(void* vctx, int64_t r) {
+  idx8_ctx* c = (idx8_ctx*)vctx;
+  int64_t flat = c->rows[r];
+  int b = (int)(flat / c->Tq), i = (int)(flat % c->Tq);
+  int64_t t = (int64_t)c->q_start[b] + i;
+  double* o = c->out + r * (int64_t)c->S_max;
+  for (int64_t s = 0; s < c->S_max; ++s) o[s] = NAN;
+  if (t >= c->kv_len[b] || t >= c->S_max) { c->err = OR_BAD_ARG; return; }
+  const uint8_t* q = c->q + flat * (int64_t)c->H_I * c->D_I;
+  const float* qs = c->qs + flat * (int64_t)c->H_I;
+  const uint16_t* w = c->w + flat * (int64_t)c->H_I;
+  const uint8_t* kb = c->k + (int64_t)b * c->S_max * c->D_I;
+  const float* ksb = c->ks + (int64_t)b * c->S_max;
+  for (int64_t s = 0; s <= t; ++s) {
+    const uint8_t* k = kb + s * c->D_I;
+    const double ks = (double)ksb[s];
+    double score = 0.0;
+    for (int j = 0; j < c->H_I; ++j) {
+      const double qsj = (double)qs[j];
+      double dot = 0.0;
+      for (int d = 0; d < c->D_I; ++d) dot += (qsj * dec8(q[j * c->D_I + d])) * (ks * dec8(k[d]));
+      const double pos = dot > 0.0 ? dot : 0.0; /* ReLU */
+      score += bf(w[j]) * pos;
+    }
+    o[s] = score;
+  }
+}
+
+/* q codes [B,Tq,H_I,D_I] + q_scale [B,Tq,H_I]; w [B,Tq,H_I] BF16;
+ * k codes [B,S_max,D_I] + k_scale [B,S_max]: the indexer scores of the
+ * dequantised rows, every causal key, NaN beyond t (as oracle_indexer_scores). */
+int oracle_indexer_scores_fp8(const uint8_t* q_codes, const float* q_scale, const uint16_t* w,
+                              const uint8_t* k_codes, const float* k_scale,
+                              const int32_t* q_start, const int32_t* kv_len, int B, int Tq,
+                              int S_max, int H_I, int D_I, int64_t n_rows, const int64_t* rows,
+                              double* out) {
+  if (!q_codes || !q_scale || !w || !k_codes || !k_scale || !q_start || !kv_len || !rows || !out)
+    return OR_BAD_ARG;
+  if (B <= 0 || Tq <= 0 || S_max <= 0 || H_I <= 0 || D_I <= 0 || n_rows < 0) return OR_BAD_ARG;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= (int64_t)B * Tq) return OR_BAD_ARG;
+  idx8_ctx c = {q_codes, k_codes, q_scale, k_scale, w, q_start, kv_len, Tq, S_max, H_I, D_I,
+                rows, out, OR_OK};
+  parallel_rows(n_rows, indexer_row_fp8, &c);
+  return c.err;
+}

@@ -539,4 +539,123 @@ def pin_sink_dominant_limit(lib):
     np.testing.assert_array_equal(lse, np.full((T, H), 1000.0))
 
 
+# ----------------------------------------------------------------------------
+# FP8 (E4M3) indexer variant
+# ----------------------------------------------------------------------------
+
+def _e4m3_grid():
+    """The 127 finite non-negative E4M3 magnitudes, in code order."""
+    g = json.load(open(os.path.join(GOLDEN, "e4m3_codes.json")))["codes"]
+    assert g["0x7e"] == 448.0
+    return oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+
+
+def pin_e4m3_format_table(lib):
+    """Hand-worked code values of the OFP8 E4M3 format (tests/golden/e4m3_codes.json)."""
+    g = json.load(open(os.path.join(GOLDEN, "e4m3_codes.json")))["codes"]
+    codes = np.array([int(k, 16) for k in g], np.uint8)
+    vals = oracle.e4m3_decode(codes, lib=lib)
+    for c, v, e in zip(codes, vals, g.values()):
+        if e == "nan":
+            assert math.isnan(v), (hex(c), v)
+        else:
+            assert v == e and math.copysign(1.0, v) == math.copysign(1.0, e), (hex(c), v, e)
+
+
+def pin_e4m3_roundtrip_and_order(lib):
+    """Every finite code encodes back to itself; magnitudes rise with the code."""
+    allc = np.arange(256, dtype=np.uint8)
+    v = oracle.e4m3_decode(allc, lib=lib)
+    fin = ~np.isnan(v)
+    assert fin.sum() == 254
+    back = oracle.e4m3_encode(v[fin].astype(np.float32), lib=lib)
+    assert np.array_equal(back, allc[fin])
+    pos = v[:0x7F]
+    assert np.all(np.diff(pos) > 0)
+
+
+def pin_e4m3_rounding_matches_library(lib):
+    """Round to nearest, ties to even, against torch's float8_e4m3fn cast (in
+    range) and saturation to +-448 beyond it; midpoints and their neighbours."""
+    import torch
+    grid = _e4m3_grid()
+    mids = ((grid[:-1] + grid[1:]) / 2).astype(np.float32)
+    xs = [grid.astype(np.float32), mids, np.nextafter(mids, np.float32(0)),
+          np.nextafter(mids, np.float32(1e30))]
+    rng = np.random.default_rng(81)
+    xs.append((rng.standard_normal(4000) * 60).astype(np.float32))
+    xs.append((rng.standard_normal(4000) * 0.01).astype(np.float32))
+    x = np.concatenate(xs)
+    x = np.concatenate([x, -x])
+    inr = np.abs(x) < 464
+    got = oracle.e4m3_encode(x, lib=lib)
+    ref = torch.from_numpy(x[inr]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got[inr], ref), np.nonzero(got[inr] != ref)[0][:5]
+    big = np.array([464.0, 1000.0, 3e38], np.float32)
+    assert np.array_equal(oracle.e4m3_encode(big, lib=lib), [0x7E] * 3)
+    assert np.array_equal(oracle.e4m3_encode(-big, lib=lib), [0xFE] * 3)
+    # ties: midpoint of codes 0x38 / 0x39 goes to the even 0x38, of 0x39 / 0x3a to 0x3a
+    assert list(oracle.e4m3_encode(np.array([1.0625, 1.1875, 2.0 ** -10], np.float32),
+                                   lib=lib)) == [0x38, 0x3A, 0x00]
+
+
+def pin_quant_fp8_definition(lib):
+    """Per-row scale and codes recomputed with numpy float32 arithmetic and
+    torch's E4M3 cast: scale = max(amax, 2^-100)/448, code = E4M3(x * (1/scale))."""
+    import torch
+    rng = np.random.default_rng(82)
+    x = normal_bf16(82, "q_idx", (37, 128))
+    x[3] = 0                                   # an all-zero row
+    x[5] = bf16_round(np.full(128, -2.5, np.float32))
+    x[7, :] = bf16_round((rng.standard_normal(128) * 1e-3).astype(np.float32))
+    # rows where x * (1/scale) and x / scale round to different codes: the
+    # pin fixes the two-step form (found by search over BF16 pairs)
+    for r, (amax_, xv) in enumerate([(0.19140625, 0.08544921875), (0.26953125, 0.2021484375),
+                                     (0.40625, 0.076171875)]):
+        x[10 + r, :] = 0
+        x[10 + r, :2] = bf16_round(np.array([amax_, xv], np.float32))
+    codes, scale = oracle.quant_fp8(x, lib=lib)
+    xf = bf16_to_f32(x)
+    amax = np.max(np.abs(xf), axis=1).astype(np.float32)
+    s_ref = np.maximum(amax, np.float32(2.0 ** -100)) / np.float32(448.0)
+    assert np.array_equal(scale, s_ref.astype(np.float32))
+    inv = (np.float32(1.0) / s_ref).astype(np.float32)
+    t = (xf * inv[:, None]).astype(np.float32)
+    t = np.clip(t, -448.0, 448.0)           # the saturation (values past 448 round to it)
+    ref = torch.from_numpy(np.ascontiguousarray(t)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, ref)
+    assert np.all(codes[3] == 0)
+    # the row maximum lands on +-448 (code 0x7e / 0xfe)
+    for r in (0, 5, 7):
+        assert (codes[r, np.argmax(np.abs(xf[r]))] & 0x7F) == 0x7E
+
+
+def pin_indexer_fp8_equals_bf16_on_exact_values(lib):
+    """With power-of-two scales the dequantised values are exact BF16 numbers,
+    and the FP8 scores then equal the BF16 indexer's scores exactly."""
+    rng = np.random.default_rng(83)
+    B, T, H_I, D_I = 1, 24, 3, 16
+    qc = rng.integers(0, 256, (B, T, H_I, D_I)).astype(np.uint8)
+    kc = rng.integers(0, 256, (B, T, D_I)).astype(np.uint8)
+    qc[(qc & 0x7F) == 0x7F] = 0x38            # no NaN codes
+    kc[(kc & 0x7F) == 0x7F] = 0x40
+    qs = (2.0 ** rng.integers(-6, 3, (B, T, H_I))).astype(np.float32)
+    ks = (2.0 ** rng.integers(-6, 3, (B, T))).astype(np.float32)
+    w = normal_bf16(83, "w", (B, T, H_I))
+    qv = oracle.e4m3_decode(qc, lib=lib) * qs[..., None]
+    kv = oracle.e4m3_decode(kc, lib=lib) * ks[..., None]
+    q16, k16 = _bf(qv.astype(np.float32)), _bf(kv.astype(np.float32))
+    q_start, kv_len = np.zeros(B, np.int32), np.full(B, T, np.int32)
+    a = oracle.indexer_scores_fp8(qc, qs, w, kc, ks, q_start, kv_len, lib=lib)
+    b = oracle.indexer_scores(q16, w, k16, q_start, kv_len, lib=lib)
+    assert np.array_equal(np.isnan(a), np.isnan(b))
+    assert np.array_equal(a[~np.isnan(a)], b[~np.isnan(b)])
+    # the scales matter: doubling one key's scale doubles its column of scores
+    ks2 = ks.copy()
+    ks2[0, 5] *= 2
+    c = oracle.indexer_scores_fp8(qc, qs, w, kc, ks2, q_start, kv_len, lib=lib)
+    assert np.array_equal(c[5:, 5], 2 * a[5:, 5])
+    assert np.array_equal(c[:, 6:], a[:, 6:], equal_nan=True)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

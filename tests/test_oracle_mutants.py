@@ -13,7 +13,10 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "dsa_oracle.c")
 MUTANTS = {
     "relu_dropped": ("double relu = dot > 0.0 ? dot : 0.0;", "double relu = dot;"),
     "head_weight_dropped": ("score += bf(w[j]) * relu;", "score += relu;"),
-    "causal_excludes_self": ("for (int64_t s = 0; s <= t; ++s) {", "for (int64_t s = 0; s < t; ++s) {"),
+    "causal_excludes_self": ("/* every causal key s <= t is scored */\n  for (int64_t s = 0; s <= t; ++s) {",
+                             "/* every causal key s <= t is scored */\n  for (int64_t s = 0; s < t; ++s) {"),
+    "fp8_causal_excludes_self": ("const float* ksb = c->ks + (int64_t)b * c->S_max;\n  for (int64_t s = 0; s <= t; ++s) {",
+                                 "const float* ksb = c->ks + (int64_t)b * c->S_max;\n  for (int64_t s = 0; s < t; ++s) {"),
     "tie_break_reversed": ("return (x->s < y->s) ? -1 : (x->s > y->s);",
                            "return (x->s > y->s) ? -1 : (x->s < y->s);"),
     "short_rows_sorted_not_all": ("if (n <= c->topk) {", "if (n < 0) {"),
@@ -36,6 +39,18 @@ MUTANTS = {
     "bf16_ties_away_from_zero": ("double r = nearbyint(m * 256.0);", "double r = round(m * 256.0);"),
     "sink_not_in_denominator": ("if (c->sink) l += exp(c->sink[h] - m);", ""),
     "sink_does_not_move_max": ("if (c->sink && c->sink[h] > m) m = c->sink[h];", ""),
+    "e4m3_ties_away_from_zero": ("const double v = nearbyint(a / q) * q;",
+                                 "const double v = round(a / q) * q;"),
+    "e4m3_no_subnormal_quantum": ("if (a == 0.0 || e < -6) e = -6;", "if (a == 0.0) e = -6;"),
+    "e4m3_bias_off_by_one": ("return ldexp(8.0 + m, ex - 10);", "return ldexp(8.0 + m, ex - 9);"),
+    "quant_divides_once": ("const float t = (float)bf(xr[d]) * inv;",
+                           "const float t = (float)bf(xr[d]) / s;"),
+    "quant_scale_without_floor": ("const float s = (amax > floor_ ? amax : floor_) / 448.0f;",
+                                  "const float s = amax / 448.0f;"),
+    "fp8_relu_dropped": ("const double pos = dot > 0.0 ? dot : 0.0;", "const double pos = dot;"),
+    "fp8_head_weight_dropped": ("score += bf(w[j]) * pos;", "score += pos;"),
+    "fp8_key_scale_dropped": ("* (ks * dec8(k[d]));", "* dec8(k[d]);"),
+    "fp8_query_scale_dropped": ("dot += (qsj * dec8(q[j * c->D_I + d]))", "dot += (dec8(q[j * c->D_I + d]))"),
 }
 
 
