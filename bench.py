@@ -349,6 +349,9 @@ def run_ours(args, rank, world, local):
         "gpu_launches": K * launches_per_step(dsa, B, T, cfg),
         "clocks": clk,
     }
+    res["variants"] = {"fp8_indexer": run_prefill_fp8(args, dsa, cfg, dev, stream, q_idx, w,
+                                                      k_idx, qs, kl, idx, ws, T, f_idx, peak,
+                                                      t_mla)}
     if not args.no_e2e:
         res["e2e"] = run_e2e(args, dsa, d, g, cfg, dev, stream, ws, krows, kvrows, world,
                              tensors=dict(q_idx=q_idx, w=w, k_idx=k_idx, q_lat=q_lat, kv=kv, x=x,
@@ -357,6 +360,51 @@ def run_ours(args, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(cfg, d, g, args.cpu_rows or 768)
     return res
+
+
+def run_prefill_fp8(args, dsa, cfg, dev, stream, q_idx, w, k_idx, qs, kl, idx, ws, T, f_idx,
+                    peak_bf16, t_mla):
+    """The prefill indexer with FP8 (E4M3) operands, timed on its own: the query
+    heads are quantised inside each step, the keys once (as the FP8 cache append
+    would have stored them).  Reported beside the BF16 step, not as the headline.
+    The FP8 tensor peak is taken as twice the measured BF16 one (the nominal
+    dense ratio, 4.5 vs 2.25 PFLOP/s)."""
+    import torch
+    kc, ksc = dsa.dsa_quant_fp8(k_idx)
+    krows8 = dsa.Rows(kc)
+    qc = torch.empty(q_idx.shape, dtype=torch.uint8, device=dev)
+    qsc = torch.empty(q_idx.shape[:-1], dtype=torch.float32, device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        dsa.dsa_quant_fp8(q_idx, codes=qc, scale=qsc)
+        if ev is not None:
+            ev[1].record(stream)
+        dsa.dsa_indexer_topk_fp8(qc, qsc, w, krows8, ksc, qs, kl, cfg.topk, T, out_idx=idx,
+                                 workspace=ws)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    code, where, detail = dsa.read_device_status(ws)
+    if code != dsa.DSA_OK:
+        raise RuntimeError(f"fp8 device status {code} at {where:#x} ({detail})")
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for i in range(K):
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    t_q = sum(e[0].elapsed_time(e[1]) for e in evs) / K / 1e3
+    t_i = sum(e[1].elapsed_time(e[2]) for e in evs) / K / 1e3
+    tf = f_idx / t_i / 1e12
+    return {"quant_ms": t_q * 1e3, "indexer_ms": t_i * 1e3, "tflops": tf,
+            "frac_of_fp8_peak": tf / (2 * peak_bf16),
+            "value_indexer_mla_only": cfg.B * T / (t_q + t_i + t_mla), "unit": "tokens/s",
+            "step": "dsa_quant_fp8 (queries) -> dsa_indexer_topk_fp8; sparse MLA as in the BF16 step",
+            "gpu_launches": K * 2}
 
 
 def launches_per_step(dsa, B, T, cfg):
@@ -509,6 +557,8 @@ def run_decode(args, rank, world, local, cfg):
         raise RuntimeError(f"append device status {code} at {where:#x} ({detail})")
     t_app = a0.elapsed_time(a1) / K / 1e3
     app_bytes = B * (cfg.D_I * 4 + 1152 + cfg.D_I * 2 + 1152)
+    fp8 = run_decode_fp8(args, dev, cfg, d, k_pool, bt, qs, kl, q_idx, w, q_lat, kvrows, idx,
+                         o_lat, lse, ws, flush, stream, S, hbm)
     res = {
         "metric": METRIC, "value": B * world / t_step, "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": t_step * 1e3,
@@ -525,6 +575,7 @@ def run_decode(args, rank, world, local, cfg):
                     "dsa_cache_append": {"us": t_app * 1e6, "gbs": app_bytes / t_app / 1e9,
                                          "bytes": app_bytes,
                                          "note": "timed separately, back to back; not in the step"}},
+        "variants": {"fp8_indexer": fp8},
         "roofline": {"kernel": "decode step", "bound": "hbm", "achieved": ach, "peak": hbm,
                      "unit": "GB/s", "frac": ach / hbm, "traffic": None,
                      "algorithmic": f"{nbytes} compulsory bytes per step"},
@@ -532,6 +583,59 @@ def run_decode(args, rank, world, local, cfg):
         "clocks": clk,
     }
     return res
+
+
+def run_decode_fp8(args, dev, cfg, d, k_pool, bt, qs, kl, q_idx, w, q_lat, kvrows, idx, o_lat,
+                   lse, ws, flush, stream, S, hbm):
+    """The same decode step with the FP8 (E4M3) indexer: the query heads are
+    quantised inside the step, the key cache is held as E4M3 codes plus one FP32
+    scale per token (quantised once here, as the FP8 cache append would have
+    written it).  Reported beside the BF16 step, not as the headline."""
+    import numpy as np
+    import torch
+    import sparse_attention_serving_gb300 as dsa
+    kc, ksc = dsa.dsa_quant_fp8(k_pool)
+    qc = torch.empty(q_idx.shape, dtype=torch.uint8, device=dev)
+    qsc = torch.empty(q_idx.shape[:-1], dtype=torch.float32, device=dev)
+    krows8 = dsa.Rows(kc, bt)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        dsa.dsa_quant_fp8(q_idx, codes=qc, scale=qsc)
+        dsa.dsa_indexer_topk_fp8(qc, qsc, w, krows8, ksc, qs, kl, cfg.topk, S, out_idx=idx,
+                                 workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+        dsa.sparse_mla_fwd(q_lat, kvrows, idx, qs, kl, S, cfg.scale, o_lat=o_lat, lse=lse,
+                           workspace=ws)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    code, where, detail = dsa.read_device_status(ws)
+    if code != dsa.DSA_OK:
+        raise RuntimeError(f"fp8 device status {code} at {where:#x} ({detail})")
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        flush.fill_(i & 255)
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    t_idx = sum(e[0].elapsed_time(e[1]) for e in evs) / K / 1e3
+    t_mla = sum(e[1].elapsed_time(e[2]) for e in evs) / K / 1e3
+    keys = int(d["kv_len"].astype(np.int64).sum())
+    idx_bytes = keys * (cfg.D_I + 4)
+    return {"ms_per_step": (t_idx + t_mla) * 1e3, "value": cfg.B / (t_idx + t_mla),
+            "unit": "tokens/s",
+            "indexer_ms": t_idx * 1e3, "indexer_gbs": idx_bytes / t_idx / 1e9,
+            "indexer_frac": idx_bytes / t_idx / 1e9 / hbm, "sparse_mla_ms": t_mla * 1e3,
+            "indexer_bytes": idx_bytes,
+            "step": "dsa_quant_fp8 (queries) -> dsa_indexer_topk_fp8 -> sparse_mla_fwd",
+            "gpu_launches": K * 5}
 
 
 # ----------------------------------------------------------------------------

@@ -211,6 +211,75 @@ dsa_status_t dsa_cache_append(const float* k_pre, const uint16_t* kv_new,
                               void* workspace, size_t ws_bytes, dsa_stream_t stream);
 
 /*
+ * FP8 indexer variant.  "Kimi-K3.1-Pro" (NeMo AutoModel), Implementation
+ * Limits, bullet 2, contrasts its BF16 indexer with the FP8 indexer that some
+ * serving kernels use.  The pages give nothing more, so the format is this
+ * library's reading:
+ *   - Codes are E4M3: sign, 4 exponent bits with bias 7 and 3 mantissa bits.
+ *     The largest finite value is 448 and there is no infinity.
+ *   - Each row of D values (one indexer key, or one head of one query) has one
+ *     FP32 scale and stands for scale * decode(code).
+ *
+ * dsa_quant_fp8 quantizes BF16 rows, exactly as follows:
+ *   scale[r]  = max(max_d |x[r,d]|, 2^-100) / 448
+ *               (FP32 division, rounded to nearest)
+ *   code[r,d] = E4M3(x[r,d] * (1 / scale[r]))
+ *               (FP32 reciprocal and product, each rounded to nearest;
+ *                E4M3 rounding to nearest even, saturating at +-448)
+ *   x     [n_rows, D] BF16
+ *   codes [n_rows, D] uint8
+ *   scale [n_rows]    FP32
+ * Supported: D in {64, 128}.
+ * Alignment: x 8 bytes, codes and scale 4 bytes.
+ * Nothing can fail on the device, so the call takes no workspace.
+ */
+dsa_status_t dsa_quant_fp8(const uint16_t* x, int64_t n_rows, int D, uint8_t* codes, float* scale,
+                           dsa_stream_t stream);
+
+/*
+ * dsa_cache_append with the indexer key stored in FP8.  Each key becomes
+ * D_I bytes of codes, written to k_codes (a row store of D_I-byte rows), plus
+ * one FP32 scale at the same row of k_scale.
+ *   k_scale  is laid out like k_codes' rows:
+ *              contiguous: [B, seq_stride]
+ *              paged:      [num_pages, 64], through the same block table
+ *   values   dsa_quant_fp8 applied to the BF16 row that dsa_cache_append
+ *            would have written
+ * The latent row, the checks and the device-side errors are those of
+ * dsa_cache_append.
+ */
+dsa_status_t dsa_cache_append_fp8(const float* k_pre, const uint16_t* kv_new,
+                                  const dsa_rows_t* k_codes, float* k_scale,
+                                  const dsa_rows_t* kv_cache, const int32_t* q_start, int B,
+                                  int Tq, int D_I, float eps, void* workspace, size_t ws_bytes,
+                                  dsa_stream_t stream);
+
+/*
+ * dsa_indexer_topk on FP8 operands.
+ *   q_codes [B, Tq, H_I, D_I] uint8   E4M3 query codes
+ *   q_scale [B, Tq, H_I]      FP32    one scale per query head
+ *   w       [B, Tq, H_I]      BF16    per-head weights
+ *   k_codes                           rows of D_I bytes of E4M3 key codes
+ *   k_scale                           FP32, laid out like k_codes' rows
+ *                                     (see dsa_cache_append_fp8); 16-byte
+ *                                     aligned
+ * The score of the dequantised rows is
+ *   I[t,s] = sum_j w[t,j] * max(0, (q_scale[t,j] q[t,j]) . (k_scale[s] k[s]))
+ *          = k_scale[s] * sum_j (w[t,j] q_scale[t,j]) * max(0, q[t,j] . k[s])
+ * The codes' dot products are FP32 tensor-core accumulations of exact E4M3
+ * products.  Output, workspace and errors are as for dsa_indexer_topk.
+ * Supported:
+ *   - H_I = 64, D_I = 128; Tq == 1 takes the decode kernels, Tq > 1 the fused
+ *     prefill kernel, as for dsa_indexer_topk;
+ *   - contiguous key stores need seq_stride % 4 == 0.
+ */
+dsa_status_t dsa_indexer_topk_fp8(const uint8_t* q_codes, const float* q_scale, const uint16_t* w,
+                                  const dsa_rows_t* k_codes, const float* k_scale,
+                                  const int32_t* q_start, const int32_t* kv_len, int B, int Tq,
+                                  int H_I, int D_I, int max_kv_len, int topk, int32_t* out_idx,
+                                  void* workspace, size_t ws_bytes, dsa_stream_t stream);
+
+/*
  * sparse_mla_fwd_noalloc -- sparse_mla_fwd for callers that cannot allocate
  * device memory.  The pages have no counterpart to this entry point; it exists
  * for deployment only.

@@ -11,6 +11,8 @@ Entry points (same names as the C ABI):
   sparse_mla_fwd    latent-space attention over the selected rows
   mla_gate_apply    sigmoid output gate applied after the per-head up-projection
   dsa_cache_append  LayerNorm of new indexer keys + append of keys and latent rows
+  dsa_quant_fp8, dsa_cache_append_fp8, dsa_indexer_topk_fp8
+                    the FP8 (E4M3, one FP32 scale per row) indexer variant
 """
 
 from __future__ import annotations
@@ -52,7 +54,8 @@ class _Rows(ctypes.Structure):
 
 EXPORTS = ("dsa_abi_version", "dsa_status_string", "dsa_workspace_bytes", "dsa_workspace_init",
            "dsa_read_device_status", "dsa_indexer_topk", "sparse_mla_fwd", "mla_gate_apply",
-           "dsa_cache_append", "sparse_mla_fwd_sink", "dsa_selftest_wait_timeout")
+           "dsa_cache_append", "sparse_mla_fwd_sink", "dsa_selftest_wait_timeout",
+           "dsa_quant_fp8", "dsa_cache_append_fp8", "dsa_indexer_topk_fp8")
 
 
 def _load(path: str = LIB_PATH):
@@ -77,9 +80,15 @@ def _load(path: str = LIB_PATH):
     lib.dsa_cache_append.argtypes = [P, P, ctypes.POINTER(_Rows), ctypes.POINTER(_Rows), P, I, I, I,
                                      ctypes.c_float, P, Z, P]
     lib.dsa_selftest_wait_timeout.argtypes = [P, Z, ctypes.c_uint64, P]
+    lib.dsa_quant_fp8.argtypes = [P, ctypes.c_int64, I, P, P, P]
+    lib.dsa_cache_append_fp8.argtypes = [P, P, ctypes.POINTER(_Rows), P, ctypes.POINTER(_Rows), P,
+                                         I, I, I, ctypes.c_float, P, Z, P]
+    lib.dsa_indexer_topk_fp8.argtypes = [P, P, P, ctypes.POINTER(_Rows), P, P, P, I, I, I, I, I, I,
+                                         P, P, Z, P]
     for f in ("dsa_workspace_init", "dsa_read_device_status", "dsa_indexer_topk",
               "sparse_mla_fwd", "mla_gate_apply", "dsa_cache_append", "sparse_mla_fwd_sink",
-              "dsa_selftest_wait_timeout"):
+              "dsa_selftest_wait_timeout", "dsa_quant_fp8", "dsa_cache_append_fp8",
+              "dsa_indexer_topk_fp8"):
         getattr(lib, f).restype = I
     return lib
 
@@ -119,11 +128,12 @@ def _need(t: torch.Tensor, dtype, name: str):
 
 class Rows:
     """A per-token row store: contiguous ``[B, S, width]`` or a paged pool
-    ``[num_pages, 64, width]`` with ``block_table [B, max_pages]`` (int32)."""
+    ``[num_pages, 64, width]`` with ``block_table [B, max_pages]`` (int32).
+    BF16 rows, or uint8 rows of E4M3 codes for the FP8 indexer variant."""
 
     def __init__(self, base: torch.Tensor, block_table: torch.Tensor | None = None,
                  seq_stride: int | None = None):
-        _need(base, torch.bfloat16, "rows.base")
+        _need(base, torch.uint8 if base.dtype == torch.uint8 else torch.bfloat16, "rows.base")
         self.base = base
         self.block_table = block_table
         if block_table is None:
@@ -276,3 +286,69 @@ def dsa_cache_append(k_pre, kv_new, k_cache: Rows, kv_cache: Rows, q_start,
                                 _ptr(q_start), B, Tq, D_I, float(eps), _ptr(ws), ws.numel(),
                                 _stream(stream)), "dsa_cache_append")
     return ws
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) indexer variant
+# ---------------------------------------------------------------------------
+
+def dsa_quant_fp8(x, codes=None, scale=None, stream=None):
+    """x [..., D] bf16 (D in {64, 128}) -> (codes [..., D] uint8, scale [...] float32):
+    scale = max(amax, 2^-100)/448 per row, code = E4M3(x * (1/scale))."""
+    _need(x, torch.bfloat16, "x")
+    D = x.shape[-1]
+    n = x.numel() // D if D else 0
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    _need(codes, torch.uint8, "codes")
+    _need(scale, torch.float32, "scale")
+    _check(lib.dsa_quant_fp8(_ptr(x), n, D, _ptr(codes), _ptr(scale), _stream(stream)),
+           "dsa_quant_fp8")
+    return codes, scale
+
+
+def dsa_cache_append_fp8(k_pre, kv_new, k_codes: Rows, k_scale, kv_cache: Rows, q_start,
+                         eps: float = INDEXER_KEY_EPS, workspace=None, stream=None):
+    """dsa_cache_append with the key stored as E4M3 codes (k_codes, uint8 rows of
+    D_I) plus one float32 scale per row (k_scale, laid out like k_codes' rows:
+    [B, S] contiguous or [num_pages, 64] paged).  Returns the workspace."""
+    _need(k_pre, torch.float32, "k_pre")
+    _need(kv_new, torch.bfloat16, "kv_new")
+    _need(q_start, torch.int32, "q_start")
+    _need(k_scale, torch.float32, "k_scale")
+    B, Tq, D_I = k_pre.shape
+    if tuple(kv_new.shape) != (B, Tq, RLAT):
+        raise ValueError("kv_new must be [B, Tq, 576]")
+    ws = _ws(workspace, OP_CACHE_APPEND, B, Tq, 0, 0, 0, k_pre.device, stream)
+    kr, vr = k_codes.c(), kv_cache.c()
+    _check(lib.dsa_cache_append_fp8(_ptr(k_pre), _ptr(kv_new), ctypes.byref(kr), _ptr(k_scale),
+                                    ctypes.byref(vr), _ptr(q_start), B, Tq, D_I, float(eps),
+                                    _ptr(ws), ws.numel(), _stream(stream)),
+           "dsa_cache_append_fp8")
+    return ws
+
+
+def dsa_indexer_topk_fp8(q_codes, q_scale, w, k_codes: Rows, k_scale, q_start, kv_len, topk: int,
+                         max_kv_len: int, out_idx=None, workspace=None, stream=None):
+    """q_codes [B,Tq,H_I,D_I] uint8, q_scale [B,Tq,H_I] float32, w [B,Tq,H_I] bf16,
+    k_codes Rows (uint8, width D_I), k_scale float32 laid out like k_codes' rows
+    -> out_idx [B,Tq,topk] int32 (-1 padded)."""
+    _need(q_codes, torch.uint8, "q_codes")
+    _need(q_scale, torch.float32, "q_scale")
+    _need(w, torch.bfloat16, "w")
+    _need(k_scale, torch.float32, "k_scale")
+    _need(q_start, torch.int32, "q_start")
+    _need(kv_len, torch.int32, "kv_len")
+    B, Tq, H_I, D_I = q_codes.shape
+    if out_idx is None:
+        out_idx = torch.empty((B, Tq, topk), dtype=torch.int32, device=q_codes.device)
+    _need(out_idx, torch.int32, "out_idx")
+    ws = _ws(workspace, OP_INDEXER_TOPK, B, Tq, max_kv_len, H_I, topk, q_codes.device, stream)
+    rows = k_codes.c()
+    _check(lib.dsa_indexer_topk_fp8(_ptr(q_codes), _ptr(q_scale), _ptr(w), ctypes.byref(rows),
+                                    _ptr(k_scale), _ptr(q_start), _ptr(kv_len), B, Tq, H_I, D_I,
+                                    int(max_kv_len), int(topk), _ptr(out_idx), _ptr(ws),
+                                    ws.numel(), _stream(stream)), "dsa_indexer_topk_fp8")
+    return out_idx

@@ -176,11 +176,20 @@ dsa_status_t dsa_read_device_status(void* workspace, dsa_stream_t stream, uint32
   return static_cast<dsa_status_t>(h[0]);
 }
 
-dsa_status_t dsa_indexer_topk(const uint16_t* q_idx, const uint16_t* w, const dsa_rows_t* k_idx,
-                              const int32_t* q_start, const int32_t* kv_len, int B, int Tq,
-                              int H_I, int D_I, int max_kv_len, int topk, int32_t* out_idx,
-                              void* workspace, size_t ws_bytes, dsa_stream_t stream) {
+static dsa_status_t indexer_topk(const void* q_idx, const float* q_scale, const uint16_t* w,
+                                 const dsa_rows_t* k_idx, const float* k_scale,
+                                 const int32_t* q_start, const int32_t* kv_len, int B, int Tq,
+                                 int H_I, int D_I, int max_kv_len, int topk, int32_t* out_idx,
+                                 void* workspace, size_t ws_bytes, dsa_stream_t stream, bool fp8) {
   if (!q_idx || !w || !q_start || !kv_len || !out_idx) return DSA_ERR_INVALID_ARGUMENT;
+  if (fp8) {
+    if (!q_scale || !k_scale || !aligned(q_scale, 4) || !aligned(k_scale, 16))
+      return DSA_ERR_INVALID_ARGUMENT;
+    if (!(H_I == 64 && D_I == 128)) return DSA_ERR_UNSUPPORTED;
+    // contiguous keys: each tile's scales are copied in whole 16-byte units
+    if (k_idx != nullptr && k_idx->block_table == nullptr && k_idx->seq_stride % 4 != 0)
+      return DSA_ERR_UNSUPPORTED;
+  }
   if (!aligned(q_idx, 16) || !aligned(w, 2) || !aligned(out_idx, 4) || !aligned(q_start, 4) ||
       !aligned(kv_len, 4))
     return DSA_ERR_INVALID_ARGUMENT;
@@ -195,7 +204,10 @@ dsa_status_t dsa_indexer_topk(const uint16_t* q_idx, const uint16_t* w, const ds
   st = check_ws(workspace, ws_bytes,
                 dsa_workspace_bytes(DSA_OP_INDEXER_TOPK, B, Tq, max_kv_len, H_I, topk));
   if (st != DSA_OK) return st;
-  a.q_idx = q_idx;
+  a.q_idx = static_cast<const uint16_t*>(q_idx);
+  a.q_scale = q_scale;
+  a.k_scale = k_scale;
+  a.fp8 = fp8;
   a.w = w;
   a.q_start = q_start;
   a.kv_len = kv_len;
@@ -210,6 +222,33 @@ dsa_status_t dsa_indexer_topk(const uint16_t* q_idx, const uint16_t* w, const ds
   a.scratch = static_cast<uint8_t*>(workspace) + kWorkspaceHeader;
   a.scratch_bytes = ws_bytes - kWorkspaceHeader;
   return indexer_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t dsa_indexer_topk(const uint16_t* q_idx, const uint16_t* w, const dsa_rows_t* k_idx,
+                              const int32_t* q_start, const int32_t* kv_len, int B, int Tq,
+                              int H_I, int D_I, int max_kv_len, int topk, int32_t* out_idx,
+                              void* workspace, size_t ws_bytes, dsa_stream_t stream) {
+  return indexer_topk(q_idx, nullptr, w, k_idx, nullptr, q_start, kv_len, B, Tq, H_I, D_I,
+                      max_kv_len, topk, out_idx, workspace, ws_bytes, stream, false);
+}
+
+dsa_status_t dsa_indexer_topk_fp8(const uint8_t* q_codes, const float* q_scale, const uint16_t* w,
+                                  const dsa_rows_t* k_codes, const float* k_scale,
+                                  const int32_t* q_start, const int32_t* kv_len, int B, int Tq,
+                                  int H_I, int D_I, int max_kv_len, int topk, int32_t* out_idx,
+                                  void* workspace, size_t ws_bytes, dsa_stream_t stream) {
+  return indexer_topk(q_codes, q_scale, w, k_codes, k_scale, q_start, kv_len, B, Tq, H_I, D_I,
+                      max_kv_len, topk, out_idx, workspace, ws_bytes, stream, true);
+}
+
+dsa_status_t dsa_quant_fp8(const uint16_t* x, int64_t n_rows, int D, uint8_t* codes, float* scale,
+                           dsa_stream_t stream) {
+  if (!x || !codes || !scale || n_rows < 0) return DSA_ERR_INVALID_ARGUMENT;
+  if (!aligned(x, 8) || !aligned(codes, 4) || !aligned(scale, 4)) return DSA_ERR_INVALID_ARGUMENT;
+  if (D != 64 && D != 128) return DSA_ERR_UNSUPPORTED;
+  if (n_rows >= (int64_t(1) << 36)) return DSA_ERR_UNSUPPORTED;
+  if (n_rows == 0) return DSA_OK;
+  return quant_fp8_launch(x, n_rows, D, codes, scale, reinterpret_cast<cudaStream_t>(stream));
 }
 
 static dsa_status_t mla_fwd(const uint16_t* q_lat, const dsa_rows_t* kv, const int32_t* idx,
@@ -286,11 +325,13 @@ dsa_status_t mla_gate_apply(const uint16_t* x, const uint16_t* W_g, const uint16
   return gate_launch(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
-dsa_status_t dsa_cache_append(const float* k_pre, const uint16_t* kv_new,
-                              const dsa_rows_t* k_cache, const dsa_rows_t* kv_cache,
-                              const int32_t* q_start, int B, int Tq, int D_I, float eps,
-                              void* workspace, size_t ws_bytes, dsa_stream_t stream) {
+static dsa_status_t cache_append(const float* k_pre, const uint16_t* kv_new,
+                                 const dsa_rows_t* k_cache, float* k_scale,
+                                 const dsa_rows_t* kv_cache, const int32_t* q_start, int B,
+                                 int Tq, int D_I, float eps, void* workspace, size_t ws_bytes,
+                                 dsa_stream_t stream) {
   if (!k_pre || !kv_new || !q_start) return DSA_ERR_INVALID_ARGUMENT;
+  if (k_scale != nullptr && !aligned(k_scale, 4)) return DSA_ERR_INVALID_ARGUMENT;
   if (!aligned(k_pre, 16) || !aligned(kv_new, 16) || !aligned(q_start, 4))
     return DSA_ERR_INVALID_ARGUMENT;
   if (B <= 0 || Tq <= 0 || !(eps >= 0.f) || !(eps < 3.0e38f)) return DSA_ERR_INVALID_ARGUMENT;
@@ -312,8 +353,27 @@ dsa_status_t dsa_cache_append(const float* k_pre, const uint16_t* kv_new,
   a.Tq = Tq;
   a.D_I = D_I;
   a.eps = eps;
+  a.k_scale = k_scale;
   a.status = static_cast<uint32_t*>(workspace);
   return cache_append_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dsa_status_t dsa_cache_append(const float* k_pre, const uint16_t* kv_new,
+                              const dsa_rows_t* k_cache, const dsa_rows_t* kv_cache,
+                              const int32_t* q_start, int B, int Tq, int D_I, float eps,
+                              void* workspace, size_t ws_bytes, dsa_stream_t stream) {
+  return cache_append(k_pre, kv_new, k_cache, nullptr, kv_cache, q_start, B, Tq, D_I, eps,
+                      workspace, ws_bytes, stream);
+}
+
+dsa_status_t dsa_cache_append_fp8(const float* k_pre, const uint16_t* kv_new,
+                                  const dsa_rows_t* k_codes, float* k_scale,
+                                  const dsa_rows_t* kv_cache, const int32_t* q_start, int B,
+                                  int Tq, int D_I, float eps, void* workspace, size_t ws_bytes,
+                                  dsa_stream_t stream) {
+  if (k_scale == nullptr) return DSA_ERR_INVALID_ARGUMENT;
+  return cache_append(k_pre, kv_new, k_codes, k_scale, kv_cache, q_start, B, Tq, D_I, eps,
+                      workspace, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -19,6 +19,14 @@
 //   shared memory.  When a buffer nears capacity a radix select (4 x 8-bit
 //   digits over order-preserving keys) keeps the top k and raises the
 //   threshold to the k-th score.  The final select writes the indices.
+//
+// FP8 variant (E4M3 code rows with one FP32 scale per key and per query head;
+// "Kimi-K3.1-Pro", Implementation Limits, bullet 2 contrasts the BF16 indexer
+// with the FP8 one of some serving kernels): the same kernel with one
+// kind::f8f6f4 chunk per row (half the operand bytes through shared memory),
+// the query scales folded into the head weights and each key's scale streamed
+// into a ring of its own and applied to the head sum before the threshold test:
+//   I[t,s] = k_scale[s] * sum_j (w[t,j] q_scale[t,j]) max(0, c_q[t,j] . c_k[s]).
 #include <cmath>
 
 #include <cuda_bf16.h>
@@ -35,23 +43,31 @@ constexpr int NTHREADS = 64 + NEPI * 32;
 
 enum : uint32_t {
   SITE_QPOS = 0x200, SITE_PAGE = 0x201, SITE_W_Q = 0x210, SITE_W_KE = 0x211, SITE_W_KF = 0x212,
-  SITE_W_DE = 0x213, SITE_W_DF = 0x214, SITE_W_DRAIN = 0x215
+  SITE_W_DE = 0x213, SITE_W_DF = 0x214, SITE_W_DRAIN = 0x215, SITE_W_SE = 0x216, SITE_W_SF = 0x217
 };
 
-template <int H_I, int D_I>
+template <int H_I, int D_I, bool FP8>
 struct Cfg {
   // Two queries per CTA at 64 heads (N = 128): fewer queries share the
   // candidate space, so each buffer holds ~6K candidates and a query needs
   // about two radix selections instead of five.
   static constexpr int QT = (H_I >= 64) ? 128 / H_I : 16;  // queries per CTA
   static constexpr int N = QT * H_I;                          // MMA N
-  static constexpr int NCH = D_I / 64;                        // 64-dim chunks
-  static constexpr int NST = 3;                               // key-tile stages
+  static constexpr int ROWB = FP8 ? D_I : 2 * D_I;            // bytes per key / query-head row
+  static constexpr int NCH = ROWB / 128;                      // 128-byte column chunks
+  static constexpr int NST = FP8 ? 4 : 3;                     // key-tile stages
+  static constexpr int NSC = FP8 ? 8 : 0;                     // key-scale slots (FP8)
   static constexpr int Q_BYTES = NCH * N * 128;
   static constexpr int K_STAGE = NCH * BKEY * 128;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_W = OFF_K + NST * K_STAGE;
+  static constexpr int OFF_SC = OFF_K + NST * K_STAGE;
+  static constexpr int OFF_W = OFF_SC + NSC * BKEY * 4;
+  // barriers: Q, K full [NST], K empty [NST], D full [2], D empty [2], drain,
+  // scale full [NSC], scale empty [NSC]
+  static constexpr int BQ = 0, BKF = 1, BKE = BKF + NST, BDF = BKE + NST, BDE = BDF + 2,
+                       BDRAIN = BDE + 2, BSF = BDRAIN + 1, BSE = BSF + NSC, NBARS = BSE + NSC;
+  static_assert(NBARS <= 32, "barrier block");
   static constexpr int OFF_MISC = OFF_W + QT * H_I * 4;
   static constexpr int MISC_BYTES = 4096;
   static constexpr int OFF_CAND = OFF_MISC + MISC_BYTES;
@@ -66,6 +82,8 @@ struct Cfg {
 
 struct Params {
   const uint16_t* w;
+  const float* q_scale;  // FP8: [B, Tq, H_I]
+  const float* k_scale;  // FP8: one per key row, numbered like the key rows
   const int32_t* q_start;
   const int32_t* kv_len;
   const int32_t* block_table;
@@ -243,22 +261,22 @@ __device__ float select_topk(float* cs, int32_t* ci, int n, int k, int gtid, int
   return key_to_float(static_cast<uint32_t>(ctr[2]));
 }
 
-template <int H_I, int D_I>
+template <int H_I, int D_I, bool FP8>
 __global__ void __launch_bounds__(NTHREADS, 1)
     indexer_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k, const Params p) {
-  using C = Cfg<H_I, D_I>;
-  constexpr int QT = C::QT, N = C::N, NCH = C::NCH, CAP = C::CAP;
-  constexpr uint32_t IDESC = idesc_bf16(128, N, false, false);
+  using C = Cfg<H_I, D_I, FP8>;
+  constexpr int QT = C::QT, N = C::N, NCH = C::NCH, CAP = C::CAP, NST = C::NST, NSC = C::NSC;
+  constexpr uint32_t IDESC = FP8 ? idesc_e4m3(128, N) : idesc_bf16(128, N, false, false);
   constexpr int G = NEPI * 32;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   float* w_s = reinterpret_cast<float*>(sm + C::OFF_W);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_MISC);  // 16 barriers
-  // B_Q 0, K full 1..3, K empty 4..6, D full 7..8, D empty 9..10, drain 11
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_MISC);  // 32 barrier slots
+  float* s_scale = reinterpret_cast<float*>(sm + C::OFF_SC);         // FP8: [NSC][128]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 32);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
   volatile int* g_abort = s_abort + 1;   // [4]
   int* cnt = const_cast<int*>(s_abort) + 8;  // [QT] candidates per query
@@ -298,7 +316,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   const int ntiles = (t_last + BKEY) / BKEY;
   if (tid == 0) {
-    for (int k = 0; k < 12; ++k) mbar_init(&bars[k], (k == 9 || k == 10) ? G : 1);
+    for (int k = 0; k < C::NBARS; ++k)
+      mbar_init(&bars[k], ((k >= C::BDE && k < C::BDE + 2) || k >= C::BSE) ? G : 1);
     s_abort[0] = 0;
     for (int k = 0; k < 4; ++k) g_abort[k] = 0;
     fence_mbar_init();
@@ -309,9 +328,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   for (int e = tid; e < QT * H_I; e += NTHREADS) {
     const int q = e / H_I;
-    w_s[e] = q < nq ? __bfloat162float(__ushort_as_bfloat16(
-                          p.w[(static_cast<int64_t>(b) * p.Tq + qi0) * H_I + e]))
-                    : 0.f;
+    float wq = q < nq ? __bfloat162float(__ushort_as_bfloat16(
+                            p.w[(static_cast<int64_t>(b) * p.Tq + qi0) * H_I + e]))
+                      : 0.f;
+    if constexpr (FP8) {
+      if (q < nq) wq *= p.q_scale[(static_cast<int64_t>(b) * p.Tq + qi0) * H_I + e];
+    }
+    w_s[e] = wq;
   }
   for (int q = tid; q < QT; q += NTHREADS) {
     cnt[q] = 0;
@@ -324,29 +347,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (warp == 0) {
     // ============================ producer ===================================
-    int last_use[C::NST];
-    for (int k = 0; k < C::NST; ++k) last_use[k] = -1;
+    int last_use[NST];
+    for (int k = 0; k < NST; ++k) last_use[k] = -1;
+    int last_s[NSC > 0 ? NSC : 1];
+    for (int k = 0; k < NSC; ++k) last_s[k] = -1;
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      mbar_expect_tx(&bars[0], C::Q_BYTES);
+      mbar_expect_tx(&bars[C::BQ], C::Q_BYTES);
       const int qrow = (b * p.Tq + qi0) * H_I;
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) tma_load_2d(sm + C::OFF_Q + c * N * 128, &tm_q, &bars[0], 64 * c, qrow);
+      for (int c = 0; c < NCH; ++c) tma_load_2d(sm + C::OFF_Q + c * N * 128, &tm_q, &bars[C::BQ], 64 * c, qrow);
       for (int kt = 0; kt < ntiles; ++kt) {
-        const int st = kt % C::NST, use = kt / C::NST;
-        if (use > 0 && !mbar_wait(&bars[4 + st], (use - 1) & 1, p.status, kWaitLimitNs, SITE_W_KE)) {
+        const int st = kt % NST, use = kt / NST;
+        if (use > 0 && !mbar_wait(&bars[C::BKE + st], (use - 1) & 1, p.status, kWaitLimitNs, SITE_W_KE)) {
           s_abort[0] = 1;
           break;
         }
         if (vflag(s_abort)) break;
-        mbar_expect_tx(&bars[1 + st], C::K_STAGE);
+        mbar_expect_tx(&bars[C::BKF + st], C::K_STAGE);
         last_use[st] = use;
         uint8_t* dst = sm + C::OFF_K + st * C::K_STAGE;
+        int pids[2] = {0, 0};
         if (!p.paged) {
           const int row = static_cast<int>(static_cast<int64_t>(b) * p.seq_stride + kt * BKEY);
 #pragma unroll
-          for (int c = 0; c < NCH; ++c) tma_load_2d(dst + c * BKEY * 128, &tm_k, &bars[1 + st], 64 * c, row);
+          for (int c = 0; c < NCH; ++c) tma_load_2d(dst + c * BKEY * 128, &tm_k, &bars[C::BKF + st], 64 * c, row);
         } else {
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
@@ -359,40 +385,73 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 pid = 0;  // read a valid page; its keys are never selected (flagged above)
               }
             }
+            pids[hf] = pid;
 #pragma unroll
             for (int c = 0; c < NCH; ++c)
-              tma_load_2d(dst + c * BKEY * 128 + hf * 64 * 128, &tm_k, &bars[1 + st], 64 * c, pid * kPage);
+              tma_load_2d(dst + c * BKEY * 128 + hf * 64 * 128, &tm_k, &bars[C::BKF + st], 64 * c, pid * kPage);
+          }
+        }
+        if constexpr (FP8) {
+          // the tile's key scales, into a slot of their own
+          const int sc = kt % NSC, suse = kt / NSC;
+          if (suse > 0 &&
+              !mbar_wait(&bars[C::BSE + sc], (suse - 1) & 1, p.status, kWaitLimitNs, SITE_W_SE)) {
+            s_abort[0] = 1;
+            break;
+          }
+          last_s[sc] = suse;
+          float* sdst = s_scale + sc * BKEY;
+          if (!p.paged) {
+            // rows of this sequence only (seq_stride is a multiple of 4: whole
+            // 16-byte units, never past the array)
+            const int64_t r0 = static_cast<int64_t>(b) * p.seq_stride + static_cast<int64_t>(kt) * BKEY;
+            const int64_t left = p.seq_stride - static_cast<int64_t>(kt) * BKEY;
+            const uint32_t bytes = static_cast<uint32_t>(left < BKEY ? left : BKEY) * 4u;
+            mbar_expect_tx(&bars[C::BSF + sc], bytes);
+            bulk_load(sdst, p.k_scale + r0, bytes, &bars[C::BSF + sc]);
+          } else {
+            mbar_expect_tx(&bars[C::BSF + sc], 2 * kPage * 4);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+              bulk_load(sdst + hf * kPage, p.k_scale + static_cast<int64_t>(pids[hf]) * kPage,
+                        kPage * 4, &bars[C::BSF + sc]);
           }
         }
       }
-      for (int st = 0; st < C::NST; ++st)
-        if (last_use[st] >= 0) mbar_wait(&bars[1 + st], last_use[st] & 1, p.status, kWaitLimitNs, SITE_W_KF);
+      for (int k = 0; k < NSC; ++k)
+        if (last_s[k] >= 0) mbar_wait(&bars[C::BSF + k], last_s[k] & 1, p.status, kWaitLimitNs, SITE_W_SF);
+      for (int st = 0; st < NST; ++st)
+        if (last_use[st] >= 0) mbar_wait(&bars[C::BKF + st], last_use[st] & 1, p.status, kWaitLimitNs, SITE_W_KF);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ============================ MMA issuer ==================================
     if (lane == 0) {
-      bool ok = mbar_wait(&bars[0], 0, p.status, kWaitLimitNs, SITE_W_Q);
+      bool ok = mbar_wait(&bars[C::BQ], 0, p.status, kWaitLimitNs, SITE_W_Q);
       const uint64_t qd0 = smem_desc(smem_u32(sm + C::OFF_Q), 16, 1024);
       for (int kt = 0; kt < ntiles && ok; ++kt) {
         if (vflag(s_abort)) { ok = false; break; }
-        const int st = kt % C::NST, buf = kt & 1;
-        if (kt >= 2 && !mbar_wait(&bars[9 + buf], ((kt >> 1) - 1) & 1, p.status, kWaitLimitNs, SITE_W_DE)) { ok = false; break; }
-        if (!mbar_wait(&bars[1 + st], (kt / C::NST) & 1, p.status, kWaitLimitNs, SITE_W_KF)) { ok = false; break; }
+        const int st = kt % NST, buf = kt & 1;
+        if (kt >= 2 && !mbar_wait(&bars[C::BDE + buf], ((kt >> 1) - 1) & 1, p.status, kWaitLimitNs, SITE_W_DE)) { ok = false; break; }
+        if (!mbar_wait(&bars[C::BKF + st], (kt / NST) & 1, p.status, kWaitLimitNs, SITE_W_KF)) { ok = false; break; }
         tc_fence_after();
         const uint64_t kd = smem_desc(smem_u32(sm + C::OFF_K + st * C::K_STAGE), 16, 1024);
 #pragma unroll
         for (int c = 0; c < NCH; ++c)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + buf * 256, desc_add(kd, c * BKEY * 128 + kk * 32),
-                      desc_add(qd0, c * N * 128 + kk * 32), IDESC, (c | kk) ? 1u : 0u);
-        umma_commit(&bars[4 + st]);
-        umma_commit(&bars[7 + buf]);
+            if constexpr (FP8)
+              umma_e4m3(tmem + buf * 256, desc_add(kd, c * BKEY * 128 + kk * 32),
+                        desc_add(qd0, c * N * 128 + kk * 32), IDESC, (c | kk) ? 1u : 0u);
+            else
+              umma_bf16(tmem + buf * 256, desc_add(kd, c * BKEY * 128 + kk * 32),
+                        desc_add(qd0, c * N * 128 + kk * 32), IDESC, (c | kk) ? 1u : 0u);
+        umma_commit(&bars[C::BKE + st]);
+        umma_commit(&bars[C::BDF + buf]);
       }
       if (!ok) s_abort[0] = 1;
-      umma_commit(&bars[11]);
-      mbar_wait(&bars[11], 0, p.status, kWaitLimitNs, SITE_W_DRAIN);
+      umma_commit(&bars[C::BDRAIN]);
+      mbar_wait(&bars[C::BDRAIN], 0, p.status, kWaitLimitNs, SITE_W_DRAIN);
     }
     __syncwarp();
   } else {
@@ -416,7 +475,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       bool want_sel = false;
       for (; kt < ntiles; ++kt) {
         const int buf = kt & 1;
-        const bool w_ok = mbar_wait(&bars[7 + buf], (kt >> 1) & 1, p.status, kWaitLimitNs, SITE_W_DF);
+        const int sc = FP8 ? kt % (NSC > 0 ? NSC : 1) : 0;
+        const bool w_ok =
+            mbar_wait(&bars[C::BDF + buf], (kt >> 1) & 1, p.status, kWaitLimitNs, SITE_W_DF) &&
+            (!FP8 || mbar_wait(&bars[C::BSF + sc], (kt / (NSC > 0 ? NSC : 1)) & 1, p.status,
+                               kWaitLimitNs, SITE_W_SF));
         if (!w_ok || vflag(s_abort)) g_abort[(kt & 1) * 2] = 1;
         named_bar_sync(1, G);
         if (vflag(&g_abort[(kt & 1) * 2])) {
@@ -451,7 +514,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int q = 0; q < QH; ++q) score[q] = (acc[q][0] + acc[q][1]) + (acc[q][2] + acc[q][3]);
         tc_fence_before();
-        mbar_arrive(&bars[9 + buf]);
+        mbar_arrive(&bars[C::BDE + buf]);
+        if constexpr (FP8) {
+          const float ks = s_scale[sc * BKEY + key_lane];
+#pragma unroll
+          for (int q = 0; q < QH; ++q) score[q] *= ks;
+          mbar_arrive(&bars[C::BSE + sc]);
+        }
         // append candidates above each query's threshold
         const int s = kt * BKEY + key_lane;
 #pragma unroll
@@ -519,18 +588,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 }  // namespace idx
 
-template <int H_I, int D_I>
+template <int H_I, int D_I, bool FP8>
 static dsa_status_t prefill_launch(const IndexerArgs& a, cudaStream_t stream) {
-  using C = idx::Cfg<H_I, D_I>;
+  using C = idx::Cfg<H_I, D_I, FP8>;
   if (a.topk > C::CAP - idx::BKEY) return DSA_ERR_UNSUPPORTED;
   CUtensorMap tq, tk;
   const uint64_t qrows = static_cast<uint64_t>(a.B) * a.Tq * H_I;
-  if (!encode_tmap_2d(&tq, a.q_idx, qrows, D_I, D_I * 2, 64, C::N, true)) return DSA_ERR_CUDA;
+  // (FP8 code rows are described as BF16 pairs: the copy moves bytes only)
+  if (!encode_tmap_2d(&tq, a.q_idx, qrows, C::ROWB / 2, C::ROWB, 64, C::N, true))
+    return DSA_ERR_CUDA;
   const bool paged = a.k.block_table != nullptr;
-  if (!encode_tmap_2d(&tk, a.k.base, a.k.total_rows, D_I, D_I * 2, 64, paged ? 64 : 128, true))
+  if (!encode_tmap_2d(&tk, a.k.base, a.k.total_rows, C::ROWB / 2, C::ROWB, 64, paged ? 64 : 128,
+                      true))
     return DSA_ERR_CUDA;
   idx::Params p{};
   p.w = a.w;
+  p.q_scale = a.q_scale;
+  p.k_scale = a.k_scale;
   p.q_start = a.q_start;
   p.kv_len = a.kv_len;
   p.block_table = a.k.block_table;
@@ -544,7 +618,7 @@ static dsa_status_t prefill_launch(const IndexerArgs& a, cudaStream_t stream) {
   p.ntq = (a.Tq + C::QT - 1) / C::QT;
   p.out_idx = a.out_idx;
   p.status = a.status;
-  auto kern = idx::indexer_prefill_kernel<H_I, D_I>;
+  auto kern = idx::indexer_prefill_kernel<H_I, D_I, FP8>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
       cudaSuccess)
     return launch_status("cudaFuncSetAttribute");
@@ -553,14 +627,18 @@ static dsa_status_t prefill_launch(const IndexerArgs& a, cudaStream_t stream) {
 }
 
 int indexer_prefill_max_topk(int H_I, int D_I) {
-  if (H_I == 64 && D_I == 128) return idx::Cfg<64, 128>::CAP - idx::BKEY;
-  if (H_I == 4 && D_I == 64) return idx::Cfg<4, 64>::CAP - idx::BKEY;
+  if (H_I == 64 && D_I == 128) return idx::Cfg<64, 128, false>::CAP - idx::BKEY;
+  if (H_I == 4 && D_I == 64) return idx::Cfg<4, 64, false>::CAP - idx::BKEY;
   return 0;
 }
 
 dsa_status_t indexer_prefill_launch(const IndexerArgs& a, cudaStream_t stream) {
-  if (a.H_I == 64 && a.D_I == 128) return prefill_launch<64, 128>(a, stream);
-  if (a.H_I == 4 && a.D_I == 64) return prefill_launch<4, 64>(a, stream);
+  if (a.fp8) {
+    if (a.H_I == 64 && a.D_I == 128) return prefill_launch<64, 128, true>(a, stream);
+    return DSA_ERR_UNSUPPORTED;
+  }
+  if (a.H_I == 64 && a.D_I == 128) return prefill_launch<64, 128, false>(a, stream);
+  if (a.H_I == 4 && a.D_I == 64) return prefill_launch<4, 64, false>(a, stream);
   return DSA_ERR_UNSUPPORTED;
 }
 

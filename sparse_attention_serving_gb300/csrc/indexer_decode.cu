@@ -16,6 +16,13 @@
 //                  against 256 bytes of key read).
 //                  Each work item also records the smallest and largest score
 //                  of its request (one atomic per warp).
+//                  FP8 variant (E4M3 code rows of 128 bytes, one FP32 scale
+//                  per key and per query head): the same pipeline with one
+//                  kind::f8f6f4 MMA chunk per tile, half the key bytes, and the
+//                  key scales streamed into a ring of their own by bulk copies;
+//                  the query scales fold into the head weights and the key
+//                  scale multiplies the head sum:
+//                    I[s] = k_scale[s] * sum_j (w[j] q_scale[j]) max(0, c_q[j] . c_k[s]).
 //   decode_select  one CTA per request: a value histogram between those
 //                  extremes finds the bin of the k-th largest score, a second
 //                  pass writes the keys above it and keeps that bin's keys in
@@ -33,24 +40,30 @@ namespace idxd {
 
 constexpr int BKEY = 128;
 constexpr int CH_TILES = 16;  // tiles per work item (2,048 keys)
-constexpr int NST = 5;
 constexpr int NTHREADS = 192;  // producer, MMA, 4 epilogue warps
 constexpr int MAXB = 1024;     // requests per call handled by the work decomposition
 
 enum : uint32_t {
   SITE_LEN = 0x400, SITE_PAGE = 0x401, SITE_W_QE = 0x410, SITE_W_QF = 0x411, SITE_W_KE = 0x412,
-  SITE_W_KF = 0x413, SITE_W_DE = 0x414, SITE_W_DF = 0x415, SITE_W_DRAIN = 0x416
+  SITE_W_KF = 0x413, SITE_W_DE = 0x414, SITE_W_DF = 0x415, SITE_W_DRAIN = 0x416,
+  SITE_W_SE = 0x417, SITE_W_SF = 0x418
 };
 
-template <int H_I, int D_I>
+template <int H_I, int D_I, bool FP8>
 struct Cfg {
-  static constexpr int NCH = D_I / 64;
+  static constexpr int ROWB = FP8 ? D_I : 2 * D_I;  // bytes per key / query-head row
+  static constexpr int NCH = ROWB / 128;            // 128-byte column chunks per row
+  static constexpr int NST = FP8 ? 8 : 5;           // key stages
+  static constexpr int NSC = FP8 ? 16 : 0;          // key-scale slots (one tile each)
   static constexpr int Q_BYTES = NCH * H_I * 128 < 1024 ? 1024 : NCH * H_I * 128;
   static constexpr int K_STAGE = NCH * BKEY * 128;
   static constexpr int N = H_I < 16 ? 16 : H_I;  // MMA N (rows of q beyond H_I are ignored)
   static constexpr int OFF_Q = 0;                    // two q slots
   static constexpr int OFF_K = 2 * (Q_BYTES > N * 128 * NCH ? Q_BYTES : N * 128 * NCH);
-  static constexpr int OFF_MISC = OFF_K + NST * K_STAGE;
+  static constexpr int OFF_SC = OFF_K + NST * K_STAGE;
+  static constexpr int OFF_MISC = OFF_SC + NSC * BKEY * 4;
+  static constexpr int NBARS = 4 + 2 * NST + 9 + 2 * NSC;
+  static_assert(NBARS <= 64, "barrier block");
   static constexpr int MISC_BYTES = 8192 + 1024;     // barriers + work prefix sums
   static constexpr int SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -58,6 +71,8 @@ struct Cfg {
 
 struct Params {
   const uint16_t* w;
+  const float* q_scale;  // FP8: [B, H_I]
+  const float* k_scale;  // FP8: one per key row, numbered like the key rows
   const int32_t* kv_len;
   const int32_t* block_table;
   int64_t seq_stride;
@@ -90,14 +105,14 @@ __device__ __forceinline__ void item_of(const int* pre, int B, int it, int& b, i
   c = it - pre[lo];
 }
 
-template <int H_I, int D_I>
+template <int H_I, int D_I, bool FP8>
 __global__ void __launch_bounds__(NTHREADS, 1)
     decode_scores_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k, const Params p) {
-  using C = Cfg<H_I, D_I>;
-  constexpr int NCH = C::NCH, N = C::N;
+  using C = Cfg<H_I, D_I, FP8>;
+  constexpr int NCH = C::NCH, N = C::N, NST = C::NST, NSC = C::NSC;
   constexpr int QSLOT = C::OFF_K / 2;
-  constexpr uint32_t IDESC = idesc_bf16(128, N, false, false);
+  constexpr uint32_t IDESC = FP8 ? idesc_e4m3(128, N) : idesc_bf16(128, N, false, false);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -110,9 +125,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* d_full = k_empty + NST;
   uint64_t* d_empty = d_full + 4;
   uint64_t* drain = d_empty + 4;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 32);
+  uint64_t* s_full = drain + 1;     // FP8: key-scale slots
+  uint64_t* s_empty = s_full + NSC;
+  float* s_scale = reinterpret_cast<float*>(sm + C::OFF_SC);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 64);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
   int* pre = const_cast<int*>(s_abort) + 4;  // [MAXB + 1] chunk prefix sums
+  int* s_pid = pre + MAXB + 4;               // [32] page ids of the producer's current item
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -120,20 +139,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int k = 0; k < NST; ++k) { mbar_init(&k_full[k], 1); mbar_init(&k_empty[k], 1); }
     for (int k = 0; k < 4; ++k) { mbar_init(&d_full[k], 1); mbar_init(&d_empty[k], 128); }
     mbar_init(drain, 1);
+    for (int k = 0; k < NSC; ++k) { mbar_init(&s_full[k], 1); mbar_init(&s_empty[k], 128); }
     s_abort[0] = 0;
     fence_mbar_init();
-    // per-request chunk counts -> prefix sums
-    int acc = 0;
-    for (int b = 0; b < p.B; ++b) {
-      pre[b] = acc;
-      int L = __ldg(p.kv_len + b);
-      if (L < 0 || L > p.max_kv_len) {
-        status_raise(p.status, DSA_ERR_BAD_INDEX, SITE_LEN, (uint32_t)L);
-        L = 0;
+  }
+  if (warp == 0) {
+    // per-request chunk counts -> prefix sums, 32 requests per warp scan (the
+    // lengths are loaded 32 at a time, not one dependent load per request)
+    int carry = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      const int b = b0 + lane;
+      int n = 0;
+      if (b < p.B) {
+        int L = __ldg(p.kv_len + b);
+        if (L < 0 || L > p.max_kv_len) {
+          status_raise(p.status, DSA_ERR_BAD_INDEX, SITE_LEN, (uint32_t)L);
+          L = 0;
+        }
+        n = (L + CH_TILES * BKEY - 1) / (CH_TILES * BKEY);
       }
-      acc += (L + CH_TILES * BKEY - 1) / (CH_TILES * BKEY);
+      int x = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (b < p.B) pre[b] = carry + x - n;
+      carry += __shfl_sync(0xffffffffu, x, 31);
     }
-    pre[p.B] = acc;
+    if (lane == 0) pre[p.B] = carry;
   }
   if (warp == 1) {
     tmem_alloc(tslot, 256);
@@ -146,38 +180,62 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int total = pre[p.B];
 
   if (warp == 0) {
+    // producer: lane 0 issues every copy; at the start of each work item the
+    // whole warp fetches the item's 32 block-table entries (2 pages per tile)
+    // in one coalesced load, so no copy waits on a dependent table read
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      int kcount = 0, n_items = 0;
-      int last_k[NST];
-      for (int k = 0; k < NST; ++k) last_k[k] = -1;
-      int last_q[2] = {-1, -1};
-      for (int it = blockIdx.x; it < total && !vflag(s_abort); it += gridDim.x, ++n_items) {
-        int b, c;
-        item_of(pre, p.B, it, b, c);
-        const int L = __ldg(p.kv_len + b);
-        const int qs = n_items & 1, quse = n_items >> 1;
-        if (quse > 0 && !mbar_wait(&q_empty[qs], (quse - 1) & 1, p.status, kWaitLimitNs, SITE_W_QE)) {
-          s_abort[0] = 1;
-          break;
+    }
+    int kcount = 0, n_items = 0;
+    int last_k[NST];
+    for (int k = 0; k < NST; ++k) last_k[k] = -1;
+    int last_q[2] = {-1, -1};
+    int last_s[NSC > 0 ? NSC : 1];
+    for (int k = 0; k < NSC; ++k) last_s[k] = -1;
+    bool run = true;
+    for (int it = blockIdx.x; it < total && run; it += gridDim.x, ++n_items) {
+      int b, c;
+      item_of(pre, p.B, it, b, c);
+      const int L = __ldg(p.kv_len + b);
+      const int t0 = c * CH_TILES;
+      const int t1 = min(t0 + CH_TILES, (L + BKEY - 1) / BKEY);
+      if (p.paged) {
+        const int pg = 2 * t0 + lane;
+        int pid = 0;
+        if (pg * kPage < L) {
+          pid = pg < p.max_pages ? __ldg(p.block_table + static_cast<int64_t>(b) * p.max_pages + pg) : -1;
+          if (pid < 0 || pid >= p.num_pages) {
+            status_raise(p.status, DSA_ERR_BAD_INDEX, SITE_PAGE, (uint32_t)pid);
+            pid = 0;
+          }
         }
-        mbar_expect_tx(&q_full[qs], NCH * N * 128);
-        last_q[qs] = quse;
+        s_pid[lane] = pid;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        bool fail = false;
+        const int qs = n_items & 1, quse = n_items >> 1;
+        if (quse > 0 && !mbar_wait(&q_empty[qs], (quse - 1) & 1, p.status, kWaitLimitNs, SITE_W_QE))
+          fail = true;
+        if (!fail) {
+          mbar_expect_tx(&q_full[qs], NCH * N * 128);
+          last_q[qs] = quse;
 #pragma unroll
-        for (int ch = 0; ch < NCH; ++ch)
-          tma_load_2d(sm + C::OFF_Q + qs * QSLOT + ch * N * 128, &tm_q, &q_full[qs], 64 * ch, b * H_I);
-        const int t0 = c * CH_TILES;
-        const int t1 = min(t0 + CH_TILES, (L + BKEY - 1) / BKEY);
-        for (int kt = t0; kt < t1; ++kt, ++kcount) {
+          for (int ch = 0; ch < NCH; ++ch)
+            tma_load_2d(sm + C::OFF_Q + qs * QSLOT + ch * N * 128, &tm_q, &q_full[qs], 64 * ch, b * H_I);
+        }
+        for (int kt = t0; kt < t1 && !fail; ++kt, ++kcount) {
           const int st = kcount % NST, use = kcount / NST;
           if (use > 0 && !mbar_wait(&k_empty[st], (use - 1) & 1, p.status, kWaitLimitNs, SITE_W_KE)) {
-            s_abort[0] = 1;
+            fail = true;
             break;
           }
           mbar_expect_tx(&k_full[st], C::K_STAGE);
           last_k[st] = use;
           uint8_t* dst = sm + C::OFF_K + st * C::K_STAGE;
+          const int pid0 = p.paged ? s_pid[2 * (kt - t0)] : 0;
+          const int pid1 = p.paged ? s_pid[2 * (kt - t0) + 1] : 0;
           if (!p.paged) {
             const int row = static_cast<int>(static_cast<int64_t>(b) * p.seq_stride + kt * BKEY);
 #pragma unroll
@@ -185,23 +243,44 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               tma_load_2d(dst + ch * BKEY * 128, &tm_k, &k_full[st], 64 * ch, row);
           } else {
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-              const int pg = kt * 2 + hf;
-              int pid = 0;
-              if (pg * kPage < L) {
-                pid = pg < p.max_pages ? __ldg(p.block_table + static_cast<int64_t>(b) * p.max_pages + pg) : -1;
-                if (pid < 0 || pid >= p.num_pages) {
-                  status_raise(p.status, DSA_ERR_BAD_INDEX, SITE_PAGE, (uint32_t)pid);
-                  pid = 0;
-                }
-              }
-#pragma unroll
-              for (int ch = 0; ch < NCH; ++ch)
-                tma_load_2d(dst + ch * BKEY * 128 + hf * 64 * 128, &tm_k, &k_full[st], 64 * ch, pid * kPage);
+            for (int ch = 0; ch < NCH; ++ch) {
+              tma_load_2d(dst + ch * BKEY * 128, &tm_k, &k_full[st], 64 * ch, pid0 * kPage);
+              tma_load_2d(dst + ch * BKEY * 128 + 64 * 128, &tm_k, &k_full[st], 64 * ch, pid1 * kPage);
+            }
+          }
+          if constexpr (FP8) {
+            // the tile's key scales, into a slot of their own
+            const int sc = kcount % NSC, suse = kcount / NSC;
+            if (suse > 0 && !mbar_wait(&s_empty[sc], (suse - 1) & 1, p.status, kWaitLimitNs, SITE_W_SE)) {
+              fail = true;
+              break;
+            }
+            last_s[sc] = suse;
+            float* sdst = s_scale + sc * BKEY;
+            if (!p.paged) {
+              // rows of this sequence only (seq_stride is a multiple of 4, so
+              // the copy is whole 16-byte units and never leaves the array)
+              const int64_t r0 = static_cast<int64_t>(b) * p.seq_stride + static_cast<int64_t>(kt) * BKEY;
+              const int64_t left = p.seq_stride - static_cast<int64_t>(kt) * BKEY;
+              const uint32_t bytes = static_cast<uint32_t>(left < BKEY ? left : BKEY) * 4u;
+              mbar_expect_tx(&s_full[sc], bytes);
+              bulk_load(sdst, p.k_scale + r0, bytes, &s_full[sc]);
+            } else {
+              mbar_expect_tx(&s_full[sc], 2 * kPage * 4);
+              bulk_load(sdst, p.k_scale + static_cast<int64_t>(pid0) * kPage, kPage * 4, &s_full[sc]);
+              bulk_load(sdst + kPage, p.k_scale + static_cast<int64_t>(pid1) * kPage, kPage * 4,
+                        &s_full[sc]);
             }
           }
         }
+        if (fail) s_abort[0] = 1;
       }
+      // one decision for the whole warp (other roles may set the flag at any time)
+      run = __shfl_sync(0xffffffffu, vflag(s_abort) ? 0 : 1, 0) != 0;
+    }
+    if (lane == 0) {
+      for (int k = 0; k < NSC; ++k)
+        if (last_s[k] >= 0) mbar_wait(&s_full[k], last_s[k] & 1, p.status, kWaitLimitNs, SITE_W_SF);
       for (int k = 0; k < NST; ++k)
         if (last_k[k] >= 0) mbar_wait(&k_full[k], last_k[k] & 1, p.status, kWaitLimitNs, SITE_W_KF);
       for (int k = 0; k < 2; ++k)
@@ -232,8 +311,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int ch = 0; ch < NCH; ++ch)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(tmem + buf * 64, desc_add(kd, ch * BKEY * 128 + kk * 32),
-                        desc_add(qd, ch * N * 128 + kk * 32), IDESC, (ch | kk) ? 1u : 0u);
+              if constexpr (FP8)
+                umma_e4m3(tmem + buf * 64, desc_add(kd, ch * BKEY * 128 + kk * 32),
+                          desc_add(qd, ch * N * 128 + kk * 32), IDESC, (ch | kk) ? 1u : 0u);
+              else
+                umma_bf16(tmem + buf * 64, desc_add(kd, ch * BKEY * 128 + kk * 32),
+                          desc_add(qd, ch * N * 128 + kk * 32), IDESC, (ch | kk) ? 1u : 0u);
           umma_commit(&k_empty[st]);
           umma_commit(&d_full[buf]);
         }
@@ -256,8 +339,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int L = __ldg(p.kv_len + b);
       float wv[H_I];
 #pragma unroll
-      for (int j = 0; j < H_I; ++j)
+      for (int j = 0; j < H_I; ++j) {
         wv[j] = __bfloat162float(__ushort_as_bfloat16(__ldg(p.w + static_cast<int64_t>(b) * H_I + j)));
+        if constexpr (FP8) wv[j] *= __ldg(p.q_scale + static_cast<int64_t>(b) * H_I + j);
+      }
       const int t0 = c * CH_TILES;
       const int t1 = min(t0 + CH_TILES, (L + BKEY - 1) / BKEY);
       float* out = p.scores + static_cast<int64_t>(b) * p.max_kv_len;
@@ -267,15 +352,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int kt = t0; kt < t1; ++kt, ++dcount) {
         const int buf = dcount & 3;
         // warp-uniform exit, so the warp reductions below stay convergent
+        const int sc = FP8 ? dcount % (NSC > 0 ? NSC : 1) : 0;
         const bool good =
             mbar_wait(&d_full[buf], (dcount >> 2) & 1, p.status, kWaitLimitNs, SITE_W_DF) &&
+            (!FP8 || mbar_wait(&s_full[sc], (dcount / (NSC > 0 ? NSC : 1)) & 1, p.status,
+                               kWaitLimitNs, SITE_W_SF)) &&
             !vflag(s_abort);
         if (!__all_sync(0xffffffffu, good)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        float acc = 0.f;
+        // four independent partial sums: a 64-term dependent FMA chain would
+        // cost more per tile than the tile's copy at full bandwidth
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j0 = 0; j0 < H_I; j0 += (H_I < 32 ? H_I : 32)) {
           uint32_t r[32];
@@ -288,10 +378,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < (H_I < 32 ? H_I : 32); ++e)
-            acc = fmaf(wv[j0 + e], fmaxf(__uint_as_float(r[e]), 0.f), acc);
+            part[e & 3] = fmaf(wv[j0 + e], fmaxf(__uint_as_float(r[e]), 0.f), part[e & 3]);
         }
+        float acc = (part[0] + part[1]) + (part[2] + part[3]);
         tc_fence_before();
         mbar_arrive(&d_empty[buf]);
+        if constexpr (FP8) {
+          acc *= s_scale[sc * BKEY + sub * 32 + lane];
+          mbar_arrive(&s_empty[sc]);
+        }
         const int s = kt * BKEY + sub * 32 + lane;
         if (s < L) {
           out[s] = acc;
@@ -300,6 +395,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           kinv = min(kinv, ~ok_);
         }
       }
+      if (!ok) s_abort[0] = 1;
       kmin = __reduce_min_sync(0xffffffffu, kmin);
       kinv = __reduce_min_sync(0xffffffffu, kinv);
       if (lane == 0 && ok && kmin != 0xffffffffu) {
@@ -567,21 +663,26 @@ size_t indexer_decode_scratch_bytes(int B, int max_kv_len) {
   return minmax_offset(B, max_kv_len) + static_cast<size_t>(B) * 2 * sizeof(uint32_t) + 256;
 }
 
-template <int H_I, int D_I>
+template <int H_I, int D_I, bool FP8>
 static dsa_status_t decode_launch(const IndexerArgs& a, cudaStream_t stream) {
-  using C = idxd::Cfg<H_I, D_I>;
+  using C = idxd::Cfg<H_I, D_I, FP8>;
   if (a.B > idxd::MAXB) return DSA_ERR_UNSUPPORTED;
   if (a.scratch == nullptr || a.scratch_bytes < indexer_decode_scratch_bytes(a.B, a.max_kv_len))
     return DSA_ERR_WORKSPACE_TOO_SMALL;
   CUtensorMap tq, tk;
   // q rows: one request = H_I rows of D_I; the box reads N rows (extra rows are ignored)
-  if (!encode_tmap_2d(&tq, a.q_idx, static_cast<uint64_t>(a.B) * H_I, D_I, D_I * 2, 64, C::N, true))
+  // (FP8 code rows are described as BF16 pairs: the copy moves bytes only)
+  if (!encode_tmap_2d(&tq, a.q_idx, static_cast<uint64_t>(a.B) * H_I, C::ROWB / 2, C::ROWB, 64,
+                      C::N, true))
     return DSA_ERR_CUDA;
   const bool paged = a.k.block_table != nullptr;
-  if (!encode_tmap_2d(&tk, a.k.base, a.k.total_rows, D_I, D_I * 2, 64, paged ? 64 : 128, true))
+  if (!encode_tmap_2d(&tk, a.k.base, a.k.total_rows, C::ROWB / 2, C::ROWB, 64, paged ? 64 : 128,
+                      true))
     return DSA_ERR_CUDA;
   idxd::Params p{};
   p.w = a.w;
+  p.q_scale = a.q_scale;
+  p.k_scale = a.k_scale;
   p.kv_len = a.kv_len;
   p.block_table = a.k.block_table;
   p.seq_stride = a.k.seq_stride;
@@ -598,7 +699,7 @@ static dsa_status_t decode_launch(const IndexerArgs& a, cudaStream_t stream) {
   if (cudaMemsetAsync(p.minmax, 0xff, static_cast<size_t>(a.B) * 2 * sizeof(uint32_t), stream) !=
       cudaSuccess)
     return launch_status("cudaMemsetAsync");
-  auto kern = idxd::decode_scores_kernel<H_I, D_I>;
+  auto kern = idxd::decode_scores_kernel<H_I, D_I, FP8>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
       cudaSuccess)
     return launch_status("cudaFuncSetAttribute");
@@ -616,8 +717,12 @@ static dsa_status_t decode_launch(const IndexerArgs& a, cudaStream_t stream) {
 }
 
 dsa_status_t indexer_decode_launch(const IndexerArgs& a, cudaStream_t stream) {
-  if (a.H_I == 64 && a.D_I == 128) return decode_launch<64, 128>(a, stream);
-  if (a.H_I == 4 && a.D_I == 64) return decode_launch<4, 64>(a, stream);
+  if (a.fp8) {
+    if (a.H_I == 64 && a.D_I == 128) return decode_launch<64, 128, true>(a, stream);
+    return DSA_ERR_UNSUPPORTED;
+  }
+  if (a.H_I == 64 && a.D_I == 128) return decode_launch<64, 128, false>(a, stream);
+  if (a.H_I == 4 && a.D_I == 64) return decode_launch<4, 64, false>(a, stream);
   return DSA_ERR_UNSUPPORTED;
 }
 

@@ -52,7 +52,10 @@ dsa_status_t sparse_mla_launch(const SparseMlaArgs& a, cudaStream_t stream);
 
 // --- indexer + top-k --------------------------------------------------------------
 struct IndexerArgs {
-  const uint16_t* q_idx;
+  const uint16_t* q_idx;       // BF16 queries, or E4M3 codes when fp8
+  const float* q_scale;        // fp8: [B, Tq, H_I]
+  const float* k_scale;        // fp8: one per key row, numbered like k's rows
+  bool fp8;
   const uint16_t* w;
   RowStore k;
   const int32_t* q_start;
@@ -87,9 +90,13 @@ struct AppendArgs {
   const int32_t* q_start;
   int B, Tq, D_I;
   float eps;
+  float* k_scale;     // non-null: FP8 variant (k_cache holds E4M3 code rows)
   uint32_t* status;
 };
 dsa_status_t cache_append_launch(const AppendArgs& a, cudaStream_t stream);
+// BF16 rows [n_rows, D] -> E4M3 codes + one FP32 scale per row (D in {64, 128}).
+dsa_status_t quant_fp8_launch(const uint16_t* x, int64_t n_rows, int D, uint8_t* codes,
+                              float* scale, cudaStream_t stream);
 
 int num_sms();
 

@@ -164,6 +164,18 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // D[tmem] (+)= A[smem] * B[smem], BF16 inputs, FP32 accumulation.
+// D (TMEM, FP32) (+)= A . B^T for 8-bit operands (kind::f8f6f4): one
+// instruction covers K = 32 elements, i.e. 32 bytes of each K-major row, the
+// same byte step as one BF16 instruction.
+__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -255,6 +267,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          ((static_cast<uint32_t>(M) >> 4) << 24);
 }
 
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0
+// in both fields), both K-major, and FP32 D.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((static_cast<uint32_t>(N) >> 3) << 17) |
+         ((static_cast<uint32_t>(M) >> 4) << 24);
+}
+
 // Byte offset of element (row, k) inside a K-major, 128-byte-swizzled tile
 // whose rows hold 64 BF16 elements (one 128-byte line) and whose 8-row groups
 // are packed 1024 bytes apart.  k in [0, 64).
@@ -269,6 +288,14 @@ __host__ __device__ __forceinline__ uint32_t sw128_unit(uint32_t row, uint32_t u
 // ---------------------------------------------------------------------------
 // misc
 // ---------------------------------------------------------------------------
+// Two floats -> two E4M3 codes (round to nearest even, saturating at +-448):
+// `hi` goes to bits 15:8, `lo` to bits 7:0.
+__device__ __forceinline__ uint32_t e4m3x2(float hi, float lo) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
 __device__ __forceinline__ float redux_max_f32(float v) {
   float r;
   asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));

@@ -112,3 +112,32 @@ def test_host_argument_checks(dsa):
                               None) == dsa.DSA_ERR_UNSUPPORTED
     assert lib.mla_gate_apply(fake, fake, None, fake, 16, 1024, 8, 128, fake, ws, 1 << 20,
                               None) == dsa.DSA_ERR_INVALID_ARGUMENT
+
+
+def test_host_argument_checks_fp8(dsa):
+    lib = dsa.lib
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    ws = P(1 << 24)
+    r = _rows(base=1 << 20, stride=128)
+
+    def topk8(q=fake, qs=fake, ks=fake, rows=r, B=1, Tq=1, H_I=64, D_I=128, S=128, k=64):
+        return lib.dsa_indexer_topk_fp8(q, qs, fake, ctypes.byref(rows), ks, fake, fake, B, Tq,
+                                        H_I, D_I, S, k, fake, ws, 1 << 20, None)
+
+    assert topk8(qs=None) == dsa.DSA_ERR_INVALID_ARGUMENT       # scales are required
+    assert topk8(ks=None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert topk8(ks=P((1 << 20) + 4)) == dsa.DSA_ERR_INVALID_ARGUMENT  # key scales 16-byte aligned
+    assert topk8(H_I=4, D_I=64) == dsa.DSA_ERR_UNSUPPORTED      # (64, 128) only
+    # contiguous keys with a row stride that is not a multiple of 4
+    assert topk8(rows=_rows(base=1 << 20, stride=130), S=128) == dsa.DSA_ERR_UNSUPPORTED
+    # quantizer: D other than 64 / 128, misaligned input, negative row count
+    assert lib.dsa_quant_fp8(fake, 16, 96, fake, fake, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert lib.dsa_quant_fp8(P((1 << 20) + 2), 16, 128, fake, fake, None) == \
+        dsa.DSA_ERR_INVALID_ARGUMENT
+    assert lib.dsa_quant_fp8(fake, -1, 128, fake, fake, None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert lib.dsa_quant_fp8(fake, 0, 128, fake, fake, None) == dsa.DSA_OK   # nothing to do
+    # FP8 cache append needs its scale array
+    assert lib.dsa_cache_append_fp8(fake, fake, ctypes.byref(r), None, ctypes.byref(r), fake, 1, 1,
+                                    128, ctypes.c_float(1e-5), ws, 1 << 20,
+                                    None) == dsa.DSA_ERR_INVALID_ARGUMENT
