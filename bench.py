@@ -2,7 +2,7 @@
 """Benchmark of the gated DSA attention step on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload head8192|val4096|decode64]
+                    [--workload head8192|val4096|decode64|decode16]
 
 One step = one pass of the whole prefill hot path over one batch:
 lightning indexer + top-k -> sparse MLA -> output gate, through the C ABI.
@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="head8192",
-                    choices=["head8192", "val4096", "decode64", "tiny"])
+                    choices=["head8192", "val4096", "decode64", "decode16", "tiny"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=0, help="oracle sample size (0 = auto)")

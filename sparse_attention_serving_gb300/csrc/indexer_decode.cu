@@ -18,10 +18,12 @@
 //                  of its request (one atomic per warp).
 //                  FP8 variant (E4M3 code rows of 128 bytes, one FP32 scale
 //                  per key and per query head): the same pipeline with one
-//                  kind::f8f6f4 MMA chunk per tile, half the key bytes, and the
-//                  key scales streamed into a ring of their own by bulk copies;
-//                  the query scales fold into the head weights and the key
-//                  scale multiplies the head sum:
+//                  kind::f8f6f4 MMA chunk per tile and half the key bytes.  The
+//                  key scales of a whole work item (32 pages x 64) are fetched
+//                  at its start by the 32 producer lanes with asynchronous
+//                  copies into a two-item buffer, so the per-tile issue loop
+//                  carries only the key copies; the query scales fold into the
+//                  head weights and the key scale multiplies the head sum:
 //                    I[s] = k_scale[s] * sum_j (w[j] q_scale[j]) max(0, c_q[j] . c_k[s]).
 //   decode_select  one CTA per request: a value histogram between those
 //                  extremes finds the bin of the k-th largest score, a second
@@ -40,7 +42,8 @@ namespace idxd {
 
 constexpr int BKEY = 128;
 constexpr int CH_TILES = 16;  // tiles per work item (2,048 keys)
-constexpr int NTHREADS = 192;  // producer, MMA, 4 epilogue warps
+constexpr int NGRP = 2;        // epilogue groups of 4 warps, alternating tiles
+constexpr int NTHREADS = 64 + NGRP * 128;  // producer, MMA, epilogue groups
 constexpr int MAXB = 1024;     // requests per call handled by the work decomposition
 
 enum : uint32_t {
@@ -49,21 +52,23 @@ enum : uint32_t {
   SITE_W_SE = 0x417, SITE_W_SF = 0x418
 };
 
+constexpr int ITEM_KEYS = CH_TILES * BKEY;  // 2,048 keys = 32 pages per work item
+
 template <int H_I, int D_I, bool FP8>
 struct Cfg {
   static constexpr int ROWB = FP8 ? D_I : 2 * D_I;  // bytes per key / query-head row
   static constexpr int NCH = ROWB / 128;            // 128-byte column chunks per row
-  static constexpr int NST = FP8 ? 8 : 5;           // key stages
-  static constexpr int NSC = FP8 ? 16 : 0;          // key-scale slots (one tile each)
+  static constexpr int NST = FP8 ? 10 : 5;          // key stages (bytes in flight for HBM latency)
+  static constexpr int NSB = FP8 ? 2 : 0;           // key-scale buffers (one work item each)
   static constexpr int Q_BYTES = NCH * H_I * 128 < 1024 ? 1024 : NCH * H_I * 128;
   static constexpr int K_STAGE = NCH * BKEY * 128;
   static constexpr int N = H_I < 16 ? 16 : H_I;  // MMA N (rows of q beyond H_I are ignored)
   static constexpr int OFF_Q = 0;                    // two q slots
   static constexpr int OFF_K = 2 * (Q_BYTES > N * 128 * NCH ? Q_BYTES : N * 128 * NCH);
   static constexpr int OFF_SC = OFF_K + NST * K_STAGE;
-  static constexpr int OFF_MISC = OFF_SC + NSC * BKEY * 4;
-  static constexpr int NBARS = 4 + 2 * NST + 9 + 2 * NSC;
-  static_assert(NBARS <= 64, "barrier block");
+  static constexpr int OFF_MISC = OFF_SC + NSB * ITEM_KEYS * 4;
+  static constexpr int NBARS = 4 + 2 * NST + 9 + 2 * NSB;
+  static_assert(NBARS <= 96, "barrier block");
   static constexpr int MISC_BYTES = 8192 + 1024;     // barriers + work prefix sums
   static constexpr int SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -110,7 +115,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     decode_scores_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k, const Params p) {
   using C = Cfg<H_I, D_I, FP8>;
-  constexpr int NCH = C::NCH, N = C::N, NST = C::NST, NSC = C::NSC;
+  constexpr int NCH = C::NCH, N = C::N, NST = C::NST, NSB = C::NSB;
   constexpr int QSLOT = C::OFF_K / 2;
   constexpr uint32_t IDESC = FP8 ? idesc_e4m3(128, N) : idesc_bf16(128, N, false, false);
   extern __shared__ uint8_t smem_raw[];
@@ -125,10 +130,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* d_full = k_empty + NST;
   uint64_t* d_empty = d_full + 4;
   uint64_t* drain = d_empty + 4;
-  uint64_t* s_full = drain + 1;     // FP8: key-scale slots
-  uint64_t* s_empty = s_full + NSC;
-  float* s_scale = reinterpret_cast<float*>(sm + C::OFF_SC);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 64);
+  uint64_t* si_full = drain + 1;    // FP8: key-scale buffers of a work item
+  uint64_t* si_empty = si_full + NSB;
+  float* s_scale = reinterpret_cast<float*>(sm + C::OFF_SC);  // [NSB][ITEM_KEYS]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 96);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
   int* pre = const_cast<int*>(s_abort) + 4;  // [MAXB + 1] chunk prefix sums
   int* s_pid = pre + MAXB + 4;               // [32] page ids of the producer's current item
@@ -139,7 +144,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int k = 0; k < NST; ++k) { mbar_init(&k_full[k], 1); mbar_init(&k_empty[k], 1); }
     for (int k = 0; k < 4; ++k) { mbar_init(&d_full[k], 1); mbar_init(&d_empty[k], 128); }
     mbar_init(drain, 1);
-    for (int k = 0; k < NSC; ++k) { mbar_init(&s_full[k], 1); mbar_init(&s_empty[k], 128); }
+    // full: one arrival per producer lane (its asynchronous copies landed);
+    // empty: one per epilogue warp, after its last tile of the item
+    for (int k = 0; k < NSB; ++k) { mbar_init(&si_full[k], 32); mbar_init(&si_empty[k], NGRP * 4); }
     s_abort[0] = 0;
     fence_mbar_init();
   }
@@ -191,8 +198,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int last_k[NST];
     for (int k = 0; k < NST; ++k) last_k[k] = -1;
     int last_q[2] = {-1, -1};
-    int last_s[NSC > 0 ? NSC : 1];
-    for (int k = 0; k < NSC; ++k) last_s[k] = -1;
     bool run = true;
     for (int it = blockIdx.x; it < total && run; it += gridDim.x, ++n_items) {
       int b, c;
@@ -212,9 +217,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         s_pid[lane] = pid;
       }
+      if constexpr (FP8) {
+        // the item's key scales: lane l copies those of the item's page l
+        // (64 FP32, 16 x 16 bytes) once the epilogue is done with the buffer
+        const int sb = n_items & 1, suse = n_items >> 1;
+        bool ok_e = true;
+        if (lane == 0 && suse > 0)
+          ok_e = mbar_wait(&si_empty[sb], (suse - 1) & 1, p.status, kWaitLimitNs, SITE_W_SE);
+        if (!__shfl_sync(0xffffffffu, ok_e ? 1 : 0, 0)) {
+          if (lane == 0) s_abort[0] = 1;
+        } else {
+          const float* src;
+          int nfl;
+          if (p.paged) {
+            src = p.k_scale + static_cast<int64_t>(s_pid[lane]) * kPage;
+            nfl = kPage;
+          } else {
+            // rows of this sequence only (seq_stride is a multiple of 4)
+            const int64_t off = static_cast<int64_t>(t0) * BKEY + lane * kPage;
+            const int64_t left = p.seq_stride - off;
+            src = p.k_scale + static_cast<int64_t>(b) * p.seq_stride + off;
+            nfl = left <= 0 ? 0 : (left < kPage ? static_cast<int>(left) : kPage);
+          }
+          const uint32_t dst = smem_u32(s_scale + sb * ITEM_KEYS + lane * kPage);
+          for (int u = 0; u < nfl / 4; ++u) cp_async_16(dst + 16u * u, src + 4 * u);
+          cp_async_arrive(&si_full[sb]);
+        }
+      }
       __syncwarp();
       if (lane == 0) {
-        bool fail = false;
+        bool fail = vflag(s_abort);
         const int qs = n_items & 1, quse = n_items >> 1;
         if (quse > 0 && !mbar_wait(&q_empty[qs], (quse - 1) & 1, p.status, kWaitLimitNs, SITE_W_QE))
           fail = true;
@@ -248,39 +280,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               tma_load_2d(dst + ch * BKEY * 128 + 64 * 128, &tm_k, &k_full[st], 64 * ch, pid1 * kPage);
             }
           }
-          if constexpr (FP8) {
-            // the tile's key scales, into a slot of their own
-            const int sc = kcount % NSC, suse = kcount / NSC;
-            if (suse > 0 && !mbar_wait(&s_empty[sc], (suse - 1) & 1, p.status, kWaitLimitNs, SITE_W_SE)) {
-              fail = true;
-              break;
-            }
-            last_s[sc] = suse;
-            float* sdst = s_scale + sc * BKEY;
-            if (!p.paged) {
-              // rows of this sequence only (seq_stride is a multiple of 4, so
-              // the copy is whole 16-byte units and never leaves the array)
-              const int64_t r0 = static_cast<int64_t>(b) * p.seq_stride + static_cast<int64_t>(kt) * BKEY;
-              const int64_t left = p.seq_stride - static_cast<int64_t>(kt) * BKEY;
-              const uint32_t bytes = static_cast<uint32_t>(left < BKEY ? left : BKEY) * 4u;
-              mbar_expect_tx(&s_full[sc], bytes);
-              bulk_load(sdst, p.k_scale + r0, bytes, &s_full[sc]);
-            } else {
-              mbar_expect_tx(&s_full[sc], 2 * kPage * 4);
-              bulk_load(sdst, p.k_scale + static_cast<int64_t>(pid0) * kPage, kPage * 4, &s_full[sc]);
-              bulk_load(sdst + kPage, p.k_scale + static_cast<int64_t>(pid1) * kPage, kPage * 4,
-                        &s_full[sc]);
-            }
-          }
         }
         if (fail) s_abort[0] = 1;
       }
       // one decision for the whole warp (other roles may set the flag at any time)
       run = __shfl_sync(0xffffffffu, vflag(s_abort) ? 0 : 1, 0) != 0;
     }
+    if constexpr (FP8) cp_async_wait_all();   // no copy lands after the CTA exits
     if (lane == 0) {
-      for (int k = 0; k < NSC; ++k)
-        if (last_s[k] >= 0) mbar_wait(&s_full[k], last_s[k] & 1, p.status, kWaitLimitNs, SITE_W_SF);
       for (int k = 0; k < NST; ++k)
         if (last_k[k] >= 0) mbar_wait(&k_full[k], last_k[k] & 1, p.status, kWaitLimitNs, SITE_W_KF);
       for (int k = 0; k < 2; ++k)
@@ -328,15 +335,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     __syncwarp();
   } else {
-    // epilogue: thread = key lane of the tile; no group barrier is needed
+    // epilogue: thread = key lane of the tile; no group barrier is needed.  Two
+    // groups of four warps take alternate tiles (group g the tiles with
+    // dcount % 2 == g, i.e. TMEM buffers g and g + 2), so two tiles' head sums
+    // are in flight on every scheduler.
     const int sub = warp & 3;
+    const int grp = (warp - 2) >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(sub * 32) << 16;
-    int dcount = 0;
+    int dcount = 0, n_item = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < total && ok; it += gridDim.x) {
+    for (int it = blockIdx.x; it < total && ok; it += gridDim.x, ++n_item) {
       int b, c;
       item_of(pre, p.B, it, b, c);
       const int L = __ldg(p.kv_len + b);
+      const int sb = FP8 ? (n_item & 1) : 0;
+      const float* isc = s_scale + sb * ITEM_KEYS;
       float wv[H_I];
 #pragma unroll
       for (int j = 0; j < H_I; ++j) {
@@ -346,17 +359,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int t0 = c * CH_TILES;
       const int t1 = min(t0 + CH_TILES, (L + BKEY - 1) / BKEY);
       float* out = p.scores + static_cast<int64_t>(b) * p.max_kv_len;
+      if constexpr (FP8) {
+        // the item's key scales (warp-uniform decision)
+        const bool sgood = mbar_wait(&si_full[sb], (n_item >> 1) & 1, p.status, kWaitLimitNs, SITE_W_SF);
+        if (!__all_sync(0xffffffffu, sgood)) {
+          ok = false;
+          s_abort[0] = 1;
+          break;
+        }
+      }
       // running extremes of this item's scores as order keys (the select
       // kernel bins by value between them)
       uint32_t kmin = 0xffffffffu, kinv = 0xffffffffu;
       for (int kt = t0; kt < t1; ++kt, ++dcount) {
+        if ((dcount & (NGRP - 1)) != grp) continue;
         const int buf = dcount & 3;
         // warp-uniform exit, so the warp reductions below stay convergent
-        const int sc = FP8 ? dcount % (NSC > 0 ? NSC : 1) : 0;
         const bool good =
             mbar_wait(&d_full[buf], (dcount >> 2) & 1, p.status, kWaitLimitNs, SITE_W_DF) &&
-            (!FP8 || mbar_wait(&s_full[sc], (dcount / (NSC > 0 ? NSC : 1)) & 1, p.status,
-                               kWaitLimitNs, SITE_W_SF)) &&
             !vflag(s_abort);
         if (!__all_sync(0xffffffffu, good)) {
           ok = false;
@@ -383,10 +403,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         float acc = (part[0] + part[1]) + (part[2] + part[3]);
         tc_fence_before();
         mbar_arrive(&d_empty[buf]);
-        if constexpr (FP8) {
-          acc *= s_scale[sc * BKEY + sub * 32 + lane];
-          mbar_arrive(&s_empty[sc]);
-        }
+        if constexpr (FP8) acc *= isc[(kt - t0) * BKEY + sub * 32 + lane];
         const int s = kt * BKEY + sub * 32 + lane;
         if (s < L) {
           out[s] = acc;
@@ -396,6 +413,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       if (!ok) s_abort[0] = 1;
+      if constexpr (FP8) {
+        // this warp is done with the item's scales
+        __syncwarp();
+        if (lane == 0 && ok) mbar_arrive(&si_empty[sb]);
+      }
       kmin = __reduce_min_sync(0xffffffffu, kmin);
       kinv = __reduce_min_sync(0xffffffffu, kinv);
       if (lane == 0 && ok && kmin != 0xffffffffu) {

@@ -80,6 +80,9 @@ CONFIGS = {
     # 5: serving decode over paged caches
     "decode64": Config("decode64", B=64, T=1, topk=2048, H_I=64, D_I=128, H=96, hid=7168,
                        paged=True, decode=True, L_min=16384, L_max=131072, seed=5),
+    # the same request mix at 16 requests (about 2 GB of caches): the profiling case
+    "decode16": Config("decode16", B=16, T=1, topk=2048, H_I=64, D_I=128, H=96, hid=7168,
+                       paged=True, decode=True, L_min=16384, L_max=131072, seed=6),
 }
 
 
