@@ -55,7 +55,7 @@ struct Cfg {
   static constexpr int N = QT * H_I;                          // MMA N
   static constexpr int ROWB = FP8 ? D_I : 2 * D_I;            // bytes per key / query-head row
   static constexpr int NCH = ROWB / 128;                      // 128-byte column chunks
-  static constexpr int NST = FP8 ? 4 : 3;                     // key-tile stages
+  static constexpr int NST = FP8 ? 6 : 3;                     // key-tile stages
   static constexpr int NSC = FP8 ? 8 : 0;                     // key-scale slots (FP8)
   static constexpr int Q_BYTES = NCH * N * 128;
   static constexpr int K_STAGE = NCH * BKEY * 128;
@@ -63,11 +63,12 @@ struct Cfg {
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_SC = OFF_K + NST * K_STAGE;
   static constexpr int OFF_W = OFF_SC + NSC * BKEY * 4;
-  // barriers: Q, K full [NST], K empty [NST], D full [2], D empty [2], drain,
+  // barriers: Q, K full [NST], K empty [NST], D full [4], D empty [4], drain,
   // scale full [NSC], scale empty [NSC]
-  static constexpr int BQ = 0, BKF = 1, BKE = BKF + NST, BDF = BKE + NST, BDE = BDF + 2,
-                       BDRAIN = BDE + 2, BSF = BDRAIN + 1, BSE = BSF + NSC, NBARS = BSE + NSC;
-  static_assert(NBARS <= 32, "barrier block");
+  static constexpr int BQ = 0, BKF = 1, BKE = BKF + NST, BDF = BKE + NST, BDE = BDF + 4,
+                       BDRAIN = BDE + 4, BSF = BDRAIN + 1, BSE = BSF + NSC, NBARS = BSE + NSC;
+  static_assert(NBARS <= 48, "barrier block");
+  static_assert(4 * N <= 512, "four accumulator buffers in TMEM");
   static constexpr int OFF_MISC = OFF_W + QT * H_I * 4;
   static constexpr int MISC_BYTES = 4096;
   static constexpr int OFF_CAND = OFF_MISC + MISC_BYTES;
@@ -274,9 +275,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   float* w_s = reinterpret_cast<float*>(sm + C::OFF_W);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_MISC);  // 32 barrier slots
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_MISC);  // 48 barrier slots
   float* s_scale = reinterpret_cast<float*>(sm + C::OFF_SC);         // FP8: [NSC][128]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 32);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 48);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
   volatile int* g_abort = s_abort + 1;   // [4]
   int* cnt = const_cast<int*>(s_abort) + 8;  // [QT] candidates per query
@@ -317,7 +318,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int ntiles = (t_last + BKEY) / BKEY;
   if (tid == 0) {
     for (int k = 0; k < C::NBARS; ++k)
-      mbar_init(&bars[k], ((k >= C::BDE && k < C::BDE + 2) || k >= C::BSE) ? G : 1);
+      mbar_init(&bars[k], ((k >= C::BDE && k < C::BDE + 4) || k >= C::BSE) ? G : 1);
     s_abort[0] = 0;
     for (int k = 0; k < 4; ++k) g_abort[k] = 0;
     fence_mbar_init();
@@ -431,8 +432,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint64_t qd0 = smem_desc(smem_u32(sm + C::OFF_Q), 16, 1024);
       for (int kt = 0; kt < ntiles && ok; ++kt) {
         if (vflag(s_abort)) { ok = false; break; }
-        const int st = kt % NST, buf = kt & 1;
-        if (kt >= 2 && !mbar_wait(&bars[C::BDE + buf], ((kt >> 1) - 1) & 1, p.status, kWaitLimitNs, SITE_W_DE)) { ok = false; break; }
+        const int st = kt % NST, buf = kt & 3;
+        if (kt >= 4 && !mbar_wait(&bars[C::BDE + buf], ((kt >> 2) - 1) & 1, p.status, kWaitLimitNs, SITE_W_DE)) { ok = false; break; }
         if (!mbar_wait(&bars[C::BKF + st], (kt / NST) & 1, p.status, kWaitLimitNs, SITE_W_KF)) { ok = false; break; }
         tc_fence_after();
         const uint64_t kd = smem_desc(smem_u32(sm + C::OFF_K + st * C::K_STAGE), 16, 1024);
@@ -441,10 +442,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             if constexpr (FP8)
-              umma_e4m3(tmem + buf * 256, desc_add(kd, c * BKEY * 128 + kk * 32),
+              umma_e4m3(tmem + buf * N, desc_add(kd, c * BKEY * 128 + kk * 32),
                         desc_add(qd0, c * N * 128 + kk * 32), IDESC, (c | kk) ? 1u : 0u);
             else
-              umma_bf16(tmem + buf * 256, desc_add(kd, c * BKEY * 128 + kk * 32),
+              umma_bf16(tmem + buf * N, desc_add(kd, c * BKEY * 128 + kk * 32),
                         desc_add(qd0, c * N * 128 + kk * 32), IDESC, (c | kk) ? 1u : 0u);
         umma_commit(&bars[C::BKE + st]);
         umma_commit(&bars[C::BDF + buf]);
@@ -473,83 +474,96 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
       for (int c = 0; c < QH * H_I; ++c) wreg[c] = w_s[half * QH * H_I + c];
       bool want_sel = false;
-      for (; kt < ntiles; ++kt) {
-        const int buf = kt & 1;
-        const int sc = FP8 ? kt % (NSC > 0 ? NSC : 1) : 0;
-        const bool w_ok =
-            mbar_wait(&bars[C::BDF + buf], (kt >> 1) & 1, p.status, kWaitLimitNs, SITE_W_DF) &&
-            (!FP8 || mbar_wait(&bars[C::BSF + sc], (kt / (NSC > 0 ? NSC : 1)) & 1, p.status,
-                               kWaitLimitNs, SITE_W_SF));
-        if (!w_ok || vflag(s_abort)) g_abort[(kt & 1) * 2] = 1;
-        named_bar_sync(1, G);
-        if (vflag(&g_abort[(kt & 1) * 2])) {
-          stop = true;
-          break;
+      // Tiles in pairs with one group barrier per pair: a candidate buffer keeps
+      // room for two tiles' appends between checks, and the MMA runs up to
+      // four tiles ahead (four TMEM accumulator buffers).
+      for (; kt < ntiles; kt += 2) {
+        const int n2 = ntiles - kt < 2 ? ntiles - kt : 2;
+        bool w_ok = !vflag(s_abort);
+        for (int u = 0; u < n2 && w_ok; ++u) {
+          const int k = kt + u;
+          w_ok = mbar_wait(&bars[C::BDF + (k & 3)], (k >> 2) & 1, p.status, kWaitLimitNs, SITE_W_DF) &&
+                 (!FP8 || mbar_wait(&bars[C::BSF + k % (NSC > 0 ? NSC : 1)],
+                                    (k / (NSC > 0 ? NSC : 1)) & 1, p.status, kWaitLimitNs, SITE_W_SF));
         }
-        tc_fence_after();
-        // head reduction: 4 independent FMA chains per query (the MMA's FP32
-        // accumulators are summed in a fixed order: chain c takes heads c, c+4, ...)
-        constexpr int COLS = QH * H_I;  // this half's accumulator columns
-        constexpr int NCHAIN = 4;
-        float acc[QH][NCHAIN];
+        // the TMEM loads and ballots below are warp-collective: one decision per warp
+        w_ok = __all_sync(0xffffffffu, w_ok);
+        if (!w_ok) {
+          g_abort[0] = 1;
+        } else {
+          tc_fence_after();
+          for (int u = 0; u < n2; ++u) {
+            const int k = kt + u, buf = k & 3;
+            // head reduction: 4 independent FMA chains per query (the MMA's FP32
+            // accumulators are summed in a fixed order: chain c takes heads c, c+4, ...)
+            constexpr int COLS = QH * H_I;  // this half's accumulator columns
+            constexpr int NCHAIN = 4;
+            float acc[QH][NCHAIN];
 #pragma unroll
-        for (int q = 0; q < QH; ++q)
+            for (int q = 0; q < QH; ++q)
 #pragma unroll
-          for (int c = 0; c < NCHAIN; ++c) acc[q][c] = 0.f;
-        const uint32_t col0 = buf * 256 + half * COLS;
+              for (int c = 0; c < NCHAIN; ++c) acc[q][c] = 0.f;
+            const uint32_t col0 = buf * N + half * COLS;
 #pragma unroll
-        for (int u = 0; u < COLS / 32; ++u) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_base + col0 + u * 32, r);
-          tmem_ld_wait();
+            for (int v = 0; v < COLS / 32; ++v) {
+              uint32_t r[32];
+              tmem_ld32(tmem + lane_base + col0 + v * 32, r);
+              tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int col = u * 32 + e;
-            const int q = col / H_I;
-            const float v = fmaxf(__uint_as_float(r[e]), 0.f);
-            acc[q][e % NCHAIN] = fmaf(wreg[col], v, acc[q][e % NCHAIN]);
-          }
-        }
-        float score[QH];
+              for (int e = 0; e < 32; ++e) {
+                const int col = v * 32 + e;
+                const int q = col / H_I;
+                const float x = fmaxf(__uint_as_float(r[e]), 0.f);
+                acc[q][e % NCHAIN] = fmaf(wreg[col], x, acc[q][e % NCHAIN]);
+              }
+            }
+            float score[QH];
 #pragma unroll
-        for (int q = 0; q < QH; ++q) score[q] = (acc[q][0] + acc[q][1]) + (acc[q][2] + acc[q][3]);
-        tc_fence_before();
-        mbar_arrive(&bars[C::BDE + buf]);
-        if constexpr (FP8) {
-          const float ks = s_scale[sc * BKEY + key_lane];
+            for (int q = 0; q < QH; ++q) score[q] = (acc[q][0] + acc[q][1]) + (acc[q][2] + acc[q][3]);
+            tc_fence_before();
+            mbar_arrive(&bars[C::BDE + buf]);
+            if constexpr (FP8) {
+              const int sc = k % (NSC > 0 ? NSC : 1);
+              const float ks = s_scale[sc * BKEY + key_lane];
 #pragma unroll
-          for (int q = 0; q < QH; ++q) score[q] *= ks;
-          mbar_arrive(&bars[C::BSE + sc]);
-        }
-        // append candidates above each query's threshold
-        const int s = kt * BKEY + key_lane;
+              for (int q = 0; q < QH; ++q) score[q] *= ks;
+              mbar_arrive(&bars[C::BSE + sc]);
+            }
+            // append candidates above each query's threshold
+            const int s = k * BKEY + key_lane;
 #pragma unroll
-        for (int q = 0; q < QH; ++q) {
-          const int qq = half * QH + q;
-          const bool take = qq < nq && s <= t0 + qq && score[q] > thr[qq];
-          const uint32_t bal = __ballot_sync(0xffffffffu, take);
-          if (bal) {
-            int base = 0;
-            if (lane == 0) base = atomicAdd(&cnt[qq], __popc(bal));
-            base = __shfl_sync(0xffffffffu, base, 0);
-            if (take) {
-              const int pos = base + __popc(bal & ((1u << lane) - 1u));
-              cand_s[qq * CAP + pos] = score[q];
-              cand_i[qq * CAP + pos] = s;
+            for (int q = 0; q < QH; ++q) {
+              const int qq = half * QH + q;
+              const bool take = qq < nq && s <= t0 + qq && score[q] > thr[qq];
+              const uint32_t bal = __ballot_sync(0xffffffffu, take);
+              if (bal) {
+                int base = 0;
+                if (lane == 0) base = atomicAdd(&cnt[qq], __popc(bal));
+                base = __shfl_sync(0xffffffffu, base, 0);
+                if (take) {
+                  const int pos = base + __popc(bal & ((1u << lane) - 1u));
+                  cand_s[qq * CAP + pos] = score[q];
+                  cand_i[qq * CAP + pos] = s;
+                }
+              }
             }
           }
         }
         named_bar_sync(1, G);
-        // a buffer that could overflow on the next tile is shrunk outside this loop
-        for (int qq = 0; qq < nq; ++qq) want_sel |= cnt[qq] > CAP - BKEY;
+        if (vflag(&g_abort[0])) {
+          stop = true;
+          break;
+        }
+        // a buffer that could overflow on the next pair is shrunk outside this loop
+        for (int qq = 0; qq < nq; ++qq) want_sel |= cnt[qq] > CAP - 2 * BKEY;
         if (want_sel) {
-          ++kt;
+          kt += n2;
           break;
         }
       }
       if (want_sel) {
         for (int qq = 0; qq < nq; ++qq) {
-          if (cnt[qq] > CAP - BKEY) {
+          if (cnt[qq] > CAP - 2 * BKEY) {
             const float kth = select_topk<C::EPT>(cand_s + qq * CAP, cand_i + qq * CAP, cnt[qq],
                                                   p.topk, gtid, hist, sel, ctr);
             if (gtid == 0) {
@@ -591,7 +605,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 template <int H_I, int D_I, bool FP8>
 static dsa_status_t prefill_launch(const IndexerArgs& a, cudaStream_t stream) {
   using C = idx::Cfg<H_I, D_I, FP8>;
-  if (a.topk > C::CAP - idx::BKEY) return DSA_ERR_UNSUPPORTED;
+  if (a.topk > C::CAP - 2 * idx::BKEY) return DSA_ERR_UNSUPPORTED;
   CUtensorMap tq, tk;
   const uint64_t qrows = static_cast<uint64_t>(a.B) * a.Tq * H_I;
   // (FP8 code rows are described as BF16 pairs: the copy moves bytes only)
@@ -627,8 +641,8 @@ static dsa_status_t prefill_launch(const IndexerArgs& a, cudaStream_t stream) {
 }
 
 int indexer_prefill_max_topk(int H_I, int D_I) {
-  if (H_I == 64 && D_I == 128) return idx::Cfg<64, 128, false>::CAP - idx::BKEY;
-  if (H_I == 4 && D_I == 64) return idx::Cfg<4, 64, false>::CAP - idx::BKEY;
+  if (H_I == 64 && D_I == 128) return idx::Cfg<64, 128, false>::CAP - 2 * idx::BKEY;
+  if (H_I == 4 && D_I == 64) return idx::Cfg<4, 64, false>::CAP - 2 * idx::BKEY;
   return 0;
 }
 
