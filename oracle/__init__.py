@@ -64,6 +64,9 @@ def load(path: str | None = None):
         lib.oracle_quant_fp8.argtypes = [P, i64, i32, P, P]
         lib.oracle_indexer_scores_fp8.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
                                                   i64, P, P]
+        lib.oracle_sparse_mla_f64.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f64, i64, P,
+                                              P, P]
+        lib.oracle_sparse_mla_bwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f64, P, P, P]
         lib.oracle_set_threads.argtypes = [i32]
         for f in ("oracle_indexer_scores", "oracle_topk", "oracle_sparse_mla", "oracle_dense_mla",
                   "oracle_explicit_mla", "oracle_gate", "oracle_set_threads",
@@ -358,3 +361,55 @@ def indexer_topk_fp8(q_codes, q_scale, w, k_codes, k_scale, q_start, kv_len, k, 
     n_valid = (qs[rows // Tq] + rows % Tq + 1).astype(np.int32)
     idx, kth = topk(sc, n_valid, k, lib=lib)
     return idx, kth, sc, n_valid
+
+
+# ---------------------------------------------------------------------------
+# Sparse MLA backward ("Kimi-K3.1-Pro", NeMo AutoModel, Implementation Limits:
+# bullets 1-2 (attention over the selected rows only), the paragraph after
+# bullet 4 (a native 96-head backward), bullet 3 (hard top-k gives the indexer
+# no gradient, so the index set is a constant here)).
+# ---------------------------------------------------------------------------
+
+def _as_f64(a):
+    """BF16 bit patterns (uint16) -> float64, exactly; float arrays pass through."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        a = (a.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    return _c(a, np.float64)
+
+
+def sparse_mla_f64(q_lat, kv, idx, q_start, kv_len, scale, rows=None, lib=None):
+    """The sparse MLA forward on exact (float64) values: (o [n,H,512], lse [n,H])."""
+    lib = lib or load()
+    q, k = _as_f64(q_lat), _as_f64(kv)
+    B, Tq, H, R = q.shape
+    assert R == RLAT
+    S_max = k.shape[1]
+    topk_ = idx.shape[-1]
+    rows = _rows(rows, B, Tq)
+    o = np.empty((len(rows), H, VLAT), np.float64)
+    lse = np.empty((len(rows), H), np.float64)
+    ix = _c(idx, np.int32)
+    qs, kl = _c(q_start, np.int32), _c(kv_len, np.int32)
+    _check(lib.oracle_sparse_mla_f64(_p(q), _p(k), _p(ix), _p(qs), _p(kl), B, Tq, S_max, H, topk_,
+                                     float(scale), len(rows), _p(rows), _p(o), _p(lse)),
+           "sparse_mla_f64")
+    return o, lse
+
+
+def sparse_mla_bwd(q_lat, kv, idx, q_start, kv_len, scale, dO, lib=None):
+    """Gradients of sum(dO * o) for the sparse MLA forward with a fixed index set:
+    (dq [B,Tq,H,576], dkv [B,S,576]), float64.  Inputs may be BF16 bits or floats."""
+    lib = lib or load()
+    q, k, g = _as_f64(q_lat), _as_f64(kv), _as_f64(dO)
+    B, Tq, H, R = q.shape
+    assert R == RLAT and g.shape == (B, Tq, H, VLAT)
+    S_max = k.shape[1]
+    topk_ = idx.shape[-1]
+    dq = np.empty(q.shape, np.float64)
+    dkv = np.empty(k.shape, np.float64)
+    ix = _c(idx, np.int32)
+    qs, kl = _c(q_start, np.int32), _c(kv_len, np.int32)
+    _check(lib.oracle_sparse_mla_bwd(_p(q), _p(k), _p(ix), _p(qs), _p(kl), B, Tq, S_max, H, topk_,
+                                     float(scale), _p(g), _p(dq), _p(dkv)), "sparse_mla_bwd")
+    return dq, dkv

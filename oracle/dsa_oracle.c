@@ -705,3 +705,192 @@ int oracle_indexer_scores_fp8(const uint8_t* q_codes, const float* q_scale, cons
   parallel_rows(n_rows, indexer_row_fp8, &c);
   return c.err;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Sparse MLA backward  [K31 Impl. Limits b1-b2 (attention over the selected  */
+/* rows only), the paragraph after b4 (a native 96-head backward), b3 (hard   */
+/* top-k gives the indexer no gradient: the index set is a constant here)]    */
+/* ------------------------------------------------------------------------- */
+/* The forward, per query row and head, over the selected positions s_j:
+ *   z_j = scale * q . kv[s_j]          (576 dims)
+ *   p_j = exp(z_j - lse),  lse = log sum_j exp(z_j)
+ *   o   = sum_j p_j kv[s_j, 0:512]
+ * and its gradient for an upstream gradient dO of o (the plain chain rule):
+ *   dp_j = dO . kv[s_j, 0:512],   D = sum_j p_j dp_j = dO . o
+ *   dz_j = p_j (dp_j - D)
+ *   dq   = scale * sum_j dz_j kv[s_j, 0:576]
+ *   dkv[s_j, 0:576] += scale * dz_j q,   dkv[s_j, 0:512] += p_j dO
+ * (the latent row is both the key, 576 dims, and the value, its first 512).
+ * Entries -1 are skipped; any other entry must be causal (else OR_BAD_INDEX).
+ * Inputs and outputs are double: the gradient of the function on exact values. */
+
+typedef struct {
+  const double *q, *kv, *dO;
+  const int32_t *idx, *q_start, *kv_len;
+  int Tq, S_max, H, topk;
+  double scale;
+  const int64_t* rows;
+  double *o, *lse, *D, *dq; /* o / D / dq may be NULL */
+  int err;
+} mlab_ctx;
+
+/* forward row (o, lse) and, when dO is given, D and dq */
+static void mlab_row(void* vctx, int64_t r) {
+  mlab_ctx* c = (mlab_ctx*)vctx;
+  int64_t flat = c->rows[r];
+  int b = (int)(flat / c->Tq), i = (int)(flat % c->Tq);
+  int64_t t = (int64_t)c->q_start[b] + i;
+  const int32_t* ix = c->idx + flat * (int64_t)c->topk;
+  const double* kvb = c->kv + (int64_t)b * c->S_max * RLAT;
+  double* z = (double*)malloc(sizeof(double) * (size_t)c->topk);
+  if (!z) { c->err = OR_NOMEM; return; }
+  for (int h = 0; h < c->H; ++h) {
+    const double* qh = c->q + (flat * c->H + h) * (int64_t)RLAT;
+    double m = -INFINITY;
+    int n = 0;
+    for (int j = 0; j < c->topk; ++j) {
+      int s = ix[j];
+      z[j] = -INFINITY;
+      if (s < 0) continue;
+      if (s > t || s >= c->kv_len[b] || s >= c->S_max) { c->err = OR_BAD_INDEX; continue; }
+      const double* row = kvb + (int64_t)s * RLAT;
+      double dot = 0.0;
+      for (int d = 0; d < RLAT; ++d) dot += qh[d] * row[d];
+      z[j] = dot * c->scale;
+      if (z[j] > m) m = z[j];
+      ++n;
+    }
+    double l = 0.0;
+    for (int j = 0; j < c->topk; ++j)
+      if (z[j] != -INFINITY) l += exp(z[j] - m);
+    const double lse = n > 0 ? m + log(l) : -INFINITY;
+    if (c->lse) c->lse[r * c->H + h] = lse;
+    double o[VLAT];
+    for (int d = 0; d < VLAT; ++d) o[d] = 0.0;
+    for (int j = 0; j < c->topk; ++j) {
+      if (z[j] == -INFINITY) continue;
+      const double p = exp(z[j] - lse);
+      const double* row = kvb + (int64_t)ix[j] * RLAT;
+      for (int d = 0; d < VLAT; ++d) o[d] += p * row[d];
+    }
+    if (c->o)
+      for (int d = 0; d < VLAT; ++d) c->o[(r * c->H + h) * (int64_t)VLAT + d] = o[d];
+    if (!c->dO) continue;
+    const double* dOh = c->dO + (flat * c->H + h) * (int64_t)VLAT;
+    double Dv = 0.0;
+    for (int d = 0; d < VLAT; ++d) Dv += dOh[d] * o[d];
+    if (c->D) c->D[r * c->H + h] = Dv;
+    double* dqh = c->dq + (r * c->H + h) * (int64_t)RLAT;
+    for (int d = 0; d < RLAT; ++d) dqh[d] = 0.0;
+    for (int j = 0; j < c->topk; ++j) {
+      if (z[j] == -INFINITY) continue;
+      const double p = exp(z[j] - lse);
+      const double* row = kvb + (int64_t)ix[j] * RLAT;
+      double dp = 0.0;
+      for (int d = 0; d < VLAT; ++d) dp += dOh[d] * row[d];
+      const double dz = p * (dp - Dv);
+      for (int d = 0; d < RLAT; ++d) dqh[d] += c->scale * dz * row[d];
+    }
+  }
+  free(z);
+}
+
+/* Double-input sparse MLA forward: o [n_rows, H, 512], lse [n_rows, H] (natural log).
+ * The same function as oracle_sparse_mla on exact values; the backward is its gradient. */
+int oracle_sparse_mla_f64(const double* q, const double* kv, const int32_t* idx,
+                          const int32_t* q_start, const int32_t* kv_len, int B, int Tq, int S_max,
+                          int H, int topk, double scale, int64_t n_rows, const int64_t* rows,
+                          double* o, double* lse) {
+  if (!q || !kv || !idx || !q_start || !kv_len || !rows || !o || !lse) return OR_BAD_ARG;
+  if (B <= 0 || Tq <= 0 || S_max <= 0 || H <= 0 || topk <= 0 || n_rows < 0) return OR_BAD_ARG;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= (int64_t)B * Tq) return OR_BAD_ARG;
+  mlab_ctx c = {q, kv, NULL, idx, q_start, kv_len, Tq, S_max, H, topk, scale, rows,
+                o, lse, NULL, NULL, OR_OK};
+  parallel_rows(n_rows, mlab_row, &c);
+  return c.err;
+}
+
+typedef struct {
+  const double *q, *kv, *dO, *lse, *D;
+  const int32_t* idx;
+  const int64_t *start, *list; /* inverted lists: for key row kr, entries start[kr]..start[kr+1] */
+  int Tq, S_max, H, topk;
+  double scale;
+  double* dkv;
+} dkv_ctx;
+
+/* dkv of one key row (b, s): the sum over every (query row, head) that selected it */
+static void dkv_row(void* vctx, int64_t kr) {
+  dkv_ctx* c = (dkv_ctx*)vctx;
+  int b = (int)(kr / c->S_max);
+  const double* row = c->kv + kr * RLAT;
+  double* out = c->dkv + kr * RLAT;
+  for (int d = 0; d < RLAT; ++d) out[d] = 0.0;
+  for (int64_t e = c->start[kr]; e < c->start[kr + 1]; ++e) {
+    const int64_t flat = c->list[e]; /* query row b*Tq + i (one entry per selection) */
+    (void)b;
+    for (int h = 0; h < c->H; ++h) {
+      const double* qh = c->q + (flat * c->H + h) * (int64_t)RLAT;
+      const double* dOh = c->dO + (flat * c->H + h) * (int64_t)VLAT;
+      double dot = 0.0;
+      for (int d = 0; d < RLAT; ++d) dot += qh[d] * row[d];
+      const double p = exp(dot * c->scale - c->lse[flat * c->H + h]);
+      double dp = 0.0;
+      for (int d = 0; d < VLAT; ++d) dp += dOh[d] * row[d];
+      const double dz = p * (dp - c->D[flat * c->H + h]);
+      for (int d = 0; d < RLAT; ++d) out[d] += c->scale * dz * qh[d];
+      for (int d = 0; d < VLAT; ++d) out[d] += p * dOh[d];
+    }
+  }
+}
+
+/* q [B,Tq,H,576], kv [B,S_max,576], dO [B,Tq,H,512] (double); idx [B,Tq,topk].
+ * Outputs: dq [B,Tq,H,576] and dkv [B,S_max,576] (every row written; rows no
+ * query selected are zero). */
+int oracle_sparse_mla_bwd(const double* q, const double* kv, const int32_t* idx,
+                          const int32_t* q_start, const int32_t* kv_len, int B, int Tq, int S_max,
+                          int H, int topk, double scale, const double* dO, double* dq,
+                          double* dkv) {
+  if (!q || !kv || !idx || !q_start || !kv_len || !dO || !dq || !dkv) return OR_BAD_ARG;
+  if (B <= 0 || Tq <= 0 || S_max <= 0 || H <= 0 || topk <= 0) return OR_BAD_ARG;
+  const int64_t nq = (int64_t)B * Tq, nk = (int64_t)B * S_max;
+  int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)nq);
+  double* lse = (double*)malloc(sizeof(double) * (size_t)(nq * H));
+  double* D = (double*)malloc(sizeof(double) * (size_t)(nq * H));
+  int64_t* start = (int64_t*)calloc((size_t)(nk + 1), sizeof(int64_t));
+  if (!rows || !lse || !D || !start) { free(rows); free(lse); free(D); free(start); return OR_NOMEM; }
+  for (int64_t r = 0; r < nq; ++r) rows[r] = r;
+  /* pass 1: per query row, lse, D = dO . o and dq */
+  mlab_ctx c = {q, kv, dO, idx, q_start, kv_len, Tq, S_max, H, topk, scale, rows,
+                NULL, lse, D, dq, OR_OK};
+  parallel_rows(nq, mlab_row, &c);
+  int err = c.err;
+  /* inverted lists of the selections (valid entries only, query order) */
+  for (int64_t r = 0; r < nq && err == OR_OK; ++r) {
+    const int b = (int)(r / Tq);
+    for (int j = 0; j < topk; ++j) {
+      const int s = idx[r * topk + j];
+      if (s >= 0) start[(int64_t)b * S_max + s + 1] += 1;
+    }
+  }
+  for (int64_t k = 0; k < nk; ++k) start[k + 1] += start[k];
+  int64_t* list = (int64_t*)malloc(sizeof(int64_t) * (size_t)(start[nk] > 0 ? start[nk] : 1));
+  int64_t* fill = (int64_t*)malloc(sizeof(int64_t) * (size_t)nk);
+  if (!list || !fill) { err = OR_NOMEM; }
+  if (err == OR_OK) {
+    for (int64_t k = 0; k < nk; ++k) fill[k] = start[k];
+    for (int64_t r = 0; r < nq; ++r) {
+      const int b = (int)(r / Tq);
+      for (int j = 0; j < topk; ++j) {
+        const int s = idx[r * topk + j];
+        if (s >= 0) list[fill[(int64_t)b * S_max + s]++] = r;
+      }
+    }
+    /* pass 2: per key row, dkv */
+    dkv_ctx k2 = {q, kv, dO, lse, D, idx, start, list, Tq, S_max, H, topk, scale, dkv};
+    parallel_rows(nk, dkv_row, &k2);
+  }
+  free(rows); free(lse); free(D); free(start); free(list); free(fill);
+  return err;
+}

@@ -658,4 +658,112 @@ def pin_indexer_fp8_equals_bf16_on_exact_values(lib):
     assert np.array_equal(c[:, 6:], a[:, 6:], equal_nan=True)
 
 
+# ----------------------------------------------------------------------------
+# sparse MLA backward
+# ----------------------------------------------------------------------------
+
+def _bwd_case(seed, T, H, k, amp=0.25, full=False):
+    """Float64 inputs with a random causal index set (or every causal key)."""
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((1, T, H, 576)) * amp
+    kv = rng.standard_normal((1, T, 576)) * amp
+    dO = rng.standard_normal((1, T, H, 512))
+    idx = np.full((1, T, k), -1, np.int32)
+    for t in range(T):
+        c = np.arange(t + 1) if full else rng.permutation(t + 1)[:k]
+        idx[0, t, :len(c)] = c
+    return q, kv, dO, idx, np.zeros(1, np.int32), np.full(1, T, np.int32)
+
+
+def pin_mla_f64_forward_matches_bf16_forward(lib):
+    """The float64-input forward (the function the backward differentiates) agrees
+    with the BF16-input forward on BF16 values."""
+    T, H = 40, 8
+    q = normal_bf16(91, "q_lat", (1, T, H, 576))
+    kv = normal_bf16(91, "kv", (1, T, 576))
+    rng = np.random.default_rng(91)
+    idx = np.full((1, T, 16), -1, np.int32)
+    for t in range(T):
+        c = rng.permutation(t + 1)[:16]
+        idx[0, t, :len(c)] = c
+    qs, kl = np.zeros(1, np.int32), np.full(1, T, np.int32)
+    o1, l1 = oracle.sparse_mla(q, kv, idx, qs, kl, SCALE, lib=lib)
+    o2, l2 = oracle.sparse_mla_f64(q, kv, idx, qs, kl, SCALE, lib=lib)
+    assert np.allclose(o1, o2, rtol=0, atol=1e-12) and np.allclose(l1, l2, rtol=0, atol=1e-12)
+
+
+def pin_mla_bwd_finite_differences(lib):
+    """Central differences of sum(dO * o) through the float64 forward, at query
+    and latent coordinates in the value dims and in the 64 k_pe dims."""
+    q, kv, dO, idx, qs, kl = _bwd_case(92, 6, 2, 3, amp=0.5)
+    scale = 0.3
+    dq, dkv = oracle.sparse_mla_bwd(q, kv, idx, qs, kl, scale, dO, lib=lib)
+
+    def loss(qq, kk):
+        o, _ = oracle.sparse_mla_f64(qq, kk, idx, qs, kl, scale, lib=lib)
+        return float(np.sum(o * dO.reshape(o.shape)))
+
+    eps = 1e-6
+    for (t, h, d) in [(5, 1, 3), (3, 0, 540), (4, 1, 511), (2, 0, 575)]:
+        qp, qm = q.copy(), q.copy()
+        qp[0, t, h, d] += eps
+        qm[0, t, h, d] -= eps
+        fd = (loss(qp, kv) - loss(qm, kv)) / (2 * eps)
+        assert abs(fd - dq[0, t, h, d]) <= 1e-7 * max(1.0, abs(fd)), ("dq", t, h, d, fd, dq[0, t, h, d])
+    used = sorted(set(int(v) for v in idx.ravel() if v >= 0))
+    for (s, d) in [(used[0], 7), (used[1], 530), (used[-1], 200), (used[2], 575)]:
+        kp, km = kv.copy(), kv.copy()
+        kp[0, s, d] += eps
+        km[0, s, d] -= eps
+        fd = (loss(q, kp) - loss(q, km)) / (2 * eps)
+        assert abs(fd - dkv[0, s, d]) <= 1e-7 * max(1.0, abs(fd)), ("dkv", s, d, fd, dkv[0, s, d])
+
+
+def pin_mla_bwd_matches_library_autograd(lib):
+    """With every causal key selected the sparse forward is dense causal attention;
+    torch float64 autograd of that dense attention (K = the latent row, V = its
+    first 512 dims, one shared tensor) gives the same gradients."""
+    import torch
+    T, H = 7, 3
+    q, kv, dO, idx, qs, kl = _bwd_case(93, T, H, T, full=True)
+    dq, dkv = oracle.sparse_mla_bwd(q, kv, idx, qs, kl, SCALE, dO, lib=lib)
+    tq = torch.tensor(q[0].transpose(1, 0, 2), requires_grad=True)      # [H, T, 576]
+    tk = torch.tensor(kv[0], requires_grad=True)                         # [T, 576]
+    z = torch.einsum("htd,sd->hts", tq, tk) * SCALE
+    mask = torch.triu(torch.ones(T, T, dtype=torch.bool), diagonal=1)
+    pr = torch.softmax(z.masked_fill(mask, float("-inf")), dim=-1)
+    o = torch.einsum("hts,sd->htd", pr, tk[:, :512])
+    (o * torch.tensor(dO[0].transpose(1, 0, 2))).sum().backward()
+    assert np.allclose(tq.grad.numpy().transpose(1, 0, 2), dq[0], rtol=0, atol=1e-10)
+    assert np.allclose(tk.grad.numpy(), dkv[0], rtol=0, atol=1e-10)
+
+
+def pin_mla_bwd_single_key_closed_form(lib):
+    """One selected key per query: p = 1, so dq = 0, the k_pe dims get nothing,
+    and the key's value dims receive the sum of the upstream gradients."""
+    T, H = 9, 4
+    q, kv, dO, _, qs, kl = _bwd_case(94, T, H, 1)
+    idx = (np.arange(T) // 2).astype(np.int32).reshape(1, T, 1)   # query t selects key t // 2
+    dq, dkv = oracle.sparse_mla_bwd(q, kv, idx, qs, kl, SCALE, dO, lib=lib)
+    assert np.allclose(dq, 0.0, atol=1e-12)
+    want = np.zeros((T, 512))
+    for t in range(T):
+        want[t // 2] += dO[0, t].sum(axis=0)
+    assert np.allclose(dkv[0, :, :512], want, rtol=0, atol=1e-12)
+    assert np.allclose(dkv[0, :, 512:], 0.0, atol=1e-12)
+
+
+def pin_mla_bwd_sum_rules(lib):
+    """Summed over keys: the k_pe-dim gradients cancel (sum_j dz_j = 0 per query
+    head) and the value-dim gradients add up to sum_t,h dO (sum_j p_j = 1)."""
+    T, H = 14, 3
+    q, kv, dO, idx, qs, kl = _bwd_case(95, T, H, 5, amp=0.6)
+    idx[0, 6] = -1                                  # a query with no valid entry
+    _, dkv = oracle.sparse_mla_bwd(q, kv, idx, qs, kl, 0.4, dO, lib=lib)
+    assert np.allclose(dkv[0, :, 512:].sum(axis=0), 0.0, atol=1e-10)
+    live = [t for t in range(T) if (idx[0, t] >= 0).any()]
+    want = dO[0, live].sum(axis=(0, 1))
+    assert np.allclose(dkv[0, :, :512].sum(axis=0), want, rtol=0, atol=1e-10)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

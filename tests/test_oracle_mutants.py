@@ -49,6 +49,12 @@ MUTANTS = {
                                   "const float s = amax / 448.0f;"),
     "fp8_relu_dropped": ("const double pos = dot > 0.0 ? dot : 0.0;", "const double pos = dot;"),
     "fp8_head_weight_dropped": ("score += bf(w[j]) * pos;", "score += pos;"),
+    "bwd_D_dropped_in_dq": ("      const double dz = p * (dp - Dv);", "      const double dz = p * dp;"),
+    "bwd_D_dropped_in_dkv": ("const double dz = p * (dp - c->D[flat * c->H + h]);", "const double dz = p * dp;"),
+    "bwd_dq_scale_dropped": ("dqh[d] += c->scale * dz * row[d];", "dqh[d] += dz * row[d];"),
+    "bwd_dq_rope_dims_dropped": ("for (int d = 0; d < RLAT; ++d) dqh[d] += c->scale", "for (int d = 0; d < VLAT; ++d) dqh[d] += c->scale"),
+    "bwd_value_grad_dropped": ("for (int d = 0; d < VLAT; ++d) out[d] += p * dOh[d];", ""),
+    "bwd_key_grad_sign_flipped": ("out[d] += c->scale * dz * qh[d];", "out[d] -= c->scale * dz * qh[d];"),
     "fp8_key_scale_dropped": ("* (ks * dec8(k[d]));", "* dec8(k[d]);"),
     "fp8_query_scale_dropped": ("dot += (qsj * dec8(q[j * c->D_I + d]))", "dot += (dec8(q[j * c->D_I + d]))"),
 }
