@@ -756,7 +756,7 @@ static void mlab_row(void* vctx, int64_t r) {
       const double* row = kvb + (int64_t)s * RLAT;
       double dot = 0.0;
       for (int d = 0; d < RLAT; ++d) dot += qh[d] * row[d];
-      z[j] = dot * c->scale;
+      z[j] = c->scale * dot;
       if (z[j] > m) m = z[j];
       ++n;
     }

@@ -31,8 +31,8 @@ MUTANTS = {
     "gate_sign_flipped": ("o[col] = u / (1.0 + exp(-g));", "o[col] = u / (1.0 + exp(g));"),
     "explicit_value_uses_key_weight": ("acc += Wv[(int64_t)e * c->R + d] * ck[d];",
                                        "acc += Wk[(int64_t)e * c->R + d] * ck[d];"),
-    "sparse_ignores_minus_one_wrongly": ("if (s < 0) continue;\n      if (s > t",
-                                         "if (s < 0) s = 0;\n      if (s > t"),
+    "sparse_ignores_minus_one_wrongly": ("int32_t s = ix[j];\n      if (s < 0) continue;\n      if (s > t",
+                                         "int32_t s = ix[j];\n      if (s < 0) s = 0;\n      if (s > t"),
     "layernorm_sample_variance": ("    var /= D;\n", "    var /= (D - 1);\n"),
     "layernorm_eps_dropped": ("const double inv = 1.0 / sqrt(var + eps);",
                               "const double inv = 1.0 / sqrt(var);"),
