@@ -351,7 +351,9 @@ def run_ours(args, rank, world, local):
     }
     res["variants"] = {"fp8_indexer": run_prefill_fp8(args, dsa, cfg, dev, stream, q_idx, w,
                                                       k_idx, qs, kl, idx, ws, T, f_idx, peak,
-                                                      t_mla)}
+                                                      t_mla),
+                       "sparse_mla_bwd": run_prefill_bwd(dsa, cfg, dev, stream, q_lat, kvrows,
+                                                         idx, o_lat, lse, T, peak)}
     if not args.no_e2e:
         res["e2e"] = run_e2e(args, dsa, d, g, cfg, dev, stream, ws, krows, kvrows, world,
                              tensors=dict(q_idx=q_idx, w=w, k_idx=k_idx, q_lat=q_lat, kv=kv, x=x,
@@ -405,6 +407,48 @@ def run_prefill_fp8(args, dsa, cfg, dev, stream, q_idx, w, k_idx, qs, kl, idx, w
             "value_indexer_mla_only": cfg.B * T / (t_q + t_i + t_mla), "unit": "tokens/s",
             "step": "dsa_quant_fp8 (queries) -> dsa_indexer_topk_fp8; sparse MLA as in the BF16 step",
             "gpu_launches": K * 2}
+
+
+def run_prefill_bwd(dsa, cfg, dev, stream, q_lat, kvrows, idx, o_lat, lse, T, peak_bf16, nq=512):
+    """The sparse MLA backward on a bounded slice of the workload: the last `nq`
+    queries of sequence 0 (each with the full k selected keys), using the step's
+    own forward outputs; upstream gradient seeded N(0,1) BF16.  Work per
+    (query, selected key): 2*H*(3*576 + 2*512) FLOP (the logits and dp again,
+    dq, the key and the value gradients)."""
+    import numpy as np
+    import torch
+    from workloads import normal_bf16
+    q0 = T - nq
+    sl = lambda t: t[0:1, q0:T].contiguous()
+    q, ix, o, ls = sl(q_lat), sl(idx), sl(o_lat), sl(lse)
+    g = normal_bf16(cfg.seed, "w", (1, nq, cfg.H, 512), sub=7)
+    d_o = torch.from_numpy(g.view(np.int16)).to(dev).view(torch.bfloat16)
+    qs = torch.tensor([q0], dtype=torch.int32, device=dev)
+    kl = torch.tensor([T], dtype=torch.int32, device=dev)
+    dkv = torch.zeros((1, T, 576), dtype=torch.float32, device=dev)
+    dq = torch.empty((1, nq, cfg.H, 576), dtype=torch.float32, device=dev)
+    ws = dsa.new_workspace(256, dev)
+    run = lambda: dsa.sparse_mla_bwd(q, kvrows, ix, qs, kl, T, o, ls, d_o, dkv, cfg.scale, dq=dq,
+                                     workspace=ws)
+    run()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    K = 2
+    a.record(stream)
+    for _ in range(K):
+        run()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    code, where, detail = dsa.read_device_status(ws)
+    if code != dsa.DSA_OK:
+        raise RuntimeError(f"bwd device status {code} at {where:#x} ({detail})")
+    t = a.elapsed_time(b) / K / 1e3
+    flop = nq * cfg.topk * 2 * cfg.H * (3 * 576 + 2 * 512)
+    tf = flop / t / 1e12
+    return {"ms": t * 1e3, "queries": nq, "tflops": tf, "frac_of_bf16_peak": tf / peak_bf16,
+            "flop": flop, "unit": "TFLOP/s",
+            "note": "first version on the CUDA cores in FP32 (dq kernel + dkv kernel with "
+                    "vector atomics); slice: last 512 queries of sequence 0", "gpu_launches": K * 2}
 
 
 def launches_per_step(dsa, B, T, cfg):

@@ -169,6 +169,35 @@ dsa_status_t sparse_mla_fwd_sink(const uint16_t* q_lat, const dsa_rows_t* kv, co
                                  dsa_stream_t stream);
 
 /*
+ * Sparse MLA backward ("Kimi-K3.1-Pro", Implementation Limits: attention over
+ * the selected rows only, bullets 1-2; a native 96-head backward, the paragraph
+ * after bullet 4; hard top-k passes no gradient to the indexer, bullet 3, so
+ * idx is a constant).  The gradient of sum(d_o * o_lat) given the forward's
+ * outputs:
+ *   p_j  = exp(scale * q . kv[s_j] - lse),  dp_j = d_o . kv[s_j, 0:512]
+ *   dz_j = p_j (dp_j - D),  D = d_o . o_lat
+ *   dq   = scale * sum_j dz_j kv[s_j, 0:576]                       (written)
+ *   dkv[s_j, 0:576] += scale * dz_j q,  dkv[s_j, 0:512] += p_j d_o  (added)
+ * Arguments as for sparse_mla_fwd, plus
+ *   o_lat, lse          the forward's outputs for the same inputs
+ *   d_o   [B,Tq,H,512]  BF16   upstream gradient of o_lat
+ *   dq    [B,Tq,H,576]  FP32   written; a query with no valid entry gets 0
+ *   dkv                 FP32   rows of 576 numbered like kv's rows
+ *                              ([B, seq_stride, 576] or [num_pages, 64, 576]),
+ *                              16-byte aligned, ADDED to (zero it first).
+ *                              Additions come from many queries in no fixed
+ *                              order, so the FP32 rounding varies run to run.
+ * -1 entries are skipped; other invalid entries raise DSA_ERR_BAD_INDEX and are
+ * skipped.  Workspace: the 256-byte status header.  Supported: H <= 128,
+ * topk <= 2048.  This first version runs on the CUDA cores in FP32.
+ */
+dsa_status_t sparse_mla_bwd(const uint16_t* q_lat, const dsa_rows_t* kv, const int32_t* idx,
+                            const int32_t* q_start, const int32_t* kv_len, int B, int Tq, int H,
+                            int topk, int max_kv_len, float scale, const uint16_t* o_lat,
+                            const float* lse, const uint16_t* d_o, float* dq, float* dkv,
+                            void* workspace, size_t ws_bytes, dsa_stream_t stream);
+
+/*
  * Output gate ("Kimi K3.1 Pro" archdiff blueprint: sigma(x W_g) (.) o;
  * "Kimi-K3.1-Pro", Implementation Limits, closing paragraph: the gate is kept;
  * KimiK3TextConfig mla_use_output_gate, v_head_dim 128).

@@ -13,6 +13,7 @@ Entry points (same names as the C ABI):
   dsa_cache_append  LayerNorm of new indexer keys + append of keys and latent rows
   dsa_quant_fp8, dsa_cache_append_fp8, dsa_indexer_topk_fp8
                     the FP8 (E4M3, one FP32 scale per row) indexer variant
+  sparse_mla_bwd    gradients of sparse MLA for q_lat and the latent rows
 """
 
 from __future__ import annotations
@@ -55,7 +56,7 @@ class _Rows(ctypes.Structure):
 EXPORTS = ("dsa_abi_version", "dsa_status_string", "dsa_workspace_bytes", "dsa_workspace_init",
            "dsa_read_device_status", "dsa_indexer_topk", "sparse_mla_fwd", "mla_gate_apply",
            "dsa_cache_append", "sparse_mla_fwd_sink", "dsa_selftest_wait_timeout",
-           "dsa_quant_fp8", "dsa_cache_append_fp8", "dsa_indexer_topk_fp8")
+           "dsa_quant_fp8", "dsa_cache_append_fp8", "dsa_indexer_topk_fp8", "sparse_mla_bwd")
 
 
 def _load(path: str = LIB_PATH):
@@ -85,7 +86,9 @@ def _load(path: str = LIB_PATH):
                                          I, I, I, ctypes.c_float, P, Z, P]
     lib.dsa_indexer_topk_fp8.argtypes = [P, P, P, ctypes.POINTER(_Rows), P, P, P, I, I, I, I, I, I,
                                          P, P, Z, P]
-    for f in ("dsa_workspace_init", "dsa_read_device_status", "dsa_indexer_topk",
+    lib.sparse_mla_bwd.argtypes = [P, ctypes.POINTER(_Rows), P, P, P, I, I, I, I, I,
+                                   ctypes.c_float, P, P, P, P, P, P, Z, P]
+    for f in ("sparse_mla_bwd", "dsa_workspace_init", "dsa_read_device_status", "dsa_indexer_topk",
               "sparse_mla_fwd", "mla_gate_apply", "dsa_cache_append", "sparse_mla_fwd_sink",
               "dsa_selftest_wait_timeout", "dsa_quant_fp8", "dsa_cache_append_fp8",
               "dsa_indexer_topk_fp8"):
@@ -352,3 +355,30 @@ def dsa_indexer_topk_fp8(q_codes, q_scale, w, k_codes: Rows, k_scale, q_start, k
                                     int(max_kv_len), int(topk), _ptr(out_idx), _ptr(ws),
                                     ws.numel(), _stream(stream)), "dsa_indexer_topk_fp8")
     return out_idx
+
+
+def sparse_mla_bwd(q_lat, kv: Rows, idx, q_start, kv_len, max_kv_len: int, o_lat, lse, d_o,
+                   dkv, scale: float = MLA_SCALE, dq=None, workspace=None, stream=None):
+    """Backward of sparse_mla_fwd for a fixed index set: returns dq [B,Tq,H,576]
+    float32 and ADDS the latent-row gradients into dkv (float32, laid out like
+    kv's rows: [B, S, 576] or [num_pages, 64, 576]; zero it first)."""
+    _need(q_lat, torch.bfloat16, "q_lat")
+    _need(idx, torch.int32, "idx")
+    _need(o_lat, torch.bfloat16, "o_lat")
+    _need(lse, torch.float32, "lse")
+    _need(d_o, torch.bfloat16, "d_o")
+    _need(dkv, torch.float32, "dkv")
+    _need(q_start, torch.int32, "q_start")
+    _need(kv_len, torch.int32, "kv_len")
+    B, Tq, H, _ = q_lat.shape
+    topk = idx.shape[-1]
+    if dq is None:
+        dq = torch.empty((B, Tq, H, RLAT), dtype=torch.float32, device=q_lat.device)
+    _need(dq, torch.float32, "dq")
+    ws = _ws(workspace, OP_GATE, B, Tq, 0, 0, 0, q_lat.device, stream)
+    rows = kv.c()
+    _check(lib.sparse_mla_bwd(_ptr(q_lat), ctypes.byref(rows), _ptr(idx), _ptr(q_start),
+                              _ptr(kv_len), B, Tq, H, topk, int(max_kv_len), float(scale),
+                              _ptr(o_lat), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dkv), _ptr(ws),
+                              ws.numel(), _stream(stream)), "sparse_mla_bwd")
+    return dq

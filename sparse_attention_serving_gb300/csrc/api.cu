@@ -310,6 +310,45 @@ dsa_status_t sparse_mla_fwd_sink(const uint16_t* q_lat, const dsa_rows_t* kv, co
                  lse, workspace, ws_bytes, stream);
 }
 
+dsa_status_t sparse_mla_bwd(const uint16_t* q_lat, const dsa_rows_t* kv, const int32_t* idx,
+                            const int32_t* q_start, const int32_t* kv_len, int B, int Tq, int H,
+                            int topk, int max_kv_len, float scale, const uint16_t* o_lat,
+                            const float* lse, const uint16_t* d_o, float* dq, float* dkv,
+                            void* workspace, size_t ws_bytes, dsa_stream_t stream) {
+  if (!q_lat || !idx || !q_start || !kv_len || !o_lat || !lse || !d_o || !dq || !dkv)
+    return DSA_ERR_INVALID_ARGUMENT;
+  if (!aligned(q_lat, 16) || !aligned(idx, 4) || !aligned(q_start, 4) || !aligned(kv_len, 4) ||
+      !aligned(o_lat, 4) || !aligned(lse, 4) || !aligned(d_o, 4) || !aligned(dq, 4) ||
+      !aligned(dkv, 16))
+    return DSA_ERR_INVALID_ARGUMENT;
+  if (B <= 0 || Tq <= 0 || H <= 0 || topk <= 0 || max_kv_len <= 0) return DSA_ERR_INVALID_ARGUMENT;
+  if (!(scale > 0.f) || scale != scale) return DSA_ERR_INVALID_ARGUMENT;
+  if (H > 128 || topk > 2048) return DSA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * Tq * ((H + 15) / 16) >= (int64_t(1) << 31)) return DSA_ERR_UNSUPPORTED;
+  SparseMlaBwdArgs a{};
+  dsa_status_t st = resolve_rows(kv, B, max_kv_len, kRlat, &a.kv);
+  if (st != DSA_OK) return st;
+  st = check_ws(workspace, ws_bytes, kWorkspaceHeader);
+  if (st != DSA_OK) return st;
+  a.q_lat = q_lat;
+  a.idx = idx;
+  a.q_start = q_start;
+  a.kv_len = kv_len;
+  a.B = B;
+  a.Tq = Tq;
+  a.H = H;
+  a.topk = topk;
+  a.max_kv_len = max_kv_len;
+  a.scale = scale;
+  a.o_lat = o_lat;
+  a.lse = lse;
+  a.d_o = d_o;
+  a.dq = dq;
+  a.dkv = dkv;
+  a.status = static_cast<uint32_t*>(workspace);
+  return sparse_mla_bwd_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 dsa_status_t mla_gate_apply(const uint16_t* x, const uint16_t* W_g, const uint16_t* o_lat,
                             const uint16_t* W_uv, int N, int hid, int H, int dv, uint16_t* out,
                             void* workspace, size_t ws_bytes, dsa_stream_t stream) {

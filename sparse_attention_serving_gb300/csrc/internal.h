@@ -50,6 +50,24 @@ struct SparseMlaArgs {
 size_t sparse_mla_scratch_bytes(int B, int Tq, int H, int topk);
 dsa_status_t sparse_mla_launch(const SparseMlaArgs& a, cudaStream_t stream);
 
+// --- sparse MLA backward ----------------------------------------------------------
+struct SparseMlaBwdArgs {
+  const uint16_t* q_lat;
+  RowStore kv;
+  const int32_t* idx;
+  const int32_t* q_start;
+  const int32_t* kv_len;
+  int B, Tq, H, topk, max_kv_len;
+  float scale;
+  const uint16_t* o_lat;
+  const float* lse;
+  const uint16_t* d_o;
+  float* dq;
+  float* dkv;        // FP32 rows numbered like kv's rows (accumulated into)
+  uint32_t* status;
+};
+dsa_status_t sparse_mla_bwd_launch(const SparseMlaBwdArgs& a, cudaStream_t stream);
+
 // --- indexer + top-k --------------------------------------------------------------
 struct IndexerArgs {
   const uint16_t* q_idx;       // BF16 queries, or E4M3 codes when fp8

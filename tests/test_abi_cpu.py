@@ -141,3 +141,22 @@ def test_host_argument_checks_fp8(dsa):
     assert lib.dsa_cache_append_fp8(fake, fake, ctypes.byref(r), None, ctypes.byref(r), fake, 1, 1,
                                     128, ctypes.c_float(1e-5), ws, 1 << 20,
                                     None) == dsa.DSA_ERR_INVALID_ARGUMENT
+
+
+def test_host_argument_checks_bwd(dsa):
+    lib = dsa.lib
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    ws = P(1 << 24)
+    r = _rows(base=1 << 20, stride=128)
+
+    def bwd(q=fake, dkv=fake, H=96, k=64, scale=0.07, d_o=fake):
+        return lib.sparse_mla_bwd(q, ctypes.byref(r), fake, fake, fake, 1, 128, H, k, 128,
+                                  ctypes.c_float(scale), fake, fake, d_o, fake, dkv, ws, 1 << 20,
+                                  None)
+
+    assert bwd(d_o=None) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert bwd(dkv=P((1 << 20) + 4)) == dsa.DSA_ERR_INVALID_ARGUMENT   # dkv 16-byte aligned
+    assert bwd(scale=0.0) == dsa.DSA_ERR_INVALID_ARGUMENT
+    assert bwd(H=160) == dsa.DSA_ERR_UNSUPPORTED
+    assert bwd(k=4096) == dsa.DSA_ERR_UNSUPPORTED

@@ -1,0 +1,151 @@
+"""GPU parity of sparse_mla_bwd against the oracle's float64 gradient.
+
+The GPU backward takes its own forward's o_lat and lse (as a training step
+would); the oracle recomputes everything in float64 from the same BF16 inputs
+and the same index set.  dq and dkv must each satisfy, against the float64
+values: relative L2 error <= 1e-2 and max-abs error <= 2e-2 of the largest
+reference magnitude (the output bar of the forward, applied relative to the
+gradient's scale, which grows with the number of queries sharing a row).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import bf, i32
+from workloads import normal_bf16, page_table, to_pages
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 1e-2
+MAX_ABS_REL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    import sparse_attention_serving_gb300 as m
+    return m
+
+
+def _check(gpu, ref, what):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert np.all(np.isfinite(gpu)), f"{what}: non-finite values"
+    err = np.abs(gpu - ref)
+    scale = float(np.abs(ref).max()) or 1.0
+    rl = float(np.linalg.norm(gpu - ref) / (np.linalg.norm(ref) or 1.0))
+    assert err.max() <= MAX_ABS_REL * scale, f"{what}: max-abs {err.max():.3g} > {MAX_ABS_REL} x {scale:.3g}"
+    assert rl <= REL_L2, f"{what}: rel-L2 {rl:.3g}"
+    return rl
+
+
+def _indices(seed, B, Tq, q0, k, frac_short=0.25):
+    """A causal index set per query (distinct positions in [0, t]), -1 padded;
+    some queries keep fewer than k entries, and the order is shuffled."""
+    rng = np.random.default_rng([seed, 7])
+    idx = np.full((B, Tq, k), -1, np.int32)
+    for b in range(B):
+        for i in range(Tq):
+            t = q0 + i
+            n = min(t + 1, k)
+            if rng.random() < frac_short:
+                n = int(rng.integers(0, n + 1))
+            c = rng.permutation(t + 1)[:n]
+            idx[b, i, :n] = c
+            rng.shuffle(idx[b, i])
+    return idx
+
+
+def _run(dsa, q, kv_rows_dev, idx, q_start, kv_len, S, dO, dkv_shape, scale):
+    qt, dOt = bf(q), bf(dO)
+    it, qs, kl = i32(idx), i32(q_start), i32(kv_len)
+    o_lat, lse = dsa.sparse_mla_fwd(qt, kv_rows_dev, it, qs, kl, S, scale)
+    dkv = torch.zeros(dkv_shape, dtype=torch.float32, device="cuda")
+    ws = dsa.new_workspace(256)
+    dq = dsa.sparse_mla_bwd(qt, kv_rows_dev, it, qs, kl, S, o_lat, lse, dOt, dkv, scale,
+                            workspace=ws)
+    code, where, detail = dsa.read_device_status(ws)
+    return dq.cpu().numpy(), dkv.cpu().numpy(), code
+
+
+@pytest.mark.parametrize("B,T,H,k", [(1, 256, 8, 64), (2, 300, 96, 64), (1, 160, 96, 200)])
+def test_bwd_contiguous(dsa, B, T, H, k):
+    """Contiguous latent rows; ragged key counts (some queries keep fewer than k,
+    some none), k not a multiple of the 32-key block."""
+    seed = 100 + T + H
+    q = normal_bf16(seed, "q_lat", (B, T, H, 576))
+    kv = normal_bf16(seed, "kv", (B, T, 576))
+    dO = normal_bf16(seed, "w", (B, T, H, 512))
+    idx = _indices(seed, B, T, 0, k)
+    q_start, kv_len = np.zeros(B, np.int32), np.full(B, T, np.int32)
+    scale = 1.0 / np.sqrt(192.0)
+    dq, dkv, code = _run(dsa, q, dsa.Rows(bf(kv)), idx, q_start, kv_len, T, dO, (B, T, 576), scale)
+    assert code == dsa.DSA_OK
+    rdq, rdkv = oracle.sparse_mla_bwd(q, kv, idx, q_start, kv_len, scale, dO)
+    _check(dq, rdq, "dq")
+    _check(dkv, rdkv, "dkv")
+    # queries with no valid entry have zero dq
+    empty = (idx < 0).all(axis=-1)
+    assert np.all(dq[empty] == 0.0)
+
+
+def test_bwd_paged_chunk(dsa):
+    """Queries 256..383 of a sequence over a paged latent cache (q_start > 0);
+    dkv is a page pool and is added to, not overwritten."""
+    B, S, q0, Tq, H, k = 1, 384, 256, 128, 96, 128
+    seed = 131
+    kv_log = normal_bf16(seed, "kv", (B, S, 576))
+    q = normal_bf16(seed, "q_lat", (B, Tq, H, 576))
+    dO = normal_bf16(seed, "w", (B, Tq, H, 512))
+    idx = _indices(seed, B, Tq, q0, k)
+    lens = np.full(B, S, np.int32)
+    bt, npages = page_table(seed, lens)
+    pool = to_pages(kv_log, lens, bt, npages)
+    q_start, kv_len = np.full(B, q0, np.int32), np.full(B, q0 + Tq, np.int32)
+    scale = 1.0 / np.sqrt(192.0)
+    rows = dsa.Rows(bf(pool), i32(bt))
+    qt, dOt = bf(q), bf(dO)
+    it, qs, kl = i32(idx), i32(q_start), i32(kv_len)
+    o_lat, lse = dsa.sparse_mla_fwd(qt, rows, it, qs, kl, S, scale)
+    base = np.random.default_rng(5).standard_normal((npages, 64, 576)).astype(np.float32)
+    dkv = torch.from_numpy(base.copy()).cuda()
+    dq = dsa.sparse_mla_bwd(qt, rows, it, qs, kl, S, o_lat, lse, dOt, dkv, scale)
+    torch.cuda.synchronize()
+    rdq, rdkv = oracle.sparse_mla_bwd(q, kv_log[:, :q0 + Tq], idx, q_start, kv_len, scale, dO)
+    _check(dq.cpu().numpy(), rdq, "dq")
+    got = dkv.cpu().numpy() - base
+    want = np.zeros_like(base, dtype=np.float64)
+    for s in range(q0 + Tq):
+        want[bt[0, s // 64], s % 64] = rdkv[0, s]
+    _check(got, want, "dkv (pool, added)")
+
+
+def test_bwd_bad_index_is_flagged_and_skipped(dsa):
+    """A non-causal entry: DSA_ERR_BAD_INDEX, and the gradients equal those of
+    the index set without it."""
+    B, T, H, k = 1, 96, 8, 32
+    seed = 141
+    q = normal_bf16(seed, "q_lat", (B, T, H, 576))
+    kv = normal_bf16(seed, "kv", (B, T, 576))
+    dO = normal_bf16(seed, "w", (B, T, H, 512))
+    idx = _indices(seed, B, T, 0, k, frac_short=0.0)
+    clean = idx.copy()
+    idx[0, 40, 3] = 77          # key 77 is in the future of query 40
+    clean[0, 40, 3] = -1
+    q_start, kv_len = np.zeros(B, np.int32), np.full(B, T, np.int32)
+    scale = 1.0 / np.sqrt(192.0)
+    rows = dsa.Rows(bf(kv))
+    qt, dOt = bf(q), bf(dO)
+    qs, kl = i32(q_start), i32(kv_len)
+    # the forward on the clean set (it would flag the bad entry too)
+    o_lat, lse = dsa.sparse_mla_fwd(qt, rows, i32(clean), qs, kl, T, scale)
+    dkv = torch.zeros((B, T, 576), dtype=torch.float32, device="cuda")
+    ws = dsa.new_workspace(256)
+    dq = dsa.sparse_mla_bwd(qt, rows, i32(idx), qs, kl, T, o_lat, lse, dOt, dkv, scale, workspace=ws)
+    code, where, detail = dsa.read_device_status(ws)
+    assert code == dsa.DSA_ERR_BAD_INDEX and detail == 77
+    rdq, rdkv = oracle.sparse_mla_bwd(q, kv, clean, q_start, kv_len, scale, dO)
+    _check(dq.cpu().numpy(), rdq, "dq")
+    _check(dkv.cpu().numpy(), rdkv, "dkv")
