@@ -103,3 +103,74 @@ def test_decode64_fullsize(dsa):
                            one(d["kv_len"]), cfg.topk, np.array([0]), f"decode req {b}")
         check_mla_rows(one(ol), one(ls), one(d["q_lat"]), kv_log, one(gi), one(d["q_start"]),
                        one(d["kv_len"]), cfg.scale, np.array([0]), f"decode req {b}")
+
+
+def test_decode64_fp8_fullsize(dsa):
+    """The FP8 indexer on the full decode64 cache, checked on three requests.  The
+    checked requests' pages hold the oracle's quantisation of the seeded BF16 keys;
+    the other pages hold seeded random codes and scales (their results are not
+    checked), so no FP8 operand comes from the CUDA path."""
+    import oracle
+    from workloads import from_pages
+    cfg = CONFIGS["decode64"]
+    d = decode(cfg)
+    S = int(d["kv_len"].max())
+    npages = d["num_pages"]
+    rng = np.random.default_rng(64)
+    kc_pool = rng.integers(0, 0x7F, (npages, 64, 128), dtype=np.uint8)   # finite codes
+    ks_pool = rng.uniform(1e-3, 1e-2, (npages, 64)).astype(np.float32)
+    checked = (0, 17, 63)
+    for b in checked:
+        L = int(d["kv_len"][b])
+        pages = d["block_table"][b, :(L + 63) // 64]
+        c, sc = oracle.quant_fp8(d["k_pool"][pages])
+        kc_pool[pages], ks_pool[pages] = c, sc
+    qc, qsc = oracle.quant_fp8(d["q_idx"])
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    bt = i32(d["block_table"])
+    idx = dsa.dsa_indexer_topk_fp8(dev(qc), dev(qsc), bf(d["w"]), dsa.Rows(dev(kc_pool), bt),
+                                   dev(ks_pool), i32(d["q_start"]), i32(d["kv_len"]), cfg.topk, S)
+    torch.cuda.synchronize()
+    gi = idx.cpu().numpy()
+    from parity import check_index_row
+    for b in checked:
+        L = int(d["kv_len"][b])
+        kc = from_pages(kc_pool, d["block_table"], b, L)[None]
+        ks = from_pages(ks_pool[..., None], d["block_table"], b, L)[None, :, 0]
+        one = lambda a: a[b:b + 1]
+        o_idx, kth, sc, nv = oracle.indexer_topk_fp8(one(qc), one(qsc), one(d["w"]), kc, ks,
+                                                     one(d["q_start"]), one(d["kv_len"]),
+                                                     cfg.topk, np.array([0]))
+        check_index_row(gi[b, 0], sc[0], int(nv[0]), cfg.topk, o_idx[0], kth[0],
+                        f"fp8 decode req {b}")
+
+
+def test_bwd_fullsize_slice(dsa):
+    """The backward on full-size index sets: the indexer and forward run on the whole
+    val4096 sequence; the backward takes its last 8 queries (each with k = 2,048
+    selected keys) and is checked against the float64 gradient."""
+    import oracle
+    from test_gpu_bwd import _check
+    cfg = CONFIGS["val4096"]
+    T, nq = cfg.T, 8
+    d = prefill(cfg)
+    qs, kl = i32(d["q_start"]), i32(d["kv_len"])
+    idx = dsa.dsa_indexer_topk(bf(d["q_idx"]), bf(d["w"]), dsa.Rows(bf(d["k_idx"])), qs, kl,
+                               cfg.topk, T)
+    kvrows = dsa.Rows(bf(d["kv"]))
+    o_lat, lse = dsa.sparse_mla_fwd(bf(d["q_lat"]), kvrows, idx, qs, kl, T, cfg.scale)
+    q0 = T - nq
+    sl = lambda t: t[:, q0:].contiguous()
+    dO = np.random.default_rng(4096).standard_normal((1, nq, cfg.H, 512)).astype(np.float32)
+    from workloads import bf16_round
+    dO = bf16_round(dO)
+    dkv = torch.zeros((1, T, 576), dtype=torch.float32, device="cuda")
+    ws = dsa.new_workspace(256)
+    dq = dsa.sparse_mla_bwd(sl(bf(d["q_lat"])), kvrows, sl(idx), i32([q0]), i32([T]), T, sl(o_lat),
+                            sl(lse), bf(dO), dkv, cfg.scale, workspace=ws)
+    assert dsa.read_device_status(ws)[0] == dsa.DSA_OK
+    gi = idx[:, q0:].cpu().numpy()
+    rdq, rdkv = oracle.sparse_mla_bwd(d["q_lat"][:, q0:], d["kv"], gi, np.array([q0], np.int32),
+                                      np.array([T], np.int32), cfg.scale, dO)
+    _check(dq.cpu().numpy(), rdq, "dq (val4096 slice)")
+    _check(dkv.cpu().numpy(), rdkv, "dkv (val4096 slice)")
