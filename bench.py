@@ -447,8 +447,9 @@ def run_prefill_bwd(dsa, cfg, dev, stream, q_lat, kvrows, idx, o_lat, lse, T, pe
     tf = flop / t / 1e12
     return {"ms": t * 1e3, "queries": nq, "tflops": tf, "frac_of_bf16_peak": tf / peak_bf16,
             "flop": flop, "unit": "TFLOP/s",
-            "note": "first version on the CUDA cores in FP32 (dq kernel + dkv kernel with "
-                    "vector atomics); slice: last 512 queries of sequence 0", "gpu_launches": K * 2}
+            "note": "warp-level tensor-core MMA (m16n8k16 BF16, FP32 accumulate): dq kernel + "
+                    "dkv kernel with vector atomics; slice: last 512 queries of sequence 0",
+            "gpu_launches": K * 2}
 
 
 def launches_per_step(dsa, B, T, cfg):

@@ -189,7 +189,8 @@ dsa_status_t sparse_mla_fwd_sink(const uint16_t* q_lat, const dsa_rows_t* kv, co
  *                              order, so the FP32 rounding varies run to run.
  * -1 entries are skipped; other invalid entries raise DSA_ERR_BAD_INDEX and are
  * skipped.  Workspace: the 256-byte status header.  Supported: H <= 128,
- * topk <= 2048.  This first version runs on the CUDA cores in FP32.
+ * topk <= 2048.  The products run on the warp-level tensor-core MMA (BF16 in,
+ * FP32 accumulate).
  */
 dsa_status_t sparse_mla_bwd(const uint16_t* q_lat, const dsa_rows_t* kv, const int32_t* idx,
                             const int32_t* q_start, const int32_t* kv_len, int B, int Tq, int H,
