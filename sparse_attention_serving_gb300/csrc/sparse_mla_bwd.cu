@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(NT, 2) bwd_dq_kernel(const Params p) {
 // ---------------------------------------------------------------------------
 // dkv: one CTA per query row, every head group in turn per key block
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(NT, 1) bwd_dkv_kernel(const Params p) {
+__global__ void __launch_bounds__(NT, 2) bwd_dkv_kernel(const Params p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int64_t qf = blockIdx.x;
