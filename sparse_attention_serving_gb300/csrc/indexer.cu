@@ -262,6 +262,137 @@ __device__ float select_topk(float* cs, int32_t* ci, int n, int k, int gtid, int
   return key_to_float(static_cast<uint32_t>(ctr[2]));
 }
 
+// Final selection of one query by one epilogue half (128 threads, named
+// barrier `bar`, its own scratch): the indices of the k largest of the n
+// candidates go straight to out[0..k) (in no particular order; ties at the cut
+// broken arbitrarily), -1 padded when n < k.  The candidates stay in shared
+// memory and each radix pass re-reads them, so the two halves select their
+// queries at the same time without holding them in registers.
+__device__ void final_select_half(const float* cs, const int32_t* ci, int n, int k, int htid,
+                                  uint32_t bar, int* hist, int* sel, int* ctr, int32_t* out) {
+  constexpr int GH = 128;
+  const int lane = htid & 31, hw = htid >> 5;
+  if (n <= k) {
+    for (int e = htid; e < k; e += GH) out[e] = e < n ? ci[e] : -1;
+    return;
+  }
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  for (int e = htid; e < n; e += GH) {
+    const uint32_t key = order_key(cs[e]);
+    kmin = min(kmin, key);
+    kmax = max(kmax, key);
+  }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (htid == 0) {
+    ctr[2] = static_cast<int>(0xffffffffu);
+    ctr[3] = 0;
+  }
+  named_bar_sync(bar, GH);
+  if (lane == 0) {
+    atomicMin(reinterpret_cast<unsigned*>(&ctr[2]), kmin);
+    atomicMax(reinterpret_cast<unsigned*>(&ctr[3]), kmax);
+  }
+  named_bar_sync(bar, GH);
+  const uint32_t lo = static_cast<uint32_t>(ctr[2]), hi = static_cast<uint32_t>(ctr[3]);
+  const uint32_t diff = lo ^ hi;
+  uint32_t prefix, mask;
+  int need = k;
+  if (diff == 0u) {
+    prefix = hi;
+    mask = 0xffffffffu;
+  } else {
+    const int top = 31 - __clz(diff);  // highest differing bit
+    mask = top >= 31 ? 0u : ~((2u << top) - 1u);
+    prefix = hi & mask;
+    int shift = top - 7;
+#pragma unroll 1
+    while (true) {
+      const int width = shift >= 0 ? 8 : 8 + shift;
+      if (shift < 0) shift = 0;
+      const uint32_t dm = (1u << width) - 1u;
+      for (int e = htid; e < 256; e += GH) hist[e] = 0;
+      named_bar_sync(bar, GH);
+      for (int e = htid; e < n; e += GH) {
+        const uint32_t key = order_key(cs[e]);
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & dm], 1);
+      }
+      named_bar_sync(bar, GH);
+      if (htid < 32) {
+        // lane l covers digits 255-8l .. 248-8l (descending)
+        int c[8], tot = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { c[e] = hist[255 - 8 * htid - e]; tot += c[e]; }
+        int incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (htid >= o) incl += v;
+        }
+        const int excl = incl - tot;
+        if (excl < need && need <= incl) {
+          int run = excl;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            if (run < need && need <= run + c[e]) {
+              sel[0] = 255 - 8 * htid - e;
+              sel[1] = need - run;
+              sel[2] = c[e];
+            }
+            run += c[e];
+          }
+        }
+      }
+      named_bar_sync(bar, GH);
+      prefix |= static_cast<uint32_t>(sel[0]) << shift;
+      mask |= dm << shift;
+      need = sel[1];
+      const bool done = sel[2] == need || shift == 0;  // bin kept whole, or every bit fixed
+      named_bar_sync(bar, GH);
+      if (done) break;
+      shift -= 8;
+    }
+  }
+  // positions from one prefix sum over the half: keys above the prefix go to
+  // [0, total_hi), the first `need` equal ones (in thread order) after them
+  int n_hi = 0, n_eq = 0;
+  for (int e = htid; e < n; e += GH) {
+    const uint32_t m = order_key(cs[e]) & mask;
+    n_hi += m > prefix;
+    n_eq += m == prefix;
+  }
+  const int packed = n_hi | (n_eq << 16);
+  int incl = packed;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int* wtot = hist;  // [4] warp totals (the histogram is no longer needed)
+  if (lane == 31) wtot[hw] = incl;
+  named_bar_sync(bar, GH);
+  int before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < GH / 32; ++w) {
+    const int t = wtot[w];
+    if (w < hw) before += t;
+    total += t;
+  }
+  const int excl = before + incl - packed;
+  const int total_hi = total & 0xffff;
+  int pos_hi = excl & 0xffff, pos_eq = excl >> 16;
+  for (int e = htid; e < n; e += GH) {
+    const uint32_t m = order_key(cs[e]) & mask;
+    if (m > prefix) {
+      out[pos_hi++] = ci[e];
+    } else if (m == prefix) {
+      if (pos_eq < need) out[total_hi + pos_eq] = ci[e];
+      ++pos_eq;
+    }
+  }
+  named_bar_sync(bar, GH);  // the scratch is reused by the half's next query
+}
+
 template <int H_I, int D_I, bool FP8>
 __global__ void __launch_bounds__(NTHREADS, 1)
     indexer_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -285,6 +416,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   int* hist = reinterpret_cast<int*>(thr + 64);     // [256]
   int* sel = hist + 256;                            // [4]
   int* ctr = sel + 4;                               // [4]
+  int* hist1 = ctr + 4;                             // [256] the second half's final-select scratch
+  int* sel1 = hist1 + 256;                          // [4]
+  int* ctr1 = sel1 + 4;                             // [4]
   float* cand_s = reinterpret_cast<float*>(sm + C::OFF_CAND);
   int32_t* cand_i = reinterpret_cast<int32_t*>(cand_s + QT * CAP);
 
@@ -580,16 +714,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (gtid == 0) g_abort[1] = vflag(s_abort) ? 1 : 0;
     named_bar_sync(1, G);
     const bool aborted = vflag(&g_abort[1]);
-    for (int qq = 0; qq < nq; ++qq) {
-      if (!aborted && cnt[qq] > p.topk) {
-        select_topk<C::EPT>(cand_s + qq * CAP, cand_i + qq * CAP, cnt[qq], p.topk, gtid, hist, sel,
-                            ctr);
-        if (gtid == 0) cnt[qq] = p.topk;
-        named_bar_sync(1, G);
-      }
-      const int n = aborted ? 0 : cnt[qq];
+    // the two epilogue halves select their queries (even / odd) at the same time
+    const int htid = gtid - 128 * half;
+    for (int qq = half; qq < nq; qq += 2) {
       int32_t* o = out + static_cast<int64_t>(qq) * p.topk;
-      for (int e = gtid; e < p.topk; e += G) o[e] = e < n ? cand_i[qq * CAP + e] : -1;
+      if (aborted) {
+        for (int e = htid; e < p.topk; e += 128) o[e] = -1;
+        continue;
+      }
+      final_select_half(cand_s + qq * CAP, cand_i + qq * CAP, cnt[qq], p.topk, htid, 2u + half,
+                        half ? hist1 : hist, half ? sel1 : sel, half ? ctr1 : ctr, o);
     }
   }
   tc_fence_before();
