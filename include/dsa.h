@@ -101,7 +101,8 @@ typedef enum {
   DSA_OP_INDEXER_TOPK = 0,
   DSA_OP_SPARSE_MLA = 1,
   DSA_OP_GATE = 2,
-  DSA_OP_CACHE_APPEND = 3
+  DSA_OP_CACHE_APPEND = 3,
+  DSA_OP_SPARSE_MLA_BWD = 4
 } dsa_op_t;
 
 /* Bytes of workspace an op needs for the given sizes (heads = H_I for the
@@ -188,7 +189,8 @@ dsa_status_t sparse_mla_fwd_sink(const uint16_t* q_lat, const dsa_rows_t* kv, co
  *                              Additions come from many queries in no fixed
  *                              order, so the FP32 rounding varies run to run.
  * -1 entries are skipped; other invalid entries raise DSA_ERR_BAD_INDEX and are
- * skipped.  Workspace: the 256-byte status header.  Supported: H <= 128,
+ * skipped.  Workspace: dsa_workspace_bytes(DSA_OP_SPARSE_MLA_BWD, ...) = the
+ * 256-byte status header.  Supported: H <= 128,
  * topk <= 2048.  The products run on the warp-level tensor-core MMA (BF16 in,
  * FP32 accumulate).
  */

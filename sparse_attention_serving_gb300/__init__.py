@@ -35,7 +35,7 @@ DSA_ERR_DEVICE_TIMEOUT = 4
 DSA_ERR_BAD_INDEX = 5
 DSA_ERR_WORKSPACE_TOO_SMALL = 6
 
-OP_INDEXER_TOPK, OP_SPARSE_MLA, OP_GATE, OP_CACHE_APPEND = 0, 1, 2, 3
+OP_INDEXER_TOPK, OP_SPARSE_MLA, OP_GATE, OP_CACHE_APPEND, OP_SPARSE_MLA_BWD = 0, 1, 2, 3, 4
 INDEXER_KEY_EPS = 1e-5   # KimiK3TextConfig rms_norm_eps
 RLAT, VLAT, PAGE = 576, 512, 64
 MLA_SCALE = 1.0 / math.sqrt(128 + 64)   # qk_nope_head_dim + qk_rope_head_dim
@@ -375,7 +375,7 @@ def sparse_mla_bwd(q_lat, kv: Rows, idx, q_start, kv_len, max_kv_len: int, o_lat
     if dq is None:
         dq = torch.empty((B, Tq, H, RLAT), dtype=torch.float32, device=q_lat.device)
     _need(dq, torch.float32, "dq")
-    ws = _ws(workspace, OP_GATE, B, Tq, 0, 0, 0, q_lat.device, stream)
+    ws = _ws(workspace, OP_SPARSE_MLA_BWD, B, Tq, 0, 0, 0, q_lat.device, stream)
     rows = kv.c()
     _check(lib.sparse_mla_bwd(_ptr(q_lat), ctypes.byref(rows), _ptr(idx), _ptr(q_start),
                               _ptr(kv_len), B, Tq, H, topk, int(max_kv_len), float(scale),

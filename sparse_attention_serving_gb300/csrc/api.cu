@@ -328,7 +328,8 @@ dsa_status_t sparse_mla_bwd(const uint16_t* q_lat, const dsa_rows_t* kv, const i
   SparseMlaBwdArgs a{};
   dsa_status_t st = resolve_rows(kv, B, max_kv_len, kRlat, &a.kv);
   if (st != DSA_OK) return st;
-  st = check_ws(workspace, ws_bytes, kWorkspaceHeader);
+  st = check_ws(workspace, ws_bytes,
+                dsa_workspace_bytes(DSA_OP_SPARSE_MLA_BWD, B, Tq, max_kv_len, H, topk));
   if (st != DSA_OK) return st;
   a.q_lat = q_lat;
   a.idx = idx;
