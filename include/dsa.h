@@ -180,7 +180,9 @@ dsa_status_t sparse_mla_fwd_sink(const uint16_t* q_lat, const dsa_rows_t* kv, co
  *   dq   = scale * sum_j dz_j kv[s_j, 0:576]                       (written)
  *   dkv[s_j, 0:576] += scale * dz_j q,  dkv[s_j, 0:512] += p_j d_o  (added)
  * Arguments as for sparse_mla_fwd, plus
- *   o_lat, lse          the forward's outputs for the same inputs
+ *   o_lat, lse          the forward's outputs for the same inputs (those of
+ *                       sparse_mla_fwd_sink serve too: the sink carries no value
+ *                       and depends on neither q nor kv, so only lse sees it)
  *   d_o   [B,Tq,H,512]  BF16   upstream gradient of o_lat
  *   dq    [B,Tq,H,576]  FP32   written; a query with no valid entry gets 0
  *   dkv                 FP32   rows of 576 numbered like kv's rows

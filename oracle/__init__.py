@@ -64,9 +64,10 @@ def load(path: str | None = None):
         lib.oracle_quant_fp8.argtypes = [P, i64, i32, P, P]
         lib.oracle_indexer_scores_fp8.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
                                                   i64, P, P]
-        lib.oracle_sparse_mla_f64.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f64, i64, P,
-                                              P, P]
-        lib.oracle_sparse_mla_bwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f64, P, P, P]
+        lib.oracle_sparse_mla_f64.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f64, P, i64,
+                                              P, P, P]
+        lib.oracle_sparse_mla_bwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f64, P, P, P,
+                                              P]
         lib.oracle_set_threads.argtypes = [i32]
         for f in ("oracle_indexer_scores", "oracle_topk", "oracle_sparse_mla", "oracle_dense_mla",
                   "oracle_explicit_mla", "oracle_gate", "oracle_set_threads",
@@ -378,8 +379,17 @@ def _as_f64(a):
     return _c(a, np.float64)
 
 
-def sparse_mla_f64(q_lat, kv, idx, q_start, kv_len, scale, rows=None, lib=None):
-    """The sparse MLA forward on exact (float64) values: (o [n,H,512], lse [n,H])."""
+def _sink(sink, H):
+    if sink is None:
+        return None
+    sk = _c(sink, np.float64)
+    assert sk.shape == (H,)
+    return sk
+
+
+def sparse_mla_f64(q_lat, kv, idx, q_start, kv_len, scale, rows=None, lib=None, sink=None):
+    """The sparse MLA forward on exact (float64) values: (o [n,H,512], lse [n,H]);
+    sink: optional [H] learnable sink logits (natural log)."""
     lib = lib or load()
     q, k = _as_f64(q_lat), _as_f64(kv)
     B, Tq, H, R = q.shape
@@ -391,15 +401,17 @@ def sparse_mla_f64(q_lat, kv, idx, q_start, kv_len, scale, rows=None, lib=None):
     lse = np.empty((len(rows), H), np.float64)
     ix = _c(idx, np.int32)
     qs, kl = _c(q_start, np.int32), _c(kv_len, np.int32)
+    sk = _sink(sink, H)
     _check(lib.oracle_sparse_mla_f64(_p(q), _p(k), _p(ix), _p(qs), _p(kl), B, Tq, S_max, H, topk_,
-                                     float(scale), len(rows), _p(rows), _p(o), _p(lse)),
-           "sparse_mla_f64")
+                                     float(scale), None if sk is None else _p(sk), len(rows),
+                                     _p(rows), _p(o), _p(lse)), "sparse_mla_f64")
     return o, lse
 
 
-def sparse_mla_bwd(q_lat, kv, idx, q_start, kv_len, scale, dO, lib=None):
+def sparse_mla_bwd(q_lat, kv, idx, q_start, kv_len, scale, dO, lib=None, sink=None):
     """Gradients of sum(dO * o) for the sparse MLA forward with a fixed index set:
-    (dq [B,Tq,H,576], dkv [B,S,576]), float64.  Inputs may be BF16 bits or floats."""
+    (dq [B,Tq,H,576], dkv [B,S,576]), float64.  Inputs may be BF16 bits or floats.
+    sink: optional [H] learnable sink logits of the forward (natural log)."""
     lib = lib or load()
     q, k, g = _as_f64(q_lat), _as_f64(kv), _as_f64(dO)
     B, Tq, H, R = q.shape
@@ -410,6 +422,8 @@ def sparse_mla_bwd(q_lat, kv, idx, q_start, kv_len, scale, dO, lib=None):
     dkv = np.empty(k.shape, np.float64)
     ix = _c(idx, np.int32)
     qs, kl = _c(q_start, np.int32), _c(kv_len, np.int32)
+    sk = _sink(sink, H)
     _check(lib.oracle_sparse_mla_bwd(_p(q), _p(k), _p(ix), _p(qs), _p(kl), B, Tq, S_max, H, topk_,
-                                     float(scale), _p(g), _p(dq), _p(dkv)), "sparse_mla_bwd")
+                                     float(scale), None if sk is None else _p(sk), _p(g), _p(dq),
+                                     _p(dkv)), "sparse_mla_bwd")
     return dq, dkv

@@ -722,6 +722,10 @@ int oracle_indexer_scores_fp8(const uint8_t* q_codes, const float* q_scale, cons
  *   dkv[s_j, 0:576] += scale * dz_j q,   dkv[s_j, 0:512] += p_j dO
  * (the latent row is both the key, 576 dims, and the value, its first 512).
  * Entries -1 are skipped; any other entry must be causal (else OR_BAD_INDEX).
+ * With a learnable sink (one logit per head, no value row) the sink joins the
+ * denominator: lse = log(e^sink + sum_j e^z_j); p_j, o, D and the gradients
+ * above keep their form (the sink carries no value and depends on neither q
+ * nor the latent rows).
  * Inputs and outputs are double: the gradient of the function on exact values. */
 
 typedef struct {
@@ -731,6 +735,7 @@ typedef struct {
   double scale;
   const int64_t* rows;
   double *o, *lse, *D, *dq; /* o / D / dq may be NULL */
+  const double* sink;       /* [H] natural-log sink logits, or NULL */
   int err;
 } mlab_ctx;
 
@@ -760,10 +765,13 @@ static void mlab_row(void* vctx, int64_t r) {
       if (z[j] > m) m = z[j];
       ++n;
     }
+    const double sk = c->sink ? c->sink[h] : -INFINITY;
+    if (sk > m) m = sk;
     double l = 0.0;
     for (int j = 0; j < c->topk; ++j)
       if (z[j] != -INFINITY) l += exp(z[j] - m);
-    const double lse = n > 0 ? m + log(l) : -INFINITY;
+    if (sk != -INFINITY) l += exp(sk - m);
+    const double lse = m != -INFINITY ? m + log(l) : -INFINITY;
     if (c->lse) c->lse[r * c->H + h] = lse;
     double o[VLAT];
     for (int d = 0; d < VLAT; ++d) o[d] = 0.0;
@@ -799,14 +807,14 @@ static void mlab_row(void* vctx, int64_t r) {
  * The same function as oracle_sparse_mla on exact values; the backward is its gradient. */
 int oracle_sparse_mla_f64(const double* q, const double* kv, const int32_t* idx,
                           const int32_t* q_start, const int32_t* kv_len, int B, int Tq, int S_max,
-                          int H, int topk, double scale, int64_t n_rows, const int64_t* rows,
-                          double* o, double* lse) {
+                          int H, int topk, double scale, const double* sink, int64_t n_rows,
+                          const int64_t* rows, double* o, double* lse) {
   if (!q || !kv || !idx || !q_start || !kv_len || !rows || !o || !lse) return OR_BAD_ARG;
   if (B <= 0 || Tq <= 0 || S_max <= 0 || H <= 0 || topk <= 0 || n_rows < 0) return OR_BAD_ARG;
   for (int64_t r = 0; r < n_rows; ++r)
     if (rows[r] < 0 || rows[r] >= (int64_t)B * Tq) return OR_BAD_ARG;
   mlab_ctx c = {q, kv, NULL, idx, q_start, kv_len, Tq, S_max, H, topk, scale, rows,
-                o, lse, NULL, NULL, OR_OK};
+                o, lse, NULL, NULL, sink, OR_OK};
   parallel_rows(n_rows, mlab_row, &c);
   return c.err;
 }
@@ -850,8 +858,8 @@ static void dkv_row(void* vctx, int64_t kr) {
  * query selected are zero). */
 int oracle_sparse_mla_bwd(const double* q, const double* kv, const int32_t* idx,
                           const int32_t* q_start, const int32_t* kv_len, int B, int Tq, int S_max,
-                          int H, int topk, double scale, const double* dO, double* dq,
-                          double* dkv) {
+                          int H, int topk, double scale, const double* sink, const double* dO,
+                          double* dq, double* dkv) {
   if (!q || !kv || !idx || !q_start || !kv_len || !dO || !dq || !dkv) return OR_BAD_ARG;
   if (B <= 0 || Tq <= 0 || S_max <= 0 || H <= 0 || topk <= 0) return OR_BAD_ARG;
   const int64_t nq = (int64_t)B * Tq, nk = (int64_t)B * S_max;
@@ -863,7 +871,7 @@ int oracle_sparse_mla_bwd(const double* q, const double* kv, const int32_t* idx,
   for (int64_t r = 0; r < nq; ++r) rows[r] = r;
   /* pass 1: per query row, lse, D = dO . o and dq */
   mlab_ctx c = {q, kv, dO, idx, q_start, kv_len, Tq, S_max, H, topk, scale, rows,
-                NULL, lse, D, dq, OR_OK};
+                NULL, lse, D, dq, sink, OR_OK};
   parallel_rows(nq, mlab_row, &c);
   int err = c.err;
   /* inverted lists of the selections (valid entries only, query order) */

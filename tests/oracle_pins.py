@@ -766,4 +766,53 @@ def pin_mla_bwd_sum_rules(lib):
     assert np.allclose(dkv[0, :, :512].sum(axis=0), want, rtol=0, atol=1e-10)
 
 
+def pin_mla_bwd_with_sink(lib):
+    """With a learnable sink: a sink of -inf is exactly no sink; the float64
+    forward agrees with the BF16 sink forward; central differences of the sink
+    forward agree with the backward."""
+    T, H = 30, 8
+    q16 = normal_bf16(96, "q_lat", (1, T, H, 576))
+    kv16 = normal_bf16(96, "kv", (1, T, 576))
+    rng = np.random.default_rng(96)
+    idx = np.full((1, T, 8), -1, np.int32)
+    for t in range(T):
+        c = rng.permutation(t + 1)[:8]
+        idx[0, t, :len(c)] = c
+    idx[0, 11] = -1                                   # a query with no valid entry
+    qs, kl = np.zeros(1, np.int32), np.full(1, T, np.int32)
+    sink = rng.uniform(-1.0, 3.0, H)
+    o1, l1 = oracle.sparse_mla(q16, kv16, idx, qs, kl, SCALE, lib=lib, sink=sink)
+    o2, l2 = oracle.sparse_mla_f64(q16, kv16, idx, qs, kl, SCALE, lib=lib, sink=sink)
+    assert np.allclose(o1, o2, rtol=0, atol=1e-12) and np.allclose(l1, l2, rtol=0, atol=1e-12)
+    assert np.allclose(l2[11], sink) and np.all(o2[11] == 0.0)
+    dO = rng.standard_normal((1, T, H, 512))
+    a = oracle.sparse_mla_bwd(q16, kv16, idx, qs, kl, SCALE, dO, lib=lib)
+    b = oracle.sparse_mla_bwd(q16, kv16, idx, qs, kl, SCALE, dO, lib=lib, sink=np.full(H, -np.inf))
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    # central differences on a small float64 case with a sink
+    q, kv, dO2, idx2, qs2, kl2 = _bwd_case(97, 6, 2, 3, amp=0.5)
+    sk = np.array([0.7, -0.4])
+    scale = 0.3
+    dq, dkv = oracle.sparse_mla_bwd(q, kv, idx2, qs2, kl2, scale, dO2, lib=lib, sink=sk)
+
+    def loss(qq, kk):
+        o, _ = oracle.sparse_mla_f64(qq, kk, idx2, qs2, kl2, scale, lib=lib, sink=sk)
+        return float(np.sum(o * dO2.reshape(o.shape)))
+
+    eps = 1e-6
+    for (t, h, d) in [(5, 1, 3), (4, 0, 550)]:
+        qp, qm = q.copy(), q.copy()
+        qp[0, t, h, d] += eps
+        qm[0, t, h, d] -= eps
+        fd = (loss(qp, kv) - loss(qm, kv)) / (2 * eps)
+        assert abs(fd - dq[0, t, h, d]) <= 1e-7 * max(1.0, abs(fd)), ("dq", t, h, d, fd)
+    s0 = int(idx2[0, 5, 0])
+    for d in (9, 560):
+        kp, km = kv.copy(), kv.copy()
+        kp[0, s0, d] += eps
+        km[0, s0, d] -= eps
+        fd = (loss(q, kp) - loss(q, km)) / (2 * eps)
+        assert abs(fd - dkv[0, s0, d]) <= 1e-7 * max(1.0, abs(fd)), ("dkv", s0, d, fd)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -149,3 +149,30 @@ def test_bwd_bad_index_is_flagged_and_skipped(dsa):
     rdq, rdkv = oracle.sparse_mla_bwd(q, kv, clean, q_start, kv_len, scale, dO)
     _check(dq.cpu().numpy(), rdq, "dq")
     _check(dkv.cpu().numpy(), rdkv, "dkv")
+
+
+def test_bwd_with_sink(dsa):
+    """The backward of the learnable-sink forward: the same kernels, fed the sink
+    forward's o_lat and lse (the sink is in the denominator; it has no value and
+    depends on neither q nor the latent rows), against the oracle with the sink."""
+    B, T, H, k = 1, 200, 96, 64
+    seed = 151
+    q = normal_bf16(seed, "q_lat", (B, T, H, 576))
+    kv = normal_bf16(seed, "kv", (B, T, 576))
+    dO = normal_bf16(seed, "w", (B, T, H, 512))
+    idx = _indices(seed, B, T, 0, k)
+    sink = np.random.default_rng(seed).normal(0.0, 2.0, H).astype(np.float32)
+    sink[0], sink[1] = -np.inf, 40.0
+    q_start, kv_len = np.zeros(B, np.int32), np.full(B, T, np.int32)
+    scale = 1.0 / np.sqrt(192.0)
+    rows = dsa.Rows(bf(kv))
+    qt, dOt, it, qs, kl = bf(q), bf(dO), i32(idx), i32(q_start), i32(kv_len)
+    o_lat, lse = dsa.sparse_mla_fwd(qt, rows, it, qs, kl, T, scale,
+                                    sink=torch.from_numpy(sink).cuda())
+    dkv = torch.zeros((B, T, 576), dtype=torch.float32, device="cuda")
+    dq = dsa.sparse_mla_bwd(qt, rows, it, qs, kl, T, o_lat, lse, dOt, dkv, scale)
+    torch.cuda.synchronize()
+    rdq, rdkv = oracle.sparse_mla_bwd(q, kv, idx, q_start, kv_len, scale, dO,
+                                      sink=sink.astype(np.float64))
+    _check(dq.cpu().numpy(), rdq, "dq (sink)")
+    _check(dkv.cpu().numpy(), rdkv, "dkv (sink)")

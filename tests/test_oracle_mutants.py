@@ -55,6 +55,7 @@ MUTANTS = {
     "bwd_dq_rope_dims_dropped": ("for (int d = 0; d < RLAT; ++d) dqh[d] += c->scale", "for (int d = 0; d < VLAT; ++d) dqh[d] += c->scale"),
     "bwd_value_grad_dropped": ("for (int d = 0; d < VLAT; ++d) out[d] += p * dOh[d];", ""),
     "bwd_key_grad_sign_flipped": ("out[d] += c->scale * dz * qh[d];", "out[d] -= c->scale * dz * qh[d];"),
+    "bwd_sink_not_in_denominator": ("    if (sk != -INFINITY) l += exp(sk - m);\n", ""),
     "fp8_key_scale_dropped": ("* (ks * dec8(k[d]));", "* dec8(k[d]);"),
     "fp8_query_scale_dropped": ("dot += (qsj * dec8(q[j * c->D_I + d]))", "dot += (dec8(q[j * c->D_I + d]))"),
 }
