@@ -600,7 +600,14 @@ __global__ void __launch_bounds__(1024) decode_select_kernel(const float* __rest
     need = sel[1];
   }
   if (binnable && sel[2] <= SEL_CAP) {
-    for_each_score(sc, L, [&](int e, float x) {
+    // Keys above the boundary bin go to out, those in it to the candidate
+    // buffer.  Each iteration a thread flags its 16 scores; one warp scan gives
+    // the lanes' offsets and one atomic per warp reserves the slots, so no
+    // store waits on a per-key atomic.  The loop runs warp-uniformly.
+    const int lane = tid & 31;
+    const int head = min(L, static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(sc) >> 2) & 3u)) & 3u));
+    auto scalar = [&](int e) {
+      const float x = sc[e];
       const int bn = bin_of(x);
       if (bn > bstar) {
         out[atomicAdd(&ctr[0], 1)] = e;
@@ -609,7 +616,60 @@ __global__ void __launch_bounds__(1024) decode_select_kernel(const float* __rest
         ckey[c] = order_key(x);
         cidx[c] = e;
       }
-    });
+    };
+    if (tid < head) scalar(tid);
+    const float4* v4 = reinterpret_cast<const float4*>(sc + head);
+    const int n4 = (L - head) >> 2;
+    for (int i0 = tid; __any_sync(0xffffffffu, i0 < n4); i0 += 4 * 1024) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i0 + u * 1024 < n4) v[u] = __ldg(v4 + i0 + u * 1024);
+      uint32_t hi = 0u, eq = 0u;  // element u*4+c of this iteration
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (i0 + u * 1024 < n4) {
+          const float xs[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int bn = bin_of(xs[c]);
+            hi |= static_cast<uint32_t>(bn > bstar) << (4 * u + c);
+            eq |= static_cast<uint32_t>(bn == bstar) << (4 * u + c);
+          }
+        }
+      }
+      const int cnt = __popc(hi) | (__popc(eq) << 16);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const int tot = __shfl_sync(0xffffffffu, incl, 31);
+      int base_hi = 0, base_eq = 0;
+      if (lane == 31 && tot != 0) {
+        if (tot & 0xffff) base_hi = atomicAdd(&ctr[0], tot & 0xffff);
+        if (tot >> 16) base_eq = atomicAdd(&ctr[1], tot >> 16);
+      }
+      base_hi = __shfl_sync(0xffffffffu, base_hi, 31);
+      base_eq = __shfl_sync(0xffffffffu, base_eq, 31);
+      int ph = base_hi + ((incl - cnt) & 0xffff), pe = base_eq + ((incl - cnt) >> 16);
+      while (hi | eq) {
+        const int bit = __ffs(hi | eq) - 1;
+        const int e = head + 4 * (i0 + (bit >> 2) * 1024) + (bit & 3);
+        if ((hi >> bit) & 1u) {
+          out[ph++] = e;
+        } else {
+          ckey[pe] = order_key(sc[e]);
+          cidx[pe] = e;
+          ++pe;
+        }
+        hi &= ~(1u << bit);
+        eq &= ~(1u << bit);
+      }
+    }
+    const int t0 = head + 4 * n4;
+    if (t0 + tid < L) scalar(t0 + tid);
     __syncthreads();
     const int nc = ctr[1];
     uint32_t prefix = 0u, mask = 0u;
