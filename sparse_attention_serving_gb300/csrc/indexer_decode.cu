@@ -606,6 +606,7 @@ __global__ void __launch_bounds__(1024) decode_select_kernel(const float* __rest
     // store waits on a per-key atomic.  The loop runs warp-uniformly.
     const int lane = tid & 31;
     const int head = min(L, static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(sc) >> 2) & 3u)) & 3u));
+    const float pre_t = lo + static_cast<float>(bstar - 2) / scale;
     auto scalar = [&](int e) {
       const float x = sc[e];
       const int bn = bin_of(x);
@@ -625,18 +626,26 @@ __global__ void __launch_bounds__(1024) decode_select_kernel(const float* __rest
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         if (i0 + u * 1024 < n4) v[u] = __ldg(v4 + i0 + u * 1024);
-      uint32_t hi = 0u, eq = 0u;  // element u*4+c of this iteration
+      // almost every score lies below the boundary bin: one compare against a
+      // value two bins below it (a margin for the rounding of bin_of) rules it
+      // out; the few others are binned exactly, re-read from the cache
+      uint32_t cand = 0u;  // element u*4+c of this iteration
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         if (i0 + u * 1024 < n4) {
-          const float xs[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int bn = bin_of(xs[c]);
-            hi |= static_cast<uint32_t>(bn > bstar) << (4 * u + c);
-            eq |= static_cast<uint32_t>(bn == bstar) << (4 * u + c);
-          }
+          cand |= static_cast<uint32_t>(v[u].x > pre_t) << (4 * u);
+          cand |= static_cast<uint32_t>(v[u].y > pre_t) << (4 * u + 1);
+          cand |= static_cast<uint32_t>(v[u].z > pre_t) << (4 * u + 2);
+          cand |= static_cast<uint32_t>(v[u].w > pre_t) << (4 * u + 3);
         }
+      }
+      uint32_t hi = 0u, eq = 0u;
+      while (cand) {
+        const int bit = __ffs(cand) - 1;
+        cand &= cand - 1u;
+        const int bn = bin_of(sc[head + 4 * (i0 + (bit >> 2) * 1024) + (bit & 3)]);
+        hi |= static_cast<uint32_t>(bn > bstar) << bit;
+        eq |= static_cast<uint32_t>(bn == bstar) << bit;
       }
       const int cnt = __popc(hi) | (__popc(eq) << 16);
       int incl = cnt;
