@@ -25,11 +25,15 @@
 //                  carries only the key copies; the query scales fold into the
 //                  head weights and the key scale multiplies the head sum:
 //                    I[s] = k_scale[s] * sum_j (w[j] q_scale[j]) max(0, c_q[j] . c_k[s]).
-//   decode_select  one CTA per request: a value histogram between those
-//                  extremes finds the bin of the k-th largest score, a second
-//                  pass writes the keys above it and keeps that bin's keys in
-//                  shared memory, and an exact radix select over them picks
-//                  the rest.
+//   decode_select  one CTA per request.  A strided sample of 4,096 scores,
+//                  binned between those extremes, gives a threshold that about
+//                  2.5 k scores reach; one pass copies every score at or above
+//                  it into shared memory and an exact radix select over them
+//                  picks the k.  When the threshold catches fewer than k or
+//                  more than fit, a value histogram of all scores finds the bin
+//                  of the k-th largest, a second pass writes the keys above it
+//                  and keeps that bin's keys, and the radix select picks the
+//                  rest.
 #include <cmath>
 
 #include <cuda_bf16.h>
@@ -587,10 +591,118 @@ __global__ void __launch_bounds__(1024) decode_select_kernel(const float* __rest
     const float f = (x - lo) * scale;  // monotone in x
     return f >= static_cast<float>(SEL_NBIN - 1) ? SEL_NBIN - 1 : (f > 0.f ? static_cast<int>(f) : 0);
   };
-  for (int e = tid; e < SEL_NBIN; e += 1024) hist[e] = 0;
+  // The `need` largest of the nc candidates in ckey / cidx go to out (after
+  // the ctr[0] keys already there): exact radix select over the order keys
+  // (8-bit digits from the top, stopping once the bin of the last one is
+  // kept whole), then one compaction.
+  auto select_candidates = [&](int nc, int need_) {
+    uint32_t prefix = 0u, mask = 0u;
+#pragma unroll 1
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      if (tid < 256) h256[tid] = 0;
+      __syncthreads();
+      for (int i = tid; i < nc; i += 1024) {
+        const uint32_t k = ckey[i];
+        if ((k & mask) == prefix) atomicAdd(&h256[(k >> shift) & 255u], 1);
+      }
+      __syncthreads();
+      find_bin256(h256, need_, sel);
+      prefix |= static_cast<uint32_t>(sel[0]) << shift;
+      mask |= 255u << shift;
+      need_ = sel[1];
+      const bool done = sel[2] == need_;
+      __syncthreads();
+      if (done) break;
+    }
+    for (int i = tid; i < nc; i += 1024) {
+      const uint32_t m = ckey[i] & mask;
+      bool keep = m > prefix;
+      if (!keep && m == prefix) keep = atomicAdd(&ctr[2], 1) < need_;
+      if (keep) out[atomicAdd(&ctr[0], 1)] = cidx[i];
+    }
+  };
   if (tid == 0) { ctr[0] = 0; ctr[1] = 0; ctr[2] = 0; }
-  __syncthreads();
   const bool binnable = scale > 0.f && scale < 3.0e38f;
+  // ---- single pass: every score at or above a sampled threshold T becomes a
+  // candidate.  T comes from a strided sample of 4,096 scores, binned 256 ways
+  // between the extremes: the lower edge of the bin of the sample's r-th
+  // largest, r chosen so that about 2.5 k of the L scores exceed T.  Exact
+  // whenever at least k and at most SEL_CAP scores reach T (then the top k are
+  // all candidates); otherwise the two-pass path below runs instead.
+  if (binnable) {
+    float T = -INFINITY;
+    if (L > SEL_CAP) {
+      constexpr int NS = 4096;
+      const float s256 = 256.f / (hi - lo);
+      if (tid < 256) h256[tid] = 0;
+      __syncthreads();
+      for (int i = tid; i < NS; i += 1024) {
+        const float f = (sc[static_cast<int64_t>(i) * L / NS] - lo) * s256;
+        atomicAdd(&h256[f >= 255.f ? 255 : (f > 0.f ? static_cast<int>(f) : 0)], 1);
+      }
+      __syncthreads();
+      const int r = min(NS, static_cast<int>(2.5f * static_cast<float>(topk) *
+                                             static_cast<float>(NS) / static_cast<float>(L)) + 32);
+      find_bin256(h256, r, sel);
+      T = lo + static_cast<float>(sel[0]) / s256;
+    }
+    const int lane = tid & 31;
+    const int head = min(L, static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(sc) >> 2) & 3u)) & 3u));
+    auto put = [&](int e, float x, int pos) {
+      if (pos < SEL_CAP) {
+        ckey[pos] = order_key(x);
+        cidx[pos] = e;
+      }
+    };
+    if (tid < head && sc[tid] >= T) put(tid, sc[tid], atomicAdd(&ctr[1], 1));
+    const float4* v4 = reinterpret_cast<const float4*>(sc + head);
+    const int n4 = (L - head) >> 2;
+    for (int i0 = tid; __any_sync(0xffffffffu, i0 < n4); i0 += 4 * 1024) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i0 + u * 1024 < n4) v[u] = __ldg(v4 + i0 + u * 1024);
+      uint32_t fl = 0u;  // element u*4+c of this iteration
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (i0 + u * 1024 < n4) {
+          fl |= static_cast<uint32_t>(v[u].x >= T) << (4 * u);
+          fl |= static_cast<uint32_t>(v[u].y >= T) << (4 * u + 1);
+          fl |= static_cast<uint32_t>(v[u].z >= T) << (4 * u + 2);
+          fl |= static_cast<uint32_t>(v[u].w >= T) << (4 * u + 3);
+        }
+      }
+      const int cnt = __popc(fl);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const int tot = __shfl_sync(0xffffffffu, incl, 31);
+      int base = 0;
+      if (lane == 31 && tot != 0) base = atomicAdd(&ctr[1], tot);
+      int pos = __shfl_sync(0xffffffffu, base, 31) + incl - cnt;
+      while (fl) {
+        const int bit = __ffs(fl) - 1;
+        fl &= fl - 1u;
+        const int e = head + 4 * (i0 + (bit >> 2) * 1024) + (bit & 3);
+        put(e, sc[e], pos++);
+      }
+    }
+    const int t0 = head + 4 * n4;
+    if (t0 + tid < L && sc[t0 + tid] >= T) put(t0 + tid, sc[t0 + tid], atomicAdd(&ctr[1], 1));
+    __syncthreads();
+    const int nc = ctr[1];
+    if (nc >= topk && nc <= SEL_CAP) {
+      select_candidates(nc, topk);
+      return;
+    }
+    __syncthreads();
+    if (tid == 0) ctr[1] = 0;
+  }
+  for (int e = tid; e < SEL_NBIN; e += 1024) hist[e] = 0;
+  __syncthreads();
   if (binnable) for_each_score(sc, L, [&](int, float x) { atomicAdd(&hist[bin_of(x)], 1); });
   __syncthreads();
   int need = topk, bstar = -1;
@@ -680,31 +792,7 @@ __global__ void __launch_bounds__(1024) decode_select_kernel(const float* __rest
     const int t0 = head + 4 * n4;
     if (t0 + tid < L) scalar(t0 + tid);
     __syncthreads();
-    const int nc = ctr[1];
-    uint32_t prefix = 0u, mask = 0u;
-#pragma unroll 1
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      if (tid < 256) h256[tid] = 0;
-      __syncthreads();
-      for (int i = tid; i < nc; i += 1024) {
-        const uint32_t k = ckey[i];
-        if ((k & mask) == prefix) atomicAdd(&h256[(k >> shift) & 255u], 1);
-      }
-      __syncthreads();
-      find_bin256(h256, need, sel);
-      prefix |= static_cast<uint32_t>(sel[0]) << shift;
-      mask |= 255u << shift;
-      need = sel[1];
-      const bool done = sel[2] == need;
-      __syncthreads();
-      if (done) break;
-    }
-    for (int i = tid; i < nc; i += 1024) {
-      const uint32_t m = ckey[i] & mask;
-      bool keep = m > prefix;
-      if (!keep && m == prefix) keep = atomicAdd(&ctr[2], 1) < need;
-      if (keep) out[atomicAdd(&ctr[0], 1)] = cidx[i];
-    }
+    select_candidates(ctr[1], need);
     return;
   }
   // ---- slow path: radix passes over the whole row ----
