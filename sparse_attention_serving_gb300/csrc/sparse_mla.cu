@@ -370,6 +370,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int e = (blk0 + jj + 1) * BK + key[i];
           s_next[i] = (jj + 1 < nb && e < n_list) ? __ldg(U.ix + e) : -1;
         }
+        if (p.nsplit > 1) {
+          // split units (decode): the rows come from HBM, not L2.  Ask L2 for
+          // the next block's rows now (the 8 threads of a key take one
+          // 128-byte chunk each, the first also the ninth), so their gather
+          // one block later finds them there.
+#pragma unroll
+          for (int i = 0; i < KPT; ++i) {
+            const int r = entry_row(p, U.b, U.t, s_next[i]);
+            if (r >= 0) {
+              const uint16_t* row = p.kv + static_cast<int64_t>(r) * kRlat;
+              prefetch_l2(row + unit * 64);
+              if (unit == 0) prefetch_l2(row + 8 * 64);
+            }
+          }
+        }
         // parts in the order the MMA consumes them: pair 0, pair 1, rope, pair 2, pair 3
         for (int part = 0; part < 5; ++part) {
           const bool rope = part == 2;
