@@ -629,7 +629,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int u = 0; u < n2; ++u) {
             const int k = kt + u, buf = k & 3;
             // head reduction: 4 independent FMA chains per query (the MMA's FP32
-            // accumulators are summed in a fixed order: chain c takes heads c, c+4, ...)
+            // accumulators are summed in a fixed order: chain c takes heads c, c+4, ...),
+            // issued as 2-wide FP32 FMAs on the chain pairs (0,1) and (2,3), each
+            // lane an ordinary round-to-nearest FMA
             constexpr int COLS = QH * H_I;  // this half's accumulator columns
             constexpr int NCHAIN = 4;
             float acc[QH][NCHAIN];
@@ -644,11 +646,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               tmem_ld32(tmem + lane_base + col0 + v * 32, r);
               tmem_ld_wait();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
+              for (int e = 0; e < 32; e += 2) {
                 const int col = v * 32 + e;
                 const int q = col / H_I;
-                const float x = fmaxf(__uint_as_float(r[e]), 0.f);
-                acc[q][e % NCHAIN] = fmaf(wreg[col], x, acc[q][e % NCHAIN]);
+                const int c = e % NCHAIN;  // 0 or 2
+                fma2_rn(acc[q][c], acc[q][c + 1], wreg[col], wreg[col + 1],
+                        fmaxf(__uint_as_float(r[e]), 0.f), fmaxf(__uint_as_float(r[e + 1]), 0.f));
               }
             }
             float score[QH];

@@ -312,6 +312,20 @@ __device__ __forceinline__ float redux_max_f32(float v) {
   return r;
 }
 
+// (d0, d1) = (a0 * b0 + d0, a1 * b1 + d1), each lane one round-to-nearest FMA,
+// as one 2-wide FP32 instruction.
+__device__ __forceinline__ void fma2_rn(float& d0, float& d1, float a0, float a1, float b0,
+                                        float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rd, {%0, %1};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rd;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
