@@ -452,7 +452,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int ntiles = (t_last + BKEY) / BKEY;
   if (tid == 0) {
     for (int k = 0; k < C::NBARS; ++k)
-      mbar_init(&bars[k], ((k >= C::BDE && k < C::BDE + 4) || k >= C::BSE) ? G : 1);
+      mbar_init(&bars[k], ((k >= C::BDE && k < C::BDE + 4) || k >= C::BSE) ? NEPI : 1);  // warps
     s_abort[0] = 0;
     for (int k = 0; k < 4; ++k) g_abort[k] = 0;
     fence_mbar_init();
@@ -658,13 +658,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int q = 0; q < QH; ++q) score[q] = (acc[q][0] + acc[q][1]) + (acc[q][2] + acc[q][3]);
             tc_fence_before();
-            mbar_arrive(&bars[C::BDE + buf]);
+            mbar_arrive_warp(&bars[C::BDE + buf]);
             if constexpr (FP8) {
               const int sc = k % (NSC > 0 ? NSC : 1);
               const float ks = s_scale[sc * BKEY + key_lane];
 #pragma unroll
               for (int q = 0; q < QH; ++q) score[q] *= ks;
-              mbar_arrive(&bars[C::BSE + sc]);
+              mbar_arrive_warp(&bars[C::BSE + sc]);
             }
             // append candidates above each query's threshold
             const int s = k * BKEY + key_lane;

@@ -45,6 +45,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
                    smem_u32(bar))
                : "memory");
 }
+// One arrival for the whole warp once every lane has got here: __syncwarp
+// orders each lane's earlier accesses (and its own fences) before lane 0's
+// release.  The barrier then counts warps, not threads.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile(
       "{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(
