@@ -40,7 +40,7 @@ METRIC = "DSA indexer+sparse-MLA tokens/s at T=8192,k=2048; % of TC / HBM roofli
 # ncu capture summarised in profiles/sparse_mla_val4096.md (855 MB for 4,096
 # queries).  The traffic is q_lat + idx in and o_lat out, so it scales with the
 # number of queries; reset to None whenever the kernel changes.
-MLA_DRAM_BYTES_PER_QUERY = (491.387648e6 + 364.545024e6) / 4096
+MLA_DRAM_BYTES_PER_QUERY = (491.475968e6 + 363.690240e6) / 4096
 
 
 def parse():
