@@ -376,6 +376,7 @@ def run_prefill_fp8(args, dsa, cfg, dev, stream, q_idx, w, k_idx, qs, kl, idx, w
     krows8 = dsa.Rows(kc)
     qc = torch.empty(q_idx.shape, dtype=torch.uint8, device=dev)
     qsc = torch.empty(q_idx.shape[:-1], dtype=torch.float32, device=dev)
+    idx8 = torch.empty_like(idx)  # the BF16 step's index sets stay as they are
 
     def step(ev=None):
         if ev is not None:
@@ -383,7 +384,7 @@ def run_prefill_fp8(args, dsa, cfg, dev, stream, q_idx, w, k_idx, qs, kl, idx, w
         dsa.dsa_quant_fp8(q_idx, codes=qc, scale=qsc)
         if ev is not None:
             ev[1].record(stream)
-        dsa.dsa_indexer_topk_fp8(qc, qsc, w, krows8, ksc, qs, kl, cfg.topk, T, out_idx=idx,
+        dsa.dsa_indexer_topk_fp8(qc, qsc, w, krows8, ksc, qs, kl, cfg.topk, T, out_idx=idx8,
                                  workspace=ws)
         if ev is not None:
             ev[2].record(stream)
@@ -460,44 +461,116 @@ def launches_per_step(dsa, B, T, cfg):
 
 
 def run_e2e(args, dsa, d, g, cfg, dev, stream, ws, krows, kvrows, world, tensors):
-    """Same step through the C ABI with pinned host inputs copied in and the gated
-    output copied out inside the timed region (weights stay resident)."""
+    """The step through the C ABI with pinned host inputs copied in and the gated
+    output copied out inside the timed region (weights stay resident), run the
+    way a serving loop runs it: each sequence's queries in chunks of 2,048 (a
+    chunk is the public calls at q_start = its offset, kv_len = its end, over the
+    sequence's keys and latent rows, which are copied in first).  A chunk's
+    inputs go in on one stream, its indexer + sparse MLA + gate run on a second
+    and its output comes back on a third, so that copies and kernels overlap.
+    Every byte of the step's inputs and outputs crosses the host link every step;
+    the keys and latent rows alternate between two device copies from step to
+    step, and each chunk's buffers are reused only once the previous step is
+    done with them."""
     import numpy as np
     import torch
     t = tensors
     B, T, N = cfg.B, cfg.T, cfg.B * cfg.T
+    C = min(T, 2048)
+    nc = (T + C - 1) // C
     host = {k: torch.from_numpy(d[k].view(np.int16)).view(torch.bfloat16).pin_memory()
             for k in ("q_idx", "w", "k_idx", "q_lat", "kv")}
     host["x"] = torch.from_numpy(g["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
     out_h = torch.empty(t["out"].shape, dtype=torch.bfloat16).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = out_h.numel() * out_h.element_size()
+    # the step's own output, to check the chunked pipeline against: the same
+    # computation per query, up to the order of each index list (candidates are
+    # appended by racing warps), hence of the attention's FP32 sums
+    ref_out = t["out"].clone()
+    kb = [t["k_idx"], torch.empty_like(t["k_idx"])]
+    kvb = [t["kv"], torch.empty_like(t["kv"])]
+    rows = [[(dsa.Rows(kb[p][b:b + 1]), dsa.Rows(kvb[p][b:b + 1])) for b in range(B)]
+            for p in range(2)]
+    qs_c = [torch.tensor([c * C], dtype=torch.int32, device=dev) for c in range(nc)]
+    kl_c = [torch.tensor([min(T, (c + 1) * C)], dtype=torch.int32, device=dev) for c in range(nc)]
+    s_in, s_out, s_cmp = torch.cuda.Stream(dev), torch.cuda.Stream(dev), stream
+    done, drained, keys_free = {}, {}, [None, None]
 
-    def step():
-        for k in ("q_idx", "w", "k_idx", "q_lat", "kv", "x"):
-            t[k].copy_(host[k], non_blocking=True)
-        dsa.dsa_indexer_topk(t["q_idx"], t["w"], krows, t["qs"], t["kl"], cfg.topk, T,
-                             out_idx=t["idx"], workspace=ws)
-        dsa.sparse_mla_fwd(t["q_lat"], kvrows, t["idx"], t["qs"], t["kl"], T, cfg.scale,
-                           o_lat=t["o_lat"], lse=t["lse"], workspace=ws)
-        dsa.mla_gate_apply(t["x"], t["W_g"], t["o_lat"].view(N, cfg.H, 512), t["W_uv"],
-                           out=t["out"], workspace=ws)
-        out_h.copy_(t["out"], non_blocking=True)
+    def step(i, first):
+        p = i & 1
+        ev_keys = torch.cuda.Event()
+        if first:  # the copies start after the caller's point (the start event)
+            s_in.wait_stream(s_cmp)
+        with torch.cuda.stream(s_in):
+            if keys_free[p] is not None:
+                s_in.wait_event(keys_free[p])
+            kb[p].copy_(host["k_idx"], non_blocking=True)
+            kvb[p].copy_(host["kv"], non_blocking=True)
+            ev_keys.record(s_in)
+        s_cmp.wait_event(ev_keys)
+        for b in range(B):
+            for c in range(nc):
+                q0, q1 = c * C, min(T, (c + 1) * C)
+                r0, r1 = b * T + q0, b * T + q1
+                ev_in = torch.cuda.Event()
+                with torch.cuda.stream(s_in):
+                    if (b, c) in done:
+                        s_in.wait_event(done[(b, c)])
+                    for k in ("q_idx", "w", "q_lat"):
+                        t[k][b, q0:q1].copy_(host[k][b, q0:q1], non_blocking=True)
+                    t["x"][r0:r1].copy_(host["x"][r0:r1], non_blocking=True)
+                    ev_in.record(s_in)
+                s_cmp.wait_event(ev_in)
+                if (b, c) in drained:
+                    s_cmp.wait_event(drained[(b, c)])
+                kr, kvr = rows[p][b]
+                idx_c, o_c = t["idx"][b:b + 1, q0:q1], t["o_lat"][b:b + 1, q0:q1]
+                dsa.dsa_indexer_topk(t["q_idx"][b:b + 1, q0:q1], t["w"][b:b + 1, q0:q1], kr,
+                                     qs_c[c], kl_c[c], cfg.topk, T, out_idx=idx_c, workspace=ws,
+                                     stream=s_cmp)
+                dsa.sparse_mla_fwd(t["q_lat"][b:b + 1, q0:q1], kvr, idx_c, qs_c[c], kl_c[c], T,
+                                   cfg.scale, o_lat=o_c, lse=t["lse"][b:b + 1, q0:q1],
+                                   workspace=ws, stream=s_cmp)
+                dsa.mla_gate_apply(t["x"][r0:r1], t["W_g"], o_c.view(q1 - q0, cfg.H, 512),
+                                   t["W_uv"], out=t["out"][r0:r1], workspace=ws, stream=s_cmp)
+                ev_done = torch.cuda.Event()
+                ev_done.record(s_cmp)
+                done[(b, c)] = ev_done
+                s_out.wait_event(ev_done)
+                with torch.cuda.stream(s_out):
+                    out_h[r0:r1].copy_(t["out"][r0:r1], non_blocking=True)
+                    ev_out = torch.cuda.Event()
+                    ev_out.record(s_out)
+                    drained[(b, c)] = ev_out
+        kf = torch.cuda.Event()
+        kf.record(s_cmp)
+        keys_free[p] = kf
 
-    for _ in range(2):
-        step()
+    for i in range(2):
+        step(i, i == 0)
     torch.cuda.synchronize(dev)
+    diff = out_h.to(dev).float() - ref_out.float()
+    rel_l2 = float(diff.norm() / ref_out.float().norm())
+    max_abs = float(diff.abs().max())
     K = max(2, min(args.steps, 10))
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
-    a.record(stream)
-    for _ in range(K):
-        step()
-    b.record(stream)
+    a.record(s_cmp)
+    for i in range(K):
+        step(i, i == 0)
+    s_cmp.wait_stream(s_out)
+    b_.record(s_cmp)
     torch.cuda.synchronize(dev)
-    el = max_over_ranks(a.elapsed_time(b) / 1e3, world)
+    el = max_over_ranks(a.elapsed_time(b_) / 1e3, world)
+    code, where, detail = dsa.read_device_status(ws)
+    if code != dsa.DSA_OK:
+        raise RuntimeError(f"e2e device status {code} at {where:#x} ({detail})")
     return {"value": N * world * K / el, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": K, "ms_per_step": el / K * 1e3}
+            "d2h_bytes_per_step": d2h, "steps": K, "ms_per_step": el / K * 1e3,
+            "pipeline": f"{B * nc} chunks of {C} queries; copy in, kernels and copy out on "
+                        "three streams",
+            "vs_step_output": {"rel_l2": rel_l2, "max_abs": max_abs}}
 
 
 def decode_bytes(lens, topk, H, H_I, D_I):
