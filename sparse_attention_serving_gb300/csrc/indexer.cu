@@ -12,8 +12,8 @@
 //   A CTA owns QT consecutive queries of one sequence (QT * H_I = 256 or 64
 //   accumulator columns) and streams every causal key tile of 128 keys:
 //     D^T[128 keys x QT*H_I] = K_tile[128 x D_I] . Q^T[D_I x QT*H_I]   (tcgen05, M=128)
-//   with TMEM double-buffered, so the head reduction of one tile overlaps the
-//   MMA of the next.  Each epilogue thread owns one key (a TMEM lane) and
+//   with four TMEM accumulator buffers, so the head reductions of one pair of
+//   tiles overlap the MMAs of the next.  Each epilogue thread owns one key (a TMEM lane) and
 //   reduces over heads without any cross-lane traffic; scores above the
 //   query's running threshold are appended to a per-query candidate buffer in
 //   shared memory.  When a buffer nears capacity a radix select (4 x 8-bit
