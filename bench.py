@@ -16,6 +16,12 @@ pinned host buffers copied in and the gated output copied out inside the
 timed region; ``roofline`` describes the dominant kernel (sparse MLA);
 ``cpu_baseline`` times the CPU oracle on a bounded sample of the workload.
 
+With the default workload the same line also carries two more of the pages'
+workloads, each timed on its own with its own roofline and clocks:
+``decode64`` (64 decode requests over paged caches, HBM-bound) and
+``chunk32k`` (a 32,768-token sequence prefilled as 4 chunks of 8,192 queries
+over a growing paged cache).  ``--no-extra`` leaves them out.
+
 Multi-GPU: ``torchrun --nproc-per-node N bench.py --gpus N``: every rank runs
 an independent replica (no collective on the data path; the path shards by
 sequence), timing is the max over ranks.
@@ -36,11 +42,13 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "DSA indexer+sparse-MLA tokens/s at T=8192,k=2048; % of TC / HBM roofline"
-# DRAM bytes (read + write) of one sparse_mla_kernel launch per query, from the
-# ncu capture summarised in profiles/sparse_mla_val4096.md (855 MB for 4,096
-# queries).  The traffic is q_lat + idx in and o_lat out, so it scales with the
-# number of queries; reset to None whenever the kernel changes.
-MLA_DRAM_BYTES_PER_QUERY = (491.475968e6 + 363.690240e6) / 4096
+CSRC = os.path.join(ROOT, "sparse_attention_serving_gb300", "csrc")
+# Measured DRAM traffic per unit of work for the dominant kernels, one record
+# per kernel: the ncu dram read + write bytes of one captured launch divided by
+# the units it processed, with the SHA-256 of the kernel's sources at the time
+# of the capture.  A record whose sources have changed since is not used
+# (traffic is reported as null).
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
 def parse():
@@ -50,8 +58,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="head8192",
-                    choices=["head8192", "val4096", "decode64", "decode16", "tiny"])
+                    choices=["head8192", "val4096", "decode64", "decode16", "tiny", "chunk32k"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only the chosen workload (no decode64 / chunk32k sub-objects)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=0, help="oracle sample size (0 = auto)")
     return ap.parse_args()
@@ -173,6 +183,63 @@ def measured_peaks():
         return {}
 
 
+def tensor_peaks(peaks):
+    """(burst, sustained, source) dense BF16 TFLOP/s.  A kernel timed on its own
+    for a fraction of a second is held against the burst figure; the sustained
+    one (a seconds-long loop under the power cap) is reported beside it."""
+    if peaks.get("bf16_tflops"):
+        return peaks["bf16_tflops"], peaks.get("bf16_tflops_sustained"), "measured"
+    return 1900.0, 1700.0, "fallback"
+
+
+def hbm_peak(peaks):
+    if peaks.get("hbm_gbs"):
+        return peaks["hbm_gbs"], "measured"
+    return 6800.0, "fallback"
+
+
+def _sources_sha(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def traffic_per_unit(kernel: str):
+    """(bytes per unit, capture note) of a kernel's measured DRAM traffic, or
+    (None, reason) when there is no record or the kernel has changed since."""
+    try:
+        rec = json.load(open(TRAFFIC_FILE))[kernel]
+    except Exception:
+        return None, "no ncu capture recorded for this kernel"
+    if _sources_sha(rec["sources"]) != rec["sources_sha256"]:
+        return None, "kernel sources changed since the ncu capture"
+    return rec["bytes_per_unit"], rec["capture"]
+
+
+def shared_config(cfg, world):
+    """The workload description both arms print (the same dict, key for key)."""
+    c = {"workload": cfg.name, "B": cfg.B, "T": cfg.T, "topk": cfg.topk, "H": cfg.H,
+         "H_I": cfg.H_I, "D_I": cfg.D_I, "latent": 576, "hid": cfg.hid,
+         "parallelism": f"replicas x{world}"}
+    if cfg.decode:
+        c.update({"T": 1, "context": [cfg.L_min, cfg.L_max], "page": 64,
+                  "step": "dsa_indexer_topk (decode) -> sparse_mla_fwd (split-K)",
+                  "l2": "caches 6.6 GB > L2; between timed steps a 256 MB buffer is "
+                        "rewritten, then another 256 MB read (no dirty lines left in L2)"})
+    elif cfg.chunk:
+        c.update({"chunk": cfg.chunk, "page": 64,
+                  "step": "per chunk: dsa_indexer_topk -> sparse_mla_fwd -> mla_gate_apply",
+                  "l2": "inputs larger than L2 each step (q_lat alone 3.6 GB)"})
+    else:
+        c.update({"step": "dsa_indexer_topk -> sparse_mla_fwd -> mla_gate_apply",
+                  "l2": "inputs larger than L2 each step (q_lat alone 1.81 GB at head8192); "
+                        "a sequence's latent rows stay L2-resident as they do in serving"})
+    return c
+
+
 # ----------------------------------------------------------------------------
 # CPU oracle sample
 # ----------------------------------------------------------------------------
@@ -229,6 +296,8 @@ def run_ours(args, rank, world, local):
     cfg = CONFIGS[args.workload]
     if cfg.decode:
         return run_decode(args, rank, world, local, cfg)
+    if cfg.chunk:
+        return run_chunked(args, dsa, world, local, cfg)
     B, T = cfg.B, cfg.T
     N = B * T
     d = prefill(cfg)
@@ -298,23 +367,19 @@ def run_ours(args, rank, world, local):
     t_gate = sum(e[2].elapsed_time(e[3]) for e in evs) / K / 1e3
 
     peaks = measured_peaks()
-    pk_sust = peaks.get("bf16_tflops_sustained")
-    pk_burst = peaks.get("bf16_tflops")
-    peak_src = "measured" if pk_sust else "fallback"
-    peak = pk_sust or 1700.0
+    peak, pk_sust, peak_src = tensor_peaks(peaks)
     f_idx = B * indexer_flops(T, cfg.topk, cfg.H_I, cfg.D_I)
     pairs = B * sel_pairs(T, cfg.topk)
     f_mla = pairs * mla_flops_per_pair(cfg.H)
     f_gate = gate_flops(N, cfg.hid, cfg.H, cfg.dv)
     tflops = lambda f, t: f / t / 1e12
     ach = tflops(f_mla, t_mla)
-    kernels = {
-        "dsa_indexer_topk": {"ms": t_idx * 1e3, "tflops": tflops(f_idx, t_idx),
-                             "frac": tflops(f_idx, t_idx) / peak, "flop": f_idx},
-        "sparse_mla_fwd": {"ms": t_mla * 1e3, "tflops": ach, "frac": ach / peak, "flop": f_mla},
-        "mla_gate_apply": {"ms": t_gate * 1e3, "tflops": tflops(f_gate, t_gate),
-                           "frac": tflops(f_gate, t_gate) / peak, "flop": f_gate},
-    }
+    kern = lambda f, t: {"ms": t * 1e3, "tflops": tflops(f, t), "frac": tflops(f, t) / peak,
+                         "frac_of_sustained": tflops(f, t) / pk_sust if pk_sust else None,
+                         "flop": f}
+    kernels = {"dsa_indexer_topk": kern(f_idx, t_idx), "sparse_mla_fwd": kern(f_mla, t_mla),
+               "mla_gate_apply": kern(f_gate, t_gate)}
+    bpq, tnote = traffic_per_unit("sparse_mla_kernel")
     tokens = N * world * K
     res = {
         "metric": METRIC,
@@ -329,22 +394,19 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) BF16 activations, N(0,0.02) weights)",
-        "config": {"workload": cfg.name, "B": B, "T": T, "topk": cfg.topk, "H": cfg.H,
-                   "H_I": cfg.H_I, "D_I": cfg.D_I, "latent": 576, "hid": cfg.hid,
-                   "step": "dsa_indexer_topk -> sparse_mla_fwd -> mla_gate_apply",
-                   "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 each step (q_lat alone 1.81 GB); the 9.4 MB "
-                         "latent KV of a sequence stays L2-resident as it does in serving"},
+        "config": shared_config(cfg, world),
         "value_indexer_mla_only": N * world / max(t_idx + t_mla, 1e-12),
         "kernels": kernels,
         "roofline": {"kernel": "sparse_mla_fwd", "bound": "tensor", "achieved": ach,
                      "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
-                     "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a step)",
-                     "peak_burst": pk_burst, "frac_of_burst": ach / pk_burst if pk_burst else None,
-                     "traffic": (MLA_DRAM_BYTES_PER_QUERY * N
-                                 if MLA_DRAM_BYTES_PER_QUERY is not None else None),
-                     "traffic_unit": "bytes per launch (ncu dram read+write on val4096, "
-                                     "scaled by queries)",
+                     "peak_source": f"{peak_src} bf16 burst (the kernel timed on its own "
+                                    "launches, each well under a second)",
+                     "peak_sustained": pk_sust,
+                     "frac_of_sustained": ach / pk_sust if pk_sust else None,
+                     "traffic": bpq * N if bpq is not None else None,
+                     "traffic_unit": "bytes per launch: ncu dram read+write per query of one "
+                                     "captured launch, times the launch's queries",
+                     "traffic_capture": tnote,
                      "algorithmic": f"{pairs} (query, selected key) pairs x 2*H*(576+512) FLOP"},
         "gpu_launches": K * launches_per_step(dsa, B, T, cfg),
         "clocks": clk,
@@ -361,6 +423,15 @@ def run_ours(args, rank, world, local):
                                           lse=lse, out=out))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(cfg, d, g, args.cpu_rows or 768)
+    if cfg.name == "head8192" and not args.no_extra:
+        # free the headline's buffers before the other workloads allocate theirs
+        del q_idx, w, k_idx, q_lat, kv, x, W_g, W_uv, idx, o_lat, lse, out, ws, krows, kvrows
+        d = g = None
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        res["decode64"] = run_decode(args, rank, world, local, CONFIGS["decode64"])
+        torch.cuda.empty_cache()
+        res["chunk32k"] = run_chunked(args, dsa, world, local, CONFIGS["chunk32k"])
     return res
 
 
@@ -585,6 +656,16 @@ def decode_bytes(lens, topk, H, H_I, D_I):
     return keys + rows + q + out
 
 
+def decode_mla_bytes(lens, topk, H):
+    """Compulsory HBM bytes of the decode sparse MLA alone: the selected latent
+    rows once, the queries and index lists in, the outputs out."""
+    import numpy as np
+    lens = np.asarray(lens, np.int64)
+    rows = int(np.minimum(lens, topk).sum()) * 576 * 2
+    per_req = H * 576 * 2 + topk * 4 + H * 512 * 2 + H * 4
+    return rows + len(lens) * per_req
+
+
 class L2Flush:
     """Empties L2 between timed steps: rewrites a 256 MB buffer (twice L2), then
     reads a second one, so the write-back of the rewrite's dirty lines happens
@@ -668,10 +749,11 @@ def run_decode(args, rank, world, local, cfg):
     t_mla = sum(e[1].elapsed_time(e[2]) for e in evs) / K / 1e3
     t_step = max_over_ranks(t_idx + t_mla, world)
     peaks = measured_peaks()
-    hbm = peaks.get("hbm_gbs") or 6800.0
+    hbm, hbm_src = hbm_peak(peaks)
     nbytes = decode_bytes(d["kv_len"], cfg.topk, cfg.H, cfg.H_I, cfg.D_I)
     ach = nbytes / t_step / 1e9
     idx_bytes = int(d["kv_len"].astype(np.int64).sum()) * cfg.D_I * 2
+    mla_bytes = decode_mla_bytes(d["kv_len"], cfg.topk, cfg.H)
     # the cache append that precedes a decode step (indexer-key LayerNorm + the
     # two row writes), timed on its own after the steps so that the caches the
     # steps read are not changed under them; not part of the step's number
@@ -695,28 +777,36 @@ def run_decode(args, rank, world, local, cfg):
     app_bytes = B * (cfg.D_I * 4 + 1152 + cfg.D_I * 2 + 1152)
     fp8 = run_decode_fp8(args, dev, cfg, d, k_pool, bt, qs, kl, q_idx, w, q_lat, kvrows, idx,
                          o_lat, lse, ws, flush, stream, S, hbm)
+    gbs = lambda nb, t: nb / t / 1e9
+    bps_mla, tnote = traffic_per_unit("sparse_mla_kernel_decode")
     res = {
         "metric": METRIC, "value": B * world / t_step, "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": t_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) BF16, paged caches with permuted pages)",
-        "config": {"workload": cfg.name, "B": B, "context": [cfg.L_min, cfg.L_max],
-                   "topk": cfg.topk, "H": cfg.H, "H_I": cfg.H_I, "D_I": cfg.D_I, "page": 64,
-                   "step": "dsa_indexer_topk (decode) -> sparse_mla_fwd (split-K)",
-                   "l2": "caches 6.6 GB > L2; between timed steps a 256 MB buffer is "
-                         "rewritten, then another 256 MB read (no dirty lines left in L2)"},
-        "kernels": {"dsa_indexer_topk": {"ms": t_idx * 1e3,
-                                         "gbs": idx_bytes / t_idx / 1e9,
-                                         "frac": idx_bytes / t_idx / 1e9 / hbm},
-                    "sparse_mla_fwd": {"ms": t_mla * 1e3},
-                    "dsa_cache_append": {"us": t_app * 1e6, "gbs": app_bytes / t_app / 1e9,
+        "config": shared_config(cfg, world),
+        "kernels": {"dsa_indexer_topk": {"ms": t_idx * 1e3, "bytes": idx_bytes,
+                                         "gbs": gbs(idx_bytes, t_idx),
+                                         "frac": gbs(idx_bytes, t_idx) / hbm},
+                    "sparse_mla_fwd": {"ms": t_mla * 1e3, "bytes": mla_bytes,
+                                       "gbs": gbs(mla_bytes, t_mla),
+                                       "frac": gbs(mla_bytes, t_mla) / hbm,
+                                       "traffic": (bps_mla * B if bps_mla is not None
+                                                   else None),
+                                       "traffic_capture": tnote,
+                                       "bytes_what": "selected latent rows (min(L,k) x 1,152 B "
+                                                     "per request) + q_lat + idx in, o_lat + "
+                                                     "lse out"},
+                    "dsa_cache_append": {"us": t_app * 1e6, "gbs": gbs(app_bytes, t_app),
                                          "bytes": app_bytes,
                                          "note": "timed separately, back to back; not in the step"}},
         "variants": {"fp8_indexer": fp8},
         "roofline": {"kernel": "decode step", "bound": "hbm", "achieved": ach, "peak": hbm,
                      "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+                     "peak_source": f"{hbm_src} HBM copy bandwidth",
                      "algorithmic": f"{nbytes} compulsory bytes per step"},
-        "gpu_launches": K * 4,
+        # scores + select, sparse MLA (+ split combine): no gate in the decode step
+        "gpu_launches": K * launches_per_step(dsa, B, 1, cfg),
         "clocks": clk,
     }
     return res
@@ -775,6 +865,126 @@ def run_decode_fp8(args, dev, cfg, d, k_pool, bt, qs, kl, q_idx, w, q_lat, kvrow
             "gpu_launches": K * 5}
 
 
+def run_chunked(args, dsa, world, local, cfg):
+    """Chunked long-context prefill: one sequence of cfg.T tokens whose queries
+    are processed in chunks of cfg.chunk against a paged cache (page 64, pages
+    permuted) that holds the keys up to the chunk's end.  One step = every
+    chunk's indexer + top-k, sparse MLA and gate, in order, through the C ABI."""
+    import numpy as np
+    import torch
+    from workloads import gate_inputs, page_table, prefill_keys, prefill_queries, to_pages
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    T, C = cfg.T, cfg.chunk
+    nc = T // C
+    keys = prefill_keys(cfg, T)
+    lens = np.full(cfg.B, T, np.int64)
+    bt_h, num_pages = page_table(cfg.seed, lens)
+    q = prefill_queries(cfg, 0, T)
+    g = gate_inputs(cfg, T)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    k_pool = up(to_pages(keys["k_idx"], lens, bt_h, num_pages))
+    kv_pool = up(to_pages(keys["kv"], lens, bt_h, num_pages))
+    bt = torch.from_numpy(bt_h).to(dev)
+    q_idx, w, q_lat = up(q["q_idx"]), up(q["w"]), up(q["q_lat"])
+    x, W_g, W_uv = up(g["x"]), up(g["W_g"]), up(g["W_uv"])
+    del q, g, keys
+    idx = torch.empty((1, T, cfg.topk), dtype=torch.int32, device=dev)
+    o_lat = torch.empty((1, T, cfg.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((1, T, cfg.H), dtype=torch.float32, device=dev)
+    out = torch.empty((T, cfg.H * cfg.dv), dtype=torch.bfloat16, device=dev)
+    krows, kvrows = dsa.Rows(k_pool, bt), dsa.Rows(kv_pool, bt)
+    ws_bytes = max(dsa.workspace_bytes(op, 1, C, T, h, cfg.topk)
+                   for op, h in ((dsa.OP_INDEXER_TOPK, cfg.H_I), (dsa.OP_SPARSE_MLA, cfg.H),
+                                 (dsa.OP_GATE, cfg.H)))
+    ws = dsa.new_workspace(ws_bytes, dev)
+    qs = [torch.tensor([c * C], dtype=torch.int32, device=dev) for c in range(nc)]
+    kl = [torch.tensor([(c + 1) * C], dtype=torch.int32, device=dev) for c in range(nc)]
+
+    def step(ev=None):
+        for c in range(nc):
+            q0, q1 = c * C, (c + 1) * C
+            e = ev[c] if ev is not None else None
+            if e is not None:
+                e[0].record(stream)
+            dsa.dsa_indexer_topk(q_idx[:, q0:q1], w[:, q0:q1], krows, qs[c], kl[c], cfg.topk, T,
+                                 out_idx=idx[:, q0:q1], workspace=ws)
+            if e is not None:
+                e[1].record(stream)
+            dsa.sparse_mla_fwd(q_lat[:, q0:q1], kvrows, idx[:, q0:q1], qs[c], kl[c], T, cfg.scale,
+                               o_lat=o_lat[:, q0:q1], lse=lse[:, q0:q1], workspace=ws)
+            if e is not None:
+                e[2].record(stream)
+            dsa.mla_gate_apply(x[q0:q1], W_g, o_lat[0, q0:q1], W_uv, out=out[q0:q1],
+                               workspace=ws)
+            if e is not None:
+                e[3].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    code, where, detail = dsa.read_device_status(ws)
+    if code != dsa.DSA_OK:
+        raise RuntimeError(f"chunked device status {code} at {where:#x} ({detail})")
+    K = max(2, min(args.steps, 10))
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nc)]
+           for _ in range(K)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(K):
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    code, where, detail = dsa.read_device_status(ws)
+    if code != dsa.DSA_OK:
+        raise RuntimeError(f"chunked device status {code} at {where:#x} ({detail})")
+    per = lambda a, b: [sum(evs[i][c][a].elapsed_time(evs[i][c][b]) for i in range(K)) / K / 1e3
+                        for c in range(nc)]
+    t_idx_c, t_mla_c, t_gate_c = per(0, 1), per(1, 2), per(2, 3)
+    t_idx, t_mla, t_gate = sum(t_idx_c), sum(t_mla_c), sum(t_gate_c)
+    t_step = max_over_ranks(t_idx + t_mla + t_gate, world)
+    peak, pk_sust, peak_src = tensor_peaks(measured_peaks())
+    f_idx = sum(t + 1 for t in range(cfg.topk, T)) * 2 * cfg.H_I * cfg.D_I
+    f_mla = sel_pairs(T, cfg.topk) * mla_flops_per_pair(cfg.H)
+    f_gate = gate_flops(T, cfg.hid, cfg.H, cfg.dv)
+    tf = lambda f, t: f / t / 1e12
+    ach = tf(f_mla, t_mla)
+    return {
+        "metric": METRIC, "value": T * world / t_step, "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": t_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) BF16 activations, N(0,0.02) weights; paged caches "
+                "with permuted pages)",
+        "config": shared_config(cfg, world),
+        "value_indexer_mla_only": T * world / (t_idx + t_mla),
+        "kernels": {
+            "dsa_indexer_topk": {"ms": t_idx * 1e3, "ms_per_chunk": [t * 1e3 for t in t_idx_c],
+                                 "tflops": tf(f_idx, t_idx), "frac": tf(f_idx, t_idx) / peak,
+                                 "flop": f_idx},
+            "sparse_mla_fwd": {"ms": t_mla * 1e3, "ms_per_chunk": [t * 1e3 for t in t_mla_c],
+                               "tflops": ach, "frac": ach / peak, "flop": f_mla},
+            "mla_gate_apply": {"ms": t_gate * 1e3, "tflops": tf(f_gate, t_gate),
+                               "frac": tf(f_gate, t_gate) / peak, "flop": f_gate}},
+        "roofline": {"kernel": "indexer + top-k + sparse MLA (all chunks)", "bound": "tensor",
+                     "achieved": tf(f_idx + f_mla, t_idx + t_mla), "peak": peak,
+                     "unit": "TFLOP/s", "frac": tf(f_idx + f_mla, t_idx + t_mla) / peak,
+                     "peak_source": f"{peak_src} bf16 burst", "peak_sustained": pk_sust,
+                     "traffic": None,
+                     "algorithmic": f"indexer {f_idx} FLOP (2*H_I*D_I per scored pair of a "
+                                    f"query with more than k causal keys) + sparse MLA {f_mla} "
+                                    "FLOP (2*H*(576+512) per selected pair)"},
+        "gpu_launches": K * nc * launches_per_step(dsa, 1, C, cfg),
+        "clocks": clk,
+    }
+
+
 # ----------------------------------------------------------------------------
 # reference arm: the CPU oracle, as it stands, on the box's host cores
 # ----------------------------------------------------------------------------
@@ -786,8 +996,8 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     cfg = CONFIGS[args.workload]
-    if cfg.decode:
-        return {"impl": "reference", "unavailable": "decode reference arm not wired"}
+    if cfg.decode or cfg.chunk:
+        return {"impl": "reference", "unavailable": "reference arm wired for unchunked prefill only"}
     d = prefill(cfg)
     g = gate_inputs(cfg, cfg.B * cfg.T)
     lib = oracle.load()
@@ -812,8 +1022,7 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": W, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) BF16 activations, N(0,0.02) weights)",
-        "config": {"workload": cfg.name, "B": cfg.B, "T": cfg.T, "topk": cfg.topk, "H": cfg.H,
-                   "H_I": cfg.H_I, "D_I": cfg.D_I, "latent": 576, "hid": cfg.hid},
+        "config": shared_config(cfg, world),
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -326,12 +326,16 @@ dsa_status_t dsa_indexer_topk_fp8(const uint8_t* q_codes, const float* q_scale, 
  *   - Scratch (the split-K partial results used when B*Tq is below the SM
  *     count) lives in one fixed 32 MiB array of device memory inside this
  *     library, held by every GPU that loads the library until the process
- *     exits.  Sizes whose partials do not fit (B*Tq*splits*H*513*4 bytes above
- *     32 MiB minus 256) are rejected with DSA_ERR_WORKSPACE_TOO_SMALL before
- *     anything is launched.  The call allocates and frees nothing.
- *   - The first call on a device looks up that array's device address (with
- *     the caller's current device); make that first call before any stream
- *     capture.
+ *     exits.  A split launch needs B*Tq*splits*H*(512*2 + 4) + 256 bytes, and
+ *     the library keeps B*Tq*splits at or below the SM count: with 96 heads
+ *     every split fits on parts with up to about 340 SMs.  Larger needs are
+ *     rejected with DSA_ERR_WORKSPACE_TOO_SMALL before anything is launched;
+ *     that is the only failure this fixed size adds.  The call allocates and
+ *     frees nothing.
+ *   - Every call looks up that array's device address on the caller's
+ *     current device (a lookup, no allocation).  The first call on a device
+ *     also loads this library's device code there; make that first call
+ *     before any stream capture.
  *   - Every call on a device shares the array and it keeps the last call's
  *     contents: two calls whose kernels may overlap on the GPU (different
  *     streams without ordering) race on it.  Serialise them.

@@ -249,7 +249,6 @@ typedef struct {
   double scale;
   const int64_t* rows;
   double *o, *lse;
-  int dense;
   const double* sink; /* [H] learnable sink logits (natural log), or NULL */
   int err;
 } mla_ctx;
@@ -264,24 +263,16 @@ static void mla_row(void* vctx, int64_t r) {
   double* lse = c->lse + r * (int64_t)c->H;
   if (t >= c->kv_len[b] || t >= c->S_max) { c->err = OR_BAD_ARG; return; }
 
-  /* the set of attended keys: the given indices (skipping -1), or all s <= t */
+  /* the set of attended keys: the given indices, skipping -1 */
   int n = 0;
-  int32_t* sel;
-  if (c->dense) {
-    n = (int)(t + 1);
-    sel = (int32_t*)malloc(sizeof(int32_t) * (size_t)n);
-    if (!sel) { c->err = OR_NOMEM; return; }
-    for (int s = 0; s < n; ++s) sel[s] = s;
-  } else {
-    const int32_t* ix = c->idx + flat * (int64_t)c->topk;
-    sel = (int32_t*)malloc(sizeof(int32_t) * (size_t)c->topk);
-    if (!sel) { c->err = OR_NOMEM; return; }
-    for (int j = 0; j < c->topk; ++j) {
-      int32_t s = ix[j];
-      if (s < 0) continue;
-      if (s > t || s >= c->kv_len[b]) { c->err = OR_BAD_INDEX; continue; }
-      sel[n++] = s;
-    }
+  const int32_t* ix = c->idx + flat * (int64_t)c->topk;
+  int32_t* sel = (int32_t*)malloc(sizeof(int32_t) * (size_t)c->topk);
+  if (!sel) { c->err = OR_NOMEM; return; }
+  for (int j = 0; j < c->topk; ++j) {
+    int32_t s = ix[j];
+    if (s < 0) continue;
+    if (s > t || s >= c->kv_len[b]) { c->err = OR_BAD_INDEX; continue; }
+    sel[n++] = s;
   }
   double* z = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
   if (!z) { free(sel); c->err = OR_NOMEM; return; }
@@ -321,14 +312,14 @@ static void mla_row(void* vctx, int64_t r) {
 static int mla_common(const uint16_t* q_lat, const uint16_t* kv, const int32_t* idx,
                       const int32_t* q_start, const int32_t* kv_len, int B, int Tq, int S_max,
                       int H, int topk, double scale, int64_t n_rows, const int64_t* rows,
-                      double* o, double* lse, int dense, const double* sink) {
+                      double* o, double* lse, const double* sink) {
   if (!q_lat || !kv || !q_start || !kv_len || !rows || !o || !lse) return OR_BAD_ARG;
-  if (!dense && (!idx || topk <= 0)) return OR_BAD_ARG;
+  if (!idx || topk <= 0) return OR_BAD_ARG;
   if (B <= 0 || Tq <= 0 || S_max <= 0 || H <= 0 || n_rows < 0) return OR_BAD_ARG;
   for (int64_t r = 0; r < n_rows; ++r)
     if (rows[r] < 0 || rows[r] >= (int64_t)B * Tq) return OR_BAD_ARG;
   mla_ctx c = {q_lat, kv, idx, q_start, kv_len, Tq, S_max, H, topk, scale,
-               rows, o, lse, dense, sink, OR_OK};
+               rows, o, lse, sink, OR_OK};
   parallel_rows(n_rows, mla_row, &c);
   return c.err;
 }
@@ -340,7 +331,7 @@ int oracle_sparse_mla(const uint16_t* q_lat, const uint16_t* kv, const int32_t* 
                       int H, int topk, double scale, int64_t n_rows, const int64_t* rows,
                       double* o, double* lse) {
   return mla_common(q_lat, kv, idx, q_start, kv_len, B, Tq, S_max, H, topk, scale, n_rows,
-                    rows, o, lse, 0, NULL);
+                    rows, o, lse, NULL);
 }
 
 /* The same with a learnable sink: sink [H] logits (natural log) that join the
@@ -352,15 +343,73 @@ int oracle_sparse_mla_sink(const uint16_t* q_lat, const uint16_t* kv, const int3
                            const int64_t* rows, double* o, double* lse) {
   if (!sink) return OR_BAD_ARG;
   return mla_common(q_lat, kv, idx, q_start, kv_len, B, Tq, S_max, H, topk, scale, n_rows,
-                    rows, o, lse, 0, sink);
+                    rows, o, lse, sink);
 }
 
-/* Dense causal MLA over every key s <= t: the dense-mask reference path. */
+/* Dense causal MLA over every key s <= t: the dense-mask reference path, with
+ * no index list at all.  Written as its own loops (keys outer, heads inner for
+ * the logits; then one normalisation per head) so that it does not share the
+ * sparse path's code: the "a sequence of at most k tokens keeps every causal
+ * key" check ("Kimi-K3.1-Pro", Implementation Limits, bullet 4) then compares
+ * two programs. */
+typedef struct {
+  const uint16_t *q, *kv;
+  const int32_t *q_start, *kv_len;
+  int Tq, S_max, H;
+  double scale;
+  const int64_t* rows;
+  double *o, *lse;
+  int err;
+} dense_ctx;
+
+static void dense_row(void* vctx, int64_t r) {
+  dense_ctx* c = (dense_ctx*)vctx;
+  const int64_t flat = c->rows[r];
+  const int b = (int)(flat / c->Tq), i = (int)(flat % c->Tq);
+  const int64_t t = (int64_t)c->q_start[b] + i;
+  if (t < 0 || t >= c->kv_len[b] || t >= c->S_max) { c->err = OR_BAD_ARG; return; }
+  const int64_t nk = t + 1;
+  const uint16_t* qrow = c->q + flat * c->H * (int64_t)RLAT;
+  const uint16_t* keys = c->kv + (int64_t)b * c->S_max * RLAT;
+  /* z[h * nk + s]: every head's logit against every causal key */
+  double* z = (double*)malloc(sizeof(double) * (size_t)(nk * c->H));
+  if (!z) { c->err = OR_NOMEM; return; }
+  for (int64_t s = 0; s < nk; ++s) {
+    const uint16_t* krow = keys + s * RLAT;
+    for (int h = 0; h < c->H; ++h) {
+      const uint16_t* qh = qrow + (int64_t)h * RLAT;
+      double acc = 0.0;
+      for (int d = 0; d < RLAT; ++d) acc += bf(qh[d]) * bf(krow[d]);
+      z[(int64_t)h * nk + s] = c->scale * acc;
+    }
+  }
+  for (int h = 0; h < c->H; ++h) {
+    const double* zh = z + (int64_t)h * nk;
+    double m = zh[0];
+    for (int64_t s = 1; s < nk; ++s) m = zh[s] > m ? zh[s] : m;
+    double denom = 0.0;
+    for (int64_t s = 0; s < nk; ++s) denom += exp(zh[s] - m);
+    double* oh = c->o + (r * c->H + h) * (int64_t)VLAT;
+    for (int d = 0; d < VLAT; ++d) {
+      double num = 0.0;
+      for (int64_t s = 0; s < nk; ++s) num += exp(zh[s] - m) * bf(keys[s * RLAT + d]);
+      oh[d] = num / denom;
+    }
+    c->lse[r * c->H + h] = m + log(denom);
+  }
+  free(z);
+}
+
 int oracle_dense_mla(const uint16_t* q_lat, const uint16_t* kv, const int32_t* q_start,
                      const int32_t* kv_len, int B, int Tq, int S_max, int H, double scale,
                      int64_t n_rows, const int64_t* rows, double* o, double* lse) {
-  return mla_common(q_lat, kv, NULL, q_start, kv_len, B, Tq, S_max, H, 0, scale, n_rows, rows,
-                    o, lse, 1, NULL);
+  if (!q_lat || !kv || !q_start || !kv_len || !rows || !o || !lse) return OR_BAD_ARG;
+  if (B <= 0 || Tq <= 0 || S_max <= 0 || H <= 0 || n_rows < 0) return OR_BAD_ARG;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= (int64_t)B * Tq) return OR_BAD_ARG;
+  dense_ctx c = {q_lat, kv, q_start, kv_len, Tq, S_max, H, scale, rows, o, lse, OR_OK};
+  parallel_rows(n_rows, dense_row, &c);
+  return c.err;
 }
 
 /* ------------------------------------------------------------------------- */

@@ -11,38 +11,35 @@
 // library routine.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "dsa_status.cuh"
 #include "internal.h"
 
 namespace {
 
 // 32 MiB of scratch, held by every GPU that loads the library until the
-// process exits.  Enough for the split-K partials of 64 decode requests with
-// 96 heads.
+// process exits.  The split count keeps (queries x splits) at or below the SM
+// count, and a (query, split) pair needs H x 512 BF16 outputs and H FP32
+// log-sum-exps: with 96 heads at most SMs x 98,688 bytes, which fits for any
+// part with up to about 340 SMs.
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
 // In host code `g_noalloc_scratch` is only a host-side stand-in for the device
-// array; the device address must be looked up once per device, with that
-// device current.
+// array: passing it to a kernel would fault (or, where the GPU can reach host
+// memory, silently use the wrong memory).  The device address is looked up on
+// every call, with the caller's device current.  The lookup allocates nothing,
+// and a fresh lookup stays right after cudaDeviceReset or when the caller
+// switches contexts, where an address kept from an earlier call would point at
+// memory that is no longer mapped.  The first lookup on a device also loads
+// this library's device code there, which is why the first call should come
+// before any stream capture.
 dsa_status_t scratch_on_current_device(unsigned char** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return DSA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return DSA_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+    (void)cudaGetLastError();  // the failed lookup must not stick to later launches
+    return DSA_ERR_CUDA;
   }
-  *out = static_cast<unsigned char*>(g_scratch_addr[dev]);
+  *out = static_cast<unsigned char*>(p);
   return DSA_OK;
 }
 

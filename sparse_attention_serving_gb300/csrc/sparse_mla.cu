@@ -136,7 +136,7 @@ struct Params {
   uint16_t* o_lat;
   float* lse;
   const float* sink;  // [H] learnable sink logits (natural log), or null
-  float* part_o;     // [q, split, H, 512] normalised partial outputs (nsplit > 1)
+  uint16_t* part_o;  // [q, split, H, 512] normalised partial outputs, BF16 (nsplit > 1)
   float* part_lse;   // [q, split, H] partial log2-sum-exp
   uint32_t* status;
 };
@@ -803,8 +803,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       named_bar_sync(1, NSMX);
       // O^T tile i (128 dims x H heads): each thread owns one dim of the two tiles
       // of its half (0: tiles 0-1, 1: tiles 2-3) and writes that dim of every
-      // head straight to global memory (a warp covers 32 consecutive dims: 64
-      // contiguous bytes per head in BF16, 128 in FP32).  No shared-memory
+      // head straight to global memory as BF16 (a warp covers 32 consecutive
+      // dims: 64 contiguous bytes per head).  No shared-memory
       // staging: the pair slots already hold the next unit's rows.
       const int64_t pq = static_cast<int64_t>(U.qflat) * p.nsplit + U.sp;
       const int dloc = 32 * sub + lane;
@@ -833,10 +833,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 ob[e * kVlat] = __bfloat16_as_ushort(
                     __float2bfloat16_rn(have_o ? __uint_as_float(r[e]) * iv[e] : 0.f));
           } else {
-            float* ob = p.part_o + (pq * H + c0) * kVlat + 128 * i + dloc;
+            uint16_t* ob = p.part_o + (pq * H + c0) * kVlat + 128 * i + dloc;
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              if (c0 + e < H) ob[e * kVlat] = have_o ? __uint_as_float(r[e]) * iv[e] : 0.f;
+              if (c0 + e < H)
+                ob[e * kVlat] = __bfloat16_as_ushort(
+                    __float2bfloat16_rn(have_o ? __uint_as_float(r[e]) * iv[e] : 0.f));
           }
         }
       }
@@ -863,10 +865,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
-// Merge the per-split partial results: lse = log2 (sum_p 2^lse_p [+ 2^sink]),
-// o = sum_p 2^(lse_p - lse) o_p; a learnable sink (no value row) enters here
-// once, not in every split.  One thread per (query, head, 4 dims).
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_o,
+// Merge the per-split partial results (o_p normalised and stored as BF16, lse_p
+// FP32): lse = log2 (sum_p 2^lse_p [+ 2^sink]), o = sum_p 2^(lse_p - lse) o_p,
+// summed in FP32; a learnable sink (no value row) enters here once, not in
+// every split.  One thread per (query, head, 4 dims).
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ part_o,
                                                       const float* __restrict__ part_lse,
                                                       int nq, int H, int nsplit,
                                                       const float* __restrict__ sink,
@@ -889,9 +892,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       if (ls == -INFINITY) continue;
       const float wgt = exp2f(ls - mx);
       wsum += wgt;
-      const float4 v =
-          *reinterpret_cast<const float4*>(part_o + ((q * nsplit + s) * H + h) * kVlat + d4);
-      acc[0] += wgt * v.x; acc[1] += wgt * v.y; acc[2] += wgt * v.z; acc[3] += wgt * v.w;
+      const uint2 v =
+          *reinterpret_cast<const uint2*>(part_o + ((q * nsplit + s) * H + h) * kVlat + d4);
+      acc[0] += wgt * __uint_as_float(v.x << 16);
+      acc[1] += wgt * __uint_as_float(v.x & 0xffff0000u);
+      acc[2] += wgt * __uint_as_float(v.y << 16);
+      acc[3] += wgt * __uint_as_float(v.y & 0xffff0000u);
     }
     if (s2 != -INFINITY) wsum += exp2f(s2 - mx);
   }
@@ -918,8 +924,9 @@ size_t sparse_mla_scratch_bytes(int B, int Tq, int H, int topk) {
   (void)topk;
   const int ns = mla_nsplit(B, Tq);
   if (ns <= 1) return 0;
+  // per (query, split): H x 512 BF16 outputs and H FP32 log-sum-exps
   const size_t nq = static_cast<size_t>(B) * Tq;
-  return nq * ns * H * (kVlat + 1) * sizeof(float) + 256;
+  return nq * ns * H * (kVlat * sizeof(uint16_t) + sizeof(float)) + 256;
 }
 
 template <int H>
@@ -954,8 +961,8 @@ static dsa_status_t launch_h(const SparseMlaArgs& a, cudaStream_t stream) {
     const size_t nq = static_cast<size_t>(a.B) * a.Tq;
     if (a.scratch == nullptr || a.scratch_bytes < sparse_mla_scratch_bytes(a.B, a.Tq, H, a.topk))
       return DSA_ERR_WORKSPACE_TOO_SMALL;
-    p.part_o = static_cast<float*>(a.scratch);
-    p.part_lse = p.part_o + nq * ns * H * kVlat;
+    p.part_o = static_cast<uint16_t*>(a.scratch);
+    p.part_lse = reinterpret_cast<float*>(p.part_o + nq * ns * H * kVlat);
   }
   auto kern = sparse_mla_kernel<H>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=

@@ -54,10 +54,22 @@ def test_prefill_fullsize(dsa, name):
     check_indexer_rows(gi, d["q_idx"], d["w"], d["k_idx"], d["q_start"], d["kv_len"], cfg.topk,
                        rows, name)
     ol = to_u16(o_lat)
+    # the persistent sparse MLA kernel: CTA c takes queries c, c + P, c + 2P, ...
+    # (P = SM count), and each unit's start overlaps the previous unit's tail, so
+    # check the first two and the last unit of a few CTAs as well
+    P = torch.cuda.get_device_properties(0).multi_processor_count
+    unit_rows = []
+    for c in (0, 1, P // 2, P - 1):
+        last = c + P * ((N - 1 - c) // P)
+        unit_rows += [c, c + P, last]
+    mla_rows = np.unique(np.concatenate([rows, np.array(unit_rows, np.int64)]))
     check_mla_rows(ol, lse.cpu().numpy(), d["q_lat"], d["kv"], gi, d["q_start"], d["kv_len"],
-                   cfg.scale, rows, name)
+                   cfg.scale, mla_rows, name)
+    # the gate: every row of three whole 128-token tiles (first, middle, last)
+    tiles = [0, (N // 128 // 2) * 128, N - 128]
+    gate_rows = np.concatenate([np.arange(t0, t0 + 128) for t0 in tiles]).astype(np.int64)
     check_gate_rows(to_u16(out), g["x"], g["W_g"], ol.reshape(N, cfg.H, 512), g["W_uv"],
-                    rows[:12], name)
+                    gate_rows, name)
 
 
 def test_chunked_32k_fullsize(dsa):
@@ -94,13 +106,18 @@ def test_decode64_fullsize(dsa):
     torch.cuda.synchronize()
     gi = idx.cpu().numpy()
     ol, ls = to_u16(o_lat), lse.cpu().numpy()
-    for b in (0, 17, 63):
+    # the split sparse MLA cuts the 64 x 32 list blocks into one contiguous range
+    # per CTA, so each request's partials come from 3 or 4 CTAs with different
+    # range boundaries: check the attention of a dozen requests spread over the
+    # batch, the indexer of three
+    for b in (0, 1, 2, 9, 17, 30, 31, 32, 47, 55, 62, 63):
         L = int(d["kv_len"][b])
-        k_log = from_pages(d["k_pool"], d["block_table"], b, L)[None]
         kv_log = from_pages(d["kv_pool"], d["block_table"], b, L)[None]
         one = lambda a: a[b:b + 1]
-        check_indexer_rows(one(gi), one(d["q_idx"]), one(d["w"]), k_log, one(d["q_start"]),
-                           one(d["kv_len"]), cfg.topk, np.array([0]), f"decode req {b}")
+        if b in (0, 17, 63):
+            k_log = from_pages(d["k_pool"], d["block_table"], b, L)[None]
+            check_indexer_rows(one(gi), one(d["q_idx"]), one(d["w"]), k_log, one(d["q_start"]),
+                               one(d["kv_len"]), cfg.topk, np.array([0]), f"decode req {b}")
         check_mla_rows(one(ol), one(ls), one(d["q_lat"]), kv_log, one(gi), one(d["q_start"]),
                        one(d["kv_len"]), cfg.scale, np.array([0]), f"decode req {b}")
 

@@ -31,8 +31,13 @@ MUTANTS = {
     "gate_sign_flipped": ("o[col] = u / (1.0 + exp(-g));", "o[col] = u / (1.0 + exp(g));"),
     "explicit_value_uses_key_weight": ("acc += Wv[(int64_t)e * c->R + d] * ck[d];",
                                        "acc += Wk[(int64_t)e * c->R + d] * ck[d];"),
-    "sparse_ignores_minus_one_wrongly": ("int32_t s = ix[j];\n      if (s < 0) continue;\n      if (s > t",
-                                         "int32_t s = ix[j];\n      if (s < 0) s = 0;\n      if (s > t"),
+    "sparse_ignores_minus_one_wrongly": ("int32_t s = ix[j];\n    if (s < 0) continue;\n    if (s > t",
+                                         "int32_t s = ix[j];\n    if (s < 0) s = 0;\n    if (s > t"),
+    "dense_excludes_self": ("const int64_t nk = t + 1;", "const int64_t nk = t > 0 ? t : 1;"),
+    "dense_rope_dims_dropped": ("for (int d = 0; d < RLAT; ++d) acc += bf(qh[d]) * bf(krow[d]);",
+                                "for (int d = 0; d < VLAT; ++d) acc += bf(qh[d]) * bf(krow[d]);"),
+    "dense_scale_dropped": ("z[(int64_t)h * nk + s] = c->scale * acc;",
+                            "z[(int64_t)h * nk + s] = acc;"),
     "layernorm_sample_variance": ("    var /= D;\n", "    var /= (D - 1);\n"),
     "layernorm_eps_dropped": ("const double inv = 1.0 / sqrt(var + eps);",
                               "const double inv = 1.0 / sqrt(var);"),

@@ -12,9 +12,10 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import bf, i32, to_u16
+from gpu_helpers import bf, check_mla_rows, i32, to_u16
 from parity import check_close, check_lse
-from workloads import Config, bf16_to_f32, normal_bf16, page_table, prefill_queries, to_pages
+from workloads import (Config, bf16_to_f32, from_pages, normal_bf16, page_table, prefill_queries,
+                       to_pages)
 
 pytestmark = pytest.mark.gpu
 
@@ -60,6 +61,17 @@ def _noalloc(dsa, q_lat, rows, idx, qs, kl, S, scale, status=None):
     return rc, o, lse
 
 
+def _check_oracle(o, l, q_lat, kv_pool, bt, lens, idx, scale, what):
+    """Every request of the decode case against the float64 oracle, each over its
+    own logical rows read back from the page pool."""
+    for b in range(len(lens)):
+        L = int(lens[b])
+        kv_log = from_pages(kv_pool, bt, b, L)[None]
+        one = lambda a: a[b:b + 1]
+        check_mla_rows(one(to_u16(o)), one(l.cpu().numpy()), one(q_lat), kv_log, one(idx),
+                       one(lens - 1), one(lens), scale, np.array([0]), f"{what} req {b}")
+
+
 def test_noalloc_matches_workspace_entry_point_twice(dsa):
     for call, seed in enumerate((21, 22)):  # two calls in a row, different inputs
         cfg, q_lat, kv_pool, bt, lens, idx, S = _decode_case(seed)
@@ -73,3 +85,64 @@ def test_noalloc_matches_workspace_entry_point_twice(dsa):
         assert int(status[0]) == 0
         check_close(bf16_to_f32(to_u16(o)), bf16_to_f32(to_u16(o_ref)), f"call {call} o_lat")
         check_lse(l.cpu().numpy(), l_ref.cpu().numpy(), f"call {call} lse")
+        # and against the oracle itself, not only against the other entry point
+        _check_oracle(o, l, q_lat, kv_pool, bt, lens, idx, cfg.scale, f"call {call}")
+
+
+def test_noalloc_without_status_pointer(dsa):
+    """device_status = NULL: errors go to the array's own header, which the call
+    clears first; the output must still match the workspace entry point."""
+    cfg, q_lat, kv_pool, bt, lens, idx, S = _decode_case(23, B=3)
+    qd, kvr = bf(q_lat), dsa.Rows(bf(kv_pool), i32(bt))
+    ix, qs, kl = i32(idx), i32(lens - 1), i32(lens)
+    o_ref, l_ref = dsa.sparse_mla_fwd(qd, kvr, ix, qs, kl, S, cfg.scale)
+    for _ in range(2):
+        rc, o, l = _noalloc(dsa, qd, kvr, ix, qs, kl, S, cfg.scale, None)
+        assert rc == dsa.DSA_OK, dsa.status_string(rc)
+        torch.cuda.synchronize()
+        check_close(bf16_to_f32(to_u16(o)), bf16_to_f32(to_u16(o_ref)), "no status o_lat")
+        check_lse(l.cpu().numpy(), l_ref.cpu().numpy(), "no status lse")
+
+
+def test_noalloc_unsplit_prefill(dsa):
+    """B*Tq at or above the SM count: no split, so no scratch is used at all."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T, topk = sms + 37, 64
+    cfg = Config("noalloc_pf", B=1, T=T, topk=topk, H_I=4, D_I=64, H=8, hid=1024, seed=31)
+    q = prefill_queries(cfg, 0, T)
+    kv = normal_bf16(cfg.seed, "kv", (1, T, 576))
+    rng = np.random.default_rng(31)
+    idx = np.full((1, T, topk), -1, np.int32)
+    for t in range(T):
+        n = min(t + 1, topk)
+        idx[0, t, :n] = rng.choice(t + 1, n, replace=False)
+    qd, kvr = bf(q["q_lat"]), dsa.Rows(bf(kv))
+    ix, qs, kl = i32(idx), i32([0]), i32([T])
+    o_ref, l_ref = dsa.sparse_mla_fwd(qd, kvr, ix, qs, kl, T, cfg.scale)
+    status = torch.zeros(3, dtype=torch.int32, device="cuda")
+    rc, o, l = _noalloc(dsa, qd, kvr, ix, qs, kl, T, cfg.scale, status)
+    assert rc == dsa.DSA_OK, dsa.status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+    check_close(bf16_to_f32(to_u16(o)), bf16_to_f32(to_u16(o_ref)), "unsplit o_lat")
+    check_lse(l.cpu().numpy(), l_ref.cpu().numpy(), "unsplit lse")
+    rows = np.array([0, 1, 63, 64, T // 2, T - 1])
+    check_mla_rows(to_u16(o), l.cpu().numpy(), q["q_lat"], kv, idx, np.array([0]),
+                   np.array([T]), cfg.scale, rows, "unsplit")
+
+
+def test_noalloc_bad_index_recorded(dsa):
+    """A non-causal entry is flagged in the caller's status and left out."""
+    cfg, q_lat, kv_pool, bt, lens, idx, S = _decode_case(24, B=2)
+    bad = idx.copy()
+    bad[1, 0, 5] = int(lens[1]) + 3          # beyond the query position
+    qd, kvr = bf(q_lat), dsa.Rows(bf(kv_pool), i32(bt))
+    qs, kl = i32(lens - 1), i32(lens)
+    status = torch.zeros(3, dtype=torch.int32, device="cuda")
+    rc, o, l = _noalloc(dsa, qd, kvr, i32(bad), qs, kl, S, cfg.scale, status)
+    assert rc == dsa.DSA_OK, dsa.status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status[0]) == dsa.DSA_ERR_BAD_INDEX
+    kept = bad.copy()
+    kept[1, 0, 5] = -1
+    _check_oracle(o, l, q_lat, kv_pool, bt, lens, kept, cfg.scale, "bad index")
