@@ -64,6 +64,17 @@ def parse():
                     help="time only the chosen workload (no decode64 / chunk32k sub-objects)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=0, help="oracle sample size (0 = auto)")
+    ap.add_argument("--record-traffic", metavar="NCU_CSV",
+                    help="store a kernel's measured DRAM bytes per unit from an ncu --csv log "
+                         "(dram__bytes_read.sum / write.sum of one launch) and exit")
+    ap.add_argument("--traffic-kernel", default="sparse_mla_kernel",
+                    help="kernel-name substring to pick in the ncu log")
+    ap.add_argument("--traffic-key", default=None, help="record name (default: the kernel)")
+    ap.add_argument("--traffic-units", type=float, default=0.0,
+                    help="units the captured launch processed (queries, or requests)")
+    ap.add_argument("--traffic-launch", type=int, default=0,
+                    help="which matching launch of the log to use (0 = first)")
+    ap.add_argument("--traffic-note", default="", help="how the capture was taken")
     return ap.parse_args()
 
 
@@ -217,6 +228,49 @@ def traffic_per_unit(kernel: str):
     if _sources_sha(rec["sources"]) != rec["sources_sha256"]:
         return None, "kernel sources changed since the ncu capture"
     return rec["bytes_per_unit"], rec["capture"]
+
+
+# sources whose change invalidates a kernel's traffic record
+TRAFFIC_SOURCES = {
+    "sparse_mla_kernel": ["sparse_mla.cu", "sm103.cuh", "internal.h", "dsa_status.cuh"],
+    "sparse_mla_kernel_decode": ["sparse_mla.cu", "sm103.cuh", "internal.h", "dsa_status.cuh"],
+}
+
+
+def record_traffic(args):
+    """Read one launch's dram__bytes_read.sum + dram__bytes_write.sum for a kernel
+    from an ncu --csv log and store bytes per unit with the SHA-256 of the
+    kernel's sources (so the record goes stale when they change)."""
+    import csv
+    rows = list(csv.reader(open(args.record_traffic)))
+    hdr = next(i for i, r in enumerate(rows) if "Kernel Name" in r and "Metric Name" in r)
+    H = rows[hdr]
+    ki, ii, mi = H.index("Kernel Name"), H.index("ID"), H.index("Metric Name")
+    vi, ui = H.index("Metric Value"), H.index("Metric Unit")
+    launches = {}
+    for r in rows[hdr + 1:]:
+        if len(r) <= vi or args.traffic_kernel not in r[ki]:
+            continue
+        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}.get(r[ui], 1)
+        launches.setdefault(r[ii], {})[r[mi]] = float(r[vi].replace(",", "")) * scale
+    ids = sorted(launches, key=int)
+    m = launches[ids[args.traffic_launch]]
+    total = m["dram__bytes_read.sum"] + m["dram__bytes_write.sum"]
+    key = args.traffic_key or args.traffic_kernel
+    src = TRAFFIC_SOURCES[key]
+    try:
+        recs = json.load(open(TRAFFIC_FILE))
+    except Exception:
+        recs = {}
+    recs[key] = {"bytes_per_unit": total / args.traffic_units, "sources": src,
+                 "sources_sha256": _sources_sha(src),
+                 "capture": f"{args.traffic_note}: dram read {m['dram__bytes_read.sum']:.0f} + "
+                            f"write {m['dram__bytes_write.sum']:.0f} bytes over "
+                            f"{args.traffic_units:g} units"}
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(recs, f, indent=1, sort_keys=True)
+        f.write("\n")
+    print(json.dumps({key: recs[key]}))
 
 
 def shared_config(cfg, world):
@@ -1031,6 +1085,9 @@ def run_reference(args, rank, world):
 
 def main():
     args = parse()
+    if args.record_traffic:
+        record_traffic(args)
+        return
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         res = run_reference(args, rank, world)

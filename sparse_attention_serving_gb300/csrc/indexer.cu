@@ -8,17 +8,21 @@
 // a query with at most k causal keys keeps all of them, Implementation Limits,
 // bullet 4).
 //
-// Prefill (Tq > 1): one fused kernel, no score buffer in global memory.
-//   A CTA owns QT consecutive queries of one sequence (QT * H_I = 256 or 64
-//   accumulator columns) and streams every causal key tile of 128 keys:
+// Prefill (Tq > 1): one fused, persistent kernel, no score buffer in global
+// memory.  One CTA per SM walks work items -- tiles of QT consecutive queries
+// of one sequence (QT * H_I = 128 or 64 accumulator columns), heaviest first --
+// and streams every causal key tile of 128 keys of each item:
 //     D^T[128 keys x QT*H_I] = K_tile[128 x D_I] . Q^T[D_I x QT*H_I]   (tcgen05, M=128)
 //   with four TMEM accumulator buffers, so the head reductions of one pair of
-//   tiles overlap the MMAs of the next.  Each epilogue thread owns one key (a TMEM lane) and
-//   reduces over heads without any cross-lane traffic; scores above the
-//   query's running threshold are appended to a per-query candidate buffer in
-//   shared memory.  When a buffer nears capacity a radix select (4 x 8-bit
-//   digits over order-preserving keys) keeps the top k and raises the
-//   threshold to the k-th score.  The final select writes the indices.
+//   tiles overlap the MMAs of the next; the barrier phases run off per-CTA
+//   tile counters, so the next item's query load and first MMAs overlap the
+//   current item's final selections.  Each epilogue thread owns one key (a
+//   TMEM lane) and reduces over heads without any cross-lane traffic; scores
+//   above the query's running threshold are appended to a per-query candidate
+//   buffer in shared memory.  When a buffer nears capacity a radix select
+//   (11-bit digits over order-preserving keys, candidates held in registers)
+//   keeps the top k and raises the threshold to the k-th score.  The final
+//   select writes the indices.
 //
 // FP8 variant (E4M3 code rows with one FP32 scale per key and per query head;
 // "Kimi-K3.1-Pro", Implementation Limits, bullet 2 contrasts the BF16 indexer
@@ -63,14 +67,18 @@ struct Cfg {
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_SC = OFF_K + NST * K_STAGE;
   static constexpr int OFF_W = OFF_SC + NSC * BKEY * 4;
-  // barriers: Q, K full [NST], K empty [NST], D full [4], D empty [4], drain,
-  // scale full [NSC], scale empty [NSC]
-  static constexpr int BQ = 0, BKF = 1, BKE = BKF + NST, BDF = BKE + NST, BDE = BDF + 4,
-                       BDRAIN = BDE + 4, BSF = BDRAIN + 1, BSE = BSF + NSC, NBARS = BSE + NSC;
+  // barriers: Q full, Q empty, K full [NST], K empty [NST], D full [4], D empty
+  // [4], drain, scale full [NSC], scale empty [NSC]
+  static constexpr int BQ = 0, BQE = 1, BKF = 2, BKE = BKF + NST, BDF = BKE + NST,
+                       BDE = BDF + 4, BDRAIN = BDE + 4, BSF = BDRAIN + 1, BSE = BSF + NSC,
+                       NBARS = BSE + NSC;
   static_assert(NBARS <= 48, "barrier block");
   static_assert(4 * N <= 512, "four accumulator buffers in TMEM");
   static constexpr int OFF_MISC = OFF_W + QT * H_I * 4;
-  static constexpr int MISC_BYTES = 4096;
+  // barriers (48 x 8 B), flags, per-query counts and thresholds, then the
+  // selection scratch (RBINS histogram bins and 16 counters)
+  static constexpr int MISC_HDR = 1024;
+  static constexpr int MISC_BYTES = MISC_HDR + (2048 + 16) * 4;
   static constexpr int OFF_CAND = OFF_MISC + MISC_BYTES;
   static constexpr int AVAIL = 232448 - 1024 - OFF_CAND;
   static constexpr int CAP_RAW = (AVAIL / (QT * 8)) / 32 * 32;
@@ -91,7 +99,7 @@ struct Params {
   int64_t seq_stride;
   int32_t max_pages, num_pages;
   int paged;
-  int Tq, topk, max_kv_len, ntq;  // ntq = query tiles per sequence
+  int B, Tq, topk, max_kv_len, ntq;  // ntq = query tiles per sequence
   int32_t* out_idx;
   uint32_t* status;
 };
@@ -105,116 +113,174 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
 }
 __device__ __forceinline__ bool vflag(const volatile int* p) { return *p != 0; }
 
-// Keep exactly `k` of the `n` candidates of one query (the k largest scores;
-// ties at the cut are broken arbitrarily) and return the k-th score.  Called
-// by all epilogue threads together; `gtid` in [0, NEPI*32).
+// ---------------------------------------------------------------------------
+// Radix selection of the k largest candidates of one query, by all NEPI*32
+// epilogue threads together (named barrier 1).  Scores are compared as
+// order-preserving 32-bit keys.  The digits start at the highest bit where the
+// smallest and the largest key differ and are RBITS wide, so the first
+// histogram already spreads the candidates; the descent stops as soon as the
+// bin holding the k-th key is kept whole (typically after one or two passes).
+// Ties at the cut are broken arbitrarily.
 //
-// Radix select over order-preserving 32-bit keys.  The candidates of a query
-// share their top bits (sign, most of the exponent), so the digits start at the
-// highest bit where the smallest and largest key differ (so the first digit
-// already spreads them over the bins), and the search stops as soon as the bin
-// holding the k-th key is kept whole.
-template <int EPT>
-__device__ float select_topk(float* cs, int32_t* ci, int n, int k, int gtid, int* hist,
-                             int* sel, int* ctr) {
-  uint32_t key[EPT];
-  int32_t id[EPT];
-  constexpr int G = NEPI * 32;
-  const int lane = gtid & 31;
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
+// Scratch (shared memory): hist[RBINS] and ctr[16]:
+//   ctr[0] smallest key, ctr[1] largest key, ctr[2] chosen bin, ctr[3] count
+//   above it, ctr[4] count in it, ctr[5..12] warp totals, ctr[15] smallest
+//   kept key.
+// ---------------------------------------------------------------------------
+constexpr int RBITS = 11;
+constexpr int RBINS = 1 << RBITS;
+constexpr int SEL_G = NEPI * 32;           // selecting threads
+constexpr int SEL_CTR = 16;
+
+// Bin of the need-th largest element (bins ordered by value, counted from the
+// top): ctr[2] = bin, ctr[3] = elements in higher bins, ctr[4] = elements in it.
+__device__ __forceinline__ void find_bin(const int* hist, int need, int gtid, int* ctr) {
+  constexpr int PER = RBINS / SEL_G;
+  static_assert(PER == 8, "two 16-byte loads of bins per thread");
+  const int lane = gtid & 31, w = gtid >> 5;
+  // thread t owns bins RBINS-1-8t down to RBINS-8-8t: one contiguous, 32-byte
+  // aligned block, read as two 16-byte loads (c[e] = bin RBINS-1-8t-e)
+  const int4* hb = reinterpret_cast<const int4*>(hist + RBINS - PER * (gtid + 1));
+  const int4 v0 = hb[0], v1 = hb[1];
+  int c[PER] = {v1.w, v1.z, v1.y, v1.x, v0.w, v0.z, v0.y, v0.x};
+  int tot = 0;
 #pragma unroll
-  for (int u = 0; u < EPT; ++u) {
-    const int e = gtid + u * G;
-    key[u] = e < n ? order_key(cs[e]) : 0u;
-    id[u] = e < n ? ci[e] : -1;
-    if (id[u] >= 0) {
-      kmin = min(kmin, key[u]);
-      kmax = max(kmax, key[u]);
+  for (int e = 0; e < PER; ++e) tot += c[e];
+  int incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) ctr[5 + w] = incl;
+  named_bar_sync(1, SEL_G);
+#pragma unroll
+  for (int ww = 0; ww < NEPI; ++ww)
+    if (ww < w) incl += ctr[5 + ww];
+  int run = incl - tot;
+  if (run < need && need <= incl) {
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      if (run < need && need <= run + c[e]) {
+        ctr[2] = RBINS - 1 - PER * gtid - e;
+        ctr[3] = run;
+        ctr[4] = c[e];
+      }
+      run += c[e];
     }
   }
+  named_bar_sync(1, SEL_G);
+}
+
+// The radix descent over keys delivered by `each(f)`, which calls f(key, valid)
+// for this thread's elements (the same elements on every call).  On return the
+// k-th largest key matches `prefix` on the bits of `pmask`; every element with
+// (key & pmask) > prefix is kept, and `need` of those equal to it.
+template <class Each>
+__device__ __forceinline__ void radix_descent(Each each, int k, int gtid, int* hist, int* ctr,
+                                              uint32_t& prefix, uint32_t& pmask, int& need) {
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  each([&](uint32_t key, bool valid) {
+    if (valid) {
+      kmin = min(kmin, key);
+      kmax = max(kmax, key);
+    }
+  });
   kmin = __reduce_min_sync(0xffffffffu, kmin);
   kmax = __reduce_max_sync(0xffffffffu, kmax);
-  if (gtid == 0) {
-    ctr[2] = static_cast<int>(0xffffffffu);
-    ctr[3] = 0;
+  if ((gtid & 31) == 0) {
+    atomicMin(reinterpret_cast<unsigned*>(&ctr[0]), kmin);
+    atomicMax(reinterpret_cast<unsigned*>(&ctr[1]), kmax);
   }
-  named_bar_sync(1, G);
-  if (lane == 0) {
-    atomicMin(reinterpret_cast<unsigned*>(&ctr[2]), kmin);
-    atomicMax(reinterpret_cast<unsigned*>(&ctr[3]), kmax);
-  }
-  named_bar_sync(1, G);
-  const uint32_t lo = static_cast<uint32_t>(ctr[2]), hi = static_cast<uint32_t>(ctr[3]);
-  const uint32_t diff = lo ^ hi;
-  uint32_t prefix, mask;
-  int need = k;
-  if (diff == 0u) {
+  named_bar_sync(1, SEL_G);
+  const uint32_t lo = static_cast<uint32_t>(ctr[0]), hi = static_cast<uint32_t>(ctr[1]);
+  need = k;
+  if (lo == hi) {  // every key equal: any k of them
     prefix = hi;
-    mask = 0xffffffffu;
-  } else {
-    const int top = 31 - __clz(diff);  // highest differing bit
-    mask = top >= 31 ? 0u : ~((2u << top) - 1u);
-    prefix = hi & mask;
-    int shift = top - 7;
-#pragma unroll 1
-    while (true) {
-      const int width = shift >= 0 ? 8 : 8 + shift;
-      if (shift < 0) shift = 0;
-      const uint32_t dm = (1u << width) - 1u;
-      if (gtid < 256) hist[gtid] = 0;
-      named_bar_sync(1, G);
-#pragma unroll
-      for (int u = 0; u < EPT; ++u)
-        if (id[u] >= 0 && (key[u] & mask) == prefix) atomicAdd(&hist[(key[u] >> shift) & dm], 1);
-      named_bar_sync(1, G);
-      if (gtid < 32) {
-        // lane l covers digits 255-8l .. 248-8l (descending)
-        int c[8], tot = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) { c[e] = hist[255 - 8 * gtid - e]; tot += c[e]; }
-        int incl = tot;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (gtid >= o) incl += v;
-        }
-        const int excl = incl - tot;
-        if (excl < need && need <= incl) {
-          int run = excl;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            if (run < need && need <= run + c[e]) {
-              sel[0] = 255 - 8 * gtid - e;
-              sel[1] = need - run;
-              sel[2] = c[e];
-            }
-            run += c[e];
-          }
-        }
-      }
-      named_bar_sync(1, G);
-      prefix |= static_cast<uint32_t>(sel[0]) << shift;
-      mask |= dm << shift;
-      need = sel[1];
-      if (sel[2] == need || shift == 0) break;  // bin kept whole, or every bit fixed
-      shift -= 8;
-    }
+    pmask = 0xffffffffu;
+    return;
   }
-  // keep every key whose masked value is above the prefix, and `need` of those
-  // equal to it; the k-th score is the smallest key kept
-  if (gtid == 0) { ctr[0] = 0; ctr[1] = 0; ctr[2] = static_cast<int>(0xffffffffu); }
-  named_bar_sync(1, G);
-  // Positions come from one group-wide prefix sum, not from atomics: each
-  // thread counts its keys above the prefix (n_hi) and equal to it (n_eq),
-  // packed 16 + 16 bits (at most EPT each, at most CAP in total); keys above
-  // go to [0, total_hi) and the first `need` equal keys, in thread order,
-  // right after them.  (An atomic per key, or per warp and element slot, puts
-  // an atomic round trip on every iteration of the loop.)
+  const int top = 31 - __clz(lo ^ hi);
+  pmask = top >= 31 ? 0u : ~((2u << top) - 1u);
+  prefix = hi & pmask;
+  int low = top + 1;  // bits [low, 32) are fixed
+  while (true) {
+    const int sh = low > RBITS ? low - RBITS : 0;
+    const uint32_t dm = (1u << (low - sh)) - 1u;
+#pragma unroll
+    for (int e = 0; e < RBINS / SEL_G; ++e) hist[gtid + e * SEL_G] = 0;
+    named_bar_sync(1, SEL_G);
+    const uint32_t pm = pmask, pf = prefix;
+    each([&](uint32_t key, bool valid) {
+      if (valid && (key & pm) == pf) atomicAdd(&hist[(key >> sh) & dm], 1);
+    });
+    named_bar_sync(1, SEL_G);
+    find_bin(hist, need, gtid, ctr);
+    const uint32_t bin = static_cast<uint32_t>(ctr[2]);
+    const int above = ctr[3], inbin = ctr[4];
+    prefix |= bin << sh;
+    pmask |= dm << sh;
+    need -= above;
+    low = sh;
+    if (inbin == need || sh == 0) return;  // bin kept whole, or every bit fixed
+  }
+}
+
+__device__ __forceinline__ void sel_reset(int* ctr, int gtid) {
+  if (gtid == 0) {
+    ctr[0] = static_cast<int>(0xffffffffu);
+    ctr[1] = 0;
+    ctr[15] = static_cast<int>(0xffffffffu);
+  }
+  named_bar_sync(1, SEL_G);
+}
+
+// Keep the k largest of the n candidates of one query.  The candidates are
+// loaded into registers (EPT per thread) once; every pass of the descent runs
+// on them.  Output positions come from one group-wide prefix sum (no atomic
+// per element): keys above the cut go to [0, above), the first `need` keys
+// equal to it (in thread order) right after them.
+//   FINAL: the indices go to out[0..k) (in no particular order), -1 padded
+//          when n <= k; returns 0.
+//   else:  the kept candidates are compacted to the front of the buffer and
+//          the k-th score (the query's new threshold) is returned.
+template <int EPT, bool FINAL>
+__device__ float select_k(float* cs, int32_t* ci, int n, int k, int gtid, int* hist, int* ctr,
+                          int32_t* out, int cap) {
+  if (FINAL && n <= k) {
+    for (int e = gtid; e < k; e += SEL_G) out[e] = e < n ? ci[e] : -1;
+    return 0.f;
+  }
+  // element e = gtid + u*SEL_G sits in register slot u; the loads are not
+  // predicated (indices clamped into the buffer), so they issue back to back
+  uint32_t key[EPT];
+  int32_t id[EPT];
+#pragma unroll
+  for (int u = 0; u < EPT; ++u) {
+    const int e = min(gtid + u * SEL_G, cap - 1);
+    key[u] = order_key(cs[e]);
+    id[u] = ci[e];
+  }
+#pragma unroll
+  for (int u = 0; u < EPT; ++u)
+    if (gtid + u * SEL_G >= n) id[u] = -1;
+  sel_reset(ctr, gtid);
+  uint32_t prefix, pmask;
+  int need;
+  auto each = [&](auto f) {
+#pragma unroll
+    for (int u = 0; u < EPT; ++u) f(key[u], id[u] >= 0);
+  };
+  radix_descent(each, k, gtid, hist, ctr, prefix, pmask, need);
+  // positions: per-thread counts above / equal (16 + 16 bits), one prefix sum;
+  // keys above the cut go to [0, above), the first `need` keys equal to it (in
+  // thread order) right after them
+  const int lane = gtid & 31, w = gtid >> 5;
   int n_hi = 0, n_eq = 0;
 #pragma unroll
   for (int u = 0; u < EPT; ++u) {
     if (id[u] < 0) continue;
-    const uint32_t m = key[u] & mask;
+    const uint32_t m = key[u] & pmask;
     n_hi += m > prefix;
     n_eq += m == prefix;
   }
@@ -225,14 +291,13 @@ __device__ float select_topk(float* cs, int32_t* ci, int n, int k, int gtid, int
     const int v = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += v;
   }
-  int* wtot = hist;  // [8] warp totals (the histogram is no longer needed)
-  if (lane == 31) wtot[gtid >> 5] = incl;
-  named_bar_sync(1, G);
+  if (lane == 31) ctr[5 + w] = incl;
+  named_bar_sync(1, SEL_G);
   int before = 0, total = 0;
 #pragma unroll
-  for (int w = 0; w < NEPI; ++w) {
-    const int t = wtot[w];
-    if (w < (gtid >> 5)) before += t;
+  for (int ww = 0; ww < NEPI; ++ww) {
+    const int t = ctr[5 + ww];
+    if (ww < w) before += t;
     total += t;
   }
   const int excl = before + incl - packed;
@@ -242,7 +307,7 @@ __device__ float select_topk(float* cs, int32_t* ci, int n, int k, int gtid, int
 #pragma unroll
   for (int u = 0; u < EPT; ++u) {
     if (id[u] < 0) continue;
-    const uint32_t m = key[u] & mask;
+    const uint32_t m = key[u] & pmask;
     int pos = -1;
     if (m > prefix) {
       pos = pos_hi++;
@@ -251,154 +316,69 @@ __device__ float select_topk(float* cs, int32_t* ci, int n, int k, int gtid, int
       ++pos_eq;
     }
     if (pos >= 0) {
-      cs[pos] = key_to_float(key[u]);
-      ci[pos] = id[u];
-      kept_min = min(kept_min, key[u]);
+      if (FINAL) {
+        out[pos] = id[u];
+      } else {
+        cs[pos] = key_to_float(key[u]);
+        ci[pos] = id[u];
+        kept_min = min(kept_min, key[u]);
+      }
     }
+  }
+  if (FINAL) {
+    named_bar_sync(1, SEL_G);  // ctr / hist are reused by the next selection
+    return 0.f;
   }
   kept_min = __reduce_min_sync(0xffffffffu, kept_min);
-  if (lane == 0) atomicMin(reinterpret_cast<unsigned*>(&ctr[2]), kept_min);
-  named_bar_sync(1, G);
-  return key_to_float(static_cast<uint32_t>(ctr[2]));
+  if (lane == 0) atomicMin(reinterpret_cast<unsigned*>(&ctr[15]), kept_min);
+  named_bar_sync(1, SEL_G);
+  const float kth = key_to_float(static_cast<uint32_t>(ctr[15]));
+  named_bar_sync(1, SEL_G);
+  return kth;
 }
 
-// Final selection of one query by one epilogue half (128 threads, named
-// barrier `bar`, its own scratch): the indices of the k largest of the n
-// candidates go straight to out[0..k) (in no particular order; ties at the cut
-// broken arbitrarily), -1 padded when n < k.  The candidates stay in shared
-// memory and each radix pass re-reads them, so the two halves select their
-// queries at the same time without holding them in registers.
-__device__ void final_select_half(const float* cs, const int32_t* ci, int n, int k, int htid,
-                                  uint32_t bar, int* hist, int* sel, int* ctr, int32_t* out) {
-  constexpr int GH = 128;
-  const int lane = htid & 31, hw = htid >> 5;
-  if (n <= k) {
-    for (int e = htid; e < k; e += GH) out[e] = e < n ? ci[e] : -1;
-    return;
-  }
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
-  for (int e = htid; e < n; e += GH) {
-    const uint32_t key = order_key(cs[e]);
-    kmin = min(kmin, key);
-    kmax = max(kmax, key);
-  }
-  kmin = __reduce_min_sync(0xffffffffu, kmin);
-  kmax = __reduce_max_sync(0xffffffffu, kmax);
-  if (htid == 0) {
-    ctr[2] = static_cast<int>(0xffffffffu);
-    ctr[3] = 0;
-  }
-  named_bar_sync(bar, GH);
-  if (lane == 0) {
-    atomicMin(reinterpret_cast<unsigned*>(&ctr[2]), kmin);
-    atomicMax(reinterpret_cast<unsigned*>(&ctr[3]), kmax);
-  }
-  named_bar_sync(bar, GH);
-  const uint32_t lo = static_cast<uint32_t>(ctr[2]), hi = static_cast<uint32_t>(ctr[3]);
-  const uint32_t diff = lo ^ hi;
-  uint32_t prefix, mask;
-  int need = k;
-  if (diff == 0u) {
-    prefix = hi;
-    mask = 0xffffffffu;
-  } else {
-    const int top = 31 - __clz(diff);  // highest differing bit
-    mask = top >= 31 ? 0u : ~((2u << top) - 1u);
-    prefix = hi & mask;
-    int shift = top - 7;
-#pragma unroll 1
-    while (true) {
-      const int width = shift >= 0 ? 8 : 8 + shift;
-      if (shift < 0) shift = 0;
-      const uint32_t dm = (1u << width) - 1u;
-      for (int e = htid; e < 256; e += GH) hist[e] = 0;
-      named_bar_sync(bar, GH);
-      for (int e = htid; e < n; e += GH) {
-        const uint32_t key = order_key(cs[e]);
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & dm], 1);
-      }
-      named_bar_sync(bar, GH);
-      if (htid < 32) {
-        // lane l covers digits 255-8l .. 248-8l (descending)
-        int c[8], tot = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) { c[e] = hist[255 - 8 * htid - e]; tot += c[e]; }
-        int incl = tot;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (htid >= o) incl += v;
-        }
-        const int excl = incl - tot;
-        if (excl < need && need <= incl) {
-          int run = excl;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            if (run < need && need <= run + c[e]) {
-              sel[0] = 255 - 8 * htid - e;
-              sel[1] = need - run;
-              sel[2] = c[e];
-            }
-            run += c[e];
-          }
-        }
-      }
-      named_bar_sync(bar, GH);
-      prefix |= static_cast<uint32_t>(sel[0]) << shift;
-      mask |= dm << shift;
-      need = sel[1];
-      const bool done = sel[2] == need || shift == 0;  // bin kept whole, or every bit fixed
-      named_bar_sync(bar, GH);
-      if (done) break;
-      shift -= 8;
-    }
-  }
-  // positions from one prefix sum over the half: keys above the prefix go to
-  // [0, total_hi), the first `need` equal ones (in thread order) after them
-  int n_hi = 0, n_eq = 0;
-  for (int e = htid; e < n; e += GH) {
-    const uint32_t m = order_key(cs[e]) & mask;
-    n_hi += m > prefix;
-    n_eq += m == prefix;
-  }
-  const int packed = n_hi | (n_eq << 16);
-  int incl = packed;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  int* wtot = hist;  // [4] warp totals (the histogram is no longer needed)
-  if (lane == 31) wtot[hw] = incl;
-  named_bar_sync(bar, GH);
-  int before = 0, total = 0;
-#pragma unroll
-  for (int w = 0; w < GH / 32; ++w) {
-    const int t = wtot[w];
-    if (w < hw) before += t;
-    total += t;
-  }
-  const int excl = before + incl - packed;
-  const int total_hi = total & 0xffff;
-  int pos_hi = excl & 0xffff, pos_eq = excl >> 16;
-  for (int e = htid; e < n; e += GH) {
-    const uint32_t m = order_key(cs[e]) & mask;
-    if (m > prefix) {
-      out[pos_hi++] = ci[e];
-    } else if (m == prefix) {
-      if (pos_eq < need) out[total_hi + pos_eq] = ci[e];
-      ++pos_eq;
-    }
-  }
-  named_bar_sync(bar, GH);  // the scratch is reused by the half's next query
+// One work item: a tile of QT consecutive queries of one sequence.  Items are
+// numbered heaviest first (w -> query tile ntq-1 - w/B of sequence w%B) and
+// dealt to the persistent CTAs in snake order: in round r, CTA c takes item
+// r*P + c (r even) or r*P + P-1-c (r odd), so that every CTA gets a similar mix.
+struct Item {
+  int b, qi0, nq, t0, t_last, L, ntiles;
+  bool ok, stream;  // ok: positions valid; stream: some query has more than k keys
+  int32_t* out;
+};
+
+template <int QT>
+__device__ __forceinline__ bool item_at(const Params& p, int r, Item& I) {
+  const int P = gridDim.x, c = blockIdx.x;
+  const int64_t w = static_cast<int64_t>(r) * P + ((r & 1) ? P - 1 - c : c);
+  if (w >= static_cast<int64_t>(p.B) * p.ntq) return false;
+  I.b = static_cast<int>(w % p.B);
+  const int qt = p.ntq - 1 - static_cast<int>(w / p.B);
+  I.qi0 = qt * QT;
+  I.nq = min(QT, p.Tq - I.qi0);
+  const int q_start = __ldg(p.q_start + I.b);
+  I.L = __ldg(p.kv_len + I.b);
+  I.t0 = q_start + I.qi0;
+  I.t_last = I.t0 + I.nq - 1;
+  I.ok = q_start >= 0 && I.t_last < I.L && I.L <= p.max_kv_len;
+  I.stream = I.ok && I.t_last + 1 > p.topk;
+  I.ntiles = (I.t_last + BKEY) / BKEY;
+  I.out = p.out_idx + (static_cast<int64_t>(I.b) * p.Tq + I.qi0) * p.topk;
+  return true;
 }
 
+// Persistent: one CTA per SM walks its work items.  The barrier phases of the
+// key stages, the TMEM accumulator buffers and (FP8) the key-scale slots run
+// off per-CTA tile counters that continue across items, and the query block
+// has its own full / empty pair, so the next item's query load and first MMAs
+// overlap the current item's final selections.
 template <int H_I, int D_I, bool FP8>
 __global__ void __launch_bounds__(NTHREADS, 1)
     indexer_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k, const Params p) {
   using C = Cfg<H_I, D_I, FP8>;
   constexpr int QT = C::QT, N = C::N, NCH = C::NCH, CAP = C::CAP, NST = C::NST, NSC = C::NSC;
+  constexpr int NSC1 = NSC > 0 ? NSC : 1;
   constexpr uint32_t IDESC = FP8 ? idesc_e4m3(128, N) : idesc_bf16(128, N, false, false);
   constexpr int G = NEPI * 32;
 
@@ -413,43 +393,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   volatile int* g_abort = s_abort + 1;   // [4]
   int* cnt = const_cast<int*>(s_abort) + 8;  // [QT] candidates per query
   float* thr = reinterpret_cast<float*>(cnt + 64);  // [QT]
-  int* hist = reinterpret_cast<int*>(thr + 64);     // [256]
-  int* sel = hist + 256;                            // [4]
-  int* ctr = sel + 4;                               // [4]
-  int* hist1 = ctr + 4;                             // [256] the second half's final-select scratch
-  int* sel1 = hist1 + 256;                          // [4]
-  int* ctr1 = sel1 + 4;                             // [4]
+  int* hist = reinterpret_cast<int*>(sm + C::OFF_MISC + C::MISC_HDR);  // [RBINS]
+  int* ctr = hist + RBINS;                                              // [SEL_CTR]
+  static_assert(48 * 8 + 4 + 4 * 8 + 64 * 4 + 64 * 4 <= C::MISC_HDR, "misc header");
+  static_assert(RBINS == 2048 && SEL_CTR == 16, "selection scratch size");
   float* cand_s = reinterpret_cast<float*>(sm + C::OFF_CAND);
   int32_t* cand_i = reinterpret_cast<int32_t*>(cand_s + QT * CAP);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // heavier (later) query tiles first
-  const int b = blockIdx.x / p.ntq;
-  const int qt = p.ntq - 1 - (blockIdx.x % p.ntq);
-  const int qi0 = qt * QT;
-  const int nq = min(QT, p.Tq - qi0);
-  const int q_start = __ldg(p.q_start + b);
-  const int L = __ldg(p.kv_len + b);
-  const int t0 = q_start + qi0;
-  const int t_last = t0 + nq - 1;
-  const bool ok_pos = q_start >= 0 && t_last < L && L <= p.max_kv_len;
-  int32_t* out = p.out_idx + (static_cast<int64_t>(b) * p.Tq + qi0) * p.topk;
-
-  if (!ok_pos) {
-    if (tid == 0) status_raise(p.status, DSA_ERR_BAD_INDEX, SITE_QPOS, (uint32_t)t_last);
-    for (int e = tid; e < nq * p.topk; e += NTHREADS) out[e] = -1;
-    return;
-  }
-  if (t_last + 1 <= p.topk) {
-    // every query of the tile keeps all of its causal keys
-    for (int e = tid; e < nq * p.topk; e += NTHREADS) {
-      const int q = e / p.topk, j = e % p.topk;
-      out[e] = j <= t0 + q ? j : -1;
-    }
-    return;
-  }
-
-  const int ntiles = (t_last + BKEY) / BKEY;
   if (tid == 0) {
     for (int k = 0; k < C::NBARS; ++k)
       mbar_init(&bars[k], ((k >= C::BDE && k < C::BDE + 4) || k >= C::BSE) ? NEPI : 1);  // warps
@@ -461,20 +412,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tmem_alloc(tslot, 512);
     tmem_relinquish();
   }
-  for (int e = tid; e < QT * H_I; e += NTHREADS) {
-    const int q = e / H_I;
-    float wq = q < nq ? __bfloat162float(__ushort_as_bfloat16(
-                            p.w[(static_cast<int64_t>(b) * p.Tq + qi0) * H_I + e]))
-                      : 0.f;
-    if constexpr (FP8) {
-      if (q < nq) wq *= p.q_scale[(static_cast<int64_t>(b) * p.Tq + qi0) * H_I + e];
-    }
-    w_s[e] = wq;
-  }
-  for (int q = tid; q < QT; q += NTHREADS) {
-    cnt[q] = 0;
-    thr[q] = -INFINITY;
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -482,77 +419,91 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (warp == 0) {
     // ============================ producer ===================================
-    int last_use[NST];
-    for (int k = 0; k < NST; ++k) last_use[k] = -1;
-    int last_s[NSC > 0 ? NSC : 1];
-    for (int k = 0; k < NSC; ++k) last_s[k] = -1;
     if (lane == 0) {
+      int last_use[NST];
+      for (int k = 0; k < NST; ++k) last_use[k] = -1;
+      int last_s[NSC1];
+      for (int k = 0; k < NSC1; ++k) last_s[k] = -1;
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      mbar_expect_tx(&bars[C::BQ], C::Q_BYTES);
-      const int qrow = (b * p.Tq + qi0) * H_I;
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) tma_load_2d(sm + C::OFF_Q + c * N * 128, &tm_q, &bars[C::BQ], 64 * c, qrow);
-      for (int kt = 0; kt < ntiles; ++kt) {
-        const int st = kt % NST, use = kt / NST;
-        if (use > 0 && !mbar_wait(&bars[C::BKE + st], (use - 1) & 1, p.status, kWaitLimitNs, SITE_W_KE)) {
+      int g = 0, nit = 0;  // tiles and streaming items so far
+      Item I;
+      for (int r = 0; item_at<QT>(p, r, I) && !vflag(s_abort); ++r) {
+        if (!I.stream) continue;
+        // the query block, once the previous item's MMAs are done with it
+        if (nit > 0 &&
+            !mbar_wait(&bars[C::BQE], (nit - 1) & 1, p.status, kWaitLimitNs, SITE_W_Q)) {
           s_abort[0] = 1;
           break;
         }
-        if (vflag(s_abort)) break;
-        mbar_expect_tx(&bars[C::BKF + st], C::K_STAGE);
-        last_use[st] = use;
-        uint8_t* dst = sm + C::OFF_K + st * C::K_STAGE;
-        int pids[2] = {0, 0};
-        if (!p.paged) {
-          const int row = static_cast<int>(static_cast<int64_t>(b) * p.seq_stride + kt * BKEY);
+        mbar_expect_tx(&bars[C::BQ], C::Q_BYTES);
+        const int qrow = (I.b * p.Tq + I.qi0) * H_I;
 #pragma unroll
-          for (int c = 0; c < NCH; ++c) tma_load_2d(dst + c * BKEY * 128, &tm_k, &bars[C::BKF + st], 64 * c, row);
-        } else {
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const int pg = kt * 2 + hf;
-            int pid = 0;
-            if (pg * kPage < L) {
-              pid = pg < p.max_pages ? __ldg(p.block_table + static_cast<int64_t>(b) * p.max_pages + pg) : -1;
-              if (pid < 0 || pid >= p.num_pages) {
-                status_raise(p.status, DSA_ERR_BAD_INDEX, SITE_PAGE, (uint32_t)pid);
-                pid = 0;  // read a valid page; its keys are never selected (flagged above)
-              }
-            }
-            pids[hf] = pid;
-#pragma unroll
-            for (int c = 0; c < NCH; ++c)
-              tma_load_2d(dst + c * BKEY * 128 + hf * 64 * 128, &tm_k, &bars[C::BKF + st], 64 * c, pid * kPage);
-          }
-        }
-        if constexpr (FP8) {
-          // the tile's key scales, into a slot of their own
-          const int sc = kt % NSC, suse = kt / NSC;
-          if (suse > 0 &&
-              !mbar_wait(&bars[C::BSE + sc], (suse - 1) & 1, p.status, kWaitLimitNs, SITE_W_SE)) {
+        for (int c = 0; c < NCH; ++c)
+          tma_load_2d(sm + C::OFF_Q + c * N * 128, &tm_q, &bars[C::BQ], 64 * c, qrow);
+        ++nit;
+        for (int kt = 0; kt < I.ntiles; ++kt, ++g) {
+          const int st = g % NST, use = g / NST;
+          if (use > 0 && !mbar_wait(&bars[C::BKE + st], (use - 1) & 1, p.status, kWaitLimitNs, SITE_W_KE)) {
             s_abort[0] = 1;
             break;
           }
-          last_s[sc] = suse;
-          float* sdst = s_scale + sc * BKEY;
+          if (vflag(s_abort)) break;
+          mbar_expect_tx(&bars[C::BKF + st], C::K_STAGE);
+          last_use[st] = use;
+          uint8_t* dst = sm + C::OFF_K + st * C::K_STAGE;
+          int pids[2] = {0, 0};
           if (!p.paged) {
-            // rows of this sequence only (seq_stride is a multiple of 4: whole
-            // 16-byte units, never past the array)
-            const int64_t r0 = static_cast<int64_t>(b) * p.seq_stride + static_cast<int64_t>(kt) * BKEY;
-            const int64_t left = p.seq_stride - static_cast<int64_t>(kt) * BKEY;
-            const uint32_t bytes = static_cast<uint32_t>(left < BKEY ? left : BKEY) * 4u;
-            mbar_expect_tx(&bars[C::BSF + sc], bytes);
-            bulk_load(sdst, p.k_scale + r0, bytes, &bars[C::BSF + sc]);
-          } else {
-            mbar_expect_tx(&bars[C::BSF + sc], 2 * kPage * 4);
+            const int row = static_cast<int>(static_cast<int64_t>(I.b) * p.seq_stride + kt * BKEY);
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf)
-              bulk_load(sdst + hf * kPage, p.k_scale + static_cast<int64_t>(pids[hf]) * kPage,
-                        kPage * 4, &bars[C::BSF + sc]);
+            for (int c = 0; c < NCH; ++c) tma_load_2d(dst + c * BKEY * 128, &tm_k, &bars[C::BKF + st], 64 * c, row);
+          } else {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int pg = kt * 2 + hf;
+              int pid = 0;
+              if (pg * kPage < I.L) {
+                pid = pg < p.max_pages ? __ldg(p.block_table + static_cast<int64_t>(I.b) * p.max_pages + pg) : -1;
+                if (pid < 0 || pid >= p.num_pages) {
+                  status_raise(p.status, DSA_ERR_BAD_INDEX, SITE_PAGE, (uint32_t)pid);
+                  pid = 0;  // read a valid page; its keys are never selected (flagged above)
+                }
+              }
+              pids[hf] = pid;
+#pragma unroll
+              for (int c = 0; c < NCH; ++c)
+                tma_load_2d(dst + c * BKEY * 128 + hf * 64 * 128, &tm_k, &bars[C::BKF + st], 64 * c, pid * kPage);
+            }
+          }
+          if constexpr (FP8) {
+            // the tile's key scales, into a slot of their own
+            const int sc = g % NSC, suse = g / NSC;
+            if (suse > 0 &&
+                !mbar_wait(&bars[C::BSE + sc], (suse - 1) & 1, p.status, kWaitLimitNs, SITE_W_SE)) {
+              s_abort[0] = 1;
+              break;
+            }
+            last_s[sc] = suse;
+            float* sdst = s_scale + sc * BKEY;
+            if (!p.paged) {
+              // rows of this sequence only (seq_stride is a multiple of 4: whole
+              // 16-byte units, never past the array)
+              const int64_t r0 = static_cast<int64_t>(I.b) * p.seq_stride + static_cast<int64_t>(kt) * BKEY;
+              const int64_t left = p.seq_stride - static_cast<int64_t>(kt) * BKEY;
+              const uint32_t bytes = static_cast<uint32_t>(left < BKEY ? left : BKEY) * 4u;
+              mbar_expect_tx(&bars[C::BSF + sc], bytes);
+              bulk_load(sdst, p.k_scale + r0, bytes, &bars[C::BSF + sc]);
+            } else {
+              mbar_expect_tx(&bars[C::BSF + sc], 2 * kPage * 4);
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf)
+                bulk_load(sdst + hf * kPage, p.k_scale + static_cast<int64_t>(pids[hf]) * kPage,
+                          kPage * 4, &bars[C::BSF + sc]);
+            }
           }
         }
       }
+      // every copy issued has landed before the CTA may exit
       for (int k = 0; k < NSC; ++k)
         if (last_s[k] >= 0) mbar_wait(&bars[C::BSF + k], last_s[k] & 1, p.status, kWaitLimitNs, SITE_W_SF);
       for (int st = 0; st < NST; ++st)
@@ -562,27 +513,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == 1) {
     // ============================ MMA issuer ==================================
     if (lane == 0) {
-      bool ok = mbar_wait(&bars[C::BQ], 0, p.status, kWaitLimitNs, SITE_W_Q);
+      bool ok = true;
       const uint64_t qd0 = smem_desc(smem_u32(sm + C::OFF_Q), 16, 1024);
-      for (int kt = 0; kt < ntiles && ok; ++kt) {
-        if (vflag(s_abort)) { ok = false; break; }
-        const int st = kt % NST, buf = kt & 3;
-        if (kt >= 4 && !mbar_wait(&bars[C::BDE + buf], ((kt >> 2) - 1) & 1, p.status, kWaitLimitNs, SITE_W_DE)) { ok = false; break; }
-        if (!mbar_wait(&bars[C::BKF + st], (kt / NST) & 1, p.status, kWaitLimitNs, SITE_W_KF)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t kd = smem_desc(smem_u32(sm + C::OFF_K + st * C::K_STAGE), 16, 1024);
+      int g = 0, nit = 0;
+      Item I;
+      for (int r = 0; ok && item_at<QT>(p, r, I); ++r) {
+        if (!I.stream) continue;
+        if (!mbar_wait(&bars[C::BQ], nit & 1, p.status, kWaitLimitNs, SITE_W_Q)) { ok = false; break; }
+        ++nit;
+        for (int kt = 0; kt < I.ntiles; ++kt, ++g) {
+          if (vflag(s_abort)) { ok = false; break; }
+          const int st = g % NST, buf = g & 3;
+          if (g >= 4 && !mbar_wait(&bars[C::BDE + buf], ((g >> 2) - 1) & 1, p.status, kWaitLimitNs, SITE_W_DE)) { ok = false; break; }
+          if (!mbar_wait(&bars[C::BKF + st], (g / NST) & 1, p.status, kWaitLimitNs, SITE_W_KF)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t kd = smem_desc(smem_u32(sm + C::OFF_K + st * C::K_STAGE), 16, 1024);
 #pragma unroll
-        for (int c = 0; c < NCH; ++c)
+          for (int c = 0; c < NCH; ++c)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            if constexpr (FP8)
-              umma_e4m3(tmem + buf * N, desc_add(kd, c * BKEY * 128 + kk * 32),
-                        desc_add(qd0, c * N * 128 + kk * 32), IDESC, (c | kk) ? 1u : 0u);
-            else
-              umma_bf16(tmem + buf * N, desc_add(kd, c * BKEY * 128 + kk * 32),
-                        desc_add(qd0, c * N * 128 + kk * 32), IDESC, (c | kk) ? 1u : 0u);
-        umma_commit(&bars[C::BKE + st]);
-        umma_commit(&bars[C::BDF + buf]);
+            for (int kk = 0; kk < 4; ++kk)
+              if constexpr (FP8)
+                umma_e4m3(tmem + buf * N, desc_add(kd, c * BKEY * 128 + kk * 32),
+                          desc_add(qd0, c * N * 128 + kk * 32), IDESC, (c | kk) ? 1u : 0u);
+              else
+                umma_bf16(tmem + buf * N, desc_add(kd, c * BKEY * 128 + kk * 32),
+                          desc_add(qd0, c * N * 128 + kk * 32), IDESC, (c | kk) ? 1u : 0u);
+          umma_commit(&bars[C::BKE + st]);
+          umma_commit(&bars[C::BDF + buf]);
+        }
+        // the query block is free once this item's MMAs are done
+        umma_commit(&bars[C::BQE]);
       }
       if (!ok) s_abort[0] = 1;
       umma_commit(&bars[C::BDRAIN]);
@@ -597,136 +557,179 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     constexpr int QH = QT / 2;  // queries per epilogue half
     const uint32_t lane_base = static_cast<uint32_t>(sub * 32) << 16;
     const int key_lane = sub * 32 + lane;
-    // this thread's head weights (its half's queries), kept in registers
-    int kt = 0;
-    bool stop = false;
-    while (kt < ntiles && !stop) {
-      // The head weights stay in registers through the tile loop only and are
-      // reloaded after a selection: with them dead during select_topk its
-      // candidate arrays fit in registers instead of spilling.
-      float wreg[QH * H_I];
-#pragma unroll
-      for (int c = 0; c < QH * H_I; ++c) wreg[c] = w_s[half * QH * H_I + c];
-      bool want_sel = false;
-      // Tiles in pairs with one group barrier per pair: a candidate buffer keeps
-      // room for two tiles' appends between checks, and the MMA runs up to
-      // four tiles ahead (four TMEM accumulator buffers).
-      for (; kt < ntiles; kt += 2) {
-        const int n2 = ntiles - kt < 2 ? ntiles - kt : 2;
-        bool w_ok = !vflag(s_abort);
-        for (int u = 0; u < n2 && w_ok; ++u) {
-          const int k = kt + u;
-          w_ok = mbar_wait(&bars[C::BDF + (k & 3)], (k >> 2) & 1, p.status, kWaitLimitNs, SITE_W_DF) &&
-                 (!FP8 || mbar_wait(&bars[C::BSF + k % (NSC > 0 ? NSC : 1)],
-                                    (k / (NSC > 0 ? NSC : 1)) & 1, p.status, kWaitLimitNs, SITE_W_SF));
+    int g = 0;  // tiles of the streaming items so far
+    Item I;
+    for (int r = 0; item_at<QT>(p, r, I); ++r) {
+      const int nq = I.nq, t0 = I.t0;
+      int32_t* out = I.out;
+      if (!I.ok) {
+        if (gtid == 0) status_raise(p.status, DSA_ERR_BAD_INDEX, SITE_QPOS, (uint32_t)I.t_last);
+        for (int e = gtid; e < nq * p.topk; e += G) out[e] = -1;
+        continue;
+      }
+      if (!I.stream) {
+        // every query of the tile keeps all of its causal keys
+        for (int e = gtid; e < nq * p.topk; e += G) {
+          const int q = e / p.topk, j = e % p.topk;
+          out[e] = j <= t0 + q ? j : -1;
         }
-        // the TMEM loads and ballots below are warp-collective: one decision per warp
-        w_ok = __all_sync(0xffffffffu, w_ok);
-        if (!w_ok) {
-          g_abort[0] = 1;
-        } else {
-          tc_fence_after();
-          for (int u = 0; u < n2; ++u) {
-            const int k = kt + u, buf = k & 3;
-            // head reduction: 4 independent FMA chains per query (the MMA's FP32
-            // accumulators are summed in a fixed order: chain c takes heads c, c+4, ...),
-            // issued as 2-wide FP32 FMAs on the chain pairs (0,1) and (2,3), each
-            // lane an ordinary round-to-nearest FMA
-            constexpr int COLS = QH * H_I;  // this half's accumulator columns
-            constexpr int NCHAIN = 4;
-            float acc[QH][NCHAIN];
+        continue;
+      }
+      if (vflag(&g_abort[1])) {  // an earlier item gave up: no more tiles will come
+        for (int e = gtid; e < nq * p.topk; e += G) out[e] = -1;
+        continue;
+      }
+      // this item's head weights and empty candidate buffers (the previous
+      // item's readers of w_s, cnt and thr are past the barrier)
+      named_bar_sync(1, G);
+      for (int e = gtid; e < QT * H_I; e += G) {
+        const int q = e / H_I;
+        float wq = q < nq ? __bfloat162float(__ushort_as_bfloat16(
+                                p.w[(static_cast<int64_t>(I.b) * p.Tq + I.qi0) * H_I + e]))
+                          : 0.f;
+        if constexpr (FP8) {
+          if (q < nq) wq *= p.q_scale[(static_cast<int64_t>(I.b) * p.Tq + I.qi0) * H_I + e];
+        }
+        w_s[e] = wq;
+      }
+      for (int q = gtid; q < QT; q += G) {
+        cnt[q] = 0;
+        thr[q] = -INFINITY;
+      }
+      named_bar_sync(1, G);
+      const int ntiles = I.ntiles;
+      int kt = 0;
+      bool stop = false;
+      while (kt < ntiles && !stop) {
+        // The head weights stay in registers through the tile loop only and are
+        // reloaded after a selection: with them dead during a selection its
+        // candidate arrays fit in registers instead of spilling.
+        float wreg[QH * H_I];
 #pragma unroll
-            for (int q = 0; q < QH; ++q)
+        for (int c = 0; c < QH * H_I; ++c) wreg[c] = w_s[half * QH * H_I + c];
+        bool want_sel = false;
+        // Tiles in pairs with one group barrier per pair: a candidate buffer keeps
+        // room for two tiles' appends between checks, and the MMA runs up to
+        // four tiles ahead (four TMEM accumulator buffers).
+        for (; kt < ntiles; kt += 2) {
+          const int n2 = ntiles - kt < 2 ? ntiles - kt : 2;
+          bool w_ok = !vflag(s_abort);
+          for (int u = 0; u < n2 && w_ok; ++u) {
+            const int gk = g + kt + u;
+            w_ok = mbar_wait(&bars[C::BDF + (gk & 3)], (gk >> 2) & 1, p.status, kWaitLimitNs, SITE_W_DF) &&
+                   (!FP8 || mbar_wait(&bars[C::BSF + gk % NSC1], (gk / NSC1) & 1, p.status,
+                                      kWaitLimitNs, SITE_W_SF));
+          }
+          // the TMEM loads and ballots below are warp-collective: one decision per warp
+          w_ok = __all_sync(0xffffffffu, w_ok);
+          if (!w_ok) {
+            g_abort[0] = 1;
+          } else {
+            tc_fence_after();
+            for (int u = 0; u < n2; ++u) {
+              const int k = kt + u, gk = g + k, buf = gk & 3;
+              // head reduction: 4 independent FMA chains per query (the MMA's FP32
+              // accumulators are summed in a fixed order: chain c takes heads c, c+4, ...),
+              // issued as 2-wide FP32 FMAs on the chain pairs (0,1) and (2,3), each
+              // lane an ordinary round-to-nearest FMA
+              constexpr int COLS = QH * H_I;  // this half's accumulator columns
+              constexpr int NCHAIN = 4;
+              float acc[QH][NCHAIN];
 #pragma unroll
-              for (int c = 0; c < NCHAIN; ++c) acc[q][c] = 0.f;
-            const uint32_t col0 = buf * N + half * COLS;
+              for (int q = 0; q < QH; ++q)
 #pragma unroll
-            for (int v = 0; v < COLS / 32; ++v) {
-              uint32_t r[32];
-              tmem_ld32(tmem + lane_base + col0 + v * 32, r);
-              tmem_ld_wait();
+                for (int c = 0; c < NCHAIN; ++c) acc[q][c] = 0.f;
+              const uint32_t col0 = buf * N + half * COLS;
 #pragma unroll
-              for (int e = 0; e < 32; e += 2) {
-                const int col = v * 32 + e;
-                const int q = col / H_I;
-                const int c = e % NCHAIN;  // 0 or 2
-                fma2_rn(acc[q][c], acc[q][c + 1], wreg[col], wreg[col + 1],
-                        fmaxf(__uint_as_float(r[e]), 0.f), fmaxf(__uint_as_float(r[e + 1]), 0.f));
+              for (int v = 0; v < COLS / 32; ++v) {
+                uint32_t rr[32];
+                tmem_ld32(tmem + lane_base + col0 + v * 32, rr);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                  const int col = v * 32 + e;
+                  const int q = col / H_I;
+                  const int c = e % NCHAIN;  // 0 or 2
+                  fma2_rn(acc[q][c], acc[q][c + 1], wreg[col], wreg[col + 1],
+                          fmaxf(__uint_as_float(rr[e]), 0.f), fmaxf(__uint_as_float(rr[e + 1]), 0.f));
+                }
               }
-            }
-            float score[QH];
+              float score[QH];
 #pragma unroll
-            for (int q = 0; q < QH; ++q) score[q] = (acc[q][0] + acc[q][1]) + (acc[q][2] + acc[q][3]);
-            tc_fence_before();
-            mbar_arrive_warp(&bars[C::BDE + buf]);
-            if constexpr (FP8) {
-              const int sc = k % (NSC > 0 ? NSC : 1);
-              const float ks = s_scale[sc * BKEY + key_lane];
+              for (int q = 0; q < QH; ++q) score[q] = (acc[q][0] + acc[q][1]) + (acc[q][2] + acc[q][3]);
+              tc_fence_before();
+              mbar_arrive_warp(&bars[C::BDE + buf]);
+              if constexpr (FP8) {
+                const int sc = gk % NSC1;
+                const float ks = s_scale[sc * BKEY + key_lane];
 #pragma unroll
-              for (int q = 0; q < QH; ++q) score[q] *= ks;
-              mbar_arrive_warp(&bars[C::BSE + sc]);
-            }
-            // append candidates above each query's threshold
-            const int s = k * BKEY + key_lane;
+                for (int q = 0; q < QH; ++q) score[q] *= ks;
+                mbar_arrive_warp(&bars[C::BSE + sc]);
+              }
+              // append candidates above each query's threshold
+              const int s = k * BKEY + key_lane;
 #pragma unroll
-            for (int q = 0; q < QH; ++q) {
-              const int qq = half * QH + q;
-              const bool take = qq < nq && s <= t0 + qq && score[q] > thr[qq];
-              const uint32_t bal = __ballot_sync(0xffffffffu, take);
-              if (bal) {
-                int base = 0;
-                if (lane == 0) base = atomicAdd(&cnt[qq], __popc(bal));
-                base = __shfl_sync(0xffffffffu, base, 0);
-                if (take) {
-                  const int pos = base + __popc(bal & ((1u << lane) - 1u));
-                  cand_s[qq * CAP + pos] = score[q];
-                  cand_i[qq * CAP + pos] = s;
+              for (int q = 0; q < QH; ++q) {
+                const int qq = half * QH + q;
+                const bool take = qq < nq && s <= t0 + qq && score[q] > thr[qq];
+                const uint32_t bal = __ballot_sync(0xffffffffu, take);
+                if (bal) {
+                  int base = 0;
+                  if (lane == 0) base = atomicAdd(&cnt[qq], __popc(bal));
+                  base = __shfl_sync(0xffffffffu, base, 0);
+                  if (take) {
+                    const int pos = base + __popc(bal & ((1u << lane) - 1u));
+                    cand_s[qq * CAP + pos] = score[q];
+                    cand_i[qq * CAP + pos] = s;
+                  }
                 }
               }
             }
           }
+          named_bar_sync(1, G);
+          if (vflag(&g_abort[0])) {
+            if (gtid == 0) s_abort[0] = 1;  // no role waits for this item's tiles any more
+            stop = true;
+            break;
+          }
+          // a buffer that could overflow on the next pair is shrunk outside this loop
+          for (int qq = 0; qq < nq; ++qq) want_sel |= cnt[qq] > CAP - 2 * BKEY;
+          if (want_sel) {
+            kt += n2;
+            break;
+          }
         }
-        named_bar_sync(1, G);
-        if (vflag(&g_abort[0])) {
-          stop = true;
-          break;
-        }
-        // a buffer that could overflow on the next pair is shrunk outside this loop
-        for (int qq = 0; qq < nq; ++qq) want_sel |= cnt[qq] > CAP - 2 * BKEY;
         if (want_sel) {
-          kt += n2;
-          break;
-        }
-      }
-      if (want_sel) {
-        for (int qq = 0; qq < nq; ++qq) {
-          if (cnt[qq] > CAP - 2 * BKEY) {
-            const float kth = select_topk<C::EPT>(cand_s + qq * CAP, cand_i + qq * CAP, cnt[qq],
-                                                  p.topk, gtid, hist, sel, ctr);
-            if (gtid == 0) {
-              cnt[qq] = p.topk;
-              thr[qq] = kth;
+          for (int qq = 0; qq < nq; ++qq) {
+            if (cnt[qq] > CAP - 2 * BKEY) {
+              const float kth = select_k<C::EPT, false>(cand_s + qq * CAP, cand_i + qq * CAP,
+                                                        cnt[qq], p.topk, gtid, hist, ctr, nullptr,
+                                                        CAP);
+              if (gtid == 0) {
+                cnt[qq] = p.topk;
+                thr[qq] = kth;
+              }
+              named_bar_sync(1, G);
             }
-            named_bar_sync(1, G);
           }
         }
       }
-    }
-    // final selection and output (the abort decision is made uniform by one
-    // writer before a group barrier)
-    if (gtid == 0) g_abort[1] = vflag(s_abort) ? 1 : 0;
-    named_bar_sync(1, G);
-    const bool aborted = vflag(&g_abort[1]);
-    // the two epilogue halves select their queries (even / odd) at the same time
-    const int htid = gtid - 128 * half;
-    for (int qq = half; qq < nq; qq += 2) {
-      int32_t* o = out + static_cast<int64_t>(qq) * p.topk;
-      if (aborted) {
-        for (int e = htid; e < p.topk; e += 128) o[e] = -1;
-        continue;
+      g += ntiles;
+      // final selection and output (the abort decision is made uniform by one
+      // writer before a group barrier)
+      if (gtid == 0) g_abort[1] = vflag(s_abort) ? 1 : 0;
+      named_bar_sync(1, G);
+      const bool aborted = vflag(&g_abort[1]);
+      // the queries one after another, each by all epilogue threads
+      for (int qq = 0; qq < nq; ++qq) {
+        int32_t* o = out + static_cast<int64_t>(qq) * p.topk;
+        if (aborted) {
+          for (int e = gtid; e < p.topk; e += G) o[e] = -1;
+          continue;
+        }
+        select_k<C::EPT, true>(cand_s + qq * CAP, cand_i + qq * CAP, cnt[qq], p.topk, gtid, hist,
+                               ctr, o, CAP);
       }
-      final_select_half(cand_s + qq * CAP, cand_i + qq * CAP, cnt[qq], p.topk, htid, 2u + half,
-                        half ? hist1 : hist, half ? sel1 : sel, half ? ctr1 : ctr, o);
     }
   }
   tc_fence_before();
@@ -766,6 +769,7 @@ static dsa_status_t prefill_launch(const IndexerArgs& a, cudaStream_t stream) {
   p.Tq = a.Tq;
   p.topk = a.topk;
   p.max_kv_len = a.max_kv_len;
+  p.B = a.B;
   p.ntq = (a.Tq + C::QT - 1) / C::QT;
   p.out_idx = a.out_idx;
   p.status = a.status;
@@ -773,7 +777,10 @@ static dsa_status_t prefill_launch(const IndexerArgs& a, cudaStream_t stream) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
       cudaSuccess)
     return launch_status("cudaFuncSetAttribute");
-  kern<<<static_cast<unsigned>(a.B * p.ntq), idx::NTHREADS, C::SMEM_BYTES, stream>>>(tq, tk, p);
+  // persistent: one CTA per SM (shared memory allows no more)
+  const int64_t items = static_cast<int64_t>(a.B) * p.ntq;
+  const unsigned grid = static_cast<unsigned>(items < num_sms() ? items : num_sms());
+  kern<<<grid, idx::NTHREADS, C::SMEM_BYTES, stream>>>(tq, tk, p);
   return launch_status("indexer_prefill");
 }
 
