@@ -12,26 +12,28 @@
 // first score products overlap the current unit's last blocks and epilogue
 // (barrier phases run off a per-CTA block counter that continues across
 // units).  Roles:
-//   warps 0-3   producer: per unit, the index scan (last valid entry, bad
+//   warps 0-5   producer: per unit, the index scan (last valid entry, bad
 //               entries flagged) published to the other roles; TMA load of
 //               the query's 96x576 q_lat block once the previous unit's score
 //               products are done with it; 16-byte
 //               cp.async gather of the selected rows into a ring of six 16 KB
 //               "pair" slots (two 64-dim chunks, dims 0..511) and one 8 KB
 //               "rope" slot (dims 512..575), 128-byte swizzled.  Each thread
-//               copies one 16-byte unit of four fixed keys, so its shared and
-//               global addresses are computed once per block.  (TMA
-//               tile::gather4 moves these 1,152-byte rows about 4x slower.)
-//   warps 4-11  softmax (two warps per TMEM lane quarter: a thread owns one
+//               copies one 16-byte unit of up to three fixed keys, so its
+//               shared and global addresses are computed once per block.
+//               (TMA tile::gather4 moves these 1,152-byte rows about 4x slower;
+//               six gathering warps instead of four keep the 512-thread CTA
+//               at 128 registers and shorten the decode gathers from DRAM.)
+//   warps 6-13  softmax (two warps per TMEM lane quarter: a thread owns one
 //               head and 32 of the block's 64 keys; P = 2^(z - m_ref) against
 //               a lazy reference max, which only moves -- through a rarer,
 //               synchronised path that rescales O^T -- when an exponent would
 //               exceed 64), P^T written as BF16, then the unit's epilogue
 //               (O^T / l written straight from registers, 32 consecutive dims
 //               per warp and head, and lse).
-//   warp 12     tcgen05 issuer of the scores (one lane), TMEM owner:
+//   warp 14     tcgen05 issuer of the scores (one lane), TMEM owner:
 //                 S  [128 x 64]  = Q [128(96 heads) x 576] . KV_blk^T   (M=128, N=64)
-//   warp 13     tcgen05 issuer of the value product (one lane):
+//   warp 15     tcgen05 issuer of the value product (one lane):
 //                 O^T[512 x 96] += V_blk^T [512 x 64] . P^T [64 x 96]   (4 x M=128, N=96)
 //               S double-buffered in TMEM columns 384..511, O^T in 0..383.
 //               With six pair slots, the first two pairs and the rope chunk of
@@ -77,19 +79,20 @@ constexpr int MISC_BYTES = 2048;
 constexpr int SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-// Roles: warps 0-3 producer, 4-11 softmax, 12 score issuer, 13 value issuer.
-constexpr int NPROD = 128;                        // producer threads (warps 0-3)
+// Roles: warps 0-5 producer, 6-13 softmax, 14 score issuer, 15 value issuer.
+constexpr int NPROD = 192;                        // producer threads (warps 0-5)
 constexpr int NPW = NPROD / 32;
-constexpr int KPT = BK / (4 * NPW);               // keys per producer thread
-constexpr int SMX_WARP0 = NPW;                    // warps 4-11
+constexpr int KROW = 4 * NPW;                     // keys one pass of the producers covers
+constexpr int KPT = (BK + KROW - 1) / KROW;       // keys per producer thread (the last partly)
+constexpr int SMX_WARP0 = NPW;                    // warps 6-13
 constexpr int NSMX = 256;                         // softmax / epilogue threads
-constexpr int MMA_WARP = SMX_WARP0 + NSMX / 32;   // warp 12: scores, TMEM owner
-constexpr int PV_WARP = MMA_WARP + 1;             // warp 13: value product
+constexpr int MMA_WARP = SMX_WARP0 + NSMX / 32;   // warp 14: scores, TMEM owner
+constexpr int PV_WARP = MMA_WARP + 1;             // warp 15: value product
 constexpr int NTHREADS = NPROD + NSMX + 64;
-static_assert(KPT * 4 * NPW == BK, "producer key split");
-// 14 warps at 128 registers: the 4 warps that share an SM sub-partition
+static_assert(KPT * KROW >= BK && (KPT - 1) * KROW < BK, "producer key split");
+// 16 warps at 128 registers: the 4 warps that share an SM sub-partition
 // exactly fill its 16K-register file.
-static_assert(NTHREADS <= 448, "register budget of the 128-register build");
+static_assert(NTHREADS <= 512, "register budget of the 128-register build");
 constexpr uint32_t S_COL = 384;
 
 // barrier indices
@@ -223,8 +226,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + OFF_MISC + 260);
   volatile int* g_abort = s_abort + 1;  // [3] softmax-group abort, by block mod 3
   volatile int* s_resc = s_abort + 4;   // [3] some head needs an O^T rescale, by block mod 3
-  int* s_red = reinterpret_cast<int*>(sm + OFF_MISC + 288);              // [2][4] producer scan
-  float* s_cmax = reinterpret_cast<float*>(sm + OFF_MISC + 256 + 64);   // [2][128] rare path
+  int* s_red = reinterpret_cast<int*>(sm + OFF_MISC + 288);              // [2][8] producer scan
+  float* s_cmax = reinterpret_cast<float*>(sm + OFF_MISC + 352);         // [2][128] rare path
   float* s_alpha = s_cmax + 256;                                         // [128] rare path
   volatile uint8_t* s_hover = reinterpret_cast<volatile uint8_t*>(s_alpha + 128);  // [128]
 
@@ -265,18 +268,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = *tslot;
 
   if (warp < SMX_WARP0) {
-    // ====================== producer (4 warps, cp.async) ======================
+    // ====================== producer (6 warps, cp.async) ======================
     // Per unit: validate the index list (one batched load round trip) and
     // publish (n_list, nb, blk0); load the query block once the previous
     // unit's score products are done with it; gather the unit's blocks.
-    // thread: 16-byte unit u = lane & 7 of keys 4w + (lane >> 3) + 16i, i = 0..3
+    // thread: 16-byte unit u = lane & 7 of keys 4w + (lane >> 3) + 24i, i = 0..2
+    // (the last pass covers keys 48..63 only: warps 0-3)
     const int w = warp, unit = lane & 7;
     int key[KPT];
     uint32_t doff[KPT];
 #pragma unroll
     for (int i = 0; i < KPT; ++i) {
-      key[i] = 4 * w + (lane >> 3) + 4 * NPW * i;
-      doff[i] = sw128_unit(key[i], unit);
+      key[i] = 4 * w + (lane >> 3) + KROW * i;  // >= BK: no key (the last pass is partial)
+      doff[i] = sw128_unit(key[i] < BK ? key[i] : 0, unit);
     }
     bool ok = true;
     int gb = 0, qcnt = 0, it = 0;
@@ -315,7 +319,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       last = __reduce_max_sync(0xffffffffu, last);
-      int* red = s_red + (it & 1) * 4;
+      int* red = s_red + (it & 1) * 8;
       if (lane == 0) red[w] = last;
       named_bar_sync(2, NPROD);
       int n_list = -1;
@@ -355,7 +359,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
       for (int i = 0; i < KPT; ++i) {
         const int e = blk0 * BK + key[i];
-        s_next[i] = (nb > 0 && e < n_list) ? __ldg(U.ix + e) : -1;
+        s_next[i] = (nb > 0 && key[i] < BK && e < n_list) ? __ldg(U.ix + e) : -1;
       }
       for (int jj = 0; jj < nb && ok; ++jj) {
         const int gbj = gb + jj;
@@ -368,7 +372,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int i = 0; i < KPT; ++i) {
           const int e = (blk0 + jj + 1) * BK + key[i];
-          s_next[i] = (jj + 1 < nb && e < n_list) ? __ldg(U.ix + e) : -1;
+          s_next[i] = (jj + 1 < nb && key[i] < BK && e < n_list) ? __ldg(U.ix + e) : -1;
         }
         if (p.nsplit > 1) {
           // split units (decode): the rows come from HBM, not L2.  Ask L2 for
@@ -411,13 +415,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (vload(s_abort)) { ok = false; break; }
           if (rope) {
 #pragma unroll
-            for (int i = 0; i < KPT; ++i) cp_async_16(dbase + doff[i], src[i] + 8 * 64);
+            for (int i = 0; i < KPT; ++i)
+              if (key[i] < BK) cp_async_16(dbase + doff[i], src[i] + 8 * 64);
           } else {
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
               for (int i = 0; i < KPT; ++i)
-                cp_async_16(dbase + h2 * CHUNK + doff[i], src[i] + (2 * pr + h2) * 64);
+                if (key[i] < BK) cp_async_16(dbase + h2 * CHUNK + doff[i], src[i] + (2 * pr + h2) * 64);
           }
           cp_async_arrive(full);
         }
