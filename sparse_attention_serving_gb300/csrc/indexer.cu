@@ -59,7 +59,7 @@ struct Cfg {
   static constexpr int N = QT * H_I;                          // MMA N
   static constexpr int ROWB = FP8 ? D_I : 2 * D_I;            // bytes per key / query-head row
   static constexpr int NCH = ROWB / 128;                      // 128-byte column chunks
-  static constexpr int NST = FP8 ? 6 : 3;                     // key-tile stages
+  static constexpr int NST = FP8 ? 8 : 3;                     // key-tile stages
   static constexpr int NSC = FP8 ? 8 : 0;                     // key-scale slots (FP8)
   static constexpr int Q_BYTES = NCH * N * 128;
   static constexpr int K_STAGE = NCH * BKEY * 128;
