@@ -126,7 +126,10 @@ dsa_status_t dsa_workspace_init(void* workspace, size_t ws_bytes, dsa_stream_t s
  * multiple of 4; Tq >= 1.  Tq == 1 selects the decode kernels (key ranges
  * split across the GPU, a linear score vector per request in the workspace,
  * then a radix select); Tq > 1 the fused prefill kernel, which keeps every
- * score on chip.
+ * score on chip and only the candidates above each query's running threshold
+ * in per-CTA buffers of the workspace (at 64 heads: min(SMs, B * ceil(Tq/4))
+ * CTAs x 4 queries x 8,192 candidates x 8 bytes, about 38 MiB on 152 SMs;
+ * dsa_workspace_bytes gives the exact figure).
  */
 dsa_status_t dsa_indexer_topk(const uint16_t* q_idx, const uint16_t* w, const dsa_rows_t* k_idx,
                               const int32_t* q_start, const int32_t* kv_len, int B, int Tq,

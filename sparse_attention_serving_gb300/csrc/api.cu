@@ -70,13 +70,17 @@ int indexer_prefill_max_topk(int H_I, int D_I);
 dsa_status_t indexer_prefill_launch(const IndexerArgs& a, cudaStream_t stream);
 dsa_status_t indexer_decode_launch(const IndexerArgs& a, cudaStream_t stream);
 size_t indexer_decode_scratch_bytes(int B, int max_kv_len);
+size_t indexer_prefill_scratch_bytes(int B, int Tq, int H_I, int D_I);
 
 // Tq == 1 (one new token per request) takes the split decode path, which keeps
 // a linear FP32 score vector per request in the workspace; Tq > 1 takes the
-// fused prefill kernel, which keeps every score on chip.
+// fused prefill kernel, which keeps the candidates above each query's running
+// threshold in per-CTA buffers of the workspace.  The indexer head width is
+// 128 with 64 heads and 64 with 4 heads, the two supported shapes.
 size_t indexer_scratch_bytes(int B, int Tq, int max_kv_len, int H_I, int topk) {
-  (void)H_I; (void)topk;
-  return Tq == 1 ? indexer_decode_scratch_bytes(B, max_kv_len) : 0;
+  (void)topk;
+  if (Tq == 1) return indexer_decode_scratch_bytes(B, max_kv_len);
+  return indexer_prefill_scratch_bytes(B, Tq, H_I, H_I == 4 ? 64 : 128);
 }
 
 dsa_status_t indexer_launch(const IndexerArgs& a, cudaStream_t stream) {

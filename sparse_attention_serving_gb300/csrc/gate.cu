@@ -52,8 +52,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   constexpr uint32_t IDESC_G = idesc_bf16(128, 256, false, false);
   constexpr uint32_t IDESC_U = idesc_bf16(128, 128, false, false);
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* sm = smem_align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_MISC);  // full[4], empty[4], acc, drain
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);

@@ -10,16 +10,17 @@
 //
 // Prefill (Tq > 1): one fused, persistent kernel, no score buffer in global
 // memory.  One CTA per SM walks work items -- tiles of QT consecutive queries
-// of one sequence (QT * H_I = 128 or 64 accumulator columns), heaviest first --
-// and streams every causal key tile of 128 keys of each item:
+// of one sequence (QT * H_I = 256 accumulator columns at 64 heads, 64 at 4),
+// heaviest first -- and streams every causal key tile of 128 keys of each item:
 //     D^T[128 keys x QT*H_I] = K_tile[128 x D_I] . Q^T[D_I x QT*H_I]   (tcgen05, M=128)
-//   with four TMEM accumulator buffers, so the head reductions of one pair of
-//   tiles overlap the MMAs of the next; the barrier phases run off per-CTA
-//   tile counters, so the next item's query load and first MMAs overlap the
-//   current item's final selections.  Each epilogue thread owns one key (a
-//   TMEM lane) and reduces over heads without any cross-lane traffic; scores
-//   above the query's running threshold are appended to a per-query candidate
-//   buffer in shared memory.  When a buffer nears capacity a radix select
+//   with two TMEM accumulator buffers at N = 256 (four at N = 64), so the head
+//   reductions of one tile overlap the MMAs of the next; the barrier phases run
+//   off per-CTA tile counters, so the next item's query load and first MMAs
+//   overlap the current item's final selections.  Each epilogue thread owns
+//   one key (a TMEM lane) and reduces over heads without any cross-lane
+//   traffic; scores above the query's running threshold are appended to the
+//   query's candidate buffer (CAP entries in this CTA's slice of the
+//   workspace, L2-resident).  When a buffer nears capacity a radix select
 //   (11-bit digits over order-preserving keys, candidates held in registers)
 //   keeps the top k and raises the threshold to the k-th score.  The final
 //   select writes the indices.
@@ -52,14 +53,18 @@ enum : uint32_t {
 
 template <int H_I, int D_I, bool FP8>
 struct Cfg {
-  // Two queries per CTA at 64 heads (N = 128): fewer queries share the
-  // candidate space, so each buffer holds ~6K candidates and a query needs
-  // about two radix selections instead of five.
-  static constexpr int QT = (H_I >= 64) ? 128 / H_I : 16;  // queries per CTA
+  // Four queries per CTA at 64 heads (N = 256, two TMEM accumulator buffers):
+  // each key tile copied into shared memory feeds the MMAs of four queries.
+  // The candidate buffers are in global memory (a per-CTA slice of the
+  // workspace, L2-resident), CAP per query, so shared memory holds only the
+  // operands and a query up to CAP causal keys needs no selection before its
+  // final one.
+  static constexpr int QT = (H_I >= 64) ? 256 / H_I : 16;  // queries per CTA
   static constexpr int N = QT * H_I;                          // MMA N
+  static constexpr int NBUF = 512 / N > 4 ? 4 : 512 / N;      // TMEM accumulator buffers
   static constexpr int ROWB = FP8 ? D_I : 2 * D_I;            // bytes per key / query-head row
   static constexpr int NCH = ROWB / 128;                      // 128-byte column chunks
-  static constexpr int NST = FP8 ? 8 : 3;                     // key-tile stages
+  static constexpr int NST = FP8 ? 8 : 4;                     // key-tile stages
   static constexpr int NSC = FP8 ? 8 : 0;                     // key-scale slots (FP8)
   static constexpr int Q_BYTES = NCH * N * 128;
   static constexpr int K_STAGE = NCH * BKEY * 128;
@@ -73,20 +78,19 @@ struct Cfg {
                        BDE = BDF + 4, BDRAIN = BDE + 4, BSF = BDRAIN + 1, BSE = BSF + NSC,
                        NBARS = BSE + NSC;
   static_assert(NBARS <= 48, "barrier block");
-  static_assert(4 * N <= 512, "four accumulator buffers in TMEM");
+  static_assert(NBUF * N <= 512, "accumulator buffers in TMEM");
   static constexpr int OFF_MISC = OFF_W + QT * H_I * 4;
   // barriers (48 x 8 B), flags, per-query counts and thresholds, then the
   // selection scratch (RBINS histogram bins and 16 counters)
   static constexpr int MISC_HDR = 1024;
   static constexpr int MISC_BYTES = MISC_HDR + (2048 + 16) * 4;
-  static constexpr int OFF_CAND = OFF_MISC + MISC_BYTES;
-  static constexpr int AVAIL = 232448 - 1024 - OFF_CAND;
-  static constexpr int CAP_RAW = (AVAIL / (QT * 8)) / 32 * 32;
-  static constexpr int CAP = CAP_RAW > 6144 ? 6144 : CAP_RAW;  // candidates per query
-  static constexpr int SMEM_BYTES = OFF_CAND + QT * CAP * 8 + 1024;
+  static constexpr int SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;
+  static constexpr int CAP = (H_I >= 64) ? 8192 : 1280;  // candidates per query
+  static constexpr int CTA_SCRATCH = QT * CAP * 8;        // scores, then key indices
   static constexpr int EPT = (CAP + NEPI * 32 - 1) / (NEPI * 32);  // candidates per thread in a select
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(N % 16 == 0 && N <= 256, "MMA N");
+  static_assert(H_I % 4 == 0, "four head columns per weight load");
 };
 
 struct Params {
@@ -101,6 +105,7 @@ struct Params {
   int paged;
   int B, Tq, topk, max_kv_len, ntq;  // ntq = query tiles per sequence
   int32_t* out_idx;
+  uint8_t* cand;  // [gridDim.x][CTA_SCRATCH] candidate buffers
   uint32_t* status;
 };
 
@@ -246,24 +251,25 @@ __device__ __forceinline__ void sel_reset(int* ctr, int gtid) {
 //          the k-th score (the query's new threshold) is returned.
 template <int EPT, bool FINAL>
 __device__ float select_k(float* cs, int32_t* ci, int n, int k, int gtid, int* hist, int* ctr,
-                          int32_t* out, int cap) {
+                          int32_t* out) {
   if (FINAL && n <= k) {
     for (int e = gtid; e < k; e += SEL_G) out[e] = e < n ? ci[e] : -1;
     return 0.f;
   }
-  // element e = gtid + u*SEL_G sits in register slot u; the loads are not
-  // predicated (indices clamped into the buffer), so they issue back to back
+  // element e = gtid + u*SEL_G sits in register slot u (the buffer is in
+  // global memory: only the n filled entries are read)
   uint32_t key[EPT];
   int32_t id[EPT];
 #pragma unroll
   for (int u = 0; u < EPT; ++u) {
-    const int e = min(gtid + u * SEL_G, cap - 1);
-    key[u] = order_key(cs[e]);
-    id[u] = ci[e];
+    const int e = gtid + u * SEL_G;
+    key[u] = 0u;
+    id[u] = -1;
+    if (e < n) {
+      key[u] = order_key(cs[e]);
+      id[u] = ci[e];
+    }
   }
-#pragma unroll
-  for (int u = 0; u < EPT; ++u)
-    if (gtid + u * SEL_G >= n) id[u] = -1;
   sel_reset(ctr, gtid);
   uint32_t prefix, pmask;
   int need;
@@ -378,13 +384,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                            const __grid_constant__ CUtensorMap tm_k, const Params p) {
   using C = Cfg<H_I, D_I, FP8>;
   constexpr int QT = C::QT, N = C::N, NCH = C::NCH, CAP = C::CAP, NST = C::NST, NSC = C::NSC;
+  constexpr int NBUF = C::NBUF;
   constexpr int NSC1 = NSC > 0 ? NSC : 1;
   constexpr uint32_t IDESC = FP8 ? idesc_e4m3(128, N) : idesc_bf16(128, N, false, false);
   constexpr int G = NEPI * 32;
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* sm = smem_align1024(smem_raw);
   float* w_s = reinterpret_cast<float*>(sm + C::OFF_W);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_MISC);  // 48 barrier slots
   float* s_scale = reinterpret_cast<float*>(sm + C::OFF_SC);         // FP8: [NSC][128]
@@ -397,7 +403,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   int* ctr = hist + RBINS;                                              // [SEL_CTR]
   static_assert(48 * 8 + 4 + 4 * 8 + 64 * 4 + 64 * 4 <= C::MISC_HDR, "misc header");
   static_assert(RBINS == 2048 && SEL_CTR == 16, "selection scratch size");
-  float* cand_s = reinterpret_cast<float*>(sm + C::OFF_CAND);
+  float* cand_s = reinterpret_cast<float*>(p.cand + static_cast<int64_t>(blockIdx.x) * C::CTA_SCRATCH);
   int32_t* cand_i = reinterpret_cast<int32_t*>(cand_s + QT * CAP);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -523,8 +529,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ++nit;
         for (int kt = 0; kt < I.ntiles; ++kt, ++g) {
           if (vflag(s_abort)) { ok = false; break; }
-          const int st = g % NST, buf = g & 3;
-          if (g >= 4 && !mbar_wait(&bars[C::BDE + buf], ((g >> 2) - 1) & 1, p.status, kWaitLimitNs, SITE_W_DE)) { ok = false; break; }
+          const int st = g % NST, buf = g % NBUF;
+          if (g >= NBUF && !mbar_wait(&bars[C::BDE + buf], ((g / NBUF) - 1) & 1, p.status, kWaitLimitNs, SITE_W_DE)) { ok = false; break; }
           if (!mbar_wait(&bars[C::BKF + st], (g / NST) & 1, p.status, kWaitLimitNs, SITE_W_KF)) { ok = false; break; }
           tc_fence_after();
           const uint64_t kd = smem_desc(smem_u32(sm + C::OFF_K + st * C::K_STAGE), 16, 1024);
@@ -590,7 +596,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if constexpr (FP8) {
           if (q < nq) wq *= p.q_scale[(static_cast<int64_t>(I.b) * p.Tq + I.qi0) * H_I + e];
         }
-        w_s[e] = wq;
+        w_s[e] = 0.5f * wq;  // the head reduction takes (x + |x|) = 2 max(x, 0)
       }
       for (int q = gtid; q < QT; q += G) {
         cnt[q] = 0;
@@ -601,22 +607,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       int kt = 0;
       bool stop = false;
       while (kt < ntiles && !stop) {
-        // The head weights stay in registers through the tile loop only and are
-        // reloaded after a selection: with them dead during a selection its
-        // candidate arrays fit in registers instead of spilling.
-        float wreg[QH * H_I];
-#pragma unroll
-        for (int c = 0; c < QH * H_I; ++c) wreg[c] = w_s[half * QH * H_I + c];
+        // this half's head weights, read from shared memory (four per 16-byte
+        // broadcast load) as the columns come out of TMEM
+        const float* wh = w_s + half * QH * H_I;
         bool want_sel = false;
         // Tiles in pairs with one group barrier per pair: a candidate buffer keeps
         // room for two tiles' appends between checks, and the MMA runs up to
-        // four tiles ahead (four TMEM accumulator buffers).
+        // NBUF tiles ahead (TMEM accumulator buffers).
         for (; kt < ntiles; kt += 2) {
           const int n2 = ntiles - kt < 2 ? ntiles - kt : 2;
           bool w_ok = !vflag(s_abort);
           for (int u = 0; u < n2 && w_ok; ++u) {
             const int gk = g + kt + u;
-            w_ok = mbar_wait(&bars[C::BDF + (gk & 3)], (gk >> 2) & 1, p.status, kWaitLimitNs, SITE_W_DF) &&
+            w_ok = mbar_wait(&bars[C::BDF + gk % NBUF], (gk / NBUF) & 1, p.status, kWaitLimitNs, SITE_W_DF) &&
                    (!FP8 || mbar_wait(&bars[C::BSF + gk % NSC1], (gk / NSC1) & 1, p.status,
                                       kWaitLimitNs, SITE_W_SF));
           }
@@ -627,11 +630,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           } else {
             tc_fence_after();
             for (int u = 0; u < n2; ++u) {
-              const int k = kt + u, gk = g + k, buf = gk & 3;
+              const int k = kt + u, gk = g + k, buf = gk % NBUF;
               // head reduction: 4 independent FMA chains per query (the MMA's FP32
               // accumulators are summed in a fixed order: chain c takes heads c, c+4, ...),
               // issued as 2-wide FP32 FMAs on the chain pairs (0,1) and (2,3), each
-              // lane an ordinary round-to-nearest FMA
+              // lane an ordinary round-to-nearest FMA.  The ReLU runs on the FMA pipe
+              // as x + |x| against halved weights: (x + |x|) (w/2) is max(x, 0) w
+              // exactly (doubling and halving are exact in FP32), so every product
+              // and sum is the one of w * max(x, 0)
               constexpr int COLS = QH * H_I;  // this half's accumulator columns
               constexpr int NCHAIN = 4;
               float acc[QH][NCHAIN];
@@ -640,18 +646,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int c = 0; c < NCHAIN; ++c) acc[q][c] = 0.f;
               const uint32_t col0 = buf * N + half * COLS;
+              // 32 columns per TMEM load; the next load is in flight while the
+              // current columns are reduced
+              uint32_t rb[2][32];
+              tmem_ld32(tmem + lane_base + col0, rb[0]);
 #pragma unroll
               for (int v = 0; v < COLS / 32; ++v) {
-                uint32_t rr[32];
-                tmem_ld32(tmem + lane_base + col0 + v * 32, rr);
-                tmem_ld_wait();
+                uint32_t(&rr)[32] = rb[v & 1];
+                tmem_ld_wait_regs(rr);
+                if (v + 1 < COLS / 32) tmem_ld32(tmem + lane_base + col0 + (v + 1) * 32, rb[(v + 1) & 1]);
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
+                for (int e = 0; e < 32; e += 4) {
                   const int col = v * 32 + e;
-                  const int q = col / H_I;
-                  const int c = e % NCHAIN;  // 0 or 2
-                  fma2_rn(acc[q][c], acc[q][c + 1], wreg[col], wreg[col + 1],
-                          fmaxf(__uint_as_float(rr[e]), 0.f), fmaxf(__uint_as_float(rr[e + 1]), 0.f));
+                  const int q = col / H_I;  // columns col..col+3 belong to one query
+                  const float4 wv = *reinterpret_cast<const float4*>(wh + col);
+                  float x[4];
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    x[j] = __uint_as_float(rr[e + j]);
+                    x[j] = __fadd_rn(x[j], fabsf(x[j]));
+                  }
+                  fma2_rn(acc[q][0], acc[q][1], wv.x, wv.y, x[0], x[1]);
+                  fma2_rn(acc[q][2], acc[q][3], wv.z, wv.w, x[2], x[3]);
                 }
               }
               float score[QH];
@@ -666,22 +682,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int q = 0; q < QH; ++q) score[q] *= ks;
                 mbar_arrive_warp(&bars[C::BSE + sc]);
               }
-              // append candidates above each query's threshold
+              // append candidates above each query's threshold (the queries'
+              // slot reservations are issued back to back by lane 0)
               const int s = k * BKEY + key_lane;
+              bool take[QH];
+              uint32_t bal[QH];
+              int base[QH];
 #pragma unroll
               for (int q = 0; q < QH; ++q) {
                 const int qq = half * QH + q;
-                const bool take = qq < nq && s <= t0 + qq && score[q] > thr[qq];
-                const uint32_t bal = __ballot_sync(0xffffffffu, take);
-                if (bal) {
-                  int base = 0;
-                  if (lane == 0) base = atomicAdd(&cnt[qq], __popc(bal));
-                  base = __shfl_sync(0xffffffffu, base, 0);
-                  if (take) {
-                    const int pos = base + __popc(bal & ((1u << lane) - 1u));
-                    cand_s[qq * CAP + pos] = score[q];
-                    cand_i[qq * CAP + pos] = s;
-                  }
+                take[q] = qq < nq && s <= t0 + qq && score[q] > thr[qq];
+                bal[q] = __ballot_sync(0xffffffffu, take[q]);
+                base[q] = 0;
+              }
+              if (lane == 0) {
+#pragma unroll
+                for (int q = 0; q < QH; ++q)
+                  if (bal[q]) base[q] = atomicAdd(&cnt[half * QH + q], __popc(bal[q]));
+              }
+#pragma unroll
+              for (int q = 0; q < QH; ++q) {
+                const int qq = half * QH + q;
+                const int pos = __shfl_sync(0xffffffffu, base[q], 0) +
+                                __popc(bal[q] & ((1u << lane) - 1u));
+                if (take[q]) {
+                  cand_s[qq * CAP + pos] = score[q];
+                  cand_i[qq * CAP + pos] = s;
                 }
               }
             }
@@ -703,8 +729,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int qq = 0; qq < nq; ++qq) {
             if (cnt[qq] > CAP - 2 * BKEY) {
               const float kth = select_k<C::EPT, false>(cand_s + qq * CAP, cand_i + qq * CAP,
-                                                        cnt[qq], p.topk, gtid, hist, ctr, nullptr,
-                                                        CAP);
+                                                        cnt[qq], p.topk, gtid, hist, ctr, nullptr);
               if (gtid == 0) {
                 cnt[qq] = p.topk;
                 thr[qq] = kth;
@@ -728,7 +753,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           continue;
         }
         select_k<C::EPT, true>(cand_s + qq * CAP, cand_i + qq * CAP, cnt[qq], p.topk, gtid, hist,
-                               ctr, o, CAP);
+                               ctr, o);
       }
     }
   }
@@ -742,10 +767,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 }  // namespace idx
 
+// Persistent grid: one CTA per SM, or one per work item when there are fewer.
+template <int H_I, int D_I, bool FP8>
+static int64_t prefill_grid(int B, int Tq) {
+  using C = idx::Cfg<H_I, D_I, FP8>;
+  const int64_t items = static_cast<int64_t>(B) * ((Tq + C::QT - 1) / C::QT);
+  return items < num_sms() ? items : num_sms();
+}
+
 template <int H_I, int D_I, bool FP8>
 static dsa_status_t prefill_launch(const IndexerArgs& a, cudaStream_t stream) {
   using C = idx::Cfg<H_I, D_I, FP8>;
   if (a.topk > C::CAP - 2 * idx::BKEY) return DSA_ERR_UNSUPPORTED;
+  const int64_t grid = prefill_grid<H_I, D_I, FP8>(a.B, a.Tq);
+  if (a.scratch == nullptr ||
+      a.scratch_bytes < static_cast<size_t>(grid) * C::CTA_SCRATCH)
+    return DSA_ERR_WORKSPACE_TOO_SMALL;
   CUtensorMap tq, tk;
   const uint64_t qrows = static_cast<uint64_t>(a.B) * a.Tq * H_I;
   // (FP8 code rows are described as BF16 pairs: the copy moves bytes only)
@@ -772,17 +809,28 @@ static dsa_status_t prefill_launch(const IndexerArgs& a, cudaStream_t stream) {
   p.B = a.B;
   p.ntq = (a.Tq + C::QT - 1) / C::QT;
   p.out_idx = a.out_idx;
+  p.cand = static_cast<uint8_t*>(a.scratch);
   p.status = a.status;
   auto kern = idx::indexer_prefill_kernel<H_I, D_I, FP8>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
       cudaSuccess)
     return launch_status("cudaFuncSetAttribute");
   // persistent: one CTA per SM (shared memory allows no more)
-  const int64_t items = static_cast<int64_t>(a.B) * p.ntq;
-  const unsigned grid = static_cast<unsigned>(items < num_sms() ? items : num_sms());
-  kern<<<grid, idx::NTHREADS, C::SMEM_BYTES, stream>>>(tq, tk, p);
+  kern<<<static_cast<unsigned>(grid), idx::NTHREADS, C::SMEM_BYTES, stream>>>(tq, tk, p);
   return launch_status("indexer_prefill");
 }
+
+// The candidate buffers of the persistent grid (the same for BF16 and FP8).
+size_t indexer_prefill_scratch_bytes(int B, int Tq, int H_I, int D_I) {
+  if (H_I == 64 && D_I == 128)
+    return static_cast<size_t>(prefill_grid<64, 128, false>(B, Tq)) * idx::Cfg<64, 128, false>::CTA_SCRATCH;
+  if (H_I == 4 && D_I == 64)
+    return static_cast<size_t>(prefill_grid<4, 64, false>(B, Tq)) * idx::Cfg<4, 64, false>::CTA_SCRATCH;
+  return 0;
+}
+static_assert(idx::Cfg<64, 128, false>::CTA_SCRATCH == idx::Cfg<64, 128, true>::CTA_SCRATCH &&
+                  idx::Cfg<64, 128, false>::QT == idx::Cfg<64, 128, true>::QT,
+              "BF16 and FP8 share the workspace size");
 
 int indexer_prefill_max_topk(int H_I, int D_I) {
   if (H_I == 64 && D_I == 128) return idx::Cfg<64, 128, false>::CAP - 2 * idx::BKEY;

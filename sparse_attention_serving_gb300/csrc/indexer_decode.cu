@@ -123,8 +123,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   constexpr int QSLOT = C::OFF_K / 2;
   constexpr uint32_t IDESC = FP8 ? idesc_e4m3(128, N) : idesc_bf16(128, N, false, false);
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* sm = smem_align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_MISC);
   // q full [2] 0..1, q empty [2] 2..3, k full [NST] 4.., k empty [NST], d full [4], d empty [4], drain
   uint64_t* q_full = bars;

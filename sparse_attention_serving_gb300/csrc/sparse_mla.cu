@@ -218,8 +218,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   static_assert(HN * 4 <= (int)S_COL, "O^T columns");
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* sm = smem_align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_MISC);           // NBAR (<= 29)
   int* s_info = reinterpret_cast<int*>(sm + OFF_MISC + 232);             // [2][3] unit info ring
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_MISC + 256);

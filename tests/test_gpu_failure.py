@@ -11,12 +11,13 @@ def test_wait_timeout_is_reported_and_context_survives():
     import sparse_attention_serving_gb300 as dsa
     from gpu_helpers import bf, i32, to_u16
     from workloads import CONFIGS, prefill
-    ws = dsa.new_workspace(4096)
+    cfg = CONFIGS["tiny128"]
+    ws = dsa.new_workspace(max(4096, dsa.workspace_bytes(dsa.OP_INDEXER_TOPK, cfg.B, cfg.T, cfg.T,
+                                                         cfg.H_I, cfg.topk)))
     code, where, detail = dsa.selftest_wait_timeout(ws, 20_000_000)
     assert code == dsa.DSA_ERR_DEVICE_TIMEOUT and where == 0x500
     assert dsa.read_device_status(ws)[0] == dsa.DSA_OK  # reading clears it
     # the context is still usable: a real call afterwards succeeds
-    cfg = CONFIGS["tiny128"]
     d = prefill(cfg)
     idx = dsa.dsa_indexer_topk(bf(d["q_idx"]), bf(d["w"]), dsa.Rows(bf(d["k_idx"])),
                                i32(d["q_start"]), i32(d["kv_len"]), cfg.topk, cfg.T, workspace=ws)

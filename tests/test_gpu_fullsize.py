@@ -34,7 +34,8 @@ def test_prefill_fullsize(dsa, name):
     d = prefill(cfg)
     g = gate_inputs(cfg, N)
     qs, kl = i32(d["q_start"]), i32(d["kv_len"])
-    ws = dsa.new_workspace(1 << 20)
+    ws = dsa.new_workspace(max(dsa.workspace_bytes(op, B, T, T, h, cfg.topk) for op, h in
+                               ((dsa.OP_INDEXER_TOPK, cfg.H_I), (dsa.OP_SPARSE_MLA, cfg.H))))
     idx = dsa.dsa_indexer_topk(bf(d["q_idx"]), bf(d["w"]), dsa.Rows(bf(d["k_idx"])), qs, kl,
                                cfg.topk, T, workspace=ws)
     o_lat, lse = dsa.sparse_mla_fwd(bf(d["q_lat"]), dsa.Rows(bf(d["kv"])), idx, qs, kl, T,
