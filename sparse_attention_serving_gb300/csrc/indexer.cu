@@ -84,7 +84,12 @@ struct Cfg {
   // selection scratch (RBINS histogram bins and 16 counters)
   static constexpr int MISC_HDR = 1024;
   static constexpr int MISC_BYTES = MISC_HDR + (2048 + 16) * 4;
-  static constexpr int SMEM_BYTES = OFF_MISC + MISC_BYTES + 1024;
+  // per query, a histogram of the QHB top bits of the order keys of its
+  // candidates: it raises the append threshold while the keys stream and
+  // seeds the final selection
+  static constexpr int QHB = 10;
+  static constexpr int OFF_QH = OFF_MISC + MISC_BYTES;
+  static constexpr int SMEM_BYTES = OFF_QH + QT * (1 << QHB) * 4 + 1024;
   static constexpr int CAP = (H_I >= 64) ? 8192 : 1280;  // candidates per query
   static constexpr int CTA_SCRATCH = QT * CAP * 8;        // scores, then key indices
   static constexpr int EPT = (CAP + NEPI * 32 - 1) / (NEPI * 32);  // candidates per thread in a select
@@ -138,16 +143,24 @@ constexpr int SEL_G = NEPI * 32;           // selecting threads
 constexpr int SEL_CTR = 16;
 
 // Bin of the need-th largest element (bins ordered by value, counted from the
-// top): ctr[2] = bin, ctr[3] = elements in higher bins, ctr[4] = elements in it.
+// top) of an NB-bin histogram: ctr[2] = bin, ctr[3] = elements in higher bins,
+// ctr[4] = elements in it.  Thread t owns the PER = NB / SEL_G contiguous bins
+// NB-1-PER*t down to NB-PER*(t+1), read as 16-byte loads.
+template <int NB>
 __device__ __forceinline__ void find_bin(const int* hist, int need, int gtid, int* ctr) {
-  constexpr int PER = RBINS / SEL_G;
-  static_assert(PER == 8, "two 16-byte loads of bins per thread");
+  constexpr int PER = NB / SEL_G;
+  static_assert(PER % 4 == 0 && PER * SEL_G == NB, "whole 16-byte loads of bins per thread");
   const int lane = gtid & 31, w = gtid >> 5;
-  // thread t owns bins RBINS-1-8t down to RBINS-8-8t: one contiguous, 32-byte
-  // aligned block, read as two 16-byte loads (c[e] = bin RBINS-1-8t-e)
-  const int4* hb = reinterpret_cast<const int4*>(hist + RBINS - PER * (gtid + 1));
-  const int4 v0 = hb[0], v1 = hb[1];
-  int c[PER] = {v1.w, v1.z, v1.y, v1.x, v0.w, v0.z, v0.y, v0.x};
+  const int4* hb = reinterpret_cast<const int4*>(hist + NB - PER * (gtid + 1));
+  int c[PER];  // c[e] = bin NB-1-PER*gtid-e
+#pragma unroll
+  for (int v = 0; v < PER / 4; ++v) {
+    const int4 x = hb[v];
+    c[PER - 1 - 4 * v] = x.x;
+    c[PER - 2 - 4 * v] = x.y;
+    c[PER - 3 - 4 * v] = x.z;
+    c[PER - 4 - 4 * v] = x.w;
+  }
   int tot = 0;
 #pragma unroll
   for (int e = 0; e < PER; ++e) tot += c[e];
@@ -167,7 +180,7 @@ __device__ __forceinline__ void find_bin(const int* hist, int need, int gtid, in
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
       if (run < need && need <= run + c[e]) {
-        ctr[2] = RBINS - 1 - PER * gtid - e;
+        ctr[2] = NB - 1 - PER * gtid - e;
         ctr[3] = run;
         ctr[4] = c[e];
       }
@@ -177,10 +190,42 @@ __device__ __forceinline__ void find_bin(const int* hist, int need, int gtid, in
   named_bar_sync(1, SEL_G);
 }
 
-// The radix descent over keys delivered by `each(f)`, which calls f(key, valid)
-// for this thread's elements (the same elements on every call).  On return the
-// k-th largest key matches `prefix` on the bits of `pmask`; every element with
-// (key & pmask) > prefix is kept, and `need` of those equal to it.
+// Radix refinement over keys delivered by `each(f)`, which calls f(key, valid)
+// for this thread's elements (the same elements on every call).  On entry the
+// need-th largest key is known to match `prefix` on the bits of `pmask`
+// (= the bits [low, 32)); each pass histograms the next RBITS bits of the
+// elements that match and narrows the prefix, until the bin holding the
+// need-th key is kept whole or every bit is fixed.  On return every element
+// with (key & pmask) > prefix is kept, and `need` of those equal to it.
+template <class Each>
+__device__ __forceinline__ void radix_refine(Each each, int gtid, int* hist, int* ctr,
+                                             uint32_t& prefix, uint32_t& pmask, int& need,
+                                             int low) {
+  while (low > 0) {
+    const int sh = low > RBITS ? low - RBITS : 0;
+    const uint32_t dm = (1u << (low - sh)) - 1u;
+#pragma unroll
+    for (int e = 0; e < RBINS / SEL_G; ++e) hist[gtid + e * SEL_G] = 0;
+    named_bar_sync(1, SEL_G);
+    const uint32_t pm = pmask, pf = prefix;
+    each([&](uint32_t key, bool valid) {
+      if (valid && (key & pm) == pf) atomicAdd(&hist[(key >> sh) & dm], 1);
+    });
+    named_bar_sync(1, SEL_G);
+    find_bin<RBINS>(hist, need, gtid, ctr);
+    const uint32_t bin = static_cast<uint32_t>(ctr[2]);
+    const int above = ctr[3], inbin = ctr[4];
+    prefix |= bin << sh;
+    pmask |= dm << sh;
+    need -= above;
+    low = sh;
+    if (inbin == need) return;  // bin kept whole
+  }
+}
+
+// The full descent: the digits start at the highest bit where the smallest
+// and the largest key differ, so the first histogram already spreads the
+// candidates.
 template <class Each>
 __device__ __forceinline__ void radix_descent(Each each, int k, int gtid, int* hist, int* ctr,
                                               uint32_t& prefix, uint32_t& pmask, int& need) {
@@ -208,27 +253,7 @@ __device__ __forceinline__ void radix_descent(Each each, int k, int gtid, int* h
   const int top = 31 - __clz(lo ^ hi);
   pmask = top >= 31 ? 0u : ~((2u << top) - 1u);
   prefix = hi & pmask;
-  int low = top + 1;  // bits [low, 32) are fixed
-  while (true) {
-    const int sh = low > RBITS ? low - RBITS : 0;
-    const uint32_t dm = (1u << (low - sh)) - 1u;
-#pragma unroll
-    for (int e = 0; e < RBINS / SEL_G; ++e) hist[gtid + e * SEL_G] = 0;
-    named_bar_sync(1, SEL_G);
-    const uint32_t pm = pmask, pf = prefix;
-    each([&](uint32_t key, bool valid) {
-      if (valid && (key & pm) == pf) atomicAdd(&hist[(key >> sh) & dm], 1);
-    });
-    named_bar_sync(1, SEL_G);
-    find_bin(hist, need, gtid, ctr);
-    const uint32_t bin = static_cast<uint32_t>(ctr[2]);
-    const int above = ctr[3], inbin = ctr[4];
-    prefix |= bin << sh;
-    pmask |= dm << sh;
-    need -= above;
-    low = sh;
-    if (inbin == need || sh == 0) return;  // bin kept whole, or every bit fixed
-  }
+  radix_refine(each, gtid, hist, ctr, prefix, pmask, need, top + 1);
 }
 
 __device__ __forceinline__ void sel_reset(int* ctr, int gtid) {
@@ -240,26 +265,12 @@ __device__ __forceinline__ void sel_reset(int* ctr, int gtid) {
   named_bar_sync(1, SEL_G);
 }
 
-// Keep the k largest of the n candidates of one query.  The candidates are
-// loaded into registers (EPT per thread) once; every pass of the descent runs
-// on them.  Output positions come from one group-wide prefix sum (no atomic
-// per element): keys above the cut go to [0, above), the first `need` keys
-// equal to it (in thread order) right after them.
-//   FINAL: the indices go to out[0..k) (in no particular order), -1 padded
-//          when n <= k; returns 0.
-//   else:  the kept candidates are compacted to the front of the buffer and
-//          the k-th score (the query's new threshold) is returned.
-template <int EPT, bool FINAL>
-__device__ float select_k(float* cs, int32_t* ci, int n, int k, int gtid, int* hist, int* ctr,
-                          int32_t* out) {
-  if (FINAL && n <= k) {
-    for (int e = gtid; e < k; e += SEL_G) out[e] = e < n ? ci[e] : -1;
-    return 0.f;
-  }
-  // element e = gtid + u*SEL_G sits in register slot u (the buffer is in
-  // global memory: only the n filled entries are read)
-  uint32_t key[EPT];
-  int32_t id[EPT];
+// The n candidates of one query into registers: element e = gtid + u*SEL_G
+// sits in slot u (the buffer is in global memory: only the n filled entries
+// are read).
+template <int EPT>
+__device__ __forceinline__ void sel_load(const float* cs, const int32_t* ci, int n, int gtid,
+                                         uint32_t (&key)[EPT], int32_t (&id)[EPT]) {
 #pragma unroll
   for (int u = 0; u < EPT; ++u) {
     const int e = gtid + u * SEL_G;
@@ -270,17 +281,19 @@ __device__ float select_k(float* cs, int32_t* ci, int n, int k, int gtid, int* h
       id[u] = ci[e];
     }
   }
-  sel_reset(ctr, gtid);
-  uint32_t prefix, pmask;
-  int need;
-  auto each = [&](auto f) {
-#pragma unroll
-    for (int u = 0; u < EPT; ++u) f(key[u], id[u] >= 0);
-  };
-  radix_descent(each, k, gtid, hist, ctr, prefix, pmask, need);
-  // positions: per-thread counts above / equal (16 + 16 bits), one prefix sum;
-  // keys above the cut go to [0, above), the first `need` keys equal to it (in
-  // thread order) right after them
+}
+
+// Output positions of the kept elements once the cut is known (every element
+// with (key & pmask) > prefix, and the first `need` equal to it in thread
+// order): per-thread counts above / equal (16 + 16 bits), one prefix sum; keys
+// above the cut go to [0, above), the `need` equal ones right after them.
+//   FINAL: the indices go to out[0..k) (in no particular order); returns 0.
+//   else:  the kept candidates are compacted to the front of the buffer and
+//          the smallest kept score (the query's new threshold) is returned.
+template <int EPT, bool FINAL>
+__device__ __forceinline__ float sel_emit(const uint32_t (&key)[EPT], const int32_t (&id)[EPT],
+                                          uint32_t prefix, uint32_t pmask, int need, int gtid,
+                                          int* ctr, float* cs, int32_t* ci, int32_t* out) {
   const int lane = gtid & 31, w = gtid >> 5;
   int n_hi = 0, n_eq = 0;
 #pragma unroll
@@ -343,6 +356,108 @@ __device__ float select_k(float* cs, int32_t* ci, int n, int k, int gtid, int* h
   return kth;
 }
 
+// Keep the k largest of the n candidates of one query (a full radix descent)
+// and compact them to the front of the buffer; returns the k-th score.
+template <int EPT>
+__device__ float select_keep(float* cs, int32_t* ci, int n, int k, int gtid, int* hist, int* ctr) {
+  uint32_t key[EPT];
+  int32_t id[EPT];
+  sel_load<EPT>(cs, ci, n, gtid, key, id);
+  sel_reset(ctr, gtid);
+  uint32_t prefix, pmask;
+  int need;
+  auto each = [&](auto f) {
+#pragma unroll
+    for (int u = 0; u < EPT; ++u) f(key[u], id[u] >= 0);
+  };
+  radix_descent(each, k, gtid, hist, ctr, prefix, pmask, need);
+  return sel_emit<EPT, false>(key, id, prefix, pmask, need, gtid, ctr, cs, ci, nullptr);
+}
+
+// Final selection of one query: the indices of its k largest candidates go to
+// out[0..k) (in no particular order), -1 padded when n <= k.  qh is the
+// query's histogram of the QHB top bits of every candidate's order key, kept
+// up to date by the appends, so the first digit needs no pass over the
+// candidates: the descent starts from the bin holding the k-th key.
+template <int EPT, int QHB>
+__device__ void select_final(const float* cs, const int32_t* ci, int n, int k, const int* qh,
+                             int gtid, int* hist, int* ctr, int32_t* out) {
+  if (n <= k) {
+    for (int e = gtid; e < k; e += SEL_G) out[e] = e < n ? ci[e] : -1;
+    return;
+  }
+  uint32_t key[EPT];
+  int32_t id[EPT];
+  sel_load<EPT>(cs, ci, n, gtid, key, id);
+  find_bin<(1 << QHB)>(qh, k, gtid, ctr);
+  uint32_t prefix = static_cast<uint32_t>(ctr[2]) << (32 - QHB);
+  uint32_t pmask = ~((1u << (32 - QHB)) - 1u);
+  int need = k - ctr[3];
+  const int inbin = ctr[4];
+  auto each = [&](auto f) {
+#pragma unroll
+    for (int u = 0; u < EPT; ++u) f(key[u], id[u] >= 0);
+  };
+  if (inbin != need) radix_refine(each, gtid, hist, ctr, prefix, pmask, need, 32 - QHB);
+  sel_emit<EPT, true>(key, id, prefix, pmask, need, gtid, ctr, nullptr, nullptr, out);
+}
+
+// Raise a query's append threshold from its histogram (one warp): the lower
+// edge of the bin where the count of candidates from the top first reaches k.
+// At least k candidates lie at or above that edge, so the k-th largest score
+// of the query does too and no key below it can be in the top k.  The
+// histogram may be growing meanwhile (appends of other warps); a snapshot
+// only undercounts, which lowers the edge found, so the bound stays valid.
+// The 1024 bins are read as 32 rows of 32 (lane l reads bin 32r + l: no bank
+// conflicts); a recursive-halving exchange leaves lane l with the total of
+// row l, then suffix sums over the rows and over the bins of the row that
+// holds the k-th pick the edge.
+template <int QHB>
+__device__ __forceinline__ void raise_threshold(const int* qh, int k, int lane, uint32_t* tkey) {
+  constexpr int NR = (1 << QHB) / 32;
+  static_assert(NR == 32, "one row per lane");
+  int v[NR];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) v[r] = qh[32 * r + lane];
+  // after the step of width w, v[i] (i < w) is a partial total of row
+  // (lane & ~(w-1) & 31) + i over the lanes that differ in bit w; the last step
+  // leaves v[0] = the total of row `lane`
+#pragma unroll
+  for (int w = NR / 2; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const int send = upper ? v[i] : v[i + w];
+      const int keep = upper ? v[i + w] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  // suffix sums over the rows from the top (row 31 = the largest keys)
+  int cum = v[0];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_down_sync(0xffffffffu, cum, o);
+    if (lane + o < 32) cum += t;
+  }
+  const uint32_t hit = __ballot_sync(0xffffffffu, cum >= k);
+  if (hit == 0u) return;  // fewer than k candidates counted
+  const int row = 31 - __clz(hit);
+  const int above = __shfl_sync(0xffffffffu, cum - v[0], row);
+  // within the row, from its top bin (lane 31) down: inclusive suffix sums
+  int suf = qh[32 * row + lane];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_down_sync(0xffffffffu, suf, o);
+    if (lane + o < 32) suf += t;
+  }
+  // the highest bin with at least k counted at or above it (lane 0 always
+  // qualifies: its suffix is the whole row, read after the row totals)
+  const uint32_t hit2 = __ballot_sync(0xffffffffu, k <= above + suf);
+  if (hit2 == 0u) return;
+  const uint32_t edge = static_cast<uint32_t>(32 * row + 31 - __clz(hit2)) << (32 - QHB);
+  if (lane == 0 && edge > *tkey) *tkey = edge;
+}
+
 // One work item: a tile of QT consecutive queries of one sequence.  Items are
 // numbered heaviest first (w -> query tile ntq-1 - w/B of sequence w%B) and
 // dealt to the persistent CTAs in snake order: in round r, CTA c takes item
@@ -398,7 +513,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
   volatile int* g_abort = s_abort + 1;   // [4]
   int* cnt = const_cast<int*>(s_abort) + 8;  // [QT] candidates per query
-  float* thr = reinterpret_cast<float*>(cnt + 64);  // [QT]
+  uint32_t* tkey = reinterpret_cast<uint32_t*>(cnt + 64);  // [QT] smallest order key still taken
+  constexpr int QHB = C::QHB, QHN = 1 << QHB;
+  int* qhist = reinterpret_cast<int*>(sm + C::OFF_QH);  // [QT][QHN]
   int* hist = reinterpret_cast<int*>(sm + C::OFF_MISC + C::MISC_HDR);  // [RBINS]
   int* ctr = hist + RBINS;                                              // [SEL_CTR]
   static_assert(48 * 8 + 4 + 4 * 8 + 64 * 4 + 64 * 4 <= C::MISC_HDR, "misc header");
@@ -600,8 +717,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       for (int q = gtid; q < QT; q += G) {
         cnt[q] = 0;
-        thr[q] = -INFINITY;
+        tkey[q] = 0u;
       }
+      for (int e = gtid; e < QT * QHN; e += G) qhist[e] = 0;
       named_bar_sync(1, G);
       const int ntiles = I.ntiles;
       int kt = 0;
@@ -617,20 +735,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (; kt < ntiles; kt += 2) {
           const int n2 = ntiles - kt < 2 ? ntiles - kt : 2;
           bool w_ok = !vflag(s_abort);
-          for (int u = 0; u < n2 && w_ok; ++u) {
-            const int gk = g + kt + u;
-            w_ok = mbar_wait(&bars[C::BDF + gk % NBUF], (gk / NBUF) & 1, p.status, kWaitLimitNs, SITE_W_DF) &&
-                   (!FP8 || mbar_wait(&bars[C::BSF + gk % NSC1], (gk / NSC1) & 1, p.status,
-                                      kWaitLimitNs, SITE_W_SF));
-          }
-          // the TMEM loads and ballots below are warp-collective: one decision per warp
-          w_ok = __all_sync(0xffffffffu, w_ok);
-          if (!w_ok) {
-            g_abort[0] = 1;
-          } else {
-            tc_fence_after();
+          {
+            // each tile as soon as its accumulator is complete (with two TMEM
+            // buffers the MMA of the pair's second tile overlaps the first's
+            // reduction)
             for (int u = 0; u < n2; ++u) {
               const int k = kt + u, gk = g + k, buf = gk % NBUF;
+              if (w_ok)
+                w_ok = mbar_wait(&bars[C::BDF + buf], (gk / NBUF) & 1, p.status, kWaitLimitNs, SITE_W_DF) &&
+                       (!FP8 || mbar_wait(&bars[C::BSF + gk % NSC1], (gk / NSC1) & 1, p.status,
+                                          kWaitLimitNs, SITE_W_SF));
+              // the TMEM loads and ballots below are warp-collective: one decision per warp
+              w_ok = __all_sync(0xffffffffu, w_ok);
+              if (!w_ok) {
+                g_abort[0] = 1;
+                break;
+              }
+              tc_fence_after();
               // head reduction: 4 independent FMA chains per query (the MMA's FP32
               // accumulators are summed in a fixed order: chain c takes heads c, c+4, ...),
               // issued as 2-wide FP32 FMAs on the chain pairs (0,1) and (2,3), each
@@ -688,10 +809,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               bool take[QH];
               uint32_t bal[QH];
               int base[QH];
+              uint32_t okey[QH];
 #pragma unroll
               for (int q = 0; q < QH; ++q) {
                 const int qq = half * QH + q;
-                take[q] = qq < nq && s <= t0 + qq && score[q] > thr[qq];
+                okey[q] = order_key(score[q]);
+                take[q] = qq < nq && s <= t0 + qq && okey[q] >= tkey[qq];
                 bal[q] = __ballot_sync(0xffffffffu, take[q]);
                 base[q] = 0;
               }
@@ -708,18 +831,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (take[q]) {
                   cand_s[qq * CAP + pos] = score[q];
                   cand_i[qq * CAP + pos] = s;
+                  atomicAdd(&qhist[qq * QHN + (okey[q] >> (32 - QHB))], 1);
                 }
               }
             }
           }
+          // The pair's appends and abort flags are final after this barrier; every
+          // warp reads them before the second barrier, so that no warp's appends
+          // of the next pair can change what another warp decides here.
           named_bar_sync(1, G);
-          if (vflag(&g_abort[0])) {
+          const bool abort_now = vflag(&g_abort[0]);
+          // a buffer that could overflow on the next pair is shrunk outside this loop
+          for (int qq = 0; qq < nq; ++qq) want_sel |= cnt[qq] > CAP - 2 * BKEY;
+          named_bar_sync(1, G);
+          if (abort_now) {
             if (gtid == 0) s_abort[0] = 1;  // no role waits for this item's tiles any more
             stop = true;
             break;
           }
-          // a buffer that could overflow on the next pair is shrunk outside this loop
-          for (int qq = 0; qq < nq; ++qq) want_sel |= cnt[qq] > CAP - 2 * BKEY;
+          // warp q raises query q's threshold (no barrier: appends may read the
+          // old or the new value, both valid)
+          if (gtid / 32 < nq && cnt[gtid / 32] >= p.topk)
+            raise_threshold<QHB>(qhist + (gtid / 32) * QHN, p.topk, lane, &tkey[gtid / 32]);
           if (want_sel) {
             kt += n2;
             break;
@@ -728,12 +861,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (want_sel) {
           for (int qq = 0; qq < nq; ++qq) {
             if (cnt[qq] > CAP - 2 * BKEY) {
-              const float kth = select_k<C::EPT, false>(cand_s + qq * CAP, cand_i + qq * CAP,
-                                                        cnt[qq], p.topk, gtid, hist, ctr, nullptr);
+              const float kth = select_keep<C::EPT>(cand_s + qq * CAP, cand_i + qq * CAP, cnt[qq],
+                                                    p.topk, gtid, hist, ctr);
               if (gtid == 0) {
                 cnt[qq] = p.topk;
-                thr[qq] = kth;
+                tkey[qq] = order_key(kth);
               }
+              // the histogram now describes the k kept candidates only
+              for (int e = gtid; e < QHN; e += G) qhist[qq * QHN + e] = 0;
+              named_bar_sync(1, G);
+              for (int e = gtid; e < p.topk; e += G)
+                atomicAdd(&qhist[qq * QHN + (order_key(cand_s[qq * CAP + e]) >> (32 - QHB))], 1);
               named_bar_sync(1, G);
             }
           }
@@ -752,8 +890,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int e = gtid; e < p.topk; e += G) o[e] = -1;
           continue;
         }
-        select_k<C::EPT, true>(cand_s + qq * CAP, cand_i + qq * CAP, cnt[qq], p.topk, gtid, hist,
-                               ctr, o);
+        select_final<C::EPT, QHB>(cand_s + qq * CAP, cand_i + qq * CAP, cnt[qq], p.topk,
+                                  qhist + qq * QHN, gtid, hist, ctr, o);
       }
     }
   }
