@@ -553,29 +553,38 @@ def run_prefill_bwd(dsa, cfg, dev, stream, q_lat, kvrows, idx, o_lat, lse, T, pe
     kl = torch.tensor([T], dtype=torch.int32, device=dev)
     dkv = torch.zeros((1, T, 576), dtype=torch.float32, device=dev)
     dq = torch.empty((1, nq, cfg.H, 576), dtype=torch.float32, device=dev)
-    ws = dsa.new_workspace(256, dev)
-    run = lambda: dsa.sparse_mla_bwd(q, kvrows, ix, qs, kl, T, o, ls, d_o, dkv, cfg.scale, dq=dq,
-                                     workspace=ws)
-    run()
-    torch.cuda.synchronize(dev)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    K = 2
-    a.record(stream)
-    for _ in range(K):
+    # a workspace of dsa_workspace_bytes selects the tcgen05 kernels; the bare
+    # status header, the warp-level MMA path (timed beside it for comparison)
+    ws_tc = dsa.new_workspace(dsa.workspace_bytes(dsa.OP_SPARSE_MLA_BWD, 1, nq, T, cfg.H, cfg.topk), dev)
+    ws_w = dsa.new_workspace(256, dev)
+
+    def timed(ws, K=2):
+        run = lambda: dsa.sparse_mla_bwd(q, kvrows, ix, qs, kl, T, o, ls, d_o, dkv, cfg.scale,
+                                         dq=dq, workspace=ws)
         run()
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    code, where, detail = dsa.read_device_status(ws)
-    if code != dsa.DSA_OK:
-        raise RuntimeError(f"bwd device status {code} at {where:#x} ({detail})")
-    t = a.elapsed_time(b) / K / 1e3
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K):
+            run()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        code, where, detail = dsa.read_device_status(ws)
+        if code != dsa.DSA_OK:
+            raise RuntimeError(f"bwd device status {code} at {where:#x} ({detail})")
+        return a.elapsed_time(b) / K / 1e3
+
+    K = 2
+    t = timed(ws_tc, K)
+    t_warp = timed(ws_w, K)
     flop = nq * cfg.topk * 2 * cfg.H * (3 * 576 + 2 * 512)
     tf = flop / t / 1e12
     return {"ms": t * 1e3, "queries": nq, "tflops": tf, "frac_of_bf16_peak": tf / peak_bf16,
             "flop": flop, "unit": "TFLOP/s",
-            "note": "warp-level tensor-core MMA (m16n8k16 BF16, FP32 accumulate): dq kernel + "
-                    "dkv kernel with vector atomics; slice: last 512 queries of sequence 0",
-            "gpu_launches": K * 2}
+            "note": "tcgen05 kernels (P and dz from S^T and dP^T, dq from rows^T.dz^T, dKV from "
+                    "dz^T.q + p^T.dO with vector atomics); slice: last 512 queries of sequence 0",
+            "warp_mma_ms": t_warp * 1e3,
+            "gpu_launches": K * 3}
 
 
 def launches_per_step(dsa, B, T, cfg):

@@ -151,6 +151,11 @@ size_t dsa_workspace_bytes(dsa_op_t op, int B, int Tq, int max_kv_len, int heads
   if (B > 0 && Tq > 0) {
     if (op == DSA_OP_INDEXER_TOPK) extra = indexer_scratch_bytes(B, Tq, max_kv_len, heads, topk);
     if (op == DSA_OP_SPARSE_MLA) extra = sparse_mla_scratch_bytes(B, Tq, heads, topk);
+    if (op == DSA_OP_SPARSE_MLA_BWD && heads == 96 && topk > 0) {
+      // P and dZ of up to 512 queries at a time for the tensor-core kernels
+      const int64_t nq = static_cast<int64_t>(B) * Tq;
+      extra = static_cast<size_t>(nq < 512 ? nq : 512) * sparse_mla_bwd_tc_query_bytes(topk);
+    }
   }
   return kWorkspaceHeader + ((extra + 255) / 256) * 256;
 }
@@ -332,8 +337,9 @@ dsa_status_t sparse_mla_bwd(const uint16_t* q_lat, const dsa_rows_t* kv, const i
   SparseMlaBwdArgs a{};
   dsa_status_t st = resolve_rows(kv, B, max_kv_len, kRlat, &a.kv);
   if (st != DSA_OK) return st;
-  st = check_ws(workspace, ws_bytes,
-                dsa_workspace_bytes(DSA_OP_SPARSE_MLA_BWD, B, Tq, max_kv_len, H, topk));
+  // the status header is required; a workspace as large as dsa_workspace_bytes
+  // reports (96 heads) selects the tensor-core kernels
+  st = check_ws(workspace, ws_bytes, kWorkspaceHeader);
   if (st != DSA_OK) return st;
   a.q_lat = q_lat;
   a.idx = idx;
@@ -351,6 +357,8 @@ dsa_status_t sparse_mla_bwd(const uint16_t* q_lat, const dsa_rows_t* kv, const i
   a.dq = dq;
   a.dkv = dkv;
   a.status = static_cast<uint32_t*>(workspace);
+  a.scratch = static_cast<uint8_t*>(workspace) + kWorkspaceHeader;
+  a.scratch_bytes = ws_bytes - kWorkspaceHeader;
   return sparse_mla_bwd_launch(a, reinterpret_cast<cudaStream_t>(stream));
 }
 

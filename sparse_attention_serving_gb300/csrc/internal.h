@@ -65,8 +65,14 @@ struct SparseMlaBwdArgs {
   float* dq;
   float* dkv;        // FP32 rows numbered like kv's rows (accumulated into)
   uint32_t* status;
+  void* scratch;     // P and dZ of a chunk of queries (tensor-core path), or null
+  size_t scratch_bytes;
 };
 dsa_status_t sparse_mla_bwd_launch(const SparseMlaBwdArgs& a, cudaStream_t stream);
+// The tcgen05 path (H = 96): P and dZ scratch bytes per query, and the launch.
+size_t sparse_mla_bwd_tc_query_bytes(int topk);
+dsa_status_t sparse_mla_bwd_tc_launch(const SparseMlaBwdArgs& a, void* scratch, size_t scratch_bytes,
+                                      cudaStream_t stream);
 
 // --- indexer + top-k --------------------------------------------------------------
 struct IndexerArgs {

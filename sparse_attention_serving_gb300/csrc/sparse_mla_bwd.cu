@@ -390,6 +390,12 @@ __global__ void __launch_bounds__(NT, 2) bwd_dkv_kernel(const Params p) {
 
 dsa_status_t sparse_mla_bwd_launch(const SparseMlaBwdArgs& a, cudaStream_t stream) {
   using namespace mlab;
+  // 96 heads with room for at least one query's P and dZ: the tcgen05 kernels
+  const auto al16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  if (a.H == 96 && a.scratch != nullptr &&
+      a.scratch_bytes >= sparse_mla_bwd_tc_query_bytes(a.topk) && al16(a.d_o) && al16(a.o_lat) &&
+      al16(a.dq))
+    return sparse_mla_bwd_tc_launch(a, a.scratch, a.scratch_bytes, stream);
   Params p{};
   p.q = a.q_lat;
   p.kv = a.kv.base;

@@ -58,22 +58,33 @@ def _indices(seed, B, Tq, q0, k, frac_short=0.25):
     return idx
 
 
-def _run(dsa, q, kv_rows_dev, idx, q_start, kv_len, S, dO, dkv_shape, scale):
+def bwd_workspace(dsa, path, B, Tq, S, H, k):
+    """"tc": as large as dsa_workspace_bytes reports (at 96 heads this selects the
+    tcgen05 kernels); "warp": the bare status header (the warp-level MMA path)."""
+    n = dsa.workspace_bytes(dsa.OP_SPARSE_MLA_BWD, B, Tq, S, H, k) if path == "tc" else 256
+    return dsa.new_workspace(n)
+
+
+def _run(dsa, q, kv_rows_dev, idx, q_start, kv_len, S, dO, dkv_shape, scale, path="tc"):
     qt, dOt = bf(q), bf(dO)
     it, qs, kl = i32(idx), i32(q_start), i32(kv_len)
     o_lat, lse = dsa.sparse_mla_fwd(qt, kv_rows_dev, it, qs, kl, S, scale)
     dkv = torch.zeros(dkv_shape, dtype=torch.float32, device="cuda")
-    ws = dsa.new_workspace(256)
+    B, Tq, H = q.shape[:3]
+    ws = bwd_workspace(dsa, path, B, Tq, S, H, idx.shape[-1])
     dq = dsa.sparse_mla_bwd(qt, kv_rows_dev, it, qs, kl, S, o_lat, lse, dOt, dkv, scale,
                             workspace=ws)
     code, where, detail = dsa.read_device_status(ws)
     return dq.cpu().numpy(), dkv.cpu().numpy(), code
 
 
-@pytest.mark.parametrize("B,T,H,k", [(1, 256, 8, 64), (2, 300, 96, 64), (1, 160, 96, 200)])
-def test_bwd_contiguous(dsa, B, T, H, k):
+@pytest.mark.parametrize("B,T,H,k,path", [(1, 256, 8, 64, "warp"), (2, 300, 96, 64, "warp"),
+                                          (1, 160, 96, 200, "warp"), (2, 300, 96, 64, "tc"),
+                                          (1, 160, 96, 200, "tc"), (1, 520, 96, 384, "tc")])
+def test_bwd_contiguous(dsa, B, T, H, k, path):
     """Contiguous latent rows; ragged key counts (some queries keep fewer than k,
-    some none), k not a multiple of the 32-key block."""
+    some none), k not a multiple of the 32-key (warp path) or 128-key (tensor-core
+    path) block."""
     seed = 100 + T + H
     q = normal_bf16(seed, "q_lat", (B, T, H, 576))
     kv = normal_bf16(seed, "kv", (B, T, 576))
@@ -81,7 +92,8 @@ def test_bwd_contiguous(dsa, B, T, H, k):
     idx = _indices(seed, B, T, 0, k)
     q_start, kv_len = np.zeros(B, np.int32), np.full(B, T, np.int32)
     scale = 1.0 / np.sqrt(192.0)
-    dq, dkv, code = _run(dsa, q, dsa.Rows(bf(kv)), idx, q_start, kv_len, T, dO, (B, T, 576), scale)
+    dq, dkv, code = _run(dsa, q, dsa.Rows(bf(kv)), idx, q_start, kv_len, T, dO, (B, T, 576), scale,
+                         path)
     assert code == dsa.DSA_OK
     rdq, rdkv = oracle.sparse_mla_bwd(q, kv, idx, q_start, kv_len, scale, dO)
     _check(dq, rdq, "dq")
@@ -122,10 +134,11 @@ def test_bwd_paged_chunk(dsa):
     _check(got, want, "dkv (pool, added)")
 
 
-def test_bwd_bad_index_is_flagged_and_skipped(dsa):
+@pytest.mark.parametrize("H,path", [(8, "warp"), (96, "tc")])
+def test_bwd_bad_index_is_flagged_and_skipped(dsa, H, path):
     """A non-causal entry: DSA_ERR_BAD_INDEX, and the gradients equal those of
     the index set without it."""
-    B, T, H, k = 1, 96, 8, 32
+    B, T, k = 1, 96, 32
     seed = 141
     q = normal_bf16(seed, "q_lat", (B, T, H, 576))
     kv = normal_bf16(seed, "kv", (B, T, 576))
@@ -142,7 +155,7 @@ def test_bwd_bad_index_is_flagged_and_skipped(dsa):
     # the forward on the clean set (it would flag the bad entry too)
     o_lat, lse = dsa.sparse_mla_fwd(qt, rows, i32(clean), qs, kl, T, scale)
     dkv = torch.zeros((B, T, 576), dtype=torch.float32, device="cuda")
-    ws = dsa.new_workspace(256)
+    ws = bwd_workspace(dsa, path, B, T, T, H, k)
     dq = dsa.sparse_mla_bwd(qt, rows, i32(idx), qs, kl, T, o_lat, lse, dOt, dkv, scale, workspace=ws)
     code, where, detail = dsa.read_device_status(ws)
     assert code == dsa.DSA_ERR_BAD_INDEX and detail == 77

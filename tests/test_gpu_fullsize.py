@@ -163,12 +163,14 @@ def test_decode64_fp8_fullsize(dsa):
                         f"fp8 decode req {b}")
 
 
-def test_bwd_fullsize_slice(dsa):
+@pytest.mark.parametrize("path", ["tc", "warp"])
+def test_bwd_fullsize_slice(dsa, path):
     """The backward on full-size index sets: the indexer and forward run on the whole
     val4096 sequence; the backward takes its last 8 queries (each with k = 2,048
-    selected keys) and is checked against the float64 gradient."""
+    selected keys) and is checked against the float64 gradient, on the tcgen05
+    kernels and on the warp-level MMA path."""
     import oracle
-    from test_gpu_bwd import _check
+    from test_gpu_bwd import _check, bwd_workspace
     cfg = CONFIGS["val4096"]
     T, nq = cfg.T, 8
     d = prefill(cfg)
@@ -183,7 +185,7 @@ def test_bwd_fullsize_slice(dsa):
     from workloads import bf16_round
     dO = bf16_round(dO)
     dkv = torch.zeros((1, T, 576), dtype=torch.float32, device="cuda")
-    ws = dsa.new_workspace(256)
+    ws = bwd_workspace(dsa, path, 1, nq, T, cfg.H, cfg.topk)
     dq = dsa.sparse_mla_bwd(sl(bf(d["q_lat"])), kvrows, sl(idx), i32([q0]), i32([T]), T, sl(o_lat),
                             sl(lse), bf(dO), dkv, cfg.scale, workspace=ws)
     assert dsa.read_device_status(ws)[0] == dsa.DSA_OK
