@@ -84,21 +84,6 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// try_wait with a suspend-time hint: a waiting thread sleeps until the phase
-// completes (or the hint runs out) instead of polling the barrier's word in
-// shared memory, which competes with the tensor core's operand reads.
-__device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-constexpr uint32_t kSuspendHintNs = 100000u;  // 100 us per try: the time limit is checked every 16
-
 // Bounded wait on a phase parity.  Returns false (and records `code` in the
 // status word) when the barrier has not flipped within `limit_ns`, so that no
 // kernel can spin forever on a shared GPU.
@@ -109,7 +94,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 16; ++i)
-      if (mbar_test_sleep(bar, parity, kSuspendHintNs)) return true;
+      if (mbar_test(bar, parity)) return true;
     if (globaltimer_ns() - t0 > limit_ns) {
       status_raise(status, DSA_ERR_DEVICE_TIMEOUT, where);
       return false;

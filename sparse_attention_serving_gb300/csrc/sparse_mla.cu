@@ -155,7 +155,7 @@ __device__ __forceinline__ bool mbar_wait_unless(uint64_t* bar, uint32_t parity,
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 16; ++i)
-      if (mbar_test_sleep(bar, parity, kSuspendHintNs)) return true;
+      if (mbar_test(bar, parity)) return true;
     if (vload(abort_flag)) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       status_raise(status, DSA_ERR_DEVICE_TIMEOUT, where);

@@ -15,7 +15,7 @@
 // the work is three kernels over a chunk of queries, with P and dZ (BF16, the
 // precision the products take them in) passed through the workspace as
 // [query][head][list entry]:
-//   K1 bwd_pz   grid (queries, 2 head groups of 48).  Rows of 128 list entries
+//   K1 bwd_pz   grid (2 head groups of 48; queries).  Rows of 128 list entries
 //               are gathered one 64-dim chunk (16 KB) at a time into a ring;
 //                 S^T [128 x 48] += rows_c . q_g,c^T     (M=128 entries, N=48)
 //                 dP^T[128 x 48] += rows_c . dO_g,c^T    (c < 8)
@@ -25,15 +25,15 @@
 //               and the entries' dz (TMA, [96 heads x 64 entries]):
 //                 dq^T[512 x 96] += rows^T . dz^T        (4 x M=128 dims, N=96)
 //                 dq_rope[96 x 64] += dz . rows_rope     (M=128 heads, N=64)
-//   K3 bwd_dkv  grid (queries, 3 dim ranges: 0-255, 256-511, 512-575).  dz and
-//               p of 128 entries (TMA, entries contiguous: the MN-major A
-//               operand) against q and dO of the range (TMA, dims contiguous:
-//               the MN-major B operand):
-//                 dKV[128 x 256] = dz^T . q_r + p^T . dO_r    (M=128, N=256)
-//               then each lane (one entry) adds its row into the FP32 dkv row
-//               with 16-byte vector atomics (rows are shared by the queries
-//               that selected them, so the order of the additions, and the
-//               FP32 rounding of dkv, vary run to run).
+//   K3 bwd_dkv  grid (3 dim ranges: 0-255, 256-511, 512-575; queries).  q and
+//               dO of the range (TMA, dims contiguous) against dz and p of 128
+//               entries (TMA, entries contiguous), both MN-major:
+//                 dKV^T[128 dims x 128] = q_r^T . dz + dO_r^T . p   (M=128, N=128)
+//               then each lane (one dim) adds its value for each entry into
+//               the FP32 dkv row with atomics, a warp covering 32 consecutive
+//               dims of one row (rows are shared by the queries that selected
+//               them, so the order of the additions, and the FP32 rounding of
+//               dkv, vary run to run).
 // Every wait is bounded (an abort flag per CTA stops the other roles).
 #include <cuda_bf16.h>
 
@@ -86,12 +86,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c),
-               "f"(d)
-               : "memory");
-}
-
 // The query row's sequence, position and key count.
 struct QInfo {
   int b, t, L;
@@ -130,11 +124,11 @@ __device__ __forceinline__ int64_t entry_row(const Params& p, int64_t qg, const 
 }
 
 // =============================================================================
-// K1: p and dz.  Threads: warps 0-3 gather, warps 4-7 epilogue (one TMEM lane
-// quarter each), warp 8 MMA issuer and TMEM owner.
+// K1: p and dz.  Threads: warps 0-7 gather, warps 8-11 epilogue (one TMEM lane
+// quarter each), warp 12 MMA issuer and TMEM owner.
 // =============================================================================
 namespace k1 {
-constexpr int NT = 288;
+constexpr int NT = 416;
 constexpr int QCH = HG * 128;          // one 64-dim chunk of the group's 48 q (or dO) rows
 constexpr int SLOT = 128 * 128;        // 128 entries x one 64-dim chunk
 constexpr int NR = 7;                  // ring slots
@@ -163,7 +157,7 @@ __global__ void __launch_bounds__(k1::NT, 1)
   float* s_D = reinterpret_cast<float*>(sm + OFF_MISC + NBAR * 8 + 8);
   float* s_l2 = s_D + HG;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ql = blockIdx.x, g = blockIdx.y;
+  const int ql = blockIdx.y, g = blockIdx.x;  // the two head groups of a query adjacent
   const int64_t qg = p.q0 + ql;
   const QInfo Q = qinfo(p, qg);
   const int nblk = p.tpad / 128;
@@ -172,7 +166,7 @@ __global__ void __launch_bounds__(k1::NT, 1)
   if (tid == 0) {
     mbar_init(&bars[B_Q], 1);
     for (int i = 0; i < NR; ++i) {
-      mbar_init(&bars[B_F + i], 128);
+      mbar_init(&bars[B_F + i], 256);
       mbar_init(&bars[B_E + i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -183,7 +177,7 @@ __global__ void __launch_bounds__(k1::NT, 1)
     s_abort[0] = 0;
     fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == 12) {
     tmem_alloc(tslot, 256);
     tmem_relinquish();
   }
@@ -192,8 +186,10 @@ __global__ void __launch_bounds__(k1::NT, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  if (warp < 4) {
-    // ============ gather: thread t owns entry t of every 128-entry block ============
+  if (warp < 8) {
+    // ============ gather (8 warps): eight consecutive lanes copy the eight
+    // 16-byte units of one entry's 128-byte piece (whole 128-byte lines per
+    // request); thread t covers unit t % 8 of entries t / 8 + 32 i, i = 0..3 ============
     if (tid == 0) {
       mbar_expect_tx(&bars[B_Q], (9 + 8) * QCH);
       const int row = static_cast<int>(qg * H + g * HG);
@@ -201,12 +197,17 @@ __global__ void __launch_bounds__(k1::NT, 1)
       for (int c = 0; c < 8; ++c) tma_load_2d(sm + OFF_DO + c * QCH, &tm_do48, &bars[B_Q], 64 * c, row);
     }
     const int64_t dummy = p.paged ? 0 : static_cast<int64_t>(Q.b) * p.seq_stride;
-    uint32_t doff[8];
+    const int u8 = tid & 7, e0 = tid >> 3;
+    uint32_t doff[4];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) doff[u] = sw128_unit(tid, u);
+    for (int i = 0; i < 4; ++i) doff[i] = sw128_unit(e0 + 32 * i, u8);
     for (int j = 0; j < nblk; ++j) {
-      const int64_t r = entry_row(p, qg, Q, 128 * j + tid, false);
-      const uint16_t* src = p.kv + (r >= 0 ? r : dummy) * kRlat;
+      const uint16_t* src[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t r = entry_row(p, qg, Q, 128 * j + e0 + 32 * i, false);
+        src[i] = p.kv + (r >= 0 ? r : dummy) * kRlat + u8 * 8;
+      }
       bool stop = false;
       for (int c = 0; c < 9; ++c) {
         const int gc = 9 * j + c, slot = gc % NR, use = gc / NR;
@@ -215,15 +216,15 @@ __global__ void __launch_bounds__(k1::NT, 1)
         if (vflag(s_abort)) { stop = true; break; }
         const uint32_t dst = smem_u32(sm + OFF_RING + slot * SLOT);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) cp_async_16(dst + doff[u], src + c * 64 + u * 8);
+        for (int i = 0; i < 4; ++i) cp_async_16(dst + doff[i], src[i] + c * 64);
         cp_async_arrive(&bars[B_F + slot]);
       }
       if (stop) break;
     }
     cp_async_wait_all();
-  } else if (warp < 8) {
+  } else if (warp < 12) {
     // ============ epilogue: lane = list entry of the block ============
-    const int ew = warp - 4, sub = warp & 3;
+    const int ew = warp - 8, sub = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(sub * 32) << 16;
     const int el = sub * 32 + lane;  // entry within the block (TMEM lane)
     // D = dO . o and lse (log2) of the group's heads
@@ -287,7 +288,7 @@ __global__ void __launch_bounds__(k1::NT, 1)
         zz[static_cast<int64_t>(hh) * p.tpad + e] = __bfloat16_as_ushort(__float2bfloat16_rn(z));
       }
     }
-  } else if (warp == 8) {
+  } else if (warp == 12) {
     // ============ MMA issuer ============
     if (lane == 0) {
       bool ok = mbar_wait(&bars[B_Q], 0, p.status, kWaitLimitNs, SITE_W1_Q);
@@ -332,18 +333,18 @@ __global__ void __launch_bounds__(k1::NT, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 12) {
     tc_fence_after();
     tmem_dealloc(tmem, 256);
   }
 }
 
 // =============================================================================
-// K2: dq.  Threads: warps 0-3 gather (+ the dz TMA), warps 4-7 epilogue,
-// warp 8 MMA issuer and TMEM owner.
+// K2: dq.  Threads: warps 0-7 gather (+ the dz TMA), warps 8-11 epilogue,
+// warp 12 MMA issuer and TMEM owner.
 // =============================================================================
 namespace k2 {
-constexpr int NT = 288;
+constexpr int NT = 416;
 constexpr int PAIR = 2 * CH;                 // 64 entries x 128 dims
 constexpr int ZT = 128 * 128;                // dz tile: 96 head rows (+32 spare) x 64 entries
 constexpr int BLK = 4 * PAIR + CH + ZT;      // 88 KB per 64-entry block
@@ -351,7 +352,9 @@ constexpr int NS = 2;                        // block stages
 constexpr int OFF_BLK = 0;
 constexpr int OFF_MISC = OFF_BLK + NS * BLK;
 constexpr int B_F = 0, B_E = B_F + NS, B_D = B_E + NS, NBAR = B_D + 1;
-constexpr int SMEM = OFF_MISC + 1024 + 1024;
+constexpr int MISC = 256 + 2 * 64 * 8;       // barriers, then the row table [2][64]
+constexpr int SMEM = OFF_MISC + MISC + 1024;
+static_assert(NBAR * 8 + 8 <= 256, "barriers before the row table");
 static_assert(SMEM <= 232448, "shared memory budget");
 }  // namespace k2
 
@@ -363,6 +366,7 @@ __global__ void __launch_bounds__(k2::NT, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_MISC);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + NBAR);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
+  int64_t* s_row = reinterpret_cast<int64_t*>(sm + OFF_MISC + 256);  // [2][64]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ql = blockIdx.x;
   const int64_t qg = p.q0 + ql;
@@ -373,7 +377,7 @@ __global__ void __launch_bounds__(k2::NT, 1)
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&bars[B_F + i], 128 + 1);  // 128 gathering threads + the dz TMA
+      mbar_init(&bars[B_F + i], 256 + 1);  // 256 gathering threads + the dz TMA
       mbar_init(&bars[B_E + i], 1);
     }
     mbar_init(&bars[B_D], 1);
@@ -388,7 +392,7 @@ __global__ void __launch_bounds__(k2::NT, 1)
         make_uint4(0u, 0u, 0u, 0u);
   }
   fence_proxy_async_smem();
-  if (warp == 8) {
+  if (warp == 12) {
     tmem_alloc(tslot, 512);
     tmem_relinquish();
   }
@@ -397,34 +401,43 @@ __global__ void __launch_bounds__(k2::NT, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  if (warp < 4) {
-    // ============ gather: thread t = (entry t % 64, half t / 64 of its 72 units) ============
-    const int key = tid & 63, half = tid >> 6;
+  if (warp < 8) {
+    // ============ gather: the block's 64 x 72 16-byte units, unit U = 256 i + t
+    // (consecutive lanes take consecutive units of a row: whole 128-byte lines
+    // per request); the entries' rows are looked up once into shared memory ============
     const int64_t dummy = p.paged ? 0 : static_cast<int64_t>(Q.b) * p.seq_stride;
     for (int j = 0; j < nblk; ++j) {
       const int st = j % NS, use = j / NS;
-      if (use > 0 && !mbar_wait(&bars[B_E + st], (use - 1) & 1, p.status, kWaitLimitNs, SITE_W2_E))
+      const bool fail =
+          use > 0 && !mbar_wait(&bars[B_E + st], (use - 1) & 1, p.status, kWaitLimitNs, SITE_W2_E);
+      if (tid < 64) {
+        const int64_t r = entry_row(p, qg, Q, 64 * j + tid, false);
+        s_row[(j & 1) * 64 + tid] = r >= 0 ? r : dummy;
+      }
+      // the rows are visible to all 256 threads after this barrier, and the stop
+      // decision is the same for all of them
+      if (named_bar_or(2, 256, fail || vflag(s_abort))) {
         s_abort[0] = 1;
-      if (vflag(s_abort)) break;
+        break;
+      }
       uint8_t* base = sm + OFF_BLK + st * BLK;
       if (tid == 0) {
         mbar_expect_tx(&bars[B_F + st], 96 * 128);
         tma_load_2d(base + 4 * PAIR + CH, &tm_z, &bars[B_F + st], 64 * j, ql * H);
       }
-      const int64_t r = entry_row(p, qg, Q, 64 * j + key, false);
-      const uint16_t* src = p.kv + (r >= 0 ? r : dummy) * kRlat;
       const uint32_t b32 = smem_u32(base);
+      const int64_t* rows = s_row + (j & 1) * 64;
 #pragma unroll 4
-      for (int v = 0; v < 36; ++v) {
-        const int u = half * 36 + v, c = u >> 3, uu = u & 7;
+      for (int i = 0; i < 18; ++i) {
+        const int U = 256 * i + tid, key = U / 72, u = U - 72 * key, c = u >> 3, uu = u & 7;
         const uint32_t dst = c < 8 ? b32 + (c >> 1) * PAIR + (c & 1) * CH + sw128_unit(key, uu)
                                    : b32 + 4 * PAIR + sw128_unit(key, uu);
-        cp_async_16(dst, src + u * 8);
+        cp_async_16(dst, p.kv + rows[key] * kRlat + u * 8);
       }
       cp_async_arrive(&bars[B_F + st]);
     }
     cp_async_wait_all();
-  } else if (warp < 8) {
+  } else if (warp < 12) {
     // ============ epilogue: dq written once ============
     const int sub = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(sub * 32) << 16;
@@ -462,7 +475,7 @@ __global__ void __launch_bounds__(k2::NT, 1)
                       : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-  } else if (warp == 8) {
+  } else if (warp == 12) {
     // ============ MMA issuer ============
     if (lane == 0) {
       bool ok = true;
@@ -501,28 +514,36 @@ __global__ void __launch_bounds__(k2::NT, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 12) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
 // =============================================================================
-// K3: dkv.  Threads: warp 0 TMA producer, warp 1 MMA issuer and TMEM owner,
-// warps 2-5 epilogue (one TMEM lane quarter each).
+// K3: dkv, computed transposed so that a TMEM lane is one dim and a column one
+// list entry: each warp's atomic then covers 32 consecutive dims of one dkv
+// row (one 128-byte line) instead of 32 different rows.
+//   dKV^T[dims x 128 entries] = q_r^T . dz + dO_r^T . p    (M=128 dims, N=128)
+// A = q^T / dO^T of the range ([96 heads x 64 dims] boxes, dims contiguous:
+// MN-major), B = dz / p of 128 entries ([96 heads x 64 entries] boxes, entries
+// contiguous: MN-major).  Threads: warp 0 TMA producer, warp 1 MMA issuer and
+// TMEM owner, warps 2-9 epilogue (two 128-dim tiles x four lane quarters).
 // =============================================================================
 namespace k3 {
-constexpr int NT = 192;
+constexpr int NT = 320;
 constexpr int QB = H * 128;                // [96 heads x 64] box (12 KB)
-constexpr int OFF_QR = 0;                  // q of the range: 4 boxes (1 for the rope range)
-constexpr int OFF_DR = OFF_QR + 4 * QB;    // dO of the range: 4 boxes
-constexpr int STAGE = 4 * QB;              // dz^T (2 boxes) + p^T (2 boxes) of 128 entries
+constexpr int OFF_QR = 0;                  // q^T of the range: 4 boxes (the rope range: 2, one past the end)
+constexpr int OFF_DR = OFF_QR + 4 * QB;    // dO^T of the range: 4 boxes
+constexpr int STAGE = 4 * QB;              // dz (2 boxes) + p (2 boxes) of 128 entries
 constexpr int OFF_ST = OFF_DR + 4 * QB;
 constexpr int NS = 2;
 constexpr int OFF_MISC = OFF_ST + NS * STAGE;
 constexpr int B_B = 0, B_F = 1, B_E = B_F + NS, B_DF = B_E + NS, B_DE = B_DF + 2, B_DRAIN = B_DE + 2,
               NBAR = B_DRAIN + 1;
-constexpr int SMEM = OFF_MISC + 1024 + 1024;
+constexpr int MISC = 256 + 2 * 128 * 8;    // barriers, then the entries' rows [2][128]
+constexpr int SMEM = OFF_MISC + MISC + 1024;
+static_assert(NBAR * 8 + 8 <= 256, "barriers before the row table");
 static_assert(SMEM <= 232448, "shared memory budget");
 }  // namespace k3
 
@@ -536,15 +557,17 @@ __global__ void __launch_bounds__(k3::NT, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_MISC);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + NBAR);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
+  int64_t* s_row = reinterpret_cast<int64_t*>(sm + OFF_MISC + 256);  // [2][128]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ql = blockIdx.x, rg = blockIdx.y;  // dims [256 rg, 256 rg + nd)
+  // the three dim-range CTAs of a query are adjacent in launch order, so the
+  // second and third read that query's p and dz from L2
+  const int ql = blockIdx.y, rg = blockIdx.x;  // dims [256 rg, 256 rg + 256) (rope: 512..575)
   const int64_t qg = p.q0 + ql;
   const QInfo Q = qinfo(p, qg);
   const int nblk = p.tpad / 128;
   const bool rope = rg == 2;
-  const int nbox = rope ? 1 : 4;              // 64-dim boxes of the range
-  constexpr uint32_t IDESC_V = idesc_bf16(128, 256, true, true);
-  constexpr uint32_t IDESC_R = idesc_bf16(128, 64, true, true);
+  const int ntile = rope ? 1 : 2;             // 128-dim M tiles of the range
+  constexpr uint32_t IDESC = idesc_bf16(128, 128, true, true);
 
   if (tid == 0) {
     mbar_init(&bars[B_B], 1);
@@ -554,7 +577,7 @@ __global__ void __launch_bounds__(k3::NT, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[B_DF + i], 1);
-      mbar_init(&bars[B_DE + i], 4);
+      mbar_init(&bars[B_DE + i], 8);
     }
     mbar_init(&bars[B_DRAIN], 1);
     s_abort[0] = 0;
@@ -571,9 +594,10 @@ __global__ void __launch_bounds__(k3::NT, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // q (and dO) of the range: [96 heads x 64 dims] boxes, dims contiguous
-      mbar_expect_tx(&bars[B_B], (rope ? 1 : 8) * QB);
-      for (int c = 0; c < nbox; ++c)
+      // q (and dO) of the range: [96 heads x 64 dims] boxes; the rope range's
+      // second box lies past dim 575 and is filled with zeros by the copy
+      mbar_expect_tx(&bars[B_B], (rope ? 2 : 8) * QB);
+      for (int c = 0; c < 2 * ntile; ++c)
         tma_load_2d(sm + OFF_QR + c * QB, &tm_q96, &bars[B_B], 256 * rg + 64 * c, static_cast<int>(qg * H));
       if (!rope)
         for (int c = 0; c < 4; ++c)
@@ -602,7 +626,7 @@ __global__ void __launch_bounds__(k3::NT, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       bool ok = mbar_wait(&bars[B_B], 0, p.status, kWaitLimitNs, SITE_W3_B);
-      const uint64_t qd = smem_desc(smem_u32(sm + OFF_QR), QB, 1024);  // [K=heads][N=dims], MN-major
+      const uint64_t qd = smem_desc(smem_u32(sm + OFF_QR), QB, 1024);  // [K=heads][M=dims], MN-major
       const uint64_t dd = smem_desc(smem_u32(sm + OFF_DR), QB, 1024);
       for (int j = 0; j < nblk && ok; ++j) {
         const int st = j % NS, buf = j & 1;
@@ -617,17 +641,19 @@ __global__ void __launch_bounds__(k3::NT, 1)
         }
         tc_fence_after();
         const uint32_t base = smem_u32(sm + OFF_ST + st * STAGE);
-        const uint64_t zd = smem_desc(base, QB, 1024);           // [K=heads][M=entries], MN-major
+        const uint64_t zd = smem_desc(base, QB, 1024);           // [K=heads][N=entries], MN-major
         const uint64_t pd = smem_desc(base + 2 * QB, QB, 1024);
-        const uint32_t d = tmem + buf * 256;
-#pragma unroll
-        for (int kk = 0; kk < 6; ++kk)
-          umma_bf16(d, desc_add(zd, kk * 2048), desc_add(qd, kk * 2048), rope ? IDESC_R : IDESC_V,
-                    kk ? 1u : 0u);
-        if (!rope) {
+        for (int mt = 0; mt < ntile; ++mt) {
+          const uint32_t d = tmem + buf * 256 + mt * 128;
 #pragma unroll
           for (int kk = 0; kk < 6; ++kk)
-            umma_bf16(d, desc_add(pd, kk * 2048), desc_add(dd, kk * 2048), IDESC_V, 1u);
+            umma_bf16(d, desc_add(qd, mt * 2 * QB + kk * 2048), desc_add(zd, kk * 2048), IDESC,
+                      kk ? 1u : 0u);
+          if (!rope) {
+#pragma unroll
+            for (int kk = 0; kk < 6; ++kk)
+              umma_bf16(d, desc_add(dd, mt * 2 * QB + kk * 2048), desc_add(pd, kk * 2048), IDESC, 1u);
+          }
         }
         umma_commit(&bars[B_E + st]);
         umma_commit(&bars[B_DF + buf]);
@@ -639,30 +665,36 @@ __global__ void __launch_bounds__(k3::NT, 1)
     }
     __syncwarp();
   } else {
-    // ============ epilogue: lane = list entry; add its row ============
-    const int sub = warp & 3;
+    // ============ epilogue: lane = dim, columns = entries ============
+    const int et = tid - 64;                       // 0..255
+    const int sub = warp & 3, mt = (warp - 2) >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(sub * 32) << 16;
-    const int el = sub * 32 + lane;
-    const int nd = rope ? 64 : 256;
+    const int dim = 256 * rg + 128 * mt + sub * 32 + lane;
+    const bool act = mt < ntile;                   // a warp with a tile of this range
+    const bool dim_ok = dim < kRlat;
     for (int j = 0; j < nblk; ++j) {
       const int buf = j & 1;
+      // the block's entries' rows (the table is double-buffered by block parity)
+      if (et < 128) s_row[buf * 128 + et] = entry_row(p, qg, Q, 128 * j + et, false);
       bool ok = !vflag(s_abort) &&
                 mbar_wait(&bars[B_DF + buf], (j >> 1) & 1, p.status, kWaitLimitNs, SITE_W3_DF);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) { s_abort[0] = 1; break; }
+      // one decision for all epilogue warps; the rows are visible after it
+      if (named_bar_or(1, 256, !ok)) { s_abort[0] = 1; break; }
       tc_fence_after();
-      const int64_t r = entry_row(p, qg, Q, 128 * j + el, false);
-      float* dst = p.dkv + (r >= 0 ? r : 0) * kRlat + 256 * rg;
+      if (act) {
+        const int64_t* rows = s_row + buf * 128;
 #pragma unroll 1
-      for (int v = 0; v < nd / 32; ++v) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + buf * 256 + 32 * v, rr);
-        tmem_ld_wait();
-        if (r >= 0) {
+        for (int v = 0; v < 4; ++v) {
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_base + buf * 256 + mt * 128 + 32 * v, rr);
+          tmem_ld_wait();
+          if (dim_ok) {
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            red_add_v4(dst + 32 * v + 4 * c, __uint_as_float(rr[4 * c]), __uint_as_float(rr[4 * c + 1]),
-                       __uint_as_float(rr[4 * c + 2]), __uint_as_float(rr[4 * c + 3]));
+            for (int c = 0; c < 32; ++c) {
+              const int64_t r = rows[32 * v + c];
+              if (r >= 0) atomicAdd(p.dkv + r * kRlat + dim, __uint_as_float(rr[c]));
+            }
+          }
         }
       }
       tc_fence_before();
@@ -734,11 +766,11 @@ dsa_status_t sparse_mla_bwd_tc_launch(const SparseMlaBwdArgs& a, void* scratch, 
   for (int64_t q0 = 0; q0 < nq; q0 += qc) {
     const unsigned n = static_cast<unsigned>(nq - q0 < qc ? nq - q0 : qc);
     p.q0 = q0;
-    bwd_pz_kernel<<<dim3(n, 2), k1::NT, k1::SMEM, stream>>>(tq48, tdo48, p);
+    bwd_pz_kernel<<<dim3(2, n), k1::NT, k1::SMEM, stream>>>(tq48, tdo48, p);
     if (launch_status("bwd_pz_kernel") != DSA_OK) return DSA_ERR_CUDA;
     bwd_dq_tc_kernel<<<n, k2::NT, k2::SMEM, stream>>>(tz, p);
     if (launch_status("bwd_dq_tc_kernel") != DSA_OK) return DSA_ERR_CUDA;
-    bwd_dkv_tc_kernel<<<dim3(n, 3), k3::NT, k3::SMEM, stream>>>(tq96, tdo96, tz, tp, p);
+    bwd_dkv_tc_kernel<<<dim3(3, n), k3::NT, k3::SMEM, stream>>>(tq96, tdo96, tz, tp, p);
     if (launch_status("bwd_dkv_tc_kernel") != DSA_OK) return DSA_ERR_CUDA;
   }
   return DSA_OK;
