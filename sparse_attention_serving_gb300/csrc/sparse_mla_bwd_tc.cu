@@ -102,12 +102,15 @@ __device__ __forceinline__ QInfo qinfo(const Params& p, int64_t qg) {
   return r;
 }
 
-// Physical row of list entry e of query qg, or -1 (unused, past topk, or
-// invalid; an invalid entry is recorded when `report` is set).
-__device__ __forceinline__ int64_t entry_row(const Params& p, int64_t qg, const QInfo& Q, int e,
-                                             bool report) {
-  if (!Q.ok || e >= p.topk) return -1;
-  const int s = __ldg(p.idx + qg * p.topk + e);
+// List entry e of query qg as stored (-1 past topk or for an invalid query);
+// loaded one block ahead of its use, so that its latency overlaps work.
+__device__ __forceinline__ int entry_raw(const Params& p, int64_t qg, const QInfo& Q, int e) {
+  return (Q.ok && e < p.topk) ? __ldg(p.idx + qg * p.topk + e) : -1;
+}
+
+// Physical row of list entry s, or -1 (unused or invalid; an invalid entry is
+// recorded when `report` is set).
+__device__ __forceinline__ int64_t raw_row(const Params& p, const QInfo& Q, int s, bool report) {
   if (s < 0) return -1;
   if (s > Q.t || s >= Q.L) {
     if (report) status_raise(p.status, DSA_ERR_BAD_INDEX, SITE_IDX, static_cast<uint32_t>(s));
@@ -201,12 +204,16 @@ __global__ void __launch_bounds__(k1::NT, 1)
     uint32_t doff[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) doff[i] = sw128_unit(e0 + 32 * i, u8);
+    int nxt[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) nxt[i] = entry_raw(p, qg, Q, e0 + 32 * i);
     for (int j = 0; j < nblk; ++j) {
       const uint16_t* src[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int64_t r = entry_row(p, qg, Q, 128 * j + e0 + 32 * i, false);
+        const int64_t r = raw_row(p, Q, nxt[i], false);
         src[i] = p.kv + (r >= 0 ? r : dummy) * kRlat + u8 * 8;
+        nxt[i] = entry_raw(p, qg, Q, 128 * (j + 1) + e0 + 32 * i);
       }
       bool stop = false;
       for (int c = 0; c < 9; ++c) {
@@ -253,15 +260,18 @@ __global__ void __launch_bounds__(k1::NT, 1)
     named_bar_sync(1, 128);
     uint16_t* pz = p.pbuf + (static_cast<int64_t>(ql) * H + g * HG) * p.tpad;
     uint16_t* zz = p.zbuf + (static_cast<int64_t>(ql) * H + g * HG) * p.tpad;
+    int nxt = entry_raw(p, qg, Q, el);
     for (int j = 0; j < nblk; ++j) {
       const int buf = j & 1;
+      const int cur = nxt;
+      nxt = entry_raw(p, qg, Q, 128 * (j + 1) + el);
       bool ok = !vflag(s_abort) &&
                 mbar_wait(&bars[B_SF + buf], (j >> 1) & 1, p.status, kWaitLimitNs, SITE_W1_SF);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) { s_abort[0] = 1; break; }
       tc_fence_after();
       const int e = 128 * j + el;
-      const bool valid = entry_row(p, qg, Q, e, g == 0) >= 0;
+      const bool valid = raw_row(p, Q, cur, g == 0) >= 0;
       uint32_t sv[HG], dv[HG];
       {
         uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv);
@@ -406,14 +416,16 @@ __global__ void __launch_bounds__(k2::NT, 1)
     // (consecutive lanes take consecutive units of a row: whole 128-byte lines
     // per request); the entries' rows are looked up once into shared memory ============
     const int64_t dummy = p.paged ? 0 : static_cast<int64_t>(Q.b) * p.seq_stride;
+    int nxt = tid < 64 ? entry_raw(p, qg, Q, tid) : -1;
     for (int j = 0; j < nblk; ++j) {
       const int st = j % NS, use = j / NS;
+      if (tid < 64) {
+        const int64_t r = raw_row(p, Q, nxt, false);
+        s_row[(j & 1) * 64 + tid] = r >= 0 ? r : dummy;
+        nxt = entry_raw(p, qg, Q, 64 * (j + 1) + tid);
+      }
       const bool fail =
           use > 0 && !mbar_wait(&bars[B_E + st], (use - 1) & 1, p.status, kWaitLimitNs, SITE_W2_E);
-      if (tid < 64) {
-        const int64_t r = entry_row(p, qg, Q, 64 * j + tid, false);
-        s_row[(j & 1) * 64 + tid] = r >= 0 ? r : dummy;
-      }
       // the rows are visible to all 256 threads after this barrier, and the stop
       // decision is the same for all of them
       if (named_bar_or(2, 256, fail || vflag(s_abort))) {
@@ -672,10 +684,13 @@ __global__ void __launch_bounds__(k3::NT, 1)
     const int dim = 256 * rg + 128 * mt + sub * 32 + lane;
     const bool act = mt < ntile;                   // a warp with a tile of this range
     const bool dim_ok = dim < kRlat;
+    // the entries' rows, double-buffered by block parity: block j+1's are
+    // looked up while block j's are added (its readers of that half passed the
+    // barrier of block j first)
+    if (et < 128) s_row[et] = raw_row(p, Q, entry_raw(p, qg, Q, et), false);
+    int nxt = et < 128 ? entry_raw(p, qg, Q, 128 + et) : -1;
     for (int j = 0; j < nblk; ++j) {
       const int buf = j & 1;
-      // the block's entries' rows (the table is double-buffered by block parity)
-      if (et < 128) s_row[buf * 128 + et] = entry_row(p, qg, Q, 128 * j + et, false);
       bool ok = !vflag(s_abort) &&
                 mbar_wait(&bars[B_DF + buf], (j >> 1) & 1, p.status, kWaitLimitNs, SITE_W3_DF);
       // one decision for all epilogue warps; the rows are visible after it
@@ -699,6 +714,10 @@ __global__ void __launch_bounds__(k3::NT, 1)
       }
       tc_fence_before();
       mbar_arrive_warp(&bars[B_DE + buf]);
+      if (et < 128) {
+        s_row[(buf ^ 1) * 128 + et] = raw_row(p, Q, nxt, false);
+        nxt = entry_raw(p, qg, Q, 128 * (j + 2) + et);
+      }
     }
   }
   tc_fence_before();
