@@ -194,10 +194,15 @@ dsa_status_t sparse_mla_fwd_sink(const uint16_t* q_lat, const dsa_rows_t* kv, co
  *                              Additions come from many queries in no fixed
  *                              order, so the FP32 rounding varies run to run.
  * -1 entries are skipped; other invalid entries raise DSA_ERR_BAD_INDEX and are
- * skipped.  Workspace: dsa_workspace_bytes(DSA_OP_SPARSE_MLA_BWD, ...) = the
- * 256-byte status header.  Supported: H <= 128,
- * topk <= 2048.  The products run on the warp-level tensor-core MMA (BF16 in,
- * FP32 accumulate).
+ * skipped.  Supported: H <= 128, topk <= 2048.  All products take BF16
+ * operands with FP32 accumulation; p and scale * dz are rounded to BF16 for them.
+ * Workspace: the 256-byte status header is required.
+ *   - With H = 96 and a workspace of dsa_workspace_bytes(DSA_OP_SPARSE_MLA_BWD,
+ *     B, Tq, max_kv_len, 96, topk) bytes (the header plus P and dz of up to 512
+ *     queries: min(B*Tq, 512) * 96 * ceil(topk/128)*128 * 4 bytes), and d_o,
+ *     o_lat, dq 16-byte aligned, the tcgen05 kernels run (queries in chunks of
+ *     as many as the workspace holds, at least one).
+ *   - Otherwise the warp-level tensor-core MMA kernels run.
  */
 dsa_status_t sparse_mla_bwd(const uint16_t* q_lat, const dsa_rows_t* kv, const int32_t* idx,
                             const int32_t* q_start, const int32_t* kv_len, int B, int Tq, int H,
