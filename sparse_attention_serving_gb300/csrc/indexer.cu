@@ -43,6 +43,7 @@ namespace dsa {
 namespace idx {
 
 constexpr int BKEY = 128;  // keys per tile (MMA M)
+constexpr int GT = 4;      // tiles between the epilogue's group barriers
 constexpr int NEPI = 8;    // epilogue warps
 constexpr int NTHREADS = 64 + NEPI * 32;
 
@@ -90,7 +91,7 @@ struct Cfg {
   static constexpr int QHB = 10;
   static constexpr int OFF_QH = OFF_MISC + MISC_BYTES;
   static constexpr int SMEM_BYTES = OFF_QH + QT * (1 << QHB) * 4 + 1024;
-  static constexpr int CAP = (H_I >= 64) ? 8192 : 1280;  // candidates per query
+  static constexpr int CAP = (H_I >= 64) ? 8192 : 1536;  // candidates per query
   static constexpr int CTA_SCRATCH = QT * CAP * 8;        // scores, then key indices
   static constexpr int EPT = (CAP + NEPI * 32 - 1) / (NEPI * 32);  // candidates per thread in a select
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -729,15 +730,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // broadcast load) as the columns come out of TMEM
         const float* wh = w_s + half * QH * H_I;
         bool want_sel = false;
-        // Tiles in pairs with one group barrier per pair: a candidate buffer keeps
-        // room for two tiles' appends between checks, and the MMA runs up to
-        // NBUF tiles ahead (TMEM accumulator buffers).
-        for (; kt < ntiles; kt += 2) {
-          const int n2 = ntiles - kt < 2 ? ntiles - kt : 2;
+        // Tiles in groups of GT with one group barrier per group: a candidate
+        // buffer keeps room for GT tiles' appends between checks, and the MMA runs
+        // up to NBUF tiles ahead (TMEM accumulator buffers).
+        for (; kt < ntiles; kt += GT) {
+          const int n2 = ntiles - kt < GT ? ntiles - kt : GT;
           bool w_ok = !vflag(s_abort);
           {
             // each tile as soon as its accumulator is complete (with two TMEM
-            // buffers the MMA of the pair's second tile overlaps the first's
+            // buffers the MMA of the next tile overlaps this one's
             // reduction)
             for (int u = 0; u < n2; ++u) {
               const int k = kt + u, gk = g + k, buf = gk % NBUF;
@@ -836,13 +837,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               }
             }
           }
-          // The pair's appends and abort flags are final after this barrier; every
-          // warp reads them before the second barrier, so that no warp's appends
-          // of the next pair can change what another warp decides here.
+          // The group's appends and abort flags are final after this barrier;
+          // every warp reads them before the second barrier, so that no warp's
+          // appends of the next group can change what another warp decides here.
           named_bar_sync(1, G);
           const bool abort_now = vflag(&g_abort[0]);
-          // a buffer that could overflow on the next pair is shrunk outside this loop
-          for (int qq = 0; qq < nq; ++qq) want_sel |= cnt[qq] > CAP - 2 * BKEY;
+          // a buffer that could overflow on the next group is shrunk outside this loop
+          for (int qq = 0; qq < nq; ++qq) want_sel |= cnt[qq] > CAP - GT * BKEY;
           named_bar_sync(1, G);
           if (abort_now) {
             if (gtid == 0) s_abort[0] = 1;  // no role waits for this item's tiles any more
@@ -860,7 +861,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (want_sel) {
           for (int qq = 0; qq < nq; ++qq) {
-            if (cnt[qq] > CAP - 2 * BKEY) {
+            if (cnt[qq] > CAP - GT * BKEY) {
               const float kth = select_keep<C::EPT>(cand_s + qq * CAP, cand_i + qq * CAP, cnt[qq],
                                                     p.topk, gtid, hist, ctr);
               if (gtid == 0) {
@@ -916,7 +917,7 @@ static int64_t prefill_grid(int B, int Tq) {
 template <int H_I, int D_I, bool FP8>
 static dsa_status_t prefill_launch(const IndexerArgs& a, cudaStream_t stream) {
   using C = idx::Cfg<H_I, D_I, FP8>;
-  if (a.topk > C::CAP - 2 * idx::BKEY) return DSA_ERR_UNSUPPORTED;
+  if (a.topk > C::CAP - idx::GT * idx::BKEY) return DSA_ERR_UNSUPPORTED;
   const int64_t grid = prefill_grid<H_I, D_I, FP8>(a.B, a.Tq);
   if (a.scratch == nullptr ||
       a.scratch_bytes < static_cast<size_t>(grid) * C::CTA_SCRATCH)
@@ -971,8 +972,8 @@ static_assert(idx::Cfg<64, 128, false>::CTA_SCRATCH == idx::Cfg<64, 128, true>::
               "BF16 and FP8 share the workspace size");
 
 int indexer_prefill_max_topk(int H_I, int D_I) {
-  if (H_I == 64 && D_I == 128) return idx::Cfg<64, 128, false>::CAP - 2 * idx::BKEY;
-  if (H_I == 4 && D_I == 64) return idx::Cfg<4, 64, false>::CAP - 2 * idx::BKEY;
+  if (H_I == 64 && D_I == 128) return idx::Cfg<64, 128, false>::CAP - idx::GT * idx::BKEY;
+  if (H_I == 4 && D_I == 64) return idx::Cfg<4, 64, false>::CAP - idx::GT * idx::BKEY;
   return 0;
 }
 
