@@ -43,7 +43,7 @@ namespace dsa {
 namespace idx {
 
 constexpr int BKEY = 128;  // keys per tile (MMA M)
-constexpr int GT = 4;      // tiles between the epilogue's group barriers
+constexpr int GT = 8;      // tiles between the epilogue's group barriers
 constexpr int NEPI = 8;    // epilogue warps
 constexpr int NTHREADS = 64 + NEPI * 32;
 
