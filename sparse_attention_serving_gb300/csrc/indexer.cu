@@ -43,7 +43,6 @@ namespace dsa {
 namespace idx {
 
 constexpr int BKEY = 128;  // keys per tile (MMA M)
-constexpr int GT = 8;      // tiles between the epilogue's group barriers
 constexpr int NEPI = 8;    // epilogue warps
 constexpr int NTHREADS = 64 + NEPI * 32;
 
@@ -92,6 +91,9 @@ struct Cfg {
   static constexpr int OFF_QH = OFF_MISC + MISC_BYTES;
   static constexpr int SMEM_BYTES = OFF_QH + QT * (1 << QHB) * 4 + 1024;
   static constexpr int CAP = (H_I >= 64) ? 8192 : 1536;  // candidates per query
+  // key tiles between the epilogue's group barriers (a candidate buffer keeps
+  // room for GT tiles of appends between two checks)
+  static constexpr int GT = (H_I >= 64) ? 8 : 4;
   static constexpr int CTA_SCRATCH = QT * CAP * 8;        // scores, then key indices
   static constexpr int EPT = (CAP + NEPI * 32 - 1) / (NEPI * 32);  // candidates per thread in a select
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -730,11 +732,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // broadcast load) as the columns come out of TMEM
         const float* wh = w_s + half * QH * H_I;
         bool want_sel = false;
-        // Tiles in groups of GT with one group barrier per group: a candidate
+        // Tiles in groups of C::GT with one group barrier per group: a candidate
         // buffer keeps room for GT tiles' appends between checks, and the MMA runs
         // up to NBUF tiles ahead (TMEM accumulator buffers).
-        for (; kt < ntiles; kt += GT) {
-          const int n2 = ntiles - kt < GT ? ntiles - kt : GT;
+        for (; kt < ntiles; kt += C::GT) {
+          const int n2 = ntiles - kt < C::GT ? ntiles - kt : C::GT;
           bool w_ok = !vflag(s_abort);
           {
             // each tile as soon as its accumulator is complete (with two TMEM
@@ -843,7 +845,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           named_bar_sync(1, G);
           const bool abort_now = vflag(&g_abort[0]);
           // a buffer that could overflow on the next group is shrunk outside this loop
-          for (int qq = 0; qq < nq; ++qq) want_sel |= cnt[qq] > CAP - GT * BKEY;
+          for (int qq = 0; qq < nq; ++qq) want_sel |= cnt[qq] > CAP - C::GT * BKEY;
           named_bar_sync(1, G);
           if (abort_now) {
             if (gtid == 0) s_abort[0] = 1;  // no role waits for this item's tiles any more
@@ -861,7 +863,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (want_sel) {
           for (int qq = 0; qq < nq; ++qq) {
-            if (cnt[qq] > CAP - GT * BKEY) {
+            if (cnt[qq] > CAP - C::GT * BKEY) {
               const float kth = select_keep<C::EPT>(cand_s + qq * CAP, cand_i + qq * CAP, cnt[qq],
                                                     p.topk, gtid, hist, ctr);
               if (gtid == 0) {
@@ -917,7 +919,7 @@ static int64_t prefill_grid(int B, int Tq) {
 template <int H_I, int D_I, bool FP8>
 static dsa_status_t prefill_launch(const IndexerArgs& a, cudaStream_t stream) {
   using C = idx::Cfg<H_I, D_I, FP8>;
-  if (a.topk > C::CAP - idx::GT * idx::BKEY) return DSA_ERR_UNSUPPORTED;
+  if (a.topk > C::CAP - C::GT * idx::BKEY) return DSA_ERR_UNSUPPORTED;
   const int64_t grid = prefill_grid<H_I, D_I, FP8>(a.B, a.Tq);
   if (a.scratch == nullptr ||
       a.scratch_bytes < static_cast<size_t>(grid) * C::CTA_SCRATCH)
@@ -972,8 +974,10 @@ static_assert(idx::Cfg<64, 128, false>::CTA_SCRATCH == idx::Cfg<64, 128, true>::
               "BF16 and FP8 share the workspace size");
 
 int indexer_prefill_max_topk(int H_I, int D_I) {
-  if (H_I == 64 && D_I == 128) return idx::Cfg<64, 128, false>::CAP - idx::GT * idx::BKEY;
-  if (H_I == 4 && D_I == 64) return idx::Cfg<4, 64, false>::CAP - idx::GT * idx::BKEY;
+  using C64 = idx::Cfg<64, 128, false>;
+  using C4 = idx::Cfg<4, 64, false>;
+  if (H_I == 64 && D_I == 128) return C64::CAP - C64::GT * idx::BKEY;
+  if (H_I == 4 && D_I == 64) return C4::CAP - C4::GT * idx::BKEY;
   return 0;
 }
 
