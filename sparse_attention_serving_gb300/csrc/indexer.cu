@@ -43,7 +43,8 @@ namespace dsa {
 namespace idx {
 
 constexpr int BKEY = 128;  // keys per tile (MMA M)
-constexpr int NEPI = 8;    // epilogue warps
+constexpr int NEPI = 16;   // epilogue warps: four query groups x four TMEM lane quarters
+constexpr int NGRP = NEPI / 4;
 constexpr int NTHREADS = 64 + NEPI * 32;
 
 enum : uint32_t {
@@ -83,7 +84,7 @@ struct Cfg {
   // barriers (48 x 8 B), flags, per-query counts and thresholds, then the
   // selection scratch (RBINS histogram bins and 16 counters)
   static constexpr int MISC_HDR = 1024;
-  static constexpr int MISC_BYTES = MISC_HDR + (2048 + 16) * 4;
+  static constexpr int MISC_BYTES = MISC_HDR + (2048 + 16 + NEPI) * 4;
   // per query, a histogram of the QHB top bits of the order keys of its
   // candidates: it raises the append threshold while the keys stream and
   // seeds the final selection
@@ -135,34 +136,40 @@ __device__ __forceinline__ bool vflag(const volatile int* p) { return *p != 0; }
 // bin holding the k-th key is kept whole (typically after one or two passes).
 // Ties at the cut are broken arbitrarily.
 //
-// Scratch (shared memory): hist[RBINS] and ctr[16]:
+// Scratch (shared memory): hist[RBINS] and ctr[16 + NEPI]:
 //   ctr[0] smallest key, ctr[1] largest key, ctr[2] chosen bin, ctr[3] count
-//   above it, ctr[4] count in it, ctr[5..12] warp totals, ctr[15] smallest
-//   kept key.
+//   above it, ctr[4] count in it, ctr[15] smallest kept key, ctr[16 + w] the
+//   total of warp w in a prefix sum.
 // ---------------------------------------------------------------------------
 constexpr int RBITS = 11;
 constexpr int RBINS = 1 << RBITS;
 constexpr int SEL_G = NEPI * 32;           // selecting threads
-constexpr int SEL_CTR = 16;
+constexpr int SEL_CTR = 16 + NEPI;          // counters, then one total per selecting warp
 
 // Bin of the need-th largest element (bins ordered by value, counted from the
 // top) of an NB-bin histogram: ctr[2] = bin, ctr[3] = elements in higher bins,
 // ctr[4] = elements in it.  Thread t owns the PER = NB / SEL_G contiguous bins
-// NB-1-PER*t down to NB-PER*(t+1), read as 16-byte loads.
+// NB-1-PER*t down to NB-PER*(t+1), read as vector loads.
 template <int NB>
 __device__ __forceinline__ void find_bin(const int* hist, int need, int gtid, int* ctr) {
   constexpr int PER = NB / SEL_G;
-  static_assert(PER % 4 == 0 && PER * SEL_G == NB, "whole 16-byte loads of bins per thread");
+  static_assert((PER % 4 == 0 || PER == 2) && PER * SEL_G == NB, "whole vector loads of bins per thread");
   const int lane = gtid & 31, w = gtid >> 5;
-  const int4* hb = reinterpret_cast<const int4*>(hist + NB - PER * (gtid + 1));
   int c[PER];  // c[e] = bin NB-1-PER*gtid-e
+  if constexpr (PER == 2) {
+    const int2 x = *reinterpret_cast<const int2*>(hist + NB - PER * (gtid + 1));
+    c[0] = x.y;
+    c[1] = x.x;
+  } else {
+    const int4* hb = reinterpret_cast<const int4*>(hist + NB - PER * (gtid + 1));
 #pragma unroll
-  for (int v = 0; v < PER / 4; ++v) {
-    const int4 x = hb[v];
-    c[PER - 1 - 4 * v] = x.x;
-    c[PER - 2 - 4 * v] = x.y;
-    c[PER - 3 - 4 * v] = x.z;
-    c[PER - 4 - 4 * v] = x.w;
+    for (int v = 0; v < PER / 4; ++v) {
+      const int4 x = hb[v];
+      c[PER - 1 - 4 * v] = x.x;
+      c[PER - 2 - 4 * v] = x.y;
+      c[PER - 3 - 4 * v] = x.z;
+      c[PER - 4 - 4 * v] = x.w;
+    }
   }
   int tot = 0;
 #pragma unroll
@@ -173,11 +180,11 @@ __device__ __forceinline__ void find_bin(const int* hist, int need, int gtid, in
     const int v = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += v;
   }
-  if (lane == 31) ctr[5 + w] = incl;
+  if (lane == 31) ctr[16 + w] = incl;
   named_bar_sync(1, SEL_G);
 #pragma unroll
   for (int ww = 0; ww < NEPI; ++ww)
-    if (ww < w) incl += ctr[5 + ww];
+    if (ww < w) incl += ctr[16 + ww];
   int run = incl - tot;
   if (run < need && need <= incl) {
 #pragma unroll
@@ -313,12 +320,12 @@ __device__ __forceinline__ float sel_emit(const uint32_t (&key)[EPT], const int3
     const int v = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += v;
   }
-  if (lane == 31) ctr[5 + w] = incl;
+  if (lane == 31) ctr[16 + w] = incl;
   named_bar_sync(1, SEL_G);
   int before = 0, total = 0;
 #pragma unroll
   for (int ww = 0; ww < NEPI; ++ww) {
-    const int t = ctr[5 + ww];
+    const int t = ctr[16 + ww];
     if (ww < w) before += t;
     total += t;
   }
@@ -522,7 +529,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   int* hist = reinterpret_cast<int*>(sm + C::OFF_MISC + C::MISC_HDR);  // [RBINS]
   int* ctr = hist + RBINS;                                              // [SEL_CTR]
   static_assert(48 * 8 + 4 + 4 * 8 + 64 * 4 + 64 * 4 <= C::MISC_HDR, "misc header");
-  static_assert(RBINS == 2048 && SEL_CTR == 16, "selection scratch size");
+  static_assert(RBINS == 2048 && SEL_CTR == 16 + NEPI, "selection scratch size");
   float* cand_s = reinterpret_cast<float*>(p.cand + static_cast<int64_t>(blockIdx.x) * C::CTA_SCRATCH);
   int32_t* cand_i = reinterpret_cast<int32_t*>(cand_s + QT * CAP);
 
@@ -679,8 +686,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ========================== epilogue (8 warps) ============================
     const int gtid = tid - 64;
     const int sub = warp & 3;
-    const int half = (warp - 2) >> 2;
-    constexpr int QH = QT / 2;  // queries per epilogue half
+    const int half = (warp - 2) >> 2;  // query group of this warp
+    constexpr int QH = QT / NGRP;      // queries per group
     const uint32_t lane_base = static_cast<uint32_t>(sub * 32) << 16;
     const int key_lane = sub * 32 + lane;
     int g = 0;  // tiles of the streaming items so far
@@ -728,7 +735,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       int kt = 0;
       bool stop = false;
       while (kt < ntiles && !stop) {
-        // this half's head weights, read from shared memory (four per 16-byte
+        // this group's head weights, read from shared memory (four per 16-byte
         // broadcast load) as the columns come out of TMEM
         const float* wh = w_s + half * QH * H_I;
         bool want_sel = false;
@@ -762,7 +769,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               // as x + |x| against halved weights: (x + |x|) (w/2) is max(x, 0) w
               // exactly (doubling and halving are exact in FP32), so every product
               // and sum is the one of w * max(x, 0)
-              constexpr int COLS = QH * H_I;  // this half's accumulator columns
+              constexpr int COLS = QH * H_I;  // this group's accumulator columns
               constexpr int NCHAIN = 4;
               float acc[QH][NCHAIN];
 #pragma unroll
@@ -770,29 +777,39 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int c = 0; c < NCHAIN; ++c) acc[q][c] = 0.f;
               const uint32_t col0 = buf * N + half * COLS;
-              // 32 columns per TMEM load; the next load is in flight while the
-              // current columns are reduced
-              uint32_t rb[2][32];
-              tmem_ld32(tmem + lane_base + col0, rb[0]);
+              // four columns (one query's heads c..c+3) into the FMA chains
+              auto reduce4 = [&](int col, const uint32_t* r) {
+                const int q = col / H_I;  // columns col..col+3 belong to one query
+                const float4 wv = *reinterpret_cast<const float4*>(wh + col);
+                float x[4];
 #pragma unroll
-              for (int v = 0; v < COLS / 32; ++v) {
-                uint32_t(&rr)[32] = rb[v & 1];
-                tmem_ld_wait_regs(rr);
-                if (v + 1 < COLS / 32) tmem_ld32(tmem + lane_base + col0 + (v + 1) * 32, rb[(v + 1) & 1]);
-#pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                  const int col = v * 32 + e;
-                  const int q = col / H_I;  // columns col..col+3 belong to one query
-                  const float4 wv = *reinterpret_cast<const float4*>(wh + col);
-                  float x[4];
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) {
-                    x[j] = __uint_as_float(rr[e + j]);
-                    x[j] = __fadd_rn(x[j], fabsf(x[j]));
-                  }
-                  fma2_rn(acc[q][0], acc[q][1], wv.x, wv.y, x[0], x[1]);
-                  fma2_rn(acc[q][2], acc[q][3], wv.z, wv.w, x[2], x[3]);
+                for (int j = 0; j < 4; ++j) {
+                  x[j] = __uint_as_float(r[j]);
+                  x[j] = __fadd_rn(x[j], fabsf(x[j]));
                 }
+                fma2_rn(acc[q][0], acc[q][1], wv.x, wv.y, x[0], x[1]);
+                fma2_rn(acc[q][2], acc[q][3], wv.z, wv.w, x[2], x[3]);
+              };
+              if constexpr (COLS >= 32) {
+                // 32 columns per TMEM load; the next load is in flight while the
+                // current columns are reduced
+                uint32_t rb[2][32];
+                tmem_ld32(tmem + lane_base + col0, rb[0]);
+#pragma unroll
+                for (int v = 0; v < COLS / 32; ++v) {
+                  uint32_t(&rr)[32] = rb[v & 1];
+                  tmem_ld_wait_regs(rr);
+                  if (v + 1 < COLS / 32) tmem_ld32(tmem + lane_base + col0 + (v + 1) * 32, rb[(v + 1) & 1]);
+#pragma unroll
+                  for (int e = 0; e < 32; e += 4) reduce4(v * 32 + e, rr + e);
+                }
+              } else {
+                static_assert(COLS == 16, "a group's columns: a multiple of 32, or 16");
+                uint32_t rr[16];
+                tmem_ld16(tmem + lane_base + col0, rr);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; e += 4) reduce4(e, rr + e);
               }
               float score[QH];
 #pragma unroll
