@@ -50,9 +50,30 @@ def test_status_strings(dsa):
 
 
 def test_workspace_bytes_has_header(dsa):
-    for op in (dsa.OP_INDEXER_TOPK, dsa.OP_SPARSE_MLA, dsa.OP_GATE):
+    for op in (dsa.OP_INDEXER_TOPK, dsa.OP_SPARSE_MLA, dsa.OP_GATE, dsa.OP_SPARSE_MLA_BWD):
         n = dsa.workspace_bytes(op, 2, 8192, 8192, 96, 2048)
         assert n >= 256 and n % 256 == 0
+
+
+def test_workspace_bytes_prefill_indexer_and_backward(dsa):
+    """The prefill indexer's candidate buffers (one slice per persistent CTA, at
+    most one CTA per 4-query work item) and the tensor-core backward's p and dz
+    of up to 512 queries are part of the reported size."""
+    per_cta = 4 * 8192 * 8
+    small = dsa.workspace_bytes(dsa.OP_INDEXER_TOPK, 1, 8, 8, 64, 2048)   # 2 work items
+    assert small >= 256 + 2 * per_cta
+    big = dsa.workspace_bytes(dsa.OP_INDEXER_TOPK, 2, 8192, 8192, 64, 2048)
+    assert big >= 256 + 100 * per_cta          # one slice per SM (any GPU has 100+ here)
+    assert big < 256 + 1024 * per_cta          # bounded by the SM count, not by the sequence
+    # decode (Tq == 1) has no candidate buffers, only its score vectors
+    assert dsa.workspace_bytes(dsa.OP_INDEXER_TOPK, 4, 1, 4096, 64, 2048) >= 256 + 4 * 4096 * 4
+    per_q = 2 * 96 * 2048 * 2
+    assert dsa.workspace_bytes(dsa.OP_SPARSE_MLA_BWD, 1, 8, 4096, 96, 2048) == 256 + 8 * per_q
+    assert dsa.workspace_bytes(dsa.OP_SPARSE_MLA_BWD, 2, 8192, 8192, 96, 2048) == 256 + 512 * per_q
+    # topk rounded up to a multiple of 128 entries
+    assert dsa.workspace_bytes(dsa.OP_SPARSE_MLA_BWD, 1, 8, 4096, 96, 200) == 256 + 8 * 2 * 96 * 256 * 2
+    # other head counts take the warp-level path: the header only
+    assert dsa.workspace_bytes(dsa.OP_SPARSE_MLA_BWD, 1, 8, 4096, 8, 2048) == 256
 
 
 def _rows(base=0, bt=0, stride=0, maxp=0, page=0, npages=0):

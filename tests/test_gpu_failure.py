@@ -32,3 +32,19 @@ def test_selftest_rejects_long_limits():
     ws = dsa.new_workspace(4096)
     with pytest.raises(dsa.DsaError):
         dsa.selftest_wait_timeout(ws, 10_000_000_000)
+
+
+def test_prefill_indexer_workspace_too_small_is_rejected():
+    """The prefill indexer's candidate buffers live in the workspace: a workspace
+    smaller than dsa_workspace_bytes reports is rejected before any launch."""
+    import sparse_attention_serving_gb300 as dsa
+    from gpu_helpers import bf, i32
+    from workloads import CONFIGS, prefill
+    cfg = CONFIGS["tiny128"]
+    d = prefill(cfg)
+    need = dsa.workspace_bytes(dsa.OP_INDEXER_TOPK, cfg.B, cfg.T, cfg.T, cfg.H_I, cfg.topk)
+    ws = dsa.new_workspace(need - 256)
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.dsa_indexer_topk(bf(d["q_idx"]), bf(d["w"]), dsa.Rows(bf(d["k_idx"])),
+                             i32(d["q_start"]), i32(d["kv_len"]), cfg.topk, cfg.T, workspace=ws)
+    assert e.value.code == dsa.DSA_ERR_WORKSPACE_TOO_SMALL
