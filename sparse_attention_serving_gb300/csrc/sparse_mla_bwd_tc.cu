@@ -17,9 +17,11 @@
 // [query][head][list entry]:
 //   K1 bwd_pz   grid (2 head groups of 48; queries).  Rows of 128 list entries
 //               are gathered one 64-dim chunk (16 KB) at a time into a ring;
-//                 S^T [128 x 48] += rows_c . q_g,c^T     (M=128 entries, N=48)
-//                 dP^T[128 x 48] += rows_c . dO_g,c^T    (c < 8)
-//               and each TMEM lane (one entry) forms p and dz for its 48 heads.
+//                 [S^T | dP^T] [128 x 96] += rows_c . [q_g,c ; dO_g,c]^T   (c < 8)
+//                 S^T [128 x 48]          += rows_c . q_g,c^T              (c = 8)
+//               (M=128 entries; q and dO of a chunk stored as one 96-row
+//               operand, so the gathered rows are read once per chunk) and
+//               each TMEM lane (one entry) forms p and dz for its 48 heads.
 //   K2 bwd_dq   grid (queries).  Rows of 64 entries gathered as in the forward
 //               (four 64-key pairs of two 64-dim chunks, and the rope chunk)
 //               and the entries' dz (TMA, [96 heads x 64 entries]):
@@ -135,9 +137,10 @@ constexpr int NT = 416;
 constexpr int QCH = HG * 128;          // one 64-dim chunk of the group's 48 q (or dO) rows
 constexpr int SLOT = 128 * 128;        // 128 entries x one 64-dim chunk
 constexpr int NR = 7;                  // ring slots
-constexpr int OFF_Q = 0;
-constexpr int OFF_DO = OFF_Q + 9 * QCH;
-constexpr int OFF_RING = OFF_DO + 8 * QCH;
+// chunk c < 8: q rows at OFF_QD + 2c QCH, dO rows right after (one 96-row
+// operand); the rope chunk of q at OFF_QD + 16 QCH
+constexpr int OFF_QD = 0;
+constexpr int OFF_RING = OFF_QD + 17 * QCH;
 constexpr int OFF_MISC = OFF_RING + NR * SLOT;
 // barriers: Q/dO loaded, ring full [NR], ring empty [NR], S full [2], S empty [2], drain
 constexpr int B_Q = 0, B_F = 1, B_E = B_F + NR, B_SF = B_E + NR, B_SE = B_SF + 2, B_DRAIN = B_SE + 2,
@@ -145,7 +148,7 @@ constexpr int B_Q = 0, B_F = 1, B_E = B_F + NR, B_SF = B_E + NR, B_SE = B_SF + 2
 constexpr int SMEM = OFF_MISC + 1024 + 1024;
 static_assert(NBAR * 8 + 8 + 2 * HG * 4 <= 1024, "misc block");
 static_assert(SMEM <= 232448, "shared memory budget");
-static_assert(OFF_DO % 1024 == 0 && OFF_RING % 1024 == 0 && QCH % 1024 == 0, "swizzle atoms");
+static_assert(OFF_RING % 1024 == 0 && QCH % 1024 == 0, "swizzle atoms");
 }  // namespace k1
 
 __global__ void __launch_bounds__(k1::NT, 1)
@@ -164,7 +167,8 @@ __global__ void __launch_bounds__(k1::NT, 1)
   const int64_t qg = p.q0 + ql;
   const QInfo Q = qinfo(p, qg);
   const int nblk = p.tpad / 128;
-  constexpr uint32_t IDESC = idesc_bf16(128, HG, false, false);
+  constexpr uint32_t IDESC_SD = idesc_bf16(128, 2 * HG, false, false);  // S and dP together
+  constexpr uint32_t IDESC_S = idesc_bf16(128, HG, false, false);       // rope chunk: S only
 
   if (tid == 0) {
     mbar_init(&bars[B_Q], 1);
@@ -196,8 +200,9 @@ __global__ void __launch_bounds__(k1::NT, 1)
     if (tid == 0) {
       mbar_expect_tx(&bars[B_Q], (9 + 8) * QCH);
       const int row = static_cast<int>(qg * H + g * HG);
-      for (int c = 0; c < 9; ++c) tma_load_2d(sm + OFF_Q + c * QCH, &tm_q48, &bars[B_Q], 64 * c, row);
-      for (int c = 0; c < 8; ++c) tma_load_2d(sm + OFF_DO + c * QCH, &tm_do48, &bars[B_Q], 64 * c, row);
+      for (int c = 0; c < 9; ++c) tma_load_2d(sm + OFF_QD + 2 * c * QCH, &tm_q48, &bars[B_Q], 64 * c, row);
+      for (int c = 0; c < 8; ++c)
+        tma_load_2d(sm + OFF_QD + (2 * c + 1) * QCH, &tm_do48, &bars[B_Q], 64 * c, row);
     }
     const int64_t dummy = p.paged ? 0 : static_cast<int64_t>(Q.b) * p.seq_stride;
     const int u8 = tid & 7, e0 = tid >> 3;
@@ -302,8 +307,7 @@ __global__ void __launch_bounds__(k1::NT, 1)
     // ============ MMA issuer ============
     if (lane == 0) {
       bool ok = mbar_wait(&bars[B_Q], 0, p.status, kWaitLimitNs, SITE_W1_Q);
-      const uint64_t qd = smem_desc(smem_u32(sm + OFF_Q), 16, 1024);
-      const uint64_t dd = smem_desc(smem_u32(sm + OFF_DO), 16, 1024);
+      const uint64_t qd = smem_desc(smem_u32(sm + OFF_QD), 16, 1024);
       for (int j = 0; j < nblk && ok; ++j) {
         const int buf = j & 1;
         if (j >= 2 && !mbar_wait(&bars[B_SE + buf], ((j >> 1) - 1) & 1, p.status, kWaitLimitNs, SITE_W1_SE)) {
@@ -311,7 +315,7 @@ __global__ void __launch_bounds__(k1::NT, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t ds = tmem + buf * 96, dp = ds + HG;
+        const uint32_t ds = tmem + buf * 96;  // S^T in columns 0-47, dP^T in 48-95
         for (int c = 0; c < 9; ++c) {
           const int gc = 9 * j + c, slot = gc % NR;
           if (vflag(s_abort) ||
@@ -322,13 +326,15 @@ __global__ void __launch_bounds__(k1::NT, 1)
           fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tensor core reads
           tc_fence_after();
           const uint64_t ad = smem_desc(smem_u32(sm + OFF_RING + slot * SLOT), 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(ds, desc_add(ad, kk * 32), desc_add(qd, c * QCH + kk * 32), IDESC, (c | kk) ? 1u : 0u);
           if (c < 8) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(dp, desc_add(ad, kk * 32), desc_add(dd, c * QCH + kk * 32), IDESC, (c | kk) ? 1u : 0u);
+              umma_bf16(ds, desc_add(ad, kk * 32), desc_add(qd, 2 * c * QCH + kk * 32), IDESC_SD,
+                        (c | kk) ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(ds, desc_add(ad, kk * 32), desc_add(qd, 16 * QCH + kk * 32), IDESC_S, 1u);
           }
           umma_commit(&bars[B_E + slot]);
         }
@@ -540,10 +546,14 @@ __global__ void __launch_bounds__(k2::NT, 1)
 // A = q^T / dO^T of the range ([96 heads x 64 dims] boxes, dims contiguous:
 // MN-major), B = dz / p of 128 entries ([96 heads x 64 entries] boxes, entries
 // contiguous: MN-major).  Threads: warp 0 TMA producer, warp 1 MMA issuer and
-// TMEM owner, warps 2-9 epilogue (two 128-dim tiles x four lane quarters).
+// TMEM owner, warps 2-17 epilogue.  A warp's reductions into global memory
+// issue at a fixed rate whatever the other warps do, so every warp that can
+// reach a tile's TMEM lanes takes a share of its columns: in the two 128-dim
+// tiles, one warp per (tile, lane quarter, half of the 128 entries); in the
+// rope tile (64 live lanes), four warps per live lane quarter, 32 entries each.
 // =============================================================================
 namespace k3 {
-constexpr int NT = 320;
+constexpr int NT = 576;
 constexpr int QB = H * 128;                // [96 heads x 64] box (12 KB)
 constexpr int OFF_QR = 0;                  // q^T of the range: 4 boxes (the rope range: 2, one past the end)
 constexpr int OFF_DR = OFF_QR + 4 * QB;    // dO^T of the range: 4 boxes
@@ -589,7 +599,7 @@ __global__ void __launch_bounds__(k3::NT, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[B_DF + i], 1);
-      mbar_init(&bars[B_DE + i], 8);
+      mbar_init(&bars[B_DE + i], 16);
     }
     mbar_init(&bars[B_DRAIN], 1);
     s_abort[0] = 0;
@@ -678,11 +688,15 @@ __global__ void __launch_bounds__(k3::NT, 1)
     __syncwarp();
   } else {
     // ============ epilogue: lane = dim, columns = entries ============
-    const int et = tid - 64;                       // 0..255
-    const int sub = warp & 3, mt = (warp - 2) >> 2;
+    const int et = tid - 64;                       // 0..511
+    const int sub = warp & 3, grp = (warp - 2) >> 2;  // lane quarter; each group of four has every quarter
     const uint32_t lane_base = static_cast<uint32_t>(sub * 32) << 16;
+    // tile, first column and number of 32-column loads of this warp
+    const int mt = rope ? 0 : (grp & 1);
+    const int col0 = rope ? 32 * grp : 64 * (grp >> 1);
+    const int nld = rope ? 1 : 2;
     const int dim = 256 * rg + 128 * mt + sub * 32 + lane;
-    const bool act = mt < ntile;                   // a warp with a tile of this range
+    const bool act = !rope || sub < 2;             // the rope tile's lanes 64..127 are past dim 575
     const bool dim_ok = dim < kRlat;
     // the entries' rows, double-buffered by block parity: block j+1's are
     // looked up while block j's are added (its readers of that half passed the
@@ -694,14 +708,14 @@ __global__ void __launch_bounds__(k3::NT, 1)
       bool ok = !vflag(s_abort) &&
                 mbar_wait(&bars[B_DF + buf], (j >> 1) & 1, p.status, kWaitLimitNs, SITE_W3_DF);
       // one decision for all epilogue warps; the rows are visible after it
-      if (named_bar_or(1, 256, !ok)) { s_abort[0] = 1; break; }
+      if (named_bar_or(1, 512, !ok)) { s_abort[0] = 1; break; }
       tc_fence_after();
       if (act) {
-        const int64_t* rows = s_row + buf * 128;
+        const int64_t* rows = s_row + buf * 128 + col0;
 #pragma unroll 1
-        for (int v = 0; v < 4; ++v) {
+        for (int v = 0; v < nld; ++v) {
           uint32_t rr[32];
-          tmem_ld32(tmem + lane_base + buf * 256 + mt * 128 + 32 * v, rr);
+          tmem_ld32(tmem + lane_base + buf * 256 + mt * 128 + col0 + 32 * v, rr);
           tmem_ld_wait();
           if (dim_ok) {
 #pragma unroll
