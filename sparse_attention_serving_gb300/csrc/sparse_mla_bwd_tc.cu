@@ -137,6 +137,7 @@ constexpr int NT = 416;
 constexpr int QCH = HG * 128;          // one 64-dim chunk of the group's 48 q (or dO) rows
 constexpr int SLOT = 128 * 128;        // 128 entries x one 64-dim chunk
 constexpr int NR = 7;                  // ring slots
+constexpr int KB = 3;                  // chunks per wait of the MMA issuer (one wait and fence per three chunks)
 // chunk c < 8: q rows at OFF_QD + 2c QCH, dO rows right after (one 96-row
 // operand); the rope chunk of q at OFF_QD + 16 QCH
 constexpr int OFF_QD = 0;
@@ -239,28 +240,40 @@ __global__ void __launch_bounds__(k1::NT, 1)
     const int ew = warp - 8, sub = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(sub * 32) << 16;
     const int el = sub * 32 + lane;  // entry within the block (TMEM lane)
-    // D = dO . o and lse (log2) of the group's heads
-    for (int hh = ew; hh < HG; hh += 4) {
-      const int h = g * HG + hh;
-      const uint4* a = reinterpret_cast<const uint4*>(p.dO + (qg * H + h) * kVlat) + lane * 2;
-      const uint4* b = reinterpret_cast<const uint4*>(p.o + (qg * H + h) * kVlat) + lane * 2;
-      float acc = 0.f;
+    // D = dO . o and lse (log2) of the group's heads: a warp takes heads
+    // ew + 4i, four at a time with all their loads issued first
+    for (int h0 = ew; h0 < HG; h0 += 16) {
+      uint4 x[4][2], y[4][2];
 #pragma unroll
-      for (int v = 0; v < 2; ++v) {
-        const uint4 x = __ldg(a + v), y = __ldg(b + v);
-        const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+      for (int i = 0; i < 4; ++i) {
+        const int64_t row = qg * H + g * HG + h0 + 4 * i;
+        const uint4* a = reinterpret_cast<const uint4*>(p.dO + row * kVlat) + lane * 2;
+        const uint4* b = reinterpret_cast<const uint4*>(p.o + row * kVlat) + lane * 2;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          acc = fmaf(__uint_as_float(xs[k] << 16), __uint_as_float(ys[k] << 16), acc);
-          acc = fmaf(__uint_as_float(xs[k] & 0xffff0000u), __uint_as_float(ys[k] & 0xffff0000u), acc);
+        for (int v = 0; v < 2; ++v) {
+          x[i][v] = __ldg(a + v);
+          y[i][v] = __ldg(b + v);
         }
       }
+      const float l = lane < 4 ? __ldg(p.lse + qg * H + g * HG + h0 + 4 * lane) : 0.f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (lane == 0) {
-        s_D[hh] = acc;
-        s_l2[hh] = __ldg(p.lse + qg * H + h) * 1.4426950408889634f;
+      for (int i = 0; i < 4; ++i) {
+        float acc = 0.f;
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+          const uint32_t xs[4] = {x[i][v].x, x[i][v].y, x[i][v].z, x[i][v].w};
+          const uint32_t ys[4] = {y[i][v].x, y[i][v].y, y[i][v].z, y[i][v].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            acc = fmaf(__uint_as_float(xs[k] << 16), __uint_as_float(ys[k] << 16), acc);
+            acc = fmaf(__uint_as_float(xs[k] & 0xffff0000u), __uint_as_float(ys[k] & 0xffff0000u), acc);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) s_D[h0 + 4 * i] = acc;
       }
+      if (lane < 4) s_l2[h0 + 4 * lane] = l * 1.4426950408889634f;
     }
     named_bar_sync(1, 128);
     uint16_t* pz = p.pbuf + (static_cast<int64_t>(ql) * H + g * HG) * p.tpad;
@@ -308,35 +321,51 @@ __global__ void __launch_bounds__(k1::NT, 1)
     if (lane == 0) {
       bool ok = mbar_wait(&bars[B_Q], 0, p.status, kWaitLimitNs, SITE_W1_Q);
       const uint64_t qd = smem_desc(smem_u32(sm + OFF_QD), 16, 1024);
+      const uint64_t rd = smem_desc(smem_u32(sm + OFF_RING), 16, 1024);
+      int slot = 0;       // ring slot of the next chunk (chunk counter modulo NR) ...
+      uint32_t ph = 0;    // ... and the parity of its use
       for (int j = 0; j < nblk && ok; ++j) {
         const int buf = j & 1;
-        if (j >= 2 && !mbar_wait(&bars[B_SE + buf], ((j >> 1) - 1) & 1, p.status, kWaitLimitNs, SITE_W1_SE)) {
+        if (vflag(s_abort) || (j >= 2 && !mbar_wait(&bars[B_SE + buf], ((j >> 1) - 1) & 1, p.status,
+                                                     kWaitLimitNs, SITE_W1_SE))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t ds = tmem + buf * 96;  // S^T in columns 0-47, dP^T in 48-95
-        for (int c = 0; c < 9; ++c) {
-          const int gc = 9 * j + c, slot = gc % NR;
-          if (vflag(s_abort) ||
-              !mbar_wait(&bars[B_F + slot], (gc / NR) & 1, p.status, kWaitLimitNs, SITE_W1_F)) {
-            ok = false;
-            break;
+        // chunks taken KB at a time: one wait and one fence for KB chunks
+        for (int c = 0; c < 9 && ok; c += KB) {
+          const int nc = c + KB <= 9 ? KB : 9 - c;
+          int sl[KB];
+#pragma unroll
+          for (int i = 0; i < KB; ++i) {
+            if (i < nc) {
+              sl[i] = slot;
+              if (ok && !mbar_wait(&bars[B_F + slot], ph, p.status, kWaitLimitNs, SITE_W1_F)) ok = false;
+              if (++slot == NR) { slot = 0; ph ^= 1; }
+            }
           }
+          if (!ok) break;
           fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tensor core reads
           tc_fence_after();
-          const uint64_t ad = smem_desc(smem_u32(sm + OFF_RING + slot * SLOT), 16, 1024);
-          if (c < 8) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(ds, desc_add(ad, kk * 32), desc_add(qd, 2 * c * QCH + kk * 32), IDESC_SD,
-                        (c | kk) ? 1u : 0u);
-          } else {
+          for (int i = 0; i < KB; ++i) {
+            if (i < nc) {
+              const int cc = c + i;
+              const uint64_t ad = desc_add(rd, sl[i] * SLOT);
+              if (cc < 8) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(ds, desc_add(ad, kk * 32), desc_add(qd, 16 * QCH + kk * 32), IDESC_S, 1u);
+                for (int kk = 0; kk < 4; ++kk)
+                  umma_bf16(ds, desc_add(ad, kk * 32), desc_add(qd, 2 * cc * QCH + kk * 32), IDESC_SD,
+                            (cc | kk) ? 1u : 0u);
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  umma_bf16(ds, desc_add(ad, kk * 32), desc_add(qd, 16 * QCH + kk * 32), IDESC_S, 1u);
+              }
+              umma_commit(&bars[B_E + sl[i]]);
+            }
           }
-          umma_commit(&bars[B_E + slot]);
         }
         if (!ok) break;
         umma_commit(&bars[B_SF + buf]);
@@ -581,9 +610,12 @@ __global__ void __launch_bounds__(k3::NT, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
   int64_t* s_row = reinterpret_cast<int64_t*>(sm + OFF_MISC + 256);  // [2][128]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // the three dim-range CTAs of a query are adjacent in launch order, so the
-  // second and third read that query's p and dz from L2
-  const int ql = blockIdx.y, rg = blockIdx.x;  // dims [256 rg, 256 rg + 256) (rope: 512..575)
+  // launch order: the two 256-dim CTAs of each query next to each other (the
+  // second reads the query's p and dz from L2), then every query's rope CTA,
+  // which has a quarter of the work and so evens out the last wave
+  const int lin = blockIdx.x + 3 * blockIdx.y, n2 = 2 * gridDim.y;
+  const int ql = lin < n2 ? (lin >> 1) : lin - n2;
+  const int rg = lin < n2 ? (lin & 1) : 2;  // dims [256 rg, 256 rg + 256) (rope: 512..575)
   const int64_t qg = p.q0 + ql;
   const QInfo Q = qinfo(p, qg);
   const int nblk = p.tpad / 128;
