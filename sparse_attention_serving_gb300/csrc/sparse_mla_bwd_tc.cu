@@ -386,21 +386,30 @@ __global__ void __launch_bounds__(k1::NT, 1)
 
 // =============================================================================
 // K2: dq.  Threads: warps 0-7 gather (+ the dz TMA), warps 8-11 epilogue,
-// warp 12 MMA issuer and TMEM owner.
+// warp 12 MMA issuer and TMEM owner.  The rows of a 64-entry block move
+// through rings finer than a block, so that a slot is gathered again as soon
+// as the MMAs that read it are done: a ring of eight 16 KB pair slots (64
+// entries x 128 dims, the A operand of one 128-dim tile of dq^T) and a ring of
+// three (rope chunk, dz tile) slots per block.
 // =============================================================================
 namespace k2 {
 constexpr int NT = 416;
 constexpr int PAIR = 2 * CH;                 // 64 entries x 128 dims
 constexpr int ZT = 128 * 128;                // dz tile: 96 head rows (+32 spare) x 64 entries
-constexpr int BLK = 4 * PAIR + CH + ZT;      // 88 KB per 64-entry block
-constexpr int NS = 2;                        // block stages
-constexpr int OFF_BLK = 0;
-constexpr int OFF_MISC = OFF_BLK + NS * BLK;
-constexpr int B_F = 0, B_E = B_F + NS, B_D = B_E + NS, NBAR = B_D + 1;
+constexpr int NP = 8;                        // pair slots (two blocks)
+constexpr int NX = 3;                        // rope + dz slots
+constexpr int OFF_P = 0;
+constexpr int OFF_R = OFF_P + NP * PAIR;
+constexpr int OFF_Z = OFF_R + NX * CH;
+constexpr int OFF_MISC = OFF_Z + NX * ZT;
+// barriers: pair full / empty [NP], dz full, rope full, rope+dz empty [NX], done
+constexpr int B_PF = 0, B_PE = B_PF + NP, B_ZF = B_PE + NP, B_RF = B_ZF + NX, B_XE = B_RF + NX,
+              B_D = B_XE + NX, NBAR = B_D + 1;
 constexpr int MISC = 256 + 2 * 64 * 8;       // barriers, then the row table [2][64]
 constexpr int SMEM = OFF_MISC + MISC + 1024;
 static_assert(NBAR * 8 + 8 <= 256, "barriers before the row table");
 static_assert(SMEM <= 232448, "shared memory budget");
+static_assert((NP & (NP - 1)) == 0, "pair slot index by mask");
 }  // namespace k2
 
 __global__ void __launch_bounds__(k2::NT, 1)
@@ -421,9 +430,14 @@ __global__ void __launch_bounds__(k2::NT, 1)
   constexpr uint32_t IDESC_R = idesc_bf16(128, 64, false, true);  // dz . rope rows (MN-major B)
 
   if (tid == 0) {
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(&bars[B_F + i], 256 + 1);  // 256 gathering threads + the dz TMA
-      mbar_init(&bars[B_E + i], 1);
+    for (int i = 0; i < NP; ++i) {
+      mbar_init(&bars[B_PF + i], 256);  // the 256 gathering threads
+      mbar_init(&bars[B_PE + i], 1);
+    }
+    for (int i = 0; i < NX; ++i) {
+      mbar_init(&bars[B_ZF + i], 1);    // the dz copy
+      mbar_init(&bars[B_RF + i], 256);
+      mbar_init(&bars[B_XE + i], 1);
     }
     mbar_init(&bars[B_D], 1);
     s_abort[0] = 0;
@@ -431,10 +445,9 @@ __global__ void __launch_bounds__(k2::NT, 1)
   }
   // the spare dz rows 96..127 feed only accumulator lanes nobody reads; zero
   // them once so that they hold finite values
-  for (int i = tid; i < NS * 32 * 128 / 16; i += NT) {
-    const int st = i / (32 * 8), r = i % (32 * 8);
-    *reinterpret_cast<uint4*>(sm + OFF_BLK + st * BLK + 4 * PAIR + CH + 96 * 128 + r * 16) =
-        make_uint4(0u, 0u, 0u, 0u);
+  for (int i = tid; i < NX * 32 * 128 / 16; i += NT) {
+    const int x = i / (32 * 8), r = i % (32 * 8);
+    *reinterpret_cast<uint4*>(sm + OFF_Z + x * ZT + 96 * 128 + r * 16) = make_uint4(0u, 0u, 0u, 0u);
   }
   fence_proxy_async_smem();
   if (warp == 12) {
@@ -447,41 +460,53 @@ __global__ void __launch_bounds__(k2::NT, 1)
   const uint32_t tmem = *tslot;
 
   if (warp < 8) {
-    // ============ gather: the block's 64 x 72 16-byte units, unit U = 256 i + t
-    // (consecutive lanes take consecutive units of a row: whole 128-byte lines
-    // per request); the entries' rows are looked up once into shared memory ============
+    // ============ gather.  Pair i of a block: its 64 rows x 16 units (dims
+    // 128 i .. 128 i + 127), unit U = tid + 256 m, m = 0..3 (sixteen consecutive
+    // lanes per row: whole 128-byte lines per request); the rope chunk: 64 rows
+    // x 8 units, U = tid + 256 m, m = 0..1.  The entries' rows are looked up
+    // once per block into shared memory ============
     const int64_t dummy = p.paged ? 0 : static_cast<int64_t>(Q.b) * p.seq_stride;
     int nxt = tid < 64 ? entry_raw(p, qg, Q, tid) : -1;
     for (int j = 0; j < nblk; ++j) {
-      const int st = j % NS, use = j / NS;
       if (tid < 64) {
         const int64_t r = raw_row(p, Q, nxt, false);
         s_row[(j & 1) * 64 + tid] = r >= 0 ? r : dummy;
         nxt = entry_raw(p, qg, Q, 64 * (j + 1) + tid);
       }
-      const bool fail =
-          use > 0 && !mbar_wait(&bars[B_E + st], (use - 1) & 1, p.status, kWaitLimitNs, SITE_W2_E);
       // the rows are visible to all 256 threads after this barrier, and the stop
       // decision is the same for all of them
-      if (named_bar_or(2, 256, fail || vflag(s_abort))) {
-        s_abort[0] = 1;
-        break;
-      }
-      uint8_t* base = sm + OFF_BLK + st * BLK;
-      if (tid == 0) {
-        mbar_expect_tx(&bars[B_F + st], 96 * 128);
-        tma_load_2d(base + 4 * PAIR + CH, &tm_z, &bars[B_F + st], 64 * j, ql * H);
-      }
-      const uint32_t b32 = smem_u32(base);
+      if (named_bar_or(2, 256, vflag(s_abort))) break;
       const int64_t* rows = s_row + (j & 1) * 64;
-#pragma unroll 4
-      for (int i = 0; i < 18; ++i) {
-        const int U = 256 * i + tid, key = U / 72, u = U - 72 * key, c = u >> 3, uu = u & 7;
-        const uint32_t dst = c < 8 ? b32 + (c >> 1) * PAIR + (c & 1) * CH + sw128_unit(key, uu)
-                                   : b32 + 4 * PAIR + sw128_unit(key, uu);
-        cp_async_16(dst, p.kv + rows[key] * kRlat + u * 8);
+      const int x = j % NX, xu = j / NX;
+      bool fail = xu > 0 && !mbar_wait(&bars[B_XE + x], (xu - 1) & 1, p.status, kWaitLimitNs, SITE_W2_E);
+      if (!fail && tid == 0) {
+        mbar_expect_tx(&bars[B_ZF + x], 96 * 128);
+        tma_load_2d(sm + OFF_Z + x * ZT, &tm_z, &bars[B_ZF + x], 64 * j, ql * H);
       }
-      cp_async_arrive(&bars[B_F + st]);
+      for (int i = 0; i < 4 && !fail; ++i) {
+        const int gp = 4 * j + i, slot = gp & (NP - 1), pu = gp / NP;
+        if (pu > 0 && !mbar_wait(&bars[B_PE + slot], (pu - 1) & 1, p.status, kWaitLimitNs, SITE_W2_E)) {
+          fail = true;
+          break;
+        }
+        const uint32_t b32 = smem_u32(sm + OFF_P + slot * PAIR);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int U = tid + 256 * m, key = U >> 4, w = U & 15;
+          cp_async_16(b32 + (w >> 3) * CH + sw128_unit(key, w & 7), p.kv + rows[key] * kRlat + (16 * i + w) * 8);
+        }
+        cp_async_arrive(&bars[B_PF + slot]);
+      }
+      if (!fail) {
+        const uint32_t r32 = smem_u32(sm + OFF_R + x * CH);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const int U = tid + 256 * m, key = U >> 3, uu = U & 7;
+          cp_async_16(r32 + sw128_unit(key, uu), p.kv + rows[key] * kRlat + (64 + uu) * 8);
+        }
+        cp_async_arrive(&bars[B_RF + x]);
+      }
+      if (fail) s_abort[0] = 1;  // everyone stops at the next block's barrier
     }
     cp_async_wait_all();
   } else if (warp < 12) {
@@ -523,34 +548,53 @@ __global__ void __launch_bounds__(k2::NT, 1)
       }
     }
   } else if (warp == 12) {
-    // ============ MMA issuer ============
+    // ============ MMA issuer: per block, the dz tile, then two pairs per wait,
+    // then the rope chunk ============
     if (lane == 0) {
       bool ok = true;
+      int pslot = 0;      // pair slot of the next pair ...
+      uint32_t pph = 0;   // ... and the parity of its use
       for (int j = 0; j < nblk && ok; ++j) {
-        const int st = j % NS;
-        if (vflag(s_abort) ||
-            !mbar_wait(&bars[B_F + st], (j / NS) & 1, p.status, kWaitLimitNs, SITE_W2_F)) {
+        const int x = j % NX;
+        const uint32_t xph = (j / NX) & 1;
+        if (vflag(s_abort) || !mbar_wait(&bars[B_ZF + x], xph, p.status, kWaitLimitNs, SITE_W2_F)) {
+          ok = false;
+          break;
+        }
+        const uint64_t zd = smem_desc(smem_u32(sm + OFF_Z + x * ZT), 16, 1024);  // dz, K-major rows = heads
+        for (int i0 = 0; i0 < 4 && ok; i0 += 2) {
+          int sl[2];
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            sl[t] = pslot;
+            if (ok && !mbar_wait(&bars[B_PF + pslot], pph, p.status, kWaitLimitNs, SITE_W2_F)) ok = false;
+            if (++pslot == NP) { pslot = 0; pph ^= 1; }
+          }
+          if (!ok) break;
+          fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tensor core reads
+          tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const uint64_t vd = smem_desc(smem_u32(sm + OFF_P + sl[t] * PAIR), CH, 1024);  // 128 dims x 64 entries, MN-major
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(tmem + (i0 + t) * H, desc_add(vd, kk * 2048), desc_add(zd, kk * 32), IDESC_T,
+                        (j | kk) ? 1u : 0u);
+            umma_commit(&bars[B_PE + sl[t]]);
+          }
+        }
+        if (!ok || !mbar_wait(&bars[B_RF + x], xph, p.status, kWaitLimitNs, SITE_W2_F)) {
           ok = false;
           break;
         }
         fence_proxy_async_smem();
         tc_fence_after();
-        const uint32_t base = smem_u32(sm + OFF_BLK + st * BLK);
-        const uint64_t zd = smem_desc(base + 4 * PAIR + CH, 16, 1024);   // dz, K-major rows = heads
-        const uint64_t rd = smem_desc(base + 4 * PAIR, CH, 1024);       // rope rows, MN-major
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint64_t vd = smem_desc(base + i * PAIR, CH, 1024);     // 128 dims x 64 entries, MN-major
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + i * H, desc_add(vd, kk * 2048), desc_add(zd, kk * 32), IDESC_T,
-                      (j | kk) ? 1u : 0u);
-        }
+        const uint64_t rd = smem_desc(smem_u32(sm + OFF_R + x * CH), CH, 1024);  // rope rows, MN-major
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           umma_bf16(tmem + 4 * H, desc_add(zd, kk * 32), desc_add(rd, kk * 2048), IDESC_R,
                     (j | kk) ? 1u : 0u);
-        umma_commit(&bars[B_E + st]);
+        umma_commit(&bars[B_XE + x]);
       }
       if (!ok) s_abort[0] = 1;
       umma_commit(&bars[B_D]);
