@@ -584,7 +584,7 @@ def run_prefill_bwd(dsa, cfg, dev, stream, q_lat, kvrows, idx, o_lat, lse, T, pe
             "note": "tcgen05 kernels (P and dz from S^T and dP^T, dq from rows^T.dz^T, dKV from "
                     "dz^T.q + p^T.dO with vector atomics); slice: last 512 queries of sequence 0",
             "warp_mma_ms": t_warp * 1e3,
-            "gpu_launches": K * 3}
+            "gpu_launches": K * 2}
 
 
 def launches_per_step(dsa, B, T, cfg):

@@ -12,9 +12,10 @@
 //   dkv[s_j, 0:576] += dz_j q,   dkv[s_j, 0:512] += p_j dO
 // One query's operands do not fit one SM together (q 108 KB, dO 96 KB, a block
 // of rows, and a [96 x 576] FP32 dq accumulator that alone exceeds TMEM), so
-// the work is three kernels over a chunk of queries, with P and dZ (BF16, the
-// precision the products take them in) passed through the workspace as
-// [query][head][list entry]:
+// the work is three CTA kinds over a chunk of queries, with P and dZ (BF16,
+// the precision the products take them in) passed through the workspace as
+// [query][head][list entry].  K1 is one launch; K2 and K3 read only its output
+// and share the next (bwd_dq_dkv_kernel: the chunk's K2 CTAs, then its K3 CTAs):
 //   K1 bwd_pz   grid (2 head groups of 48; queries).  Rows of 128 list entries
 //               are gathered one 64-dim chunk (16 KB) at a time into a ring;
 //                 [S^T | dP^T] [128 x 96] += rows_c . [q_g,c ; dO_g,c]^T   (c < 8)
@@ -22,12 +23,12 @@
 //               (M=128 entries; q and dO of a chunk stored as one 96-row
 //               operand, so the gathered rows are read once per chunk) and
 //               each TMEM lane (one entry) forms p and dz for its 48 heads.
-//   K2 bwd_dq   grid (queries).  Rows of 64 entries gathered as in the forward
-//               (four 64-key pairs of two 64-dim chunks, and the rope chunk)
-//               and the entries' dz (TMA, [96 heads x 64 entries]):
+//   K2 dq       one CTA per query.  Rows of 64 entries gathered as in the
+//               forward (four 64-key pairs of two 64-dim chunks, and the rope
+//               chunk) and the entries' dz (TMA, [96 heads x 64 entries]):
 //                 dq^T[512 x 96] += rows^T . dz^T        (4 x M=128 dims, N=96)
 //                 dq_rope[96 x 64] += dz . rows_rope     (M=128 heads, N=64)
-//   K3 bwd_dkv  grid (3 dim ranges: 0-255, 256-511, 512-575; queries).  q and
+//   K3 dkv      one CTA per (dim range 0-255, 256-511, 512-575; query).  q and
 //               dO of the range (TMA, dims contiguous) against dz and p of 128
 //               entries (TMA, entries contiguous), both MN-major:
 //                 dKV^T[128 dims x 128] = q_r^T . dz + dO_r^T . p   (M=128, N=128)
@@ -412,8 +413,9 @@ static_assert(SMEM <= 232448, "shared memory budget");
 static_assert((NP & (NP - 1)) == 0, "pair slot index by mask");
 }  // namespace k2
 
-__global__ void __launch_bounds__(k2::NT, 1)
-    bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_z, const Params p) {
+// K2's CTA body (query ql of the chunk); threads past k2::NT wait at the
+// CTA-wide barriers only.
+__device__ __forceinline__ void bwd_dq_body(const CUtensorMap& tm_z, const Params& p, int ql) {
   using namespace k2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_align1024(smem_raw);
@@ -422,7 +424,6 @@ __global__ void __launch_bounds__(k2::NT, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
   int64_t* s_row = reinterpret_cast<int64_t*>(sm + OFF_MISC + 256);  // [2][64]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ql = blockIdx.x;
   const int64_t qg = p.q0 + ql;
   const QInfo Q = qinfo(p, qg);
   const int nblk = p.tpad / 64;
@@ -445,7 +446,7 @@ __global__ void __launch_bounds__(k2::NT, 1)
   }
   // the spare dz rows 96..127 feed only accumulator lanes nobody reads; zero
   // them once so that they hold finite values
-  for (int i = tid; i < NX * 32 * 128 / 16; i += NT) {
+  for (int i = tid; i < NX * 32 * 128 / 16; i += blockDim.x) {
     const int x = i / (32 * 8), r = i % (32 * 8);
     *reinterpret_cast<uint4*>(sm + OFF_Z + x * ZT + 96 * 128 + r * 16) = make_uint4(0u, 0u, 0u, 0u);
   }
@@ -642,10 +643,10 @@ static_assert(NBAR * 8 + 8 <= 256, "barriers before the row table");
 static_assert(SMEM <= 232448, "shared memory budget");
 }  // namespace k3
 
-__global__ void __launch_bounds__(k3::NT, 1)
-    bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_q96, const __grid_constant__ CUtensorMap tm_do96,
-                      const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_p,
-                      const Params p) {
+// K3's CTA body: `lin` numbers the chunk's 3 n dKV CTAs in launch order.
+__device__ __forceinline__ void bwd_dkv_body(const CUtensorMap& tm_q96, const CUtensorMap& tm_do96,
+                                             const CUtensorMap& tm_z, const CUtensorMap& tm_p,
+                                             const Params& p, int lin, int n) {
   using namespace k3;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_align1024(smem_raw);
@@ -657,7 +658,7 @@ __global__ void __launch_bounds__(k3::NT, 1)
   // launch order: the two 256-dim CTAs of each query next to each other (the
   // second reads the query's p and dz from L2), then every query's rope CTA,
   // which has a quarter of the work and so evens out the last wave
-  const int lin = blockIdx.x + 3 * blockIdx.y, n2 = 2 * gridDim.y;
+  const int n2 = 2 * n;
   const int ql = lin < n2 ? (lin >> 1) : lin - n2;
   const int rg = lin < n2 ? (lin & 1) : 2;  // dims [256 rg, 256 rg + 256) (rope: 512..575)
   const int64_t qg = p.q0 + ql;
@@ -818,6 +819,22 @@ __global__ void __launch_bounds__(k3::NT, 1)
   }
 }
 
+// K2 and K3 of a chunk in one launch: both read only K1's p and dz, so the
+// dKV CTAs (launched after the chunk's n dq CTAs) fill the SMs the last wave
+// of dq CTAs leaves idle.
+static_assert(k3::NT >= k2::NT, "one block size for both bodies");
+constexpr int KDQ_SMEM = k2::SMEM > k3::SMEM ? k2::SMEM : k3::SMEM;
+__global__ void __launch_bounds__(k3::NT, 1)
+    bwd_dq_dkv_kernel(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_q96,
+                      const __grid_constant__ CUtensorMap tm_do96, const __grid_constant__ CUtensorMap tm_p,
+                      const Params p, int n) {
+  const int b = static_cast<int>(blockIdx.x);
+  if (b < n)
+    bwd_dq_body(tm_z, p, b);
+  else
+    bwd_dkv_body(tm_q96, tm_do96, tm_z, tm_p, p, b - n, n);
+}
+
 }  // namespace mlbt
 
 // Bytes of P and dZ scratch per query (BF16, both matrices).
@@ -869,18 +886,15 @@ dsa_status_t sparse_mla_bwd_tc_launch(const SparseMlaBwdArgs& a, void* scratch, 
       !encode_tmap_2d(&tp, p.pbuf, static_cast<uint64_t>(qc) * H, p.tpad, p.tpad * 2ull, 64, H, true))
     return DSA_ERR_CUDA;
   if (cudaFuncSetAttribute(bwd_pz_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, k1::SMEM) != cudaSuccess ||
-      cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, k2::SMEM) != cudaSuccess ||
-      cudaFuncSetAttribute(bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, k3::SMEM) != cudaSuccess)
+      cudaFuncSetAttribute(bwd_dq_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, KDQ_SMEM) != cudaSuccess)
     return launch_status("cudaFuncSetAttribute");
   for (int64_t q0 = 0; q0 < nq; q0 += qc) {
     const unsigned n = static_cast<unsigned>(nq - q0 < qc ? nq - q0 : qc);
     p.q0 = q0;
     bwd_pz_kernel<<<dim3(2, n), k1::NT, k1::SMEM, stream>>>(tq48, tdo48, p);
     if (launch_status("bwd_pz_kernel") != DSA_OK) return DSA_ERR_CUDA;
-    bwd_dq_tc_kernel<<<n, k2::NT, k2::SMEM, stream>>>(tz, p);
-    if (launch_status("bwd_dq_tc_kernel") != DSA_OK) return DSA_ERR_CUDA;
-    bwd_dkv_tc_kernel<<<dim3(3, n), k3::NT, k3::SMEM, stream>>>(tq96, tdo96, tz, tp, p);
-    if (launch_status("bwd_dkv_tc_kernel") != DSA_OK) return DSA_ERR_CUDA;
+    bwd_dq_dkv_kernel<<<4 * n, k3::NT, KDQ_SMEM, stream>>>(tz, tq96, tdo96, tp, p, n);
+    if (launch_status("bwd_dq_dkv_kernel") != DSA_OK) return DSA_ERR_CUDA;
   }
   return DSA_OK;
 }
